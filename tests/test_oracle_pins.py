@@ -1,0 +1,488 @@
+"""Pins for the oracle: values the pages print, closed forms, special cases,
+brute force and invariants.  CPU only."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import stats
+
+from oracle import dspark_oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- survival / STS
+
+def test_survival_table_from_page():
+    g = _gold("survival_table.json")
+    c = np.array([g["c"]], dtype=np.float32)
+    a = O.prefix_survival(c)[0]
+    printed = np.array(g["a_printed"])
+    assert np.all(np.abs(a - printed) <= 1e-3 + 1e-7)
+    # exact product at position 4 and the page's chained 3-decimal rounding
+    assert abs(float(a[3]) - 0.96 * 0.93 * 0.86 * 0.70) < 1e-6
+    chained, acc = [], None
+    for ci in g["c"]:
+        acc = ci if acc is None else round(acc * ci, 3)
+        chained.append(round(acc, 3))
+    assert chained == g["a_printed"]
+
+
+def test_survival_is_running_product_in_fp32_order():
+    rng = np.random.default_rng(1)
+    c = rng.uniform(0.3, 1.0, size=(5, 9)).astype(np.float32)
+    a = O.prefix_survival(c)
+    for r in range(5):
+        acc = np.float32(1.0)
+        for j in range(9):
+            acc = np.float32(acc * c[r, j]) if j else c[r, 0]
+            assert a[r, j] == acc
+    assert np.all(np.diff(a, axis=1) <= 0)
+
+
+def test_sts_unit_temperature_is_identity():
+    rng = np.random.default_rng(2)
+    a = np.sort(rng.uniform(0.01, 0.99, size=(4, 8)).astype(np.float32), axis=1)[:, ::-1].copy()
+    ah = O.sts_calibrate(a, np.ones(8, dtype=np.float32))
+    # sigmoid(logit(a)) = a up to one fp32 rounding of the fp64 result
+    assert np.all(np.abs(ah.astype(np.float64) - a.astype(np.float64)) <= 6e-8 * a)
+
+
+def test_sts_limits_and_textbook_temperature_scaling():
+    a = np.array([[0.9, 0.6, 0.3, 0.1]], dtype=np.float32)
+    # very hot temperature -> 1/2 ; then clamped non-increasing
+    hot = O.sts_calibrate(a, np.full(4, 1e6, dtype=np.float32))
+    assert np.all(np.abs(hot - 0.5) < 1e-5)
+    # temperature scaling of a binary logit: sigmoid(logit(a)/T) (scipy's expit/logit)
+    from scipy.special import expit, logit
+    T = np.array([1.0, 1.2, 1.4, 1.6], dtype=np.float32)
+    ah = O.sts_calibrate(a, T)
+    ref = expit(logit(a.astype(np.float64)) / T.astype(np.float64))
+    ref = np.minimum.accumulate(ref.astype(np.float32), axis=1)
+    assert np.all(np.abs(ah - ref) <= 1e-7)
+    # cold temperature pushes towards 0/1; the clamp keeps a prefix-survival shape
+    a2 = np.array([[0.8, 0.7, 0.45, 0.40]], dtype=np.float32)
+    ah2 = O.sts_calibrate(a2, np.array([1.0, 1.0, 0.1, 5.0], dtype=np.float32))
+    assert np.all(np.diff(ah2[0]) <= 0)
+
+
+# ---------------------------------------------------------------- greedy scheduler
+
+def _objective(ah, windows, cost, B):
+    E = B + sum(float(ah[r, j]) for r in range(B) for j in range(int(windows[r])))
+    return E / float(cost[B + int(sum(windows))])
+
+
+def _cost(theta, n, bias=20.0):
+    return (bias + theta * np.arange(n, dtype=np.float64)).astype(np.float32)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_greedy_reaches_bruteforce_optimum(seed):
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 4))
+    gamma = int(rng.integers(1, 5))
+    theta = float(rng.choice([0.02, 0.19, 0.5, 2.0, 6.0]))
+    conf = rng.normal(1.0, 1.5, size=(B, gamma)).astype(np.float32)
+    temps = np.linspace(1.0, 1.5, gamma).astype(np.float32)
+    budget = int(rng.integers(B, B * (gamma + 1) + 1))
+    cost = _cost(theta, B * (gamma + 1) + 2)
+    s = O.schedule(conf, 1, temps, cost, budget, O.COMPACT)
+    best, arg = -1.0, []
+    for w in itertools.product(range(gamma + 1), repeat=B):
+        if B + sum(w) > budget:
+            continue
+        v = _objective(s.a_hat, w, cost, B)
+        if v > best + 1e-15:
+            best, arg = v, [w]
+        elif abs(v - best) <= 1e-15:
+            arg.append(w)
+    got = _objective(s.a_hat, s.windows, cost, B)
+    assert got >= best - 1e-12 * best
+    if len(arg) == 1 and not s.listed:
+        assert tuple(int(x) for x in s.windows) == arg[0]
+
+
+def test_greedy_identical_requests_round_robin():
+    gamma, B = 6, 5
+    row = np.array([2.5, 2.0, 1.2, 0.3, -0.5, -1.0], dtype=np.float32)
+    conf = np.tile(row, (B, 1))
+    s = O.schedule(conf, 1, np.ones(gamma, np.float32), _cost(0.19, 64), 64, O.COMPACT)
+    w = s.windows
+    assert w.max() - w.min() <= 1
+    # equal survival: lower request index first
+    assert np.all(np.diff(w) <= 0)
+
+
+def test_greedy_zero_slope_verifies_everything_within_budget():
+    rng = np.random.default_rng(7)
+    conf = rng.normal(0.0, 2.0, size=(4, 5)).astype(np.float32)
+    s = O.schedule(conf, 1, np.ones(5, np.float32), np.full(40, 20.0, np.float32), 100, O.COMPACT)
+    assert np.all(s.windows == 5)
+    s2 = O.schedule(conf, 1, np.ones(5, np.float32), np.full(40, 20.0, np.float32), 13, O.COMPACT)
+    assert 4 + s2.windows.sum() == 13 and s2.stop_reason == "budget"
+
+
+def test_greedy_windows_shrink_with_load_and_cost_slope():
+    rng = np.random.default_rng(11)
+    gamma = 8
+    conf = rng.normal(1.5, 1.0, size=(64, gamma)).astype(np.float32)
+    temps = np.linspace(1.0, 1.5, gamma).astype(np.float32)
+    prev = None
+    for theta in (0.01, 0.05, 0.19, 0.5, 2.0):
+        s = O.schedule(conf, 1, temps, _cost(theta, 64 * 9 + 2), 10_000, O.COMPACT)
+        if prev is not None:
+            assert np.all(s.windows <= prev)
+        prev = s.windows
+    # more concurrent requests -> the first requests' windows do not grow
+    prev = None
+    for B in (4, 8, 16, 32, 64):
+        s = O.schedule(conf[:B], 1, temps, _cost(0.19, 64 * 9 + 2), 10_000, O.COMPACT)
+        if prev is not None:
+            assert np.all(s.windows[: len(prev)] <= prev)
+        prev = s.windows
+
+
+def test_static_mode_is_whole_block():
+    conf = np.zeros((3, 4), np.float32)
+    s = O.schedule(conf, 1, np.ones(4, np.float32), _cost(5.0, 20), 8, O.STATIC)
+    assert np.all(s.windows == 4) and s.M == 15
+
+
+# ---------------------------------------------------------------- pack
+
+def test_pack_example_from_page():
+    g = _gold("pack_example.json")
+    w = np.array(g["windows"], np.int32)
+    B = len(w)
+    pk = O.pack(w, np.array([10, 20, 30]), np.array([1, 2, 3]), np.arange(B * 6).reshape(B, 6),
+                g["tiers"], O.COMPACT, 6)
+    assert pk.cu_seqlens.tolist() == g["cu_seqlens"]
+    assert pk.M == g["M"] and pk.tier == g["tier"]
+    # row contents: anchor then drafts, positions ctx + i, padding marked -1
+    assert pk.row_req.tolist() == [0] * 6 + [1] * 4 + [2] * 3 + [-1] * 3
+    assert pk.row_pos[:6].tolist() == list(range(10, 16))
+    assert pk.row_tok[:6].tolist() == [1, 0, 1, 2, 3, 4]
+    assert pk.row_tok[6:10].tolist() == [2, 6, 7, 8]
+
+
+@pytest.mark.parametrize("mode", [O.COMPACT, O.STATIC, O.CAP_ACCEPT])
+def test_pack_invariants(mode):
+    rng = np.random.default_rng(5)
+    B, gamma = 9, 5
+    w = rng.integers(0, gamma + 1, size=B).astype(np.int32)
+    if mode == O.STATIC:
+        w[:] = gamma
+    tiers = [8, 16, 32, 64]
+    pk = O.pack(w, rng.integers(0, 100, B), rng.integers(0, 50, B),
+                rng.integers(0, 50, (B, gamma)), tiers, mode, gamma)
+    n = (w + 1) if mode != O.CAP_ACCEPT else np.full(B, gamma + 1)
+    assert pk.M == int(n.sum()) == pk.cu_seqlens[-1]
+    assert np.all(np.diff(pk.cu_seqlens) == n)
+    bigger = [t for t in tiers if t >= pk.M]
+    assert pk.tier == (min(bigger) if bigger else pk.M)
+    assert np.all(pk.row_req[pk.M:] == -1)
+
+
+# ---------------------------------------------------------------- attention
+
+def _toy_gqa(rng, B=2, Hq=4, Hkv=2, D=8, P=4, ctx=(5, 0), n=(3, 2)):
+    n_pages = sum((c + P - 1) // P for c in ctx) + 2
+    kc = rng.normal(size=(n_pages, P, Hkv, D))
+    vc = rng.normal(size=(n_pages, P, Hkv, D))
+    perm = rng.permutation(n_pages)
+    pt = -np.ones((B, 4), np.int64)
+    k = 0
+    for r in range(B):
+        for p in range((ctx[r] + P - 1) // P):
+            pt[r, p] = perm[k]
+            k += 1
+    cu = np.concatenate([[0], np.cumsum(n)])
+    M = int(cu[-1])
+    q = rng.normal(size=(M, Hq, D))
+    kn = rng.normal(size=(M, Hkv, D))
+    vn = rng.normal(size=(M, Hkv, D))
+    return dict(q=q, kn=kn, vn=vn, kc=kc, vc=vc, pt=pt, ctx=np.array(ctx), cu=cu)
+
+
+def _dense_masked_reference(t, Hq, Hkv, scale):
+    """Same attention written as one dense masked matrix per request (no paging,
+    no per-row prefix concatenation)."""
+    from scipy.special import logsumexp, softmax
+    B = len(t["ctx"])
+    P = t["kc"].shape[1]
+    G = Hq // Hkv
+    outs, lses = [], []
+    for r in range(B):
+        c0, c1 = t["cu"][r], t["cu"][r + 1]
+        ctx = t["ctx"][r]
+        flat_k = np.zeros((ctx + c1 - c0, Hkv, t["kc"].shape[-1]))
+        flat_v = np.zeros_like(flat_k)
+        for p in range(ctx):
+            flat_k[p] = t["kc"][t["pt"][r, p // P], p % P]
+            flat_v[p] = t["vc"][t["pt"][r, p // P], p % P]
+        flat_k[ctx:] = t["kn"][c0:c1]
+        flat_v[ctx:] = t["vn"][c0:c1]
+        nrow = c1 - c0
+        mask = np.arange(ctx + nrow)[None, :] <= (ctx + np.arange(nrow))[:, None]
+        for i in range(nrow):
+            o_i, l_i = [], []
+            for h in range(Hq):
+                s = scale * flat_k[:, h // G] @ t["q"][c0 + i, h]
+                s = np.where(mask[i], s, -np.inf)
+                o_i.append(softmax(s) @ flat_v[:, h // G])
+                l_i.append(logsumexp(s))
+            outs.append(o_i)
+            lses.append(l_i)
+    return np.array(outs), np.array(lses)
+
+
+def test_attention_matches_dense_masked_form():
+    rng = np.random.default_rng(3)
+    t = _toy_gqa(rng, B=3, ctx=(5, 0, 9), n=(3, 2, 4))
+    o, lse = O.verify_attention_gqa(t["q"], t["kn"], t["vn"], t["kc"], t["vc"], t["pt"], t["ctx"],
+                                    t["cu"], 4, 2, 0.3)
+    o2, lse2 = _dense_masked_reference(t, 4, 2, 0.3)
+    assert np.allclose(o, o2, atol=1e-12) and np.allclose(lse, lse2, atol=1e-12)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(4)
+    t = _toy_gqa(rng, B=2, ctx=(0, 6), n=(2, 3))
+    o, lse = O.verify_attention_gqa(t["q"], t["kn"], t["vn"], t["kc"], t["vc"], t["pt"], t["ctx"],
+                                    t["cu"], 4, 2, 0.5)
+    # empty context, first block row: attends to itself only
+    for h in range(4):
+        assert np.allclose(o[0, h], t["vn"][0, h // 2])
+        assert math.isclose(lse[0, h], 0.5 * t["kn"][0, h // 2] @ t["q"][0, h], rel_tol=1e-12)
+    # constant keys -> uniform average of the visible values, lse = s + log(n)
+    t2 = dict(t)
+    t2["kc"] = np.ones_like(t["kc"])
+    t2["kn"] = np.ones_like(t["kn"])
+    o, lse = O.verify_attention_gqa(t2["q"], t2["kn"], t2["vn"], t2["kc"], t2["vc"], t2["pt"],
+                                    t2["ctx"], t2["cu"], 4, 2, 0.5)
+    r, i = 1, 1
+    row = t["cu"][r] + i
+    vis_v = [t["vc"][t["pt"][r, p // 4], p % 4] for p in range(6)] + [t["vn"][t["cu"][r] + k]
+                                                                     for k in range(i + 1)]
+    for h in range(4):
+        mean = np.mean([v[h // 2] for v in vis_v], axis=0)
+        assert np.allclose(o[row, h], mean)
+        assert math.isclose(lse[row, h], 0.5 * t["q"][row, h].sum() + math.log(8), rel_tol=1e-12)
+
+
+def test_attention_page_permutation_and_causality():
+    rng = np.random.default_rng(6)
+    t = _toy_gqa(rng, B=2, ctx=(7, 3), n=(3, 3))
+    base = O.verify_attention_gqa(t["q"], t["kn"], t["vn"], t["kc"], t["vc"], t["pt"], t["ctx"],
+                                  t["cu"], 4, 2, 0.4)
+    # relabel physical pages: same result
+    n_pages = t["kc"].shape[0]
+    perm = rng.permutation(n_pages)
+    inv = np.argsort(perm)
+    kc2, vc2 = t["kc"][perm], t["vc"][perm]
+    pt2 = np.where(t["pt"] >= 0, inv[np.maximum(t["pt"], 0)], -1)
+    o2 = O.verify_attention_gqa(t["q"], t["kn"], t["vn"], kc2, vc2, pt2, t["ctx"], t["cu"], 4, 2, 0.4)
+    assert np.allclose(base[0], o2[0]) and np.allclose(base[1], o2[1])
+    # changing block row 2 of request 0 leaves rows 0, 1 untouched
+    kn3 = t["kn"].copy()
+    kn3[2] += 5.0
+    o3 = O.verify_attention_gqa(t["q"], kn3, t["vn"], t["kc"], t["vc"], t["pt"], t["ctx"], t["cu"],
+                                4, 2, 0.4)
+    assert np.allclose(o3[0][:2], base[0][:2]) and not np.allclose(o3[0][2], base[0][2])
+
+
+def test_attention_group_to_kv_head_mapping():
+    rng = np.random.default_rng(8)
+    t = _toy_gqa(rng, B=1, Hq=4, Hkv=2, ctx=(4,), n=(1,))
+    t["kc"][:] = 0.0
+    t["kn"][:] = 0.0
+    page0 = t["pt"][0, 0]
+    t["kc"][page0, 2, 1, :] = 40.0           # a dominant key, only on KV head 1, position 2
+    t["q"][:] = 1.0
+    o, _ = O.verify_attention_gqa(t["q"], t["kn"], t["vn"], t["kc"], t["vc"], t["pt"], t["ctx"],
+                                  t["cu"], 4, 2, 1.0)
+    # query heads 2, 3 (group of KV head 1) copy that value; heads 0, 1 average uniformly
+    assert np.allclose(o[0, 2], t["vc"][page0, 2, 1]) and np.allclose(o[0, 3], t["vc"][page0, 2, 1])
+    assert not np.allclose(o[0, 0], t["vc"][page0, 2, 0])
+
+
+def test_mla_is_shared_latent_mqa():
+    rng = np.random.default_rng(9)
+    P, Dqk, Dv, H = 4, 12, 8, 3
+    ctx, n = (6, 2), (2, 3)
+    n_pages = 5
+    lc = rng.normal(size=(n_pages, P, Dqk))
+    pt = np.array([[3, 1, -1], [4, -1, -1]])
+    cu = np.array([0, 2, 5])
+    q = rng.normal(size=(5, H, Dqk))
+    ln = rng.normal(size=(5, Dqk))
+    o, lse = O.verify_attention_mla(q, ln, lc, pt, np.array(ctx), cu, Dv, 0.25)
+    # the same computation as GQA with one KV head whose K is the latent and V its first Dv dims
+    o2, lse2 = O.verify_attention_gqa(q, ln[:, None, :], ln[:, None, :Dv], lc[:, :, None, :],
+                                      lc[:, :, None, :Dv], pt, np.array(ctx), cu, H, 1, 0.25)
+    assert np.allclose(o, o2) and np.allclose(lse, lse2)
+
+
+# ---------------------------------------------------------------- acceptance
+
+def _rows_for(p_pos, cu, B):
+    """Lay per-position target rows (B, gamma+1, V) out as packed rows."""
+    V = p_pos.shape[-1]
+    out = np.zeros((int(cu[-1]), V), np.float32)
+    for r in range(B):
+        n = cu[r + 1] - cu[r]
+        out[cu[r]:cu[r + 1]] = p_pos[r, :n]
+    return out
+
+
+def _three_mode_setup(accept_first=4, gamma=6, V=8, seed=0):
+    """Target accepts exactly the first ``accept_first`` drafts: p_t(d_j) >= p_d(d_j)
+    for j <= accept_first (always accepted), p_t(d_j) = 0 at the next one."""
+    rng = np.random.default_rng(seed)
+    p_t = rng.dirichlet(np.ones(V), size=(1, gamma + 1))
+    p_d = 0.5 * rng.dirichlet(np.ones(V), size=(1, gamma)) + 0.5 / V
+    d = np.zeros((1, gamma), np.int32)
+    for j in range(gamma):
+        x = int(np.argmax(p_d[0, j]))
+        d[0, j] = x
+        if j < accept_first:
+            p_t[0, j] = 0.3 * p_t[0, j]
+            p_t[0, j, x] += 0.7
+        elif j == accept_first:
+            p_t[0, j, x] = 0.0
+            p_t[0, j] /= p_t[0, j].sum()
+    p_t, p_d = p_t.astype(np.float32), p_d.astype(np.float32)
+    for j in range(min(accept_first, gamma)):
+        assert p_t[0, j, d[0, j]] >= p_d[0, j, d[0, j]]
+    u = np.full((1, gamma), 0.999, np.float32)
+    e = rng.exponential(size=(1, V)).astype(np.float32) + np.float32(1e-3)
+    return p_t, p_d, d, u, e
+
+
+def test_three_mode_example_from_page():
+    g = _gold("three_mode_example.json")
+    gamma, w, k = g["gamma"], g["window"], g["target_accepts_first"]
+    p_t, p_d, d, u, e = _three_mode_setup(k, gamma)
+    res = {}
+    for name, mode in (("compact", O.COMPACT), ("static", O.STATIC), ("cap_accept", O.CAP_ACCEPT)):
+        win = np.array([gamma if mode == O.STATIC else w], np.int32)
+        n = gamma + 1 if mode != O.COMPACT else w + 1
+        cu = np.array([0, n])
+        a = O.accept(_rows_for(p_t, cu, 1), p_d, d, u, e, win, cu, mode, gamma)
+        res[name] = a
+        assert a.accept_len[0] == g["expect"][name]["accept_len"]
+        assert a.cap_len[0] == g["expect"][name]["cap_len"]
+    bonus = int(np.argmax((p_t[0, w] / e[0]).astype(np.float32)))
+    assert res["compact"].out_tok[0] == bonus
+    assert res["cap_accept"].out_tok[0] == res["compact"].out_tok[0]
+    resid = np.maximum(0, p_t[0, k] - p_d[0, k]).astype(np.float32)
+    assert res["static"].out_tok[0] == int(np.argmax((resid / e[0]).astype(np.float32)))
+
+
+def test_prefix_semantics_from_page():
+    g = _gold("prefix_example.json")
+    gamma = g["gamma"]
+    p_t, p_d, d, u, e = _three_mode_setup(g["reject_at"] - 1, gamma, seed=3)
+    # make the drafts after the rejection individually acceptable
+    for j in range(g["reject_at"], gamma):
+        p_t[0, j, d[0, j]] = 1.0
+    cu = np.array([0, gamma + 1])
+    a = O.accept(_rows_for(p_t, cu, 1), p_d, d, u, e, np.array([gamma], np.int32), cu,
+                 O.STATIC, gamma)
+    assert a.accept_len[0] == g["accept_len"]
+
+
+def test_identical_and_disjoint_distributions():
+    rng = np.random.default_rng(12)
+    V, gamma = 16, 4
+    p = rng.dirichlet(np.ones(V), size=(1, gamma + 1)).astype(np.float32)
+    d = np.array([[int(np.argmax(p[0, j])) for j in range(gamma)]], np.int32)
+    u = rng.uniform(0.01, 0.99, size=(1, gamma)).astype(np.float32)
+    e = rng.exponential(size=(1, V)).astype(np.float32) + np.float32(1e-3)
+    cu = np.array([0, gamma + 1])
+    a = O.accept(_rows_for(p, cu, 1), p[:, :gamma].copy(), d, u, e, np.array([gamma], np.int32),
+                 cu, O.COMPACT, gamma)
+    assert a.accept_len[0] == gamma and np.allclose(a.cstar, 1.0, atol=1e-6)
+    # disjoint supports: c* = 0 and the first draft is rejected
+    pt = np.zeros((1, gamma + 1, V), np.float32)
+    pt[..., : V // 2] = 2.0 / V
+    pd = np.zeros((1, gamma, V), np.float32)
+    pd[..., V // 2:] = 2.0 / V
+    d2 = np.full((1, gamma), V - 1, np.int32)
+    a2 = O.accept(_rows_for(pt, cu, 1), pd, d2, u, e, np.array([gamma], np.int32), cu,
+                  O.COMPACT, gamma)
+    assert a2.accept_len[0] == 0 and np.allclose(a2.cstar, 0.0, atol=1e-7)
+    assert a2.out_tok[0] < V // 2           # the correction comes from the target's support
+
+
+def test_race_argmax_lowest_index_on_ties():
+    w = np.array([0.1, 0.4, 0.2, 0.4], np.float32)
+    e = np.ones(4, np.float32)
+    assert O._race_argmax(w, e)[0] == 1
+
+
+@pytest.mark.parametrize("window", [0, 1, 2])
+def test_acceptance_preserves_target_distribution(window):
+    """Textbook speculative sampling: the first committed token is distributed
+    exactly as the target at position 1, whatever the draft distribution."""
+    rng = np.random.default_rng(20 + window)
+    V, gamma, N = 6, 2, 30000
+    p_t1 = rng.dirichlet(np.ones(V) * 0.8).astype(np.float32)
+    p_d1 = rng.dirichlet(np.ones(V) * 0.8).astype(np.float32)
+    p_t = np.tile(p_t1, (N, gamma + 1, 1))
+    p_d = np.tile(p_d1, (N, gamma, 1))
+    d = np.stack([rng.choice(V, size=N, p=p_d1 / p_d1.sum()) for _ in range(gamma)], 1).astype(np.int32)
+    u = ((rng.integers(0, 1 << 24, size=(N, gamma)) + 0.5) * 2.0 ** -24).astype(np.float32)
+    e = (-np.log((rng.integers(0, 1 << 24, size=(N, V)) + 0.5) * 2.0 ** -24)).astype(np.float32)
+    win = np.full(N, window, np.int32)
+    cu = np.arange(N + 1) * (window + 1)
+    rows = np.repeat(p_t1[None], int(cu[-1]), 0)
+    a = O.accept(rows, p_d, d, u, e, win, cu, O.COMPACT, gamma)
+    first = np.where(a.accept_len > 0, d[:, 0], a.out_tok)
+    counts = np.bincount(first, minlength=V)
+    expected = p_t1.astype(np.float64) / p_t1.sum() * N
+    chi2 = ((counts - expected) ** 2 / expected).sum()
+    assert stats.chi2.sf(chi2, V - 1) > 1e-4
+
+
+# ---------------------------------------------------------------- compaction
+
+def test_compact_hand_worked_example():
+    g = _gold("compact_example.json")
+    P = g["page_size"]
+    B = 3
+    L = np.array(g["accept_len"], np.int32)
+    cu = np.concatenate([[0], np.cumsum(L + 1)]).astype(np.int32)
+    M = int(cu[-1])
+    kn = np.arange(M, dtype=np.float32).reshape(M, 1, 1) + 100.0
+    kc = np.zeros((8, P, 1, 1), np.float32)
+    draft = np.arange(B * 5).reshape(B, 5).astype(np.int32)
+    tok = np.array([70, 71, 72], np.int32)
+    c = O.compact(kn, kn, cu, L, tok, draft, P, np.array(g["page_table"]), np.array(g["ctx_len"]),
+                  np.array([1, 2, 3]), np.array(g["free_pages"]), g["free_top"], kc, kc.copy())
+    assert c.page_table.tolist() == g["expect_page_table"]
+    assert c.ctx_len.tolist() == g["expect_ctx_len"] and c.free_top == g["expect_free_top"]
+    for r, slots in g["expect_slots"].items():
+        r = int(r)
+        for i, (page, off) in enumerate(slots):
+            assert c.k_cache[page, off, 0, 0] == 100.0 + cu[r] + i
+    assert c.anchor.tolist() == [70, 71, 72]
+    assert c.committed[2].tolist() == [10, 11, 12, 13, 72, -1]
+    assert c.n_committed.tolist() == [3, 1, 5]
+
+
+def test_compact_no_space_raises():
+    kn = np.zeros((2, 1, 1), np.float32)
+    with pytest.raises(O.NoSpace):
+        O.compact(kn, kn, np.array([0, 2]), np.array([1]), np.array([0]), np.zeros((1, 3), np.int32),
+                  2, np.array([[0, -1]]), np.array([2]), np.array([0]), np.array([], np.int32), 0,
+                  np.zeros((2, 2, 1, 1)), np.zeros((2, 2, 1, 1)))
