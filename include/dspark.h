@@ -1,0 +1,234 @@
+/*
+ * dspark.h -- C ABI of libdspark.so: DSpark's confidence-scheduled ragged
+ * verification step on one GB300 (sm_103a).
+ *
+ * The step, in the order a caller runs it on one CUDA stream:
+ *
+ *   dspark_schedule     calibrated prefix survival -> per-request verify windows
+ *   dspark_pack         head-to-tail packing, cu_seqlens, captured tier, row indices
+ *   dspark_verify_attn  varlen verify attention of the packed rows over paged KV
+ *   dspark_accept       prefix speculative-sampling acceptance, bonus/correction, c*
+ *   dspark_compact      scatter of accepted KV rows + page-table append
+ *
+ * Sources, cited by short name:
+ *   [lesson] "DFlash 到 DSpark in SGLang：解码提速 4.3×，以及 DeepSeek-V4 支持"
+ *            (AI Infra Visualized lesson on DSpark)
+ *   [csdn]   DevPress/CSDN article on DSpark in SGLang (sections 2-5)
+ *   [notes]  "DSpark：投机解码与生产级 Serving 学习笔记" (sections 02, 07, 08, 09)
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless the
+ *     argument's comment says "host".  Tensors are dense row-major, no strides.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is enqueued
+ *     on it; no call synchronises, allocates or frees memory.  Each call launches
+ *     a fixed sequence of kernels whose grid does not depend on device data, so
+ *     the sequence can be captured in a CUDA graph.
+ *   - Return value: a dspark_status.  Arguments are checked on the host before
+ *     anything is launched; a non-OK return means nothing was enqueued (except
+ *     DSPARK_ECUDA, which reports a failed launch).  Nothing throws or aborts.
+ *   - Conditions only the device can see (a packed batch larger than the row
+ *     capacity, an exhausted free-page stack, a wait that ran out) set bits of a
+ *     per-device error word (DSPARK_DEVERR_*); the kernel that sees them skips
+ *     the offending writes.  dspark_read_device_error() returns and clears it.
+ *   - The library must have been built for sm_103a; on any other device the
+ *     first call returns DSPARK_EUNSUPPORTED.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_EINVAL = -1,        /* bad argument: NULL pointer, size, alignment      */
+  DSPARK_EUNSUPPORTED = -2,  /* shape or device outside what the kernels handle  */
+  DSPARK_ECUDA = -3,         /* a CUDA runtime call or launch failed             */
+  DSPARK_ENOSPACE = -4,      /* workspace smaller than *_workspace_size()        */
+  DSPARK_EDEVICE = -5        /* device error word non-zero (read_device_error)   */
+} dspark_status;
+
+/* Verify modes ([lesson] "Confidence scheduler 与 verify 模式"; [csdn] 2.):
+ * COMPACT verifies only each request's window (the production path); STATIC
+ * verifies the whole block; CAP_ACCEPT verifies the whole block but commits
+ * only up to the window (identical commits to COMPACT) and records the cap. */
+typedef enum { DSPARK_COMPACT = 0, DSPARK_STATIC = 1, DSPARK_CAP_ACCEPT = 2 } dspark_mode;
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
+
+/* Bits of the device error word. */
+#define DSPARK_DEVERR_ROWS_OVERFLOW 0x1u   /* packed tier > max_rows               */
+#define DSPARK_DEVERR_NO_FREE_PAGE  0x2u   /* free-page stack exhausted (compact)  */
+#define DSPARK_DEVERR_PAGE_ROW_FULL 0x4u   /* page-table row too short (compact)   */
+#define DSPARK_DEVERR_WAIT_TIMEOUT  0x8u   /* a bounded in-kernel wait ran out     */
+#define DSPARK_DEVERR_BAD_INPUT     0x10u  /* index input out of range (token, page) */
+#define DSPARK_DEVERR_WORK_OVERFLOW 0x20u  /* attention work list larger than ws   */
+
+/* Limits checked on the host. */
+#define DSPARK_MAX_B        1024   /* requests per step                          */
+#define DSPARK_MAX_GAMMA    32     /* draft block length                         */
+#define DSPARK_MAX_CANDS    4096   /* B * gamma for the scheduler's sort          */
+#define DSPARK_MAX_TIERS    64
+
+const char* dspark_status_string(int status);
+
+/* Reads and clears the device error word of the current device.  Synchronises
+ * `stream`.  Returns the word (>= 0) or DSPARK_ECUDA. */
+int dspark_read_device_error(void* stream);
+
+/* Number of SMs the persistent kernels size their grids by (current device). */
+int dspark_num_sms(void);
+
+/* ---------------------------------------------------------------------------
+ * dspark_schedule -- per-request verify windows.
+ * [notes] 07 (c_k, a_j = prod_{i<=j} c_i, STS), [notes] 08.3 (global greedy:
+ * sort candidates by survival, add while expected throughput rises, stop at the
+ * first drop), [csdn] 4. (T(bs,K) = bias + alpha(bs) + theta(M), M = bs + K).
+ *
+ *   conf        fp32 [B, gamma]  confidence logits (conf_is_logit = 1) or c
+ *   sts_temp    fp32 [gamma]     per-position STS temperature T_j > 0
+ *   cost_table  fp32 [cost_len]  step cost T[M] (any unit, > 0) for M = 0..cost_len-1;
+ *                                cost_len >= min(max_tokens, B*(gamma+1)) + 1
+ *   max_tokens  largest verify row count the step may use (largest captured tier)
+ *   mode        dspark_mode; STATIC sets every window to gamma
+ *   windows     int32 [B]  out: verified drafts w_r in [0, gamma]
+ *   a_hat       fp32 [B, gamma]  out: calibrated survival (non-increasing in j)
+ *   M_out       int32 [1]  out: B + sum w_r
+ *   E_out       fp64 [1]   out: expected committed tokens B + sum of chosen a_hat
+ *
+ * Arithmetic: c = fp32(1/(1+exp(-z))) in fp64; a_j = fp32 running product;
+ * a_hat_j = fp32(1/(1+exp(-(log a - log1p(-a))/T_j))) in fp64, then the running
+ * minimum over j.  Candidates sort by a_hat descending, ties by request then
+ * position ascending.  E starts at B and M at B; candidate k is accepted iff
+ * B + k + 1 <= max_tokens and (E_k + a_k)/T[M_k+1] > E_k/T[M_k] in fp64.
+ * Limits: 1 <= B <= 1024, 1 <= gamma <= 32, B*gamma <= 4096.
+ * ------------------------------------------------------------------------- */
+int dspark_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
+                    const float* cost_table, int cost_len, int B, int gamma, int max_tokens,
+                    int mode, int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
+                    void* stream);
+
+/* ---------------------------------------------------------------------------
+ * dspark_pack -- head-to-tail ragged packing ([lesson] "Ragged verify under full
+ * CUDA graphs"; [csdn] 3.).
+ *
+ * Request r occupies n_r = 1 + v_r consecutive rows, v_r = windows[r] (COMPACT,
+ * STATIC) or gamma (CAP_ACCEPT): the anchor token then drafts d_1..d_{v_r}.
+ *   cu_seqlens  int32 [B+1] out: exclusive prefix sum of n_r
+ *   M_out       int32 [1]   out: cu_seqlens[B]
+ *   tier_out    int32 [1]   out: smallest entry of `tiers` >= M, or M if none is
+ *   row_req     int32 [max_rows] out: request of each packed row, -1 on padding
+ *   row_pos     int32 [max_rows] out: absolute position ctx_len[r] + i, -1 on padding
+ *                                     (its page is page_table[r][pos / page_size])
+ *   row_tok     int32 [max_rows] out: token of the row (anchor or d_i), -1 on padding
+ *   tiers       int32 [n_tiers] ascending captured tier sizes (device)
+ * Rows tier..max_rows-1 are left untouched.  If tier > max_rows the device sets
+ * DSPARK_DEVERR_ROWS_OVERFLOW and writes only the first max_rows rows.
+ * ------------------------------------------------------------------------- */
+int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
+                const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
+                int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out, int32_t* tier_out,
+                int32_t* row_req, int32_t* row_pos, int32_t* row_tok, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * dspark_verify_attn -- variable-length verify attention over the paged cache
+ * ([lesson] "Ragged verify under full CUDA graphs": every packed token attends
+ * only to its own request's KV; causal inside the block).
+ *
+ * Packed row cu_seqlens[r] + i (block index i) of request r, query head h, sees
+ * the ctx_len[r] committed keys (through page_table) followed by block rows
+ * 0..i of its own segment:  o = softmax(scale q.K^T) V,  lse = log sum exp.
+ *
+ * Two shapes:
+ *   GQA  d_qk = d_v = 128, Hq % Hkv == 0, Hq/Hkv <= 128.
+ *        q       bf16 [max_rows, Hq, 128]
+ *        k_new   bf16 [max_rows, Hkv, 128],  v_new   the same
+ *        k_cache bf16 [n_pages, page_size, Hkv, 128], v_cache the same
+ *   MLA  d_qk = 576, d_v = 512, Hkv = 1, Hq = 128, v_new = v_cache = NULL.
+ *        q       bf16 [max_rows, 128, 576]
+ *        k_new   bf16 [max_rows, 576]   (latent of the block rows)
+ *        k_cache bf16 [n_pages, page_size, 576]; values are the first 512 dims.
+ *   page_table  int32 [B, max_pages]; entries past ceil(ctx/page_size) unused
+ *   out         fp32 [max_rows, Hq, d_v]  out (rows >= M not written)
+ *   lse         fp32 [max_rows, Hq]       out, natural log
+ *   workspace   >= dspark_verify_attn_workspace_size(...) bytes, 256-B aligned
+ * page_size must be a multiple of 16 (GQA) or 32 (MLA).  All bases 16-B aligned.
+ * Long contexts are split across CTAs (at most max_splits pieces per request,
+ * head and row tile) and merged by a log-sum-exp combine.
+ * ------------------------------------------------------------------------- */
+size_t dspark_verify_attn_workspace_size(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v,
+                                         int max_splits);
+int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                       const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
+                       const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows,
+                       int Hq, int Hkv, int d_qk, int d_v, int page_size, float scale,
+                       int max_splits, float* out, float* lse, void* workspace, size_t ws_bytes,
+                       void* stream);
+
+/* ---------------------------------------------------------------------------
+ * dspark_accept -- prefix speculative sampling ([notes] 02; [lesson]
+ * "Background" and "Confidence scheduler 与 verify 模式"; c* label [notes] 07).
+ *
+ *   p_target   [max_rows, V] packed target rows (fp32 or bf16 per pdt); row
+ *              cu_seqlens[r] + i is the target distribution for position i + 1
+ *   p_draft    [B, gamma, V] drafter distribution for positions 1..gamma
+ *   draft_tok  int32 [B, gamma]
+ *   uniforms   fp32 [B, gamma]  u in (0, 1) for the test at each position
+ *   exp_noise  fp32 [B, V]      e ~ Exp(1) (Gumbel noise in exponential form,
+ *                               G = -log e), used for the one sampled row
+ *   windows    int32 [B]        the scheduler's windows (commit limit)
+ *   accept_len int32 [B] out: committed drafts L_r
+ *   cap_len    int32 [B] out: accepted prefix over the verified positions
+ *   out_tok    int32 [B] out: correction (after a rejection) or bonus token
+ *   cstar      fp32 [B, gamma] out: 1 - 0.5 ||p_d - p_t||_1 where a target row
+ *              exists for the position, NaN elsewhere
+ *   fallback   int32 [B] out (nullable): 1 if an all-zero residual forced the
+ *              draw from p_target
+ * Test: accept d_j iff fp32(u_j * p_d(d_j)) <= p_t(d_j).  Draws: argmax over v of
+ * w_v / e_v in fp32 (w = max(0, p_t - p_d) after a rejection, p_t for the bonus),
+ * lowest index on ties.
+ * ------------------------------------------------------------------------- */
+size_t dspark_accept_workspace_size(int B, int gamma, int max_rows, int V);
+int dspark_accept(const void* p_target, const void* p_draft, int pdt, int V,
+                  const int32_t* draft_tok, const float* uniforms, const float* exp_noise,
+                  const int32_t* windows, const int32_t* cu_seqlens, int mode, int B, int gamma,
+                  int max_rows, int32_t* accept_len, int32_t* cap_len, int32_t* out_tok,
+                  float* cstar, int32_t* fallback, void* workspace, size_t ws_bytes,
+                  void* stream);
+
+/* ---------------------------------------------------------------------------
+ * dspark_compact -- commit the step ([lesson] "Zero-overhead scheduling 与
+ * kernel": compact scatter, device-resident page table).
+ *
+ * For each request in order: rows 0..L_r of its packed segment (anchor and
+ * accepted drafts) are copied to cache positions ctx_r..ctx_r+L_r; pages are
+ * popped from the top of free_pages (free_pages[*free_top-1] first, requests in
+ * order) when a position opens a new page and appended to page_table[r];
+ * ctx_len[r] += L_r + 1; anchor[r] = out_tok[r]; committed[r] = d_1..d_L, out_tok
+ * (-1 beyond), n_committed[r] = L_r + 1.  Rejected rows are never written.
+ *   row_bytes   bytes of one K row (GQA: Hkv*128*2, MLA: 576*2); V rows the same
+ *   k_new/v_new [max_rows, row] packed block rows; v_new/v_cache NULL for MLA
+ *   k_cache/v_cache [n_pages, page_size, row]
+ *   page_table  int32 [B, max_pages] in/out; ctx_len, anchor int32 [B] in/out
+ *   free_pages  int32 [n_free]; free_top int32 [1] in/out
+ *   committed   int32 [B, gamma+1] out; n_committed int32 [B] out
+ * If the free stack or a page-table row is too short the device sets
+ * DSPARK_DEVERR_NO_FREE_PAGE / _PAGE_ROW_FULL and changes nothing.
+ * ------------------------------------------------------------------------- */
+size_t dspark_compact_workspace_size(int B);
+int dspark_compact(const void* k_new, const void* v_new, int row_bytes, const int32_t* cu_seqlens,
+                   const int32_t* accept_len, const int32_t* out_tok, const int32_t* draft_tok,
+                   int B, int gamma, int page_size, int max_pages, int n_pages,
+                   int32_t* page_table, int32_t* ctx_len, int32_t* anchor,
+                   const int32_t* free_pages, int32_t* free_top, void* k_cache, void* v_cache,
+                   int32_t* committed, int32_t* n_committed, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSPARK_H */

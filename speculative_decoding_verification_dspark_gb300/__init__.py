@@ -1,0 +1,258 @@
+"""Python binding of libdspark.so (ctypes): argument marshalling only.
+
+Every step of the verification path runs in the library's CUDA kernels; this
+module converts torch tensors to raw device pointers, passes the current CUDA
+stream, and turns non-zero status codes into exceptions.  PyTorch is used for
+device memory and streams only.  Importing works without a GPU; calling needs
+one (sm_103a) and the built library -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "COMPACT", "STATIC", "CAP_ACCEPT", "F32", "BF16", "DSparkError", "lib", "load",
+    "schedule", "pack", "verify_attn", "accept", "compact", "read_device_error",
+    "verify_attn_workspace_size", "accept_workspace_size", "compact_workspace_size",
+    "VerifyStep", "DEVERR",
+]
+
+COMPACT, STATIC, CAP_ACCEPT = 0, 1, 2
+F32, BF16 = 0, 1
+DEVERR = {
+    0x1: "rows_overflow", 0x2: "no_free_page", 0x4: "page_row_full", 0x8: "wait_timeout",
+    0x10: "bad_input", 0x20: "work_overflow",
+}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdspark.so")
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_Z = ctypes.c_size_t
+
+_SIGNATURES = {
+    "dspark_status_string": (ctypes.c_char_p, [_I]),
+    "dspark_read_device_error": (_I, [_P]),
+    "dspark_num_sms": (_I, []),
+    "dspark_schedule": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "dspark_pack": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "dspark_verify_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "dspark_verify_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                _F, _I, _P, _P, _P, _Z, _P]),
+    "dspark_accept_workspace_size": (_Z, [_I, _I, _I, _I]),
+    "dspark_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
+                           _P, _Z, _P]),
+    "dspark_compact_workspace_size": (_Z, [_I]),
+    "dspark_compact": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                            _P, _P, _P, _P, _Z, _P]),
+}
+
+_lib = None
+
+
+class DSparkError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = lib().dspark_status_string(status).decode()
+        super().__init__(f"{fn} failed: {msg} ({status})")
+        self.status = status
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the in-tree library; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it with __graft_entry__.build() "
+                              "(speculative_decoding_verification_dspark_gb300/build.py)")
+        l = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+lib = load
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise DSparkError(fn, rc)
+
+
+def read_device_error(stream=None) -> int:
+    rc = lib().dspark_read_device_error(_stream(stream))
+    if rc < 0:
+        raise DSparkError("dspark_read_device_error", rc)
+    return rc
+
+
+def num_sms() -> int:
+    return lib().dspark_num_sms()
+
+
+def schedule(conf, conf_is_logit, sts_temp, cost_table, max_tokens, mode, windows, a_hat, M_out,
+             E_out, stream=None):
+    B, gamma = conf.shape
+    _check("dspark_schedule", lib().dspark_schedule(
+        _ptr(conf), int(conf_is_logit), _ptr(sts_temp), _ptr(cost_table), cost_table.numel(), B,
+        gamma, int(max_tokens), int(mode), _ptr(windows), _ptr(a_hat), _ptr(M_out), _ptr(E_out),
+        _stream(stream)))
+
+
+def pack(windows, ctx_len, anchor, draft_tok, tiers, mode, cu_seqlens, M_out, tier_out, row_req,
+         row_pos, row_tok, stream=None):
+    B, gamma = draft_tok.shape
+    _check("dspark_pack", lib().dspark_pack(
+        _ptr(windows), _ptr(ctx_len), _ptr(anchor), _ptr(draft_tok), _ptr(tiers), tiers.numel(), B,
+        gamma, int(mode), row_req.numel(), _ptr(cu_seqlens), _ptr(M_out), _ptr(tier_out),
+        _ptr(row_req), _ptr(row_pos), _ptr(row_tok), _stream(stream)))
+
+
+def verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits) -> int:
+    return lib().dspark_verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits)
+
+
+def verify_attn(q, k_new, v_new, k_cache, v_cache, page_table, ctx_len, cu_seqlens, scale,
+                max_splits, out, lse, workspace, stream=None):
+    """GQA: q [rows, Hq, 128], k/v_new [rows, Hkv, 128], caches [pages, P, Hkv, 128].
+    MLA: q [rows, 128, 576], k_new [rows, 576], k_cache [pages, P, 576], v_* None."""
+    max_rows, Hq, d_qk = q.shape
+    mla = v_cache is None
+    Hkv = 1 if mla else k_cache.shape[2]
+    d_v = out.shape[2]
+    B = ctx_len.numel()
+    _check("dspark_verify_attn", lib().dspark_verify_attn(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(page_table), page_table.shape[1], _ptr(ctx_len), _ptr(cu_seqlens), B, max_rows, Hq,
+        Hkv, d_qk, d_v, k_cache.shape[1], float(scale), int(max_splits), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def accept_workspace_size(B, gamma, max_rows, V) -> int:
+    return lib().dspark_accept_workspace_size(B, gamma, max_rows, V)
+
+
+def accept(p_target, p_draft, draft_tok, uniforms, exp_noise, windows, cu_seqlens, mode,
+           accept_len, cap_len, out_tok, cstar, fallback, workspace, stream=None):
+    B, gamma, V = p_draft.shape
+    pdt = BF16 if p_target.dtype == torch.bfloat16 else F32
+    _check("dspark_accept", lib().dspark_accept(
+        _ptr(p_target), _ptr(p_draft), pdt, V, _ptr(draft_tok), _ptr(uniforms), _ptr(exp_noise),
+        _ptr(windows), _ptr(cu_seqlens), int(mode), B, gamma, p_target.shape[0], _ptr(accept_len),
+        _ptr(cap_len), _ptr(out_tok), _ptr(cstar), _ptr(fallback), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def compact_workspace_size(B) -> int:
+    return lib().dspark_compact_workspace_size(B)
+
+
+def compact(k_new, v_new, cu_seqlens, accept_len, out_tok, draft_tok, page_table, ctx_len, anchor,
+            free_pages, free_top, k_cache, v_cache, committed, n_committed, workspace, stream=None):
+    B, gamma = draft_tok.shape
+    row_bytes = k_new[0].numel() * k_new.element_size()
+    _check("dspark_compact", lib().dspark_compact(
+        _ptr(k_new), _ptr(v_new), row_bytes, _ptr(cu_seqlens), _ptr(accept_len), _ptr(out_tok),
+        _ptr(draft_tok), B, gamma, k_cache.shape[1], page_table.shape[1], k_cache.shape[0],
+        _ptr(page_table), _ptr(ctx_len), _ptr(anchor), _ptr(free_pages), _ptr(free_top),
+        _ptr(k_cache), _ptr(v_cache), _ptr(committed), _ptr(n_committed), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+class VerifyStep:
+    """Device buffers and workspaces for repeated verification steps of one shape.
+
+    ``run`` enqueues the five calls of one step on the current stream:
+    schedule -> pack -> verify_attn -> accept -> compact.  The per-row inputs
+    (q, k_new, v_new, p_target) are read from the packed buffers the caller
+    fills; state (caches, page table, ctx_len, anchor, free stack) is updated in
+    place by compact.
+    """
+
+    def __init__(self, B, gamma, Hq, Hkv, d_qk, d_v, vocab, max_rows, p_dtype=torch.float32,
+                 max_splits=8, device="cuda"):
+        self.B, self.gamma, self.Hq, self.Hkv, self.d_qk, self.d_v = B, gamma, Hq, Hkv, d_qk, d_v
+        self.vocab, self.max_rows, self.max_splits = vocab, max_rows, max_splits
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.windows = torch.zeros(B, **i32)
+        self.a_hat = torch.zeros(B, gamma, dtype=torch.float32, device=dev)
+        self.M = torch.zeros(1, **i32)
+        self.E = torch.zeros(1, dtype=torch.float64, device=dev)
+        self.cu_seqlens = torch.zeros(B + 1, **i32)
+        self.M_pack = torch.zeros(1, **i32)
+        self.tier = torch.zeros(1, **i32)
+        self.row_req = torch.zeros(max_rows, **i32)
+        self.row_pos = torch.zeros(max_rows, **i32)
+        self.row_tok = torch.zeros(max_rows, **i32)
+        self.out = torch.zeros(max_rows, Hq, d_v, dtype=torch.float32, device=dev)
+        self.lse = torch.zeros(max_rows, Hq, dtype=torch.float32, device=dev)
+        self.accept_len = torch.zeros(B, **i32)
+        self.cap_len = torch.zeros(B, **i32)
+        self.out_tok = torch.zeros(B, **i32)
+        self.fallback = torch.zeros(B, **i32)
+        self.cstar = torch.zeros(B, gamma, dtype=torch.float32, device=dev)
+        self.committed = torch.zeros(B, gamma + 1, **i32)
+        self.n_committed = torch.zeros(B, **i32)
+        sz = verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits)
+        if sz == 0:
+            raise ValueError("unsupported attention shape")
+        self.ws_attn = torch.empty(sz, dtype=torch.uint8, device=dev)
+        self.ws_accept = torch.empty(accept_workspace_size(B, gamma, max_rows, vocab),
+                                     dtype=torch.uint8, device=dev)
+        self.ws_compact = torch.empty(compact_workspace_size(B), dtype=torch.uint8, device=dev)
+
+    def schedule(self, inp, mode, stream=None):
+        schedule(inp["conf"], inp["conf_is_logit"], inp["sts_temp"], inp["cost_table"],
+                 inp["max_tokens"], mode, self.windows, self.a_hat, self.M, self.E, stream)
+
+    def pack(self, inp, mode, stream=None):
+        pack(self.windows, inp["ctx_len"], inp["anchor"], inp["draft_tok"], inp["tiers"], mode,
+             self.cu_seqlens, self.M_pack, self.tier, self.row_req, self.row_pos, self.row_tok,
+             stream)
+
+    def attention(self, inp, stream=None):
+        verify_attn(inp["q"], inp["k_new"], inp.get("v_new"), inp["k_cache"], inp.get("v_cache"),
+                    inp["page_table"], inp["ctx_len"], self.cu_seqlens, inp["scale"],
+                    self.max_splits, self.out, self.lse, self.ws_attn, stream)
+
+    def accept(self, inp, mode, stream=None):
+        accept(inp["p_target"], inp["p_draft"], inp["draft_tok"], inp["uniforms"],
+               inp["exp_noise"], self.windows, self.cu_seqlens, mode, self.accept_len,
+               self.cap_len, self.out_tok, self.cstar, self.fallback, self.ws_accept, stream)
+
+    def compact(self, inp, stream=None):
+        compact(inp["k_new"], inp.get("v_new"), self.cu_seqlens, self.accept_len, self.out_tok,
+                inp["draft_tok"], inp["page_table"], inp["ctx_len"], inp["anchor"],
+                inp["free_pages"], inp["free_top"], inp["k_cache"], inp.get("v_cache"),
+                self.committed, self.n_committed, self.ws_compact, stream)
+
+    def run(self, inp, mode, stream=None):
+        self.schedule(inp, mode, stream)
+        self.pack(inp, mode, stream)
+        self.attention(inp, stream)
+        self.accept(inp, mode, stream)
+        self.compact(inp, stream)

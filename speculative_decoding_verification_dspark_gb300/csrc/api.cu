@@ -1,0 +1,248 @@
+// C ABI of libdspark.so: argument checks on the host, then the launches.
+// Every entry point returns a dspark_status and launches nothing on a bad argument.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn.h"
+#include "common.cuh"
+#include "dspark.h"
+#include "kernels.h"
+
+namespace dspark {
+
+__device__ unsigned int g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool init = false;
+  bool supported = false;
+  int sms = 0;
+  unsigned int* err = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+DeviceState* state() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceState& s = g_dev[dev];
+  if (!s.init) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev);
+    void* p = nullptr;
+    const bool sym = cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess;
+    s.err = static_cast<unsigned int*>(p);
+    s.supported = sym && major == 10 && minor == 3 && s.sms > 0;
+    s.init = true;
+  }
+  return &s;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+unsigned int* device_error_word() {
+  DeviceState* s = state();
+  return s ? s->err : nullptr;
+}
+
+int num_sms_cached() {
+  DeviceState* s = state();
+  return (s && s->sms > 0) ? s->sms : 1;
+}
+
+}  // namespace dspark
+
+using namespace dspark;
+
+#define CHECK(cond, code) \
+  do {                    \
+    if (!(cond)) return (code); \
+  } while (0)
+
+static int device_ok() {
+  DeviceState* s = state();
+  if (!s) return DSPARK_ECUDA;
+  return s->supported ? DSPARK_OK : DSPARK_EUNSUPPORTED;
+}
+
+extern "C" {
+
+const char* dspark_status_string(int status) {
+  switch (status) {
+    case DSPARK_OK: return "ok";
+    case DSPARK_EINVAL: return "invalid argument";
+    case DSPARK_EUNSUPPORTED: return "unsupported shape or device";
+    case DSPARK_ECUDA: return "CUDA runtime error";
+    case DSPARK_ENOSPACE: return "workspace too small";
+    case DSPARK_EDEVICE: return "device error word set";
+    default: return "unknown status";
+  }
+}
+
+int dspark_num_sms(void) { return num_sms_cached(); }
+
+int dspark_read_device_error(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int* w = device_error_word();
+  if (!w) return DSPARK_ECUDA;
+  unsigned int h = 0;
+  if (cudaMemcpyAsync(&h, w, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DSPARK_ECUDA;
+  if (cudaMemsetAsync(w, 0, sizeof(h), st) != cudaSuccess) return DSPARK_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return DSPARK_ECUDA;
+  return static_cast<int>(h & 0x7fffffffu);
+}
+
+int dspark_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
+                    const float* cost_table, int cost_len, int B, int gamma, int max_tokens,
+                    int mode, int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
+                    void* stream) {
+  CHECK(conf && sts_temp && cost_table && windows && a_hat && M_out && E_out, DSPARK_EINVAL);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
+  CHECK(B * gamma <= DSPARK_MAX_CANDS, DSPARK_EINVAL);
+  CHECK(mode >= DSPARK_COMPACT && mode <= DSPARK_CAP_ACCEPT, DSPARK_EINVAL);
+  CHECK(max_tokens >= 1, DSPARK_EINVAL);
+  if (mode != DSPARK_STATIC) {
+    const long long need = (max_tokens < B * (gamma + 1) ? max_tokens : B * (gamma + 1)) + 1LL;
+    CHECK(cost_len >= need, DSPARK_EINVAL);
+  }
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  return launch_schedule(conf, conf_is_logit ? 1 : 0, sts_temp, cost_table, B, gamma, max_tokens,
+                         mode, windows, a_hat, M_out, E_out, static_cast<cudaStream_t>(stream));
+}
+
+int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
+                const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
+                int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out, int32_t* tier_out,
+                int32_t* row_req, int32_t* row_pos, int32_t* row_tok, void* stream) {
+  CHECK(windows && ctx_len && anchor && draft_tok && cu_seqlens && M_out && tier_out && row_req &&
+            row_pos && row_tok,
+        DSPARK_EINVAL);
+  CHECK(n_tiers >= 0 && n_tiers <= DSPARK_MAX_TIERS && (n_tiers == 0 || tiers), DSPARK_EINVAL);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
+  CHECK(mode >= DSPARK_COMPACT && mode <= DSPARK_CAP_ACCEPT, DSPARK_EINVAL);
+  CHECK(max_rows >= 1, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  return launch_pack(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode, max_rows,
+                     cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok,
+                     static_cast<cudaStream_t>(stream));
+}
+
+static bool attn_shape_ok(int Hq, int Hkv, int d_qk, int d_v, int page_size) {
+  if (d_qk == 128 && d_v == 128) {
+    if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || Hq / Hkv > 128) return false;
+    if (page_size < 16 || page_size % 16 != 0) return false;
+    return page_size <= 64 ? (64 % page_size == 0) : (page_size % 64 == 0);
+  }
+  if (d_qk == 576 && d_v == 512) {
+    if (Hkv != 1 || Hq != 128) return false;
+    if (page_size < 16 || page_size % 16 != 0) return false;
+    return page_size <= 32 ? (32 % page_size == 0) : (page_size % 32 == 0);
+  }
+  return false;
+}
+
+size_t dspark_verify_attn_workspace_size(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v,
+                                         int max_splits) {
+  if (B < 1 || max_rows < 1 || max_splits < 1 || max_splits > 32) return 0;
+  if (!attn_shape_ok(Hq, Hkv, d_qk, d_v, 16)) return 0;
+  return attn::plan(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits).bytes;
+}
+
+int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                       const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
+                       const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows,
+                       int Hq, int Hkv, int d_qk, int d_v, int page_size, float scale,
+                       int max_splits, float* out, float* lse, void* workspace, size_t ws_bytes,
+                       void* stream) {
+  CHECK(attn_shape_ok(Hq, Hkv, d_qk, d_v, page_size), DSPARK_EUNSUPPORTED);
+  const bool mla = d_qk == 576;
+  CHECK(q && k_new && k_cache && page_table && ctx_len && cu_seqlens && out && lse && workspace,
+        DSPARK_EINVAL);
+  CHECK(mla || (v_new && v_cache), DSPARK_EINVAL);
+  CHECK(aligned16(q) && aligned16(k_new) && aligned16(k_cache) && aligned16(out) &&
+            (mla || (aligned16(v_new) && aligned16(v_cache))),
+        DSPARK_EINVAL);
+  CHECK((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, DSPARK_EINVAL);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && max_rows >= 1 && n_pages >= 1 && max_pages >= 1,
+        DSPARK_EINVAL);
+  CHECK(max_splits >= 1 && max_splits <= 32, DSPARK_EINVAL);
+  CHECK(scale > 0.f, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  const attn::Plan pl = attn::plan(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits);
+  CHECK(ws_bytes >= pl.bytes, DSPARK_ENOSPACE);
+  return attn::launch(q, k_new, v_new, k_cache, v_cache, n_pages, page_table, max_pages, ctx_len,
+                      cu_seqlens, B, max_rows, Hq, Hkv, d_qk, d_v, page_size, scale, max_splits,
+                      out, lse, workspace, pl, static_cast<cudaStream_t>(stream));
+}
+
+size_t dspark_accept_workspace_size(int B, int gamma, int max_rows, int V) {
+  if (B < 1 || gamma < 1 || max_rows < 1 || V < 8) return 0;
+  return accept_workspace(B, max_rows, V);
+}
+
+int dspark_accept(const void* p_target, const void* p_draft, int pdt, int V,
+                  const int32_t* draft_tok, const float* uniforms, const float* exp_noise,
+                  const int32_t* windows, const int32_t* cu_seqlens, int mode, int B, int gamma,
+                  int max_rows, int32_t* accept_len, int32_t* cap_len, int32_t* out_tok,
+                  float* cstar, int32_t* fallback, void* workspace, size_t ws_bytes,
+                  void* stream) {
+  CHECK(p_target && p_draft && draft_tok && uniforms && exp_noise && windows && cu_seqlens &&
+            accept_len && cap_len && out_tok && cstar && workspace,
+        DSPARK_EINVAL);
+  CHECK(pdt == DSPARK_F32 || pdt == DSPARK_BF16, DSPARK_EINVAL);
+  CHECK(V >= 8 && V % 8 == 0, DSPARK_EUNSUPPORTED);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
+  CHECK(mode >= DSPARK_COMPACT && mode <= DSPARK_CAP_ACCEPT, DSPARK_EINVAL);
+  CHECK(max_rows >= 1, DSPARK_EINVAL);
+  CHECK(aligned16(p_target) && aligned16(p_draft) && aligned16(exp_noise), DSPARK_EINVAL);
+  CHECK((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  CHECK(ws_bytes >= accept_workspace(B, max_rows, V), DSPARK_ENOSPACE);
+  return launch_accept(p_target, p_draft, pdt, V, draft_tok, uniforms, exp_noise, windows,
+                       cu_seqlens, mode, B, gamma, max_rows, accept_len, cap_len, out_tok, cstar,
+                       fallback, workspace, static_cast<cudaStream_t>(stream));
+}
+
+size_t dspark_compact_workspace_size(int B) {
+  if (B < 1) return 0;
+  return compact_workspace(B);
+}
+
+int dspark_compact(const void* k_new, const void* v_new, int row_bytes, const int32_t* cu_seqlens,
+                   const int32_t* accept_len, const int32_t* out_tok, const int32_t* draft_tok,
+                   int B, int gamma, int page_size, int max_pages, int n_pages,
+                   int32_t* page_table, int32_t* ctx_len, int32_t* anchor,
+                   const int32_t* free_pages, int32_t* free_top, void* k_cache, void* v_cache,
+                   int32_t* committed, int32_t* n_committed, void* workspace, size_t ws_bytes,
+                   void* stream) {
+  CHECK(k_new && cu_seqlens && accept_len && out_tok && draft_tok && page_table && ctx_len &&
+            anchor && free_pages && free_top && k_cache && committed && n_committed && workspace,
+        DSPARK_EINVAL);
+  CHECK((v_new == nullptr) == (v_cache == nullptr), DSPARK_EINVAL);
+  CHECK(row_bytes >= 16 && row_bytes % 16 == 0, DSPARK_EINVAL);
+  CHECK(aligned16(k_new) && aligned16(k_cache) && (!v_new || (aligned16(v_new) && aligned16(v_cache))),
+        DSPARK_EINVAL);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
+  CHECK(page_size >= 1 && max_pages >= 1 && n_pages >= 1, DSPARK_EINVAL);
+  CHECK((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  CHECK(ws_bytes >= compact_workspace(B), DSPARK_ENOSPACE);
+  return launch_compact(k_new, v_new, row_bytes, cu_seqlens, accept_len, out_tok, draft_tok, B,
+                        gamma, page_size, max_pages, n_pages, page_table, ctx_len, anchor,
+                        free_pages, free_top, k_cache, v_cache, committed, n_committed, workspace,
+                        static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

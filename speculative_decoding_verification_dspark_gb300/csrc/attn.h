@@ -1,0 +1,34 @@
+// Internal interface of the verify-attention launcher (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dspark {
+namespace attn {
+
+// One unit of work: a 128-row query tile of one request against a range of its key tiles.
+struct __align__(16) AttnItem {
+  int r, kvh, i0, ni;        // request, KV head, first block row, block rows in the tile
+  int part, split, tb, te;   // value-column part, split index, key-tile range [tb, te)
+  int nsplit, pad0, pad1, pad2;
+};
+
+struct Plan {
+  bool mla;
+  int parts, rows_per_tile, nk;
+  long long max_items;
+  size_t off_items, off_nitems, off_nsplit, off_o, off_lse, bytes;
+};
+
+Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_splits);
+
+int launch(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+           const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
+           const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq, int Hkv,
+           int d_qk, int d_v, int page_size, float scale, int max_splits, float* out, float* lse,
+           void* ws, const Plan& pl, cudaStream_t stream);
+
+}  // namespace attn
+}  // namespace dspark

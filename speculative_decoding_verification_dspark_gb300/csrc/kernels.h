@@ -1,0 +1,35 @@
+// Internal launchers of the step kernels (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dspark {
+
+int launch_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
+                    const float* cost_table, int B, int gamma, int max_tokens, int mode,
+                    int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
+                    cudaStream_t stream);
+
+int launch_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
+                const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
+                int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out, int32_t* tier_out,
+                int32_t* row_req, int32_t* row_pos, int32_t* row_tok, cudaStream_t stream);
+
+size_t accept_workspace(int B, int max_rows, int V);
+int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_t* draft_tok,
+                  const float* uniforms, const float* exp_noise, const int32_t* windows,
+                  const int32_t* cu, int mode, int B, int gamma, int max_rows, int32_t* accept_len,
+                  int32_t* cap_len, int32_t* out_tok, float* cstar, int32_t* fallback, void* ws,
+                  cudaStream_t stream);
+
+size_t compact_workspace(int B);
+int launch_compact(const void* k_new, const void* v_new, int row_bytes, const int32_t* cu,
+                   const int32_t* accept_len, const int32_t* out_tok, const int32_t* draft_tok,
+                   int B, int gamma, int page_size, int max_pages, int n_pages, int32_t* page_table,
+                   int32_t* ctx_len, int32_t* anchor, const int32_t* free_pages, int32_t* free_top,
+                   void* k_cache, void* v_cache, int32_t* committed, int32_t* n_committed, void* ws,
+                   cudaStream_t stream);
+
+}  // namespace dspark

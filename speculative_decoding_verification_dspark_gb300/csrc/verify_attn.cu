@@ -1,0 +1,874 @@
+// Varlen verify attention over a paged KV cache, causal inside the draft block.
+//
+// What it computes ("DFlash 到 DSpark in SGLang", section "Ragged verify under
+// full CUDA graphs": the packed verify tokens each attend only to their own
+// request's KV): packed row cu_seqlens[r] + i, query head h, attends to the
+// ctx_len[r] committed keys of request r (read through its page table) and to
+// block rows 0..i of its own segment; o = softmax(scale q.K^T) V, lse = log-sum-exp.
+//
+// How (sm_103a):
+//   * one work item = (request, KV head, block-row tile, value-column part, KV split);
+//     its query rows (block rows x the query heads of one KV head, or the 128 heads
+//     of one block row for the latent-KV shape) form one 128-row UMMA tile;
+//   * a persistent grid (one CTA per SM) walks the item list;
+//   * warp 0 streams K/V tiles into a shared-memory ring: full pages by TMA
+//     (128-byte swizzle, no multicast), the partial last page and the draft block's
+//     own rows by plain loads written in the same swizzled layout;
+//   * warp 1 (one lane) issues tcgen05.mma: S = Q K^T into a double-buffered TMEM
+//     tile, then O += P V into a TMEM accumulator;
+//   * warps 2-5 own one query row per thread: read S from TMEM, mask, online
+//     softmax in fp32 (exp2 domain, lazy rescale of O when the running max grows
+//     by more than 2^8), write P (bf16) to shared memory, and finally normalise O;
+//   * long contexts split across items; a log-sum-exp combine merges the pieces.
+// Every mbarrier wait is bounded in time; a wait that runs out raises
+// DSPARK_DEVERR_WAIT_TIMEOUT, the CTA drains its own copies, frees TMEM and exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dspark {
+namespace attn {
+
+using namespace ptx;
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kThreads = 192;                    // 6 warps
+constexpr int kRows = 128;                       // UMMA M
+
+template <int D_QK_, int DV_, int NK_, int STAGES_, bool MLA_>
+struct Cfg {
+  static constexpr int D_QK = D_QK_;
+  static constexpr int DV = DV_;          // value columns handled by one item
+  static constexpr int NK = NK_;          // keys per tile
+  static constexpr int STAGES = STAGES_;
+  static constexpr bool MLA = MLA_;
+  static constexpr int QK_CB = D_QK / 64;                 // 64-wide swizzle column blocks
+  static constexpr int Q_CB_BYTES = kRows * 128;          // one column block of Q
+  static constexpr int Q_BYTES = QK_CB * Q_CB_BYTES;
+  static constexpr int KV_CB_BYTES = NK * 128;            // one column block of a K/V tile
+  static constexpr int K_BYTES = QK_CB * KV_CB_BYTES;
+  static constexpr int V_BYTES = MLA ? 0 : (DV / 64) * KV_CB_BYTES;
+  static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
+  static constexpr int P_ROW_BYTES = NK * 2;              // 128 (NK=64) or 64 (NK=32)
+  static constexpr int P_BYTES = kRows * P_ROW_BYTES;
+  static constexpr int P_BUFS = MLA ? 1 : 2;
+  static constexpr SwizzleMode P_SW = (NK == 64) ? SW_128B : SW_64B;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_STAGE = OFF_Q + Q_BYTES;
+  static constexpr int OFF_P = OFF_STAGE + STAGES * STAGE_BYTES;
+  static constexpr int OFF_BAR = OFF_P + P_BUFS * P_BYTES;
+  // barriers: kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full[PB], p_empty[PB], q_full
+  static constexpr int N_BARS = 2 * STAGES + 4 + 2 * P_BUFS + 1;
+  static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+  static constexpr int TMEM_S = 0;                         // two S tiles of NK columns
+  static constexpr int TMEM_O = 2 * NK;
+  static constexpr int TMEM_COLS_USED = 2 * NK + DV;
+  static constexpr int TMEM_COLS = TMEM_COLS_USED <= 256 ? 256 : 512;
+  static constexpr int PARTS = MLA ? 2 : 1;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(TMEM_COLS_USED <= 512, "tensor memory budget");
+  static_assert(NK == 64 || NK == 32, "tile width");
+  static_assert(STAGE_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0 && P_BYTES % 1024 == 0, "align");
+};
+
+using CfgGQA = Cfg<128, 128, 64, 4, false>;
+using CfgMLA = Cfg<576, 256, 32, 2, true>;
+
+struct Smem {
+  uint32_t base;  // shared-space address of the aligned base
+  uint8_t* ptr;
+};
+
+struct Ctx {
+  volatile int* abort_flag;
+  unsigned int* err;
+};
+
+// Wait for the phase of `bar` with the given parity; bounded.  Returns false if
+// the CTA is aborting.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctx& cx) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++n & 31u) == 0) {
+      if (*cx.abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *cx.abort_flag = 1;
+        raise_error(cx.err, DSPARK_DEVERR_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Used only on the way out: wait regardless of the abort flag, bounded.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned int* err) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      raise_error(err, DSPARK_DEVERR_WAIT_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// 16-byte chunk q (0-based, 8 per 128-byte row) of row `row` in a 128B-swizzled
+// K-major tile: chunk index XOR (row mod 8).
+__device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+// 64B swizzle, 64-byte rows: chunk (0..3) XOR ((row / 2) mod 4).
+__device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
+  return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Copy `nrows` rows (row stride `gstride` elements, D_QK or DV wide) from global
+// into a swizzled K-major tile of NK rows; rows in [valid, NK) are zero.  Called by
+// all 32 lanes of one warp.
+template <int WIDTH, int NK>
+__device__ __forceinline__ void warp_fill_tile(uint32_t dst, const __nv_bfloat16* src,
+                                               long long gstride, int valid, int lane) {
+  constexpr int CHUNKS = WIDTH / 8;        // 16-byte chunks per row
+  constexpr int CB_BYTES = NK * 128;
+  for (int idx = lane; idx < NK * CHUNKS; idx += 32) {
+    const int row = idx / CHUNKS;
+    const int q = idx % CHUNKS;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row < valid) v = ldg_nc_v4(src + row * gstride + q * 8);
+    st_shared_v4(dst + (q >> 3) * CB_BYTES + sw128_off(row, q & 7), v);
+  }
+}
+
+template <class C>
+struct Layout {
+  uint32_t q, stage0, p0, bar0;
+  __device__ uint32_t stage(int s) const { return stage0 + s * C::STAGE_BYTES; }
+  __device__ uint32_t pbuf(int b) const { return p0 + b * C::P_BYTES; }
+  __device__ uint32_t kv_full(int s) const { return bar0 + 8 * s; }
+  __device__ uint32_t kv_empty(int s) const { return bar0 + 8 * (C::STAGES + s); }
+  __device__ uint32_t s_full(int b) const { return bar0 + 8 * (2 * C::STAGES + b); }
+  __device__ uint32_t s_free(int b) const { return bar0 + 8 * (2 * C::STAGES + 2 + b); }
+  __device__ uint32_t p_full(int b) const { return bar0 + 8 * (2 * C::STAGES + 4 + b); }
+  __device__ uint32_t p_empty(int b) const {
+    return bar0 + 8 * (2 * C::STAGES + 4 + C::P_BUFS + b);
+  }
+  __device__ uint32_t q_full() const { return bar0 + 8 * (2 * C::STAGES + 4 + 2 * C::P_BUFS); }
+};
+
+struct Params {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
+  const int32_t* page_table;
+  const int32_t* ctx_len;
+  const int32_t* cu_seqlens;
+  const AttnItem* items;
+  const int* n_items;
+  float* out;
+  float* lse;
+  float* ws_o;
+  float* ws_lse;
+  unsigned int* err;
+  int max_pages, B, Hq, Hkv, page_size, max_rows, d_v_total, n_pages;
+  float scale_log2;
+};
+
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1)
+    verify_attn_kernel(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  Layout<C> L{base + C::OFF_Q, base + C::OFF_STAGE, base + C::OFF_P, base + C::OFF_BAR};
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::OFF_MISC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::OFF_MISC + 16);
+  const Ctx cx{abort_flag, prm.err};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(L.kv_full(s), 1);
+      mbar_init(L.kv_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(L.s_full(b), 1);
+      mbar_init(L.s_free(b), 4);
+    }
+    for (int b = 0; b < C::P_BUFS; ++b) {
+      mbar_init(L.p_full(b), 4);
+      mbar_init(L.p_empty(b), 1);
+    }
+    mbar_init(L.q_full(), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tm_k);
+    if (!C::MLA) prefetch_tensormap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int n_items = *prm.n_items;
+  const int G = C::MLA ? kRows : prm.Hq / prm.Hkv;  // query rows per block row
+  const int P = prm.page_size;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    int g = 0;
+    bool ok = true;
+    const int box_rows = P < C::NK ? P : C::NK;
+    const uint32_t box_bytes = box_rows * 128;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const AttnItem item = prm.items[it];
+      const int r = item.r;
+      const int ctx = prm.ctx_len[r];
+      const int c0 = prm.cu_seqlens[r];
+      const int n_r = prm.cu_seqlens[r + 1] - c0;
+      const int ct = ceil_div(ctx, C::NK);
+      const int32_t* ptab = prm.page_table + (long long)r * prm.max_pages;
+      for (int t = item.tb; t < item.te; ++t, ++g) {
+        const int s = g % C::STAGES;
+        if (g >= C::STAGES) {
+          ok = wait_bar(L.kv_empty(s), ((g / C::STAGES) - 1) & 1, cx);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+        }
+        const uint32_t kdst = L.stage(s);
+        const uint32_t vdst = kdst + C::K_BYTES;
+        if (t < ct) {
+          // cache tile: keys [t*NK, t*NK + NK) of the committed context
+          uint32_t tx = 0;
+          const int nbox = C::NK / box_rows;
+          for (int bx = 0; bx < nbox; ++bx) {
+            const int kg = t * C::NK + bx * box_rows;
+            if (kg + box_rows <= ctx) tx += box_bytes * (C::QK_CB + (C::MLA ? 0 : C::DV / 64));
+          }
+          if (lane == 0 && tx > 0) mbar_expect_tx(L.kv_full(s), tx);
+          for (int bx = 0; bx < nbox; ++bx) {
+            const int kg = t * C::NK + bx * box_rows;
+            int page = kg < ctx ? ptab[kg / P] : 0;
+            if (page < 0 || page >= prm.n_pages) {
+              // a corrupt page-table entry: read nothing (zeros), report it
+              if (lane == 0) raise_error(prm.err, DSPARK_DEVERR_BAD_INPUT);
+              page = kg < ctx ? -1 : 0;
+            }
+            const int in_page = kg % P;
+            const int row0 = bx * box_rows;
+            if (kg + box_rows <= ctx) {
+              if (lane == 0) {
+                for (int cb = 0; cb < C::QK_CB; ++cb) {
+                  const uint32_t dst = kdst + cb * C::KV_CB_BYTES + row0 * 128;
+                  if (C::MLA)
+                    tma_load_3d(dst, &tm_k, L.kv_full(s), cb * 64, in_page, page);
+                  else
+                    tma_load_4d(dst, &tm_k, L.kv_full(s), cb * 64, item.kvh, in_page, page);
+                }
+                if (!C::MLA) {
+                  for (int cb = 0; cb < C::DV / 64; ++cb) {
+                    const uint32_t dst = vdst + cb * C::KV_CB_BYTES + row0 * 128;
+                    tma_load_4d(dst, &tm_v, L.kv_full(s), cb * 64, item.kvh, in_page, page);
+                  }
+                }
+              }
+            } else {
+              // partial or empty box: plain loads of the valid rows, zeros elsewhere
+              const int valid = (kg < ctx && page >= 0) ? ctx - kg : 0;
+              const long long rs = C::MLA ? C::D_QK : (long long)prm.Hkv * C::D_QK;
+              const long long off =
+                  ((long long)(valid > 0 ? page : 0) * P + in_page) * rs +
+                  (C::MLA ? 0 : (long long)item.kvh * C::D_QK);
+              // rows of this box land at tile rows row0 .. row0+box_rows-1
+              constexpr int CH = C::D_QK / 8;
+              for (int idx = lane; idx < box_rows * CH; idx += 32) {
+                const int rr = idx / CH, q = idx % CH;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (rr < valid) v = ldg_nc_v4(prm.k_cache + off + rr * rs + q * 8);
+                st_shared_v4(kdst + (q >> 3) * C::KV_CB_BYTES + sw128_off(row0 + rr, q & 7), v);
+              }
+              if (!C::MLA) {
+                constexpr int CHV = C::DV / 8;
+                for (int idx = lane; idx < box_rows * CHV; idx += 32) {
+                  const int rr = idx / CHV, q = idx % CHV;
+                  uint4 v = make_uint4(0, 0, 0, 0);
+                  if (rr < valid) v = ldg_nc_v4(prm.v_cache + off + rr * rs + q * 8);
+                  st_shared_v4(vdst + (q >> 3) * C::KV_CB_BYTES + sw128_off(row0 + rr, q & 7), v);
+                }
+              }
+            }
+          }
+        } else {
+          // block tile: the request's own packed rows (anchor + drafts), from k_new/v_new
+          const int b0 = (t - ct) * C::NK;
+          const int valid = n_r - b0 < C::NK ? n_r - b0 : C::NK;
+          if (C::MLA) {
+            warp_fill_tile<C::D_QK, C::NK>(kdst, prm.k_new + (long long)(c0 + b0) * C::D_QK, C::D_QK,
+                                           valid, lane);
+          } else {
+            const long long rs = (long long)prm.Hkv * C::D_QK;
+            const long long off = (long long)(c0 + b0) * rs + (long long)item.kvh * C::D_QK;
+            warp_fill_tile<C::D_QK, C::NK>(kdst, prm.k_new + off, rs, valid, lane);
+            warp_fill_tile<C::DV, C::NK>(vdst, prm.v_new + off, rs, valid, lane);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.kv_full(s));
+      }
+    }
+    // Make sure no copy of ours is still in flight before the CTA exits.
+    if (lane == 0) {
+      const int first = g - C::STAGES > 0 ? g - C::STAGES : 0;
+      for (int gg = first; gg < g; ++gg) drain_bar(L.kv_full(gg % C::STAGES), (gg / C::STAGES) & 1, prm.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(kRows, C::NK, 0, 0);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(kRows, C::DV, 0, 1);
+      int g = 0, n_it = 0, last_pv = -1;
+      bool ok = true;
+      auto issue_pv = [&](int gp, int local, int part) -> bool {
+        const int pb = gp % C::P_BUFS;
+        if (!wait_bar(L.p_full(pb), (gp / C::P_BUFS) & 1, cx)) return false;
+        tc_fence_after();
+        const int s = gp % C::STAGES;
+        const uint32_t vbase =
+            C::MLA ? L.stage(s) + part * 4 * C::KV_CB_BYTES : L.stage(s) + C::K_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::NK / 16; ++kk) {
+          const uint64_t a = smem_desc(L.pbuf(pb) + kk * 32, 16, 8 * C::P_ROW_BYTES, C::P_SW);
+          const uint64_t b = smem_desc(vbase + kk * 2048, C::KV_CB_BYTES, 1024, SW_128B);
+          umma_bf16(tmem + C::TMEM_O, a, b, IDESC_PV, (local > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(L.p_empty(pb));
+        umma_commit(L.kv_empty(s));
+        last_pv = gp;
+        return true;
+      };
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n_it) {
+        const AttnItem item = prm.items[it];
+        if (!wait_bar(L.q_full(), n_it & 1, cx)) { ok = false; break; }
+        const int ntiles = item.te - item.tb;
+        for (int l = 0; l < ntiles; ++l, ++g) {
+          const int s = g % C::STAGES;
+          const int sb = g & 1;
+          if (!wait_bar(L.kv_full(s), (g / C::STAGES) & 1, cx)) { ok = false; break; }
+          if (g >= 2 && !wait_bar(L.s_free(sb), ((g >> 1) - 1) & 1, cx)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < C::D_QK / 16; ++kk) {
+            const uint64_t a = smem_desc(L.q + (kk >> 2) * C::Q_CB_BYTES + (kk & 3) * 32, 16, 1024, SW_128B);
+            const uint64_t b = smem_desc(L.stage(s) + (kk >> 2) * C::KV_CB_BYTES + (kk & 3) * 32, 16, 1024, SW_128B);
+            umma_bf16(tmem + C::TMEM_S + sb * C::NK, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(L.s_full(sb));
+          if (l >= 1 && !issue_pv(g - 1, l - 1, item.part)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!issue_pv(g - 1, ntiles - 1, item.part)) { ok = false; break; }
+      }
+      // all issued MMAs must finish before TMEM is released
+      if (last_pv >= 0) drain_bar(L.p_empty(last_pv % C::P_BUFS), (last_pv / C::P_BUFS) & 1, prm.err);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax / epilogue
+    const int sw = warp & 3;                 // TMEM lane quadrant of this warp
+    const int m = sw * 32 + lane;            // query row of this thread
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
+    const int stid = threadIdx.x - 64;       // 0..127
+    int g = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const AttnItem item = prm.items[it];
+      const int r = item.r;
+      const int ctx = prm.ctx_len[r];
+      const int c0 = prm.cu_seqlens[r];
+      const int n_r = prm.cu_seqlens[r + 1] - c0;
+      const int ct = ceil_div(ctx, C::NK);
+      const int rows_valid = C::MLA ? kRows : item.ni * G;
+      // ---- Q tile (rows beyond rows_valid are zero)
+      {
+        constexpr int CH = C::D_QK / 8;
+        for (int idx = stid; idx < kRows * CH; idx += 128) {
+          const int row = idx / CH, q = idx % CH;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (row < rows_valid) {
+            long long src;
+            if (C::MLA)
+              src = ((long long)(c0 + item.i0) * prm.Hq + row) * C::D_QK;
+            else
+              src = ((long long)(c0 + item.i0 + row / G) * prm.Hq + item.kvh * G + row % G) * C::D_QK;
+            v = ldg_nc_v4(prm.q + src + q * 8);
+          }
+          st_shared_v4(L.q + (q >> 3) * C::Q_CB_BYTES + sw128_off(row, q & 7), v);
+        }
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (stid == 0) mbar_arrive(L.q_full());
+      }
+      const bool row_ok = m < rows_valid;
+      const bool warp_active = __any_sync(0xffffffffu, row_ok);
+      const int bi = C::MLA ? item.i0 : item.i0 + m / G;   // block index of this row
+      float m_used = -INFINITY, l_sum = 0.f;
+      const int ntiles = item.te - item.tb;
+      for (int l = 0; l < ntiles; ++l, ++g) {
+        const int t = item.tb + l;
+        const int sb = g & 1;
+        bool w_ok = wait_bar(L.s_full(sb), (g >> 1) & 1, cx);
+        w_ok = __all_sync(0xffffffffu, w_ok);
+        if (!w_ok) { ok = false; break; }
+        tc_fence_after();
+        float s[C::NK];
+        if (warp_active) {
+#pragma unroll
+          for (int c = 0; c < C::NK / 32; ++c) {
+            float tmp[32];
+            tmem_ld32(t_lane + C::TMEM_S + sb * C::NK + c * 32, tmp);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) s[c * 32 + k] = tmp[k];
+          }
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.s_free(sb));
+        // P buffer of this tile must be free: PV(g - P_BUFS) done
+        const int pb = g % C::P_BUFS;
+        if (g >= C::P_BUFS) {
+          const int gp = g - C::P_BUFS;
+          w_ok = wait_bar(L.p_empty(gp % C::P_BUFS), (gp / C::P_BUFS) & 1, cx);
+          w_ok = __all_sync(0xffffffffu, w_ok);
+          if (!w_ok) { ok = false; break; }
+        }
+        if (warp_active) {
+          // ---- mask + scale + tile max
+          float mt = -INFINITY;
+          const bool block_tile = t >= ct;
+          const int kbase = block_tile ? (t - ct) * C::NK : t * C::NK;
+#pragma unroll
+          for (int k = 0; k < C::NK; ++k) {
+            const int key = kbase + k;
+            const bool vis = block_tile ? (key <= bi && key < n_r) : (key < ctx);
+            s[k] = vis ? s[k] * prm.scale_log2 : -INFINITY;
+            mt = fmaxf(mt, s[k]);
+          }
+          // ---- lazy rescale of O when the running max grows by more than 2^8
+          const bool need = row_ok && (mt > m_used + 8.0f);
+          const bool any_need = __any_sync(0xffffffffu, need) && l > 0;
+          if (any_need) {
+            // O must hold PV(g-1): wait for it (its P buffer's barrier)
+            const int gq = g - 1;
+            if (C::P_BUFS > 1) {
+              w_ok = wait_bar(L.p_empty(gq % C::P_BUFS), (gq / C::P_BUFS) & 1, cx);
+              w_ok = __all_sync(0xffffffffu, w_ok);
+              if (!w_ok) { ok = false; break; }
+            }
+            tc_fence_after();
+            const float alpha = need ? exp2f(m_used - mt) : 1.0f;
+#pragma unroll 1
+            for (int c = 0; c < C::DV / 32; ++c) {
+              float o[32];
+              tmem_ld32(t_lane + C::TMEM_O + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] *= alpha;
+              tmem_st32(t_lane + C::TMEM_O + c * 32, o);
+            }
+            tmem_wait_st();
+          }
+          if (need) {
+            l_sum *= (l > 0) ? exp2f(m_used - mt) : 0.f;
+            m_used = mt;
+          }
+          // ---- P = exp2(s - m_used), bf16, swizzled K-major row m
+          const uint32_t prow = L.pbuf(pb);
+          const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+          float psum = 0.f;
+#pragma unroll
+          for (int q = 0; q < C::NK / 8; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float p0 = row_ok ? exp2f(s[q * 8 + 2 * h] - mref) : 0.f;
+              const float p1 = row_ok ? exp2f(s[q * 8 + 2 * h + 1] - mref) : 0.f;
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              psum += __low2float(b2) + __high2float(b2);
+              w[h] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            const uint32_t off = (C::NK == 64) ? sw128_off(m, q) : sw64_off(m, q);
+            st_shared_v4(prow + off, make_uint4(w[0], w[1], w[2], w[3]));
+          }
+          l_sum += psum;
+          tc_fence_before();
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.p_full(pb));
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l  (split items write partials for the combine)
+      {
+        const int gl = g - 1;
+        bool w_ok = wait_bar(L.p_empty(gl % C::P_BUFS), (gl / C::P_BUFS) & 1, cx);
+        w_ok = __all_sync(0xffffffffu, w_ok);
+        if (!w_ok) { ok = false; break; }
+        tc_fence_after();
+        if (warp_active) {
+          const int row_g = c0 + bi;
+          const int head = C::MLA ? m : item.kvh * G + m % G;
+          const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+          const bool split = item.nsplit > 1;
+          float* obase;
+          if (split)
+            obase = prm.ws_o + (((long long)item.split * prm.max_rows + row_g) * prm.Hq + head) *
+                                   prm.d_v_total;
+          else
+            obase = prm.out + ((long long)row_g * prm.Hq + head) * prm.d_v_total;
+          obase += item.part * C::DV;
+#pragma unroll 1
+          for (int c = 0; c < C::DV / 32; ++c) {
+            float o[32];
+            tmem_ld32(t_lane + C::TMEM_O + c * 32, o);
+            tmem_wait_ld();
+            if (row_ok) {
+              float4* dst = reinterpret_cast<float4*>(obase + c * 32);
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                dst[k] = make_float4(o[4 * k] * inv_l, o[4 * k + 1] * inv_l, o[4 * k + 2] * inv_l,
+                                     o[4 * k + 3] * inv_l);
+            }
+          }
+          if (row_ok && item.part == 0) {
+            const float lse_v = (m_used + log2f(l_sum)) * 0.69314718055994530942f;
+            if (split)
+              prm.ws_lse[((long long)item.split * prm.max_rows + row_g) * prm.Hq + head] = lse_v;
+            else
+              prm.lse[(long long)row_g * prm.Hq + head] = lse_v;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- work list
+// One CTA.  Splits each request's key range so that the item count is near
+// `target_items` and no request is cut into more than `max_splits` pieces.
+__global__ void __launch_bounds__(1024)
+    worklist_kernel(const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ cu_seqlens,
+                    int B, int Hkv, int parts, int rows_per_tile, int NK, int max_splits,
+                    int target_items, int max_items, AttnItem* __restrict__ items,
+                    int* __restrict__ n_items, int* __restrict__ nsplit_r,
+                    unsigned int* __restrict__ err) {
+  __shared__ long long s_red[32];
+  __shared__ int s_scan[32];
+  const int r = threadIdx.x;
+  int n = 0, ctx = 0, tt = 0, rt = 0;
+  if (r < B) {
+    n = cu_seqlens[r + 1] - cu_seqlens[r];
+    ctx = ctx_len[r];
+    tt = ceil_div(ctx, NK) + ceil_div(n, NK);
+    rt = ceil_div(n, rows_per_tile);
+  }
+  long long units = (long long)tt * rt * Hkv * parts;
+  // block sum of units
+  for (int o = 16; o > 0; o >>= 1) units += __shfl_xor_sync(0xffffffffu, units, o);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = units;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    long long v = threadIdx.x < (blockDim.x >> 5) ? s_red[threadIdx.x] : 0;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) s_red[0] = v;
+  }
+  __syncthreads();
+  const long long U = s_red[0];
+  const long long chunk = U / target_items + ((U % target_items) ? 1 : 0);
+  int ns = 0, per = 1;
+  if (r < B) {
+    long long want = chunk > 0 ? (tt + chunk - 1) / chunk : 1;
+    ns = (int)(want < 1 ? 1 : (want > max_splits ? max_splits : want));
+    per = ceil_div(tt, ns);
+    ns = ceil_div(tt, per);
+  }
+  int cnt = (r < B) ? rt * Hkv * parts * ns : 0;
+  // exclusive scan of cnt
+  int v = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    int u = __shfl_up_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) >= o) v += u;
+  }
+  if ((threadIdx.x & 31) == 31) s_scan[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int w = threadIdx.x < (blockDim.x >> 5) ? s_scan[threadIdx.x] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      int u = __shfl_up_sync(0xffffffffu, w, o);
+      if (threadIdx.x >= o) w += u;
+    }
+    s_scan[threadIdx.x] = w;
+  }
+  __syncthreads();
+  const int warp_off = (threadIdx.x >> 5) ? s_scan[(threadIdx.x >> 5) - 1] : 0;
+  const int off = warp_off + v - cnt;
+  const int total = s_scan[(blockDim.x >> 5) - 1];
+  if (threadIdx.x == 0) {
+    if (total > max_items) {
+      raise_error(err, DSPARK_DEVERR_WORK_OVERFLOW);
+      *n_items = 0;
+    } else {
+      *n_items = total;
+    }
+  }
+  if (r < B) nsplit_r[r] = ns;
+  if (r < B && total <= max_items) {
+    int k = off;
+    for (int s = 0; s < ns; ++s) {
+      const int tb = s * per;
+      const int te = (tb + per < tt) ? tb + per : tt;
+      for (int t = 0; t < rt; ++t) {
+        const int i0 = t * rows_per_tile;
+        const int ni = (n - i0 < rows_per_tile) ? n - i0 : rows_per_tile;
+        for (int p = 0; p < parts; ++p) {
+          for (int h = 0; h < Hkv; ++h) {
+            AttnItem it;
+            it.r = r; it.kvh = h; it.i0 = i0; it.ni = ni;
+            it.part = p; it.split = s; it.tb = tb; it.te = te;
+            it.nsplit = ns; it.pad0 = 0; it.pad1 = 0; it.pad2 = 0;
+            items[k++] = it;
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- split combine
+// One warp per (packed row, query head) of a request that was split.
+__global__ void __launch_bounds__(256)
+    combine_kernel(const int32_t* __restrict__ cu_seqlens, int B, int Hq, int d_v,
+                   const int* __restrict__ nsplit_r, const float* __restrict__ ws_o,
+                   const float* __restrict__ ws_lse, int max_rows, float* __restrict__ out,
+                   float* __restrict__ lse) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int M = cu_seqlens[B];
+  const int row = wid / Hq, head = wid % Hq;
+  if (row >= M || row >= max_rows) return;
+  const int r = upper_segment(cu_seqlens, B, row);
+  const int ns = nsplit_r[r];
+  if (ns <= 1) return;
+  float my = -INFINITY;
+  if (lane < ns) my = ws_lse[((long long)lane * max_rows + row) * Hq + head];
+  float mx = my;
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float w = lane < ns ? expf(my - mx) : 0.f;
+  float sum = w;
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = 1.f / sum;
+  for (int c = lane; c < d_v; c += 32) {
+    float acc = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w, s);
+      acc += ws * ws_o[(((long long)s * max_rows + row) * Hq + head) * d_v + c];
+    }
+    out[((long long)row * Hq + head) * d_v + c] = acc * inv;
+  }
+  if (lane == 0) lse[(long long)row * Hq + head] = mx + logf(sum);
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  EncodeFn enc = get_encode();
+  if (!enc) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult rc = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                    strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS;
+}
+
+template <class C>
+bool configure_smem() {
+  static bool done = false, okv = false;
+  if (!done) {
+    done = true;
+    okv = cudaFuncSetAttribute(verify_attn_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_BYTES) == cudaSuccess;
+  }
+  return okv;
+}
+
+constexpr int kItemsPerSm = 2;
+
+}  // namespace
+
+Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_splits) {
+  Plan p{};
+  p.mla = (d_qk == 576);
+  const int G = p.mla ? Hq : Hq / Hkv;
+  p.parts = p.mla ? 2 : 1;
+  p.rows_per_tile = p.mla ? 1 : (kRows / G);
+  p.nk = p.mla ? CfgMLA::NK : CfgGQA::NK;
+  const long long tiles_rows = (long long)max_rows / (p.rows_per_tile > 0 ? p.rows_per_tile : 1) + B;
+  p.max_items = (long long)Hkv * p.parts * max_splits * tiles_rows;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += (bytes + 255) & ~size_t(255);
+    return o;
+  };
+  p.off_items = take(sizeof(AttnItem) * (size_t)p.max_items);
+  p.off_nitems = take(sizeof(int));
+  p.off_nsplit = take(sizeof(int) * (size_t)B);
+  p.off_o = take(sizeof(float) * (size_t)max_splits * max_rows * Hq * d_v);
+  p.off_lse = take(sizeof(float) * (size_t)max_splits * max_rows * Hq);
+  p.bytes = off;
+  return p;
+}
+
+int launch(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+           const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
+           const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq, int Hkv,
+           int d_qk, int d_v, int page_size, float scale, int max_splits, float* out, float* lse,
+           void* ws, const Plan& pl, cudaStream_t stream) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  AttnItem* items = reinterpret_cast<AttnItem*>(w + pl.off_items);
+  int* n_items = reinterpret_cast<int*>(w + pl.off_nitems);
+  int* nsplit = reinterpret_cast<int*>(w + pl.off_nsplit);
+  float* ws_o = reinterpret_cast<float*>(w + pl.off_o);
+  float* ws_lse = reinterpret_cast<float*>(w + pl.off_lse);
+  unsigned int* err = device_error_word();
+  const int sms = num_sms_cached();
+  const int target = sms * kItemsPerSm;
+  const int max_items = pl.max_items > 0x7fffffff ? 0x7fffffff : (int)pl.max_items;
+
+  worklist_kernel<<<1, 1024, 0, stream>>>(ctx_len, cu_seqlens, B, Hkv, pl.parts, pl.rows_per_tile,
+                                           pl.nk, max_splits, target, max_items, items, n_items,
+                                           nsplit, err);
+  DSPARK_LAUNCH_CHECK();
+
+  Params prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  prm.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  prm.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  prm.page_table = page_table;
+  prm.ctx_len = ctx_len;
+  prm.cu_seqlens = cu_seqlens;
+  prm.items = items;
+  prm.n_items = n_items;
+  prm.out = out;
+  prm.lse = lse;
+  prm.ws_o = ws_o;
+  prm.ws_lse = ws_lse;
+  prm.err = err;
+  prm.max_pages = max_pages;
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.page_size = page_size;
+  prm.max_rows = max_rows;
+  prm.d_v_total = d_v;
+  prm.n_pages = n_pages;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+
+  CUtensorMap tk, tv;
+  if (pl.mla) {
+    const int box_rows = page_size < CfgMLA::NK ? page_size : CfgMLA::NK;
+    cuuint64_t dims[3] = {(cuuint64_t)d_qk, (cuuint64_t)page_size, (cuuint64_t)n_pages};
+    cuuint64_t str[2] = {(cuuint64_t)d_qk * 2, (cuuint64_t)page_size * d_qk * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    if (!make_map(&tk, k_cache, 3, dims, str, box)) return DSPARK_ECUDA;
+    tv = tk;
+    if (!configure_smem<CfgMLA>()) return DSPARK_ECUDA;
+    verify_attn_kernel<CfgMLA><<<sms, kThreads, CfgMLA::SMEM_BYTES, stream>>>(tk, tv, prm);
+  } else {
+    const int box_rows = page_size < CfgGQA::NK ? page_size : CfgGQA::NK;
+    cuuint64_t dims[4] = {(cuuint64_t)d_qk, (cuuint64_t)Hkv, (cuuint64_t)page_size, (cuuint64_t)n_pages};
+    cuuint64_t str[3] = {(cuuint64_t)d_qk * 2, (cuuint64_t)Hkv * d_qk * 2,
+                         (cuuint64_t)page_size * Hkv * d_qk * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    if (!make_map(&tk, k_cache, 4, dims, str, box)) return DSPARK_ECUDA;
+    if (!make_map(&tv, v_cache, 4, dims, str, box)) return DSPARK_ECUDA;
+    if (!configure_smem<CfgGQA>()) return DSPARK_ECUDA;
+    verify_attn_kernel<CfgGQA><<<sms, kThreads, CfgGQA::SMEM_BYTES, stream>>>(tk, tv, prm);
+  }
+  DSPARK_LAUNCH_CHECK();
+  const long long warps = (long long)max_rows * Hq;
+  const int blocks = (int)((warps * 32 + 255) / 256);
+  combine_kernel<<<blocks, 256, 0, stream>>>(cu_seqlens, B, Hq, d_v, nsplit, ws_o, ws_lse, max_rows,
+                                             out, lse);
+  DSPARK_LAUNCH_CHECK();
+  return DSPARK_OK;
+}
+
+}  // namespace attn
+}  // namespace dspark

@@ -1,0 +1,65 @@
+"""The C ABI: the library builds, loads, exports every symbol the header declares,
+and rejects bad arguments on the host without touching a device.  CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dspark.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dspark_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    import speculative_decoding_verification_dspark_gb300 as pkg
+    return pkg.load()
+
+
+def test_header_declares_the_five_calls():
+    names = _declared()
+    for n in ("dspark_schedule", "dspark_pack", "dspark_verify_attn", "dspark_accept",
+              "dspark_compact"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    assert lib.dspark_status_string(0) == b"ok"
+    assert lib.dspark_status_string(-1) == b"invalid argument"
+
+
+def test_host_validation_without_device(lib):
+    # NULL pointers and out-of-range sizes are rejected before any device work
+    nul = None
+    assert lib.dspark_schedule(nul, 1, nul, nul, 10, 4, 6, 32, 0, nul, nul, nul, nul, nul) == -1
+    assert lib.dspark_pack(nul, nul, nul, nul, nul, 0, 4, 6, 0, 8, nul, nul, nul, nul, nul, nul,
+                           nul) == -1
+    # unsupported attention shape (head dim 96)
+    assert lib.dspark_verify_attn(nul, nul, nul, nul, nul, 1, nul, 1, nul, nul, 1, 8, 8, 2, 96, 96,
+                                  16, ctypes.c_float(0.1), 4, nul, nul, nul, 0, nul) == -2
+    # vocabulary not a multiple of 8
+    fake = ctypes.c_void_p(4096)
+    assert lib.dspark_accept(fake, fake, 0, 1001, fake, fake, fake, fake, fake, 0, 4, 6, 8, fake,
+                             fake, fake, fake, nul, fake, 1 << 20, nul) == -2
+
+
+def test_workspace_sizes_are_host_computable(lib):
+    s = lib.dspark_verify_attn_workspace_size(32, 512, 32, 8, 128, 128, 8)
+    assert s > 0
+    assert lib.dspark_verify_attn_workspace_size(64, 1024, 128, 1, 576, 512, 8) > 0
+    assert lib.dspark_verify_attn_workspace_size(32, 512, 32, 8, 96, 96, 8) == 0
+    assert lib.dspark_accept_workspace_size(32, 8, 512, 151936) > 0
+    assert lib.dspark_compact_workspace_size(32) > 0

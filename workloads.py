@@ -164,7 +164,7 @@ def gen_device(wl: Workload) -> str:
 
 @torch.no_grad()
 def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
-                extra_free_pages: Optional[int] = None) -> dict:
+                extra_free_pages: Optional[int] = None, ctx_override=None) -> dict:
     """Draw one verification step's inputs for workload ``wl``.
 
     Per-position tensors are dense over the block: row (r, i) of a ``*_dense``
@@ -187,6 +187,8 @@ def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
     out["tiers"] = torch.tensor(wl.tiers, dtype=torch.int32)
 
     ctx = _ctx_lengths(wl, _gen(seed, "ctx", dev), dev)
+    if ctx_override is not None:
+        ctx = torch.as_tensor(list(ctx_override), dtype=torch.int64, device=dev)
     out["ctx_len"] = ctx.to(torch.int32)
     # Paged cache: every request's committed context lives in pages drawn at random
     # from one pool; the rest of the pool is the free-page stack.
