@@ -131,6 +131,14 @@ __device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
   return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
 
+// 2^x on the SFU (ex2.approx.ftz: -inf -> +0).  The softmax weights are rounded
+// to bf16 right after, so the approximation error is far below that rounding.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
@@ -445,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = m < rows_valid;
       const bool warp_active = __any_sync(0xffffffffu, row_ok);
       const int bi = C::MLA ? item.i0 : item.i0 + m / G;   // block index of this row
-      float m_used = -INFINITY, l_sum = 0.f;
+      // l_sum: sum of the bf16 P fed to the MMA (normalises O consistently);
+      // l_lse: the same sum in fp32 before rounding (for the log-sum-exp)
+      float m_used = -INFINITY, l_sum = 0.f, l_lse = 0.f;
       const int ntiles = item.te - item.tb;
       for (int l = 0; l < ntiles; ++l, ++g) {
         const int t = item.tb + l;
@@ -478,14 +488,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (warp_active) {
           // ---- mask + scale + tile max
+          // Keys [0, lim) of this tile are visible to this row: the committed
+          // context for a cache tile, block rows 0..bi for the block tile.  One
+          // compare-select per key (no per-key branch: lanes differ in bi).
           float mt = -INFINITY;
           const bool block_tile = t >= ct;
-          const int kbase = block_tile ? (t - ct) * C::NK : t * C::NK;
+          const int lim = block_tile ? min(bi + 1, n_r) - (t - ct) * C::NK : ctx - t * C::NK;
 #pragma unroll
           for (int k = 0; k < C::NK; ++k) {
-            const int key = kbase + k;
-            const bool vis = block_tile ? (key <= bi && key < n_r) : (key < ctx);
-            s[k] = vis ? s[k] * prm.scale_log2 : -INFINITY;
+            s[k] = (k < lim) ? s[k] * prm.scale_log2 : -INFINITY;
             mt = fmaxf(mt, s[k]);
           }
           // ---- lazy rescale of O when the running max grows by more than 2^8
@@ -513,28 +524,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
           }
           if (need) {
-            l_sum *= (l > 0) ? exp2f(m_used - mt) : 0.f;
+            const float a_res = (l > 0) ? exp2f(m_used - mt) : 0.f;
+            l_sum *= a_res;
+            l_lse *= a_res;
             m_used = mt;
           }
           // ---- P = exp2(s - m_used), bf16, swizzled K-major row m
           const uint32_t prow = L.pbuf(pb);
           const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-          float psum = 0.f;
+          float psum = 0.f, psum32 = 0.f;
 #pragma unroll
           for (int q = 0; q < C::NK / 8; ++q) {
             uint32_t w[4];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-              const float p0 = row_ok ? exp2f(s[q * 8 + 2 * h] - mref) : 0.f;
-              const float p1 = row_ok ? exp2f(s[q * 8 + 2 * h + 1] - mref) : 0.f;
+              // rows past rows_valid compute harmless values: they only feed their
+              // own O rows, which are never stored
+              const float p0 = fast_exp2(s[q * 8 + 2 * h] - mref);
+              const float p1 = fast_exp2(s[q * 8 + 2 * h + 1] - mref);
               __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
               psum += __low2float(b2) + __high2float(b2);
+              psum32 += p0 + p1;
               w[h] = *reinterpret_cast<uint32_t*>(&b2);
             }
             const uint32_t off = (C::NK == 64) ? sw128_off(m, q) : sw64_off(m, q);
             st_shared_v4(prow + off, make_uint4(w[0], w[1], w[2], w[3]));
           }
           l_sum += psum;
+          l_lse += psum32;
           tc_fence_before();
           fence_proxy_async_smem();
         }
@@ -575,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (row_ok && item.part == 0) {
-            const float lse_v = (m_used + log2f(l_sum)) * 0.69314718055994530942f;
+            const float lse_v = (m_used + log2f(l_lse)) * 0.69314718055994530942f;
             if (split)
               prm.ws_lse[((long long)item.split * prm.max_rows + row_g) * prm.Hq + head] = lse_v;
             else

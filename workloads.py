@@ -207,7 +207,9 @@ def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
     idx = (starts[:, None] + col).clamp(max=n_pages - 1)
     page_table = torch.where(used, perm[idx.long()], page_table)
     out["page_table"] = page_table.contiguous()
-    out["free_pages"] = perm[n_used:].contiguous()
+    # never an empty tensor: an exhausted stack is free_top = 0 over a 1-entry buffer
+    out["free_pages"] = (perm[n_used:].contiguous() if n_free > 0
+                         else torch.zeros(1, dtype=torch.int32, device=dev))
     out["free_top"] = torch.tensor([n_free], dtype=torch.int32, device=dev)
     out["n_pages"] = n_pages
 
