@@ -156,18 +156,21 @@ int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* a
  *   out         fp32 [max_rows, Hq, d_v]  out (rows >= M not written)
  *   lse         fp32 [max_rows, Hq]       out, natural log
  *   workspace   >= dspark_verify_attn_workspace_size(...) bytes, 256-B aligned
- * page_size must be a multiple of 16 (GQA) or 32 (MLA).  All bases 16-B aligned.
+ * page_size must be a power of two >= 16.  All base pointers 16-byte aligned.
  * Long contexts are split across CTAs (at most max_splits pieces per request,
- * head and row tile) and merged by a log-sum-exp combine.
+ * head and row tile) and merged by a log-sum-exp combine.  max_block_rows is a
+ * hint: the largest row count of one request's segment (gamma + 1), used to size
+ * the query tile of the GQA kernel (<= 0: unknown); any segment length is
+ * handled correctly whatever its value.
  * ------------------------------------------------------------------------- */
 size_t dspark_verify_attn_workspace_size(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v,
-                                         int max_splits);
+                                         int max_splits, int max_block_rows);
 int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, const void* k_cache,
                        const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
                        const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows,
                        int Hq, int Hkv, int d_qk, int d_v, int page_size, float scale,
-                       int max_splits, float* out, float* lse, void* workspace, size_t ws_bytes,
-                       void* stream);
+                       int max_splits, int max_block_rows, float* out, float* lse,
+                       void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * dspark_accept -- prefix speculative sampling ([notes] 02; [lesson]

@@ -41,9 +41,9 @@ _SIGNATURES = {
     "dspark_num_sms": (_I, []),
     "dspark_schedule": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "dspark_pack": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
-    "dspark_verify_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "dspark_verify_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "dspark_verify_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I,
-                                _F, _I, _P, _P, _P, _Z, _P]),
+                                _F, _I, _I, _P, _P, _P, _Z, _P]),
     "dspark_accept_workspace_size": (_Z, [_I, _I, _I, _I]),
     "dspark_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                            _P, _Z, _P]),
@@ -131,12 +131,14 @@ def pack(windows, ctx_len, anchor, draft_tok, tiers, mode, cu_seqlens, M_out, ti
         _ptr(row_req), _ptr(row_pos), _ptr(row_tok), _stream(stream)))
 
 
-def verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits) -> int:
-    return lib().dspark_verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits)
+def verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits,
+                               max_block_rows=0) -> int:
+    return lib().dspark_verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits,
+                                                   max_block_rows)
 
 
 def verify_attn(q, k_new, v_new, k_cache, v_cache, page_table, ctx_len, cu_seqlens, scale,
-                max_splits, out, lse, workspace, stream=None):
+                max_splits, out, lse, workspace, stream=None, max_block_rows=0):
     """GQA: q [rows, Hq, 128], k/v_new [rows, Hkv, 128], caches [pages, P, Hkv, 128].
     MLA: q [rows, 128, 576], k_new [rows, 576], k_cache [pages, P, 576], v_* None."""
     max_rows, Hq, d_qk = q.shape
@@ -147,7 +149,8 @@ def verify_attn(q, k_new, v_new, k_cache, v_cache, page_table, ctx_len, cu_seqle
     _check("dspark_verify_attn", lib().dspark_verify_attn(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
         _ptr(page_table), page_table.shape[1], _ptr(ctx_len), _ptr(cu_seqlens), B, max_rows, Hq,
-        Hkv, d_qk, d_v, k_cache.shape[1], float(scale), int(max_splits), _ptr(out), _ptr(lse),
+        Hkv, d_qk, d_v, k_cache.shape[1], float(scale), int(max_splits), int(max_block_rows),
+        _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
@@ -217,7 +220,7 @@ class VerifyStep:
         self.cstar = torch.zeros(B, gamma, dtype=torch.float32, device=dev)
         self.committed = torch.zeros(B, gamma + 1, **i32)
         self.n_committed = torch.zeros(B, **i32)
-        sz = verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits)
+        sz = verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits, gamma + 1)
         if sz == 0:
             raise ValueError("unsupported attention shape")
         self.ws_attn = torch.empty(sz, dtype=torch.uint8, device=dev)
@@ -237,7 +240,8 @@ class VerifyStep:
     def attention(self, inp, stream=None):
         verify_attn(inp["q"], inp["k_new"], inp.get("v_new"), inp["k_cache"], inp.get("v_cache"),
                     inp["page_table"], inp["ctx_len"], self.cu_seqlens, inp["scale"],
-                    self.max_splits, self.out, self.lse, self.ws_attn, stream)
+                    self.max_splits, self.out, self.lse, self.ws_attn, stream,
+                    max_block_rows=self.gamma + 1)
 
     def accept(self, inp, mode, stream=None):
         accept(inp["p_target"], inp["p_draft"], inp["draft_tok"], inp["uniforms"],

@@ -137,6 +137,7 @@ int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* a
 }
 
 static bool attn_shape_ok(int Hq, int Hkv, int d_qk, int d_v, int page_size) {
+  if (page_size < 16 || (page_size & (page_size - 1)) != 0) return false;  // power of two
   if (d_qk == 128 && d_v == 128) {
     if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || Hq / Hkv > 128) return false;
     if (page_size < 16 || page_size % 16 != 0) return false;
@@ -151,18 +152,18 @@ static bool attn_shape_ok(int Hq, int Hkv, int d_qk, int d_v, int page_size) {
 }
 
 size_t dspark_verify_attn_workspace_size(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v,
-                                         int max_splits) {
+                                         int max_splits, int max_block_rows) {
   if (B < 1 || max_rows < 1 || max_splits < 1 || max_splits > 32) return 0;
   if (!attn_shape_ok(Hq, Hkv, d_qk, d_v, 16)) return 0;
-  return attn::plan(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits).bytes;
+  return attn::plan(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits, max_block_rows).bytes;
 }
 
 int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, const void* k_cache,
                        const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
                        const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows,
                        int Hq, int Hkv, int d_qk, int d_v, int page_size, float scale,
-                       int max_splits, float* out, float* lse, void* workspace, size_t ws_bytes,
-                       void* stream) {
+                       int max_splits, int max_block_rows, float* out, float* lse, void* workspace,
+                       size_t ws_bytes, void* stream) {
   CHECK(attn_shape_ok(Hq, Hkv, d_qk, d_v, page_size), DSPARK_EUNSUPPORTED);
   const bool mla = d_qk == 576;
   CHECK(q && k_new && k_cache && page_table && ctx_len && cu_seqlens && out && lse && workspace,
@@ -178,7 +179,7 @@ int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, cons
   CHECK(scale > 0.f, DSPARK_EINVAL);
   int rc = device_ok();
   if (rc != DSPARK_OK) return rc;
-  const attn::Plan pl = attn::plan(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits);
+  const attn::Plan pl = attn::plan(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits, max_block_rows);
   CHECK(ws_bytes >= pl.bytes, DSPARK_ENOSPACE);
   return attn::launch(q, k_new, v_new, k_cache, v_cache, n_pages, page_table, max_pages, ctx_len,
                       cu_seqlens, B, max_rows, Hq, Hkv, d_qk, d_v, page_size, scale, max_splits,

@@ -1,4 +1,4 @@
-// Internal interface of the verify-attention launcher (host side).
+// Internal interface of the verify-attention launchers (host side).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -8,7 +8,7 @@
 namespace dspark {
 namespace attn {
 
-// One unit of work: a 128-row query tile of one request against a range of its key tiles.
+// One unit of work: a tile of query rows of one request against a range of its key tiles.
 struct __align__(16) AttnItem {
   int r, kvh, i0, ni;        // request, KV head, first block row, block rows in the tile
   int part, split, tb, te;   // value-column part, split index, key-tile range [tb, te)
@@ -17,18 +17,31 @@ struct __align__(16) AttnItem {
 
 struct Plan {
   bool mla;
-  int parts, rows_per_tile, nk;
+  int parts, rows_per_tile, nk, nt;
   long long max_items;
   size_t off_items, off_nitems, off_nsplit, off_o, off_lse, bytes;
 };
 
-Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_splits);
+Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_splits,
+          int max_block_rows);
 
 int launch(const void* q, const void* k_new, const void* v_new, const void* k_cache,
            const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
            const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq, int Hkv,
            int d_qk, int d_v, int page_size, float scale, int max_splits, float* out, float* lse,
            void* ws, const Plan& pl, cudaStream_t stream);
+
+namespace gqa {
+// Query-row tile (32, 64 or 128) for G = Hq/Hkv heads per KV head and at most
+// max_block_rows rows per request segment (<= 0: unknown, take 128).
+int query_tile(int Hq, int Hkv, int max_block_rows);
+int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                  const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
+                  const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq,
+                  int Hkv, int page_size, float scale, const AttnItem* items, const int* n_items,
+                  float* out, float* lse, float* ws_o, float* ws_lse, cudaStream_t stream);
+constexpr int kKeyTile = 128;
+}  // namespace gqa
 
 }  // namespace attn
 }  // namespace dspark

@@ -11,19 +11,20 @@
 //     its query rows (block rows x the query heads of one KV head, or the 128 heads
 //     of one block row for the latent-KV shape) form one 128-row UMMA tile;
 //   * a persistent grid (one CTA per SM) walks the item list;
-//   * warp 0 streams K/V tiles into a shared-memory ring: full pages by TMA
-//     (128-byte swizzle, no multicast), the partial last page and the draft block's
-//     own rows by plain loads written in the same swizzled layout;
-//   * warp 1 (one lane) issues tcgen05.mma: S = Q K^T into a double-buffered TMEM
+//   * warps 0-3 stream K/V tiles into a shared-memory ring with 16-byte cp.async
+//     copies written straight into the 128-byte-swizzled K-major layout the tensor
+//     cores read (masked rows are zero-filled by the copy itself).  With 16-token
+//     pages a TMA box holds at most 2 KB, and the TMA unit's per-box cost caps it
+//     below the HBM rate; 128 threads of cp.async keep enough bytes in flight;
+//   * warp 4 (one lane) issues tcgen05.mma: S = Q K^T into a double-buffered TMEM
 //     tile, then O += P V into a TMEM accumulator;
-//   * warps 2-5 own one query row per thread: read S from TMEM, mask, online
+//   * warps 5-8 own one query row per thread: read S from TMEM, mask, online
 //     softmax in fp32 (exp2 domain, lazy rescale of O when the running max grows
 //     by more than 2^8), write P (bf16) to shared memory, and finally normalise O;
 //   * long contexts split across items; a log-sum-exp combine merges the pieces.
 // Every mbarrier wait is bounded in time; a wait that runs out raises
-// DSPARK_DEVERR_WAIT_TIMEOUT, the CTA drains its own copies, frees TMEM and exits.
+// DSPARK_DEVERR_WAIT_TIMEOUT, the CTA waits for its own copies, frees TMEM and exits.
 
-#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -38,8 +39,12 @@ namespace attn {
 using namespace ptx;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kThreads = 192;                    // 6 warps
-constexpr int kRows = 128;                       // UMMA M
+constexpr int kProducerWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kSoftmaxWarp0 = 5;
+constexpr int kThreads = 9 * 32;
+constexpr int kProducerThreads = kProducerWarps * 32;
+constexpr int kRows = 128;                         // UMMA M
 
 template <int D_QK_, int DV_, int NK_, int STAGES_, bool MLA_>
 struct Cfg {
@@ -55,6 +60,9 @@ struct Cfg {
   static constexpr int K_BYTES = QK_CB * KV_CB_BYTES;
   static constexpr int V_BYTES = MLA ? 0 : (DV / 64) * KV_CB_BYTES;
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
+  static constexpr int K_CHUNKS = NK * (D_QK / 8);        // 16-byte chunks of K per tile
+  static constexpr int V_CHUNKS = MLA ? 0 : NK * (DV / 8);
+  static constexpr int CHUNKS_PER_THREAD = (K_CHUNKS + V_CHUNKS) / kProducerThreads;
   static constexpr int P_ROW_BYTES = NK * 2;              // 128 (NK=64) or 64 (NK=32)
   static constexpr int P_BYTES = kRows * P_ROW_BYTES;
   static constexpr int P_BUFS = MLA ? 1 : 2;
@@ -71,20 +79,19 @@ struct Cfg {
   static constexpr int TMEM_O = 2 * NK;
   static constexpr int TMEM_COLS_USED = 2 * NK + DV;
   static constexpr int TMEM_COLS = TMEM_COLS_USED <= 256 ? 256 : 512;
-  static constexpr int PARTS = MLA ? 2 : 1;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(TMEM_COLS_USED <= 512, "tensor memory budget");
   static_assert(NK == 64 || NK == 32, "tile width");
+  static_assert((K_CHUNKS + V_CHUNKS) % kProducerThreads == 0, "copy split");
+  // Copy groups a producer thread keeps in flight before publishing a tile.
+  // Publishing tile g needs tile g+LAG issued, hence PV(g+LAG-STAGES) done, which
+  // the MMA warp issues only once tile g+LAG-STAGES+1 is published: LAG <= STAGES-2.
+  static constexpr int LAG = STAGES - 2;
+  static_assert(LAG >= 0, "pipeline depth");
   static_assert(STAGE_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0 && P_BYTES % 1024 == 0, "align");
 };
 
-using CfgGQA = Cfg<128, 128, 64, 4, false>;
 using CfgMLA = Cfg<576, 256, 32, 2, true>;
-
-struct Smem {
-  uint32_t base;  // shared-space address of the aligned base
-  uint8_t* ptr;
-};
 
 struct Ctx {
   volatile int* abort_flag;
@@ -153,21 +160,17 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return v;
 }
 
-// Copy `nrows` rows (row stride `gstride` elements, D_QK or DV wide) from global
-// into a swizzled K-major tile of NK rows; rows in [valid, NK) are zero.  Called by
-// all 32 lanes of one warp.
-template <int WIDTH, int NK>
-__device__ __forceinline__ void warp_fill_tile(uint32_t dst, const __nv_bfloat16* src,
-                                               long long gstride, int valid, int lane) {
-  constexpr int CHUNKS = WIDTH / 8;        // 16-byte chunks per row
-  constexpr int CB_BYTES = NK * 128;
-  for (int idx = lane; idx < NK * CHUNKS; idx += 32) {
-    const int row = idx / CHUNKS;
-    const int q = idx % CHUNKS;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < valid) v = ldg_nc_v4(src + row * gstride + q * 8);
-    st_shared_v4(dst + (q >> 3) * CB_BYTES + sw128_off(row, q & 7), v);
-  }
+// 16-byte global -> shared copy; src_bytes = 0 writes zeros without reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 template <class C>
@@ -202,14 +205,86 @@ struct Params {
   float* ws_o;
   float* ws_lse;
   unsigned int* err;
-  int max_pages, B, Hq, Hkv, page_size, max_rows, d_v_total, n_pages;
+  int max_pages, B, Hq, Hkv, page_size, log2_page, max_rows, d_v_total, n_pages;
   float scale_log2;
 };
 
+// Page indices of the (at most NK/16) pages cache tile t touches, -1 for a
+// corrupt entry (read as zeros, reported).  Issued one tile ahead so that the
+// page-table latency overlaps the previous tile's copies.
 template <class C>
-__global__ void __launch_bounds__(kThreads, 1)
-    verify_attn_kernel(const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+__device__ __forceinline__ void load_tile_pages(const Params& prm, const int32_t* ptab, int t,
+                                                int ct, int ctx, int (&pg)[C::NK / 16]) {
+  const int slot0 = (t * C::NK) >> prm.log2_page;
+#pragma unroll
+  for (int j = 0; j < C::NK / 16; ++j) {
+    const int sl = slot0 + j;
+    const bool in = t < ct && (sl << prm.log2_page) < ctx;
+    int p = in ? ptab[sl] : 0;
+    if (in && (p < 0 || p >= prm.n_pages)) {
+      raise_error(prm.err, DSPARK_DEVERR_BAD_INPUT);
+      p = -1;
+    }
+    pg[j] = p;
+  }
+}
+
+// One K/V tile into the stage at `kdst`: cache tile t < ct (keys t*NK ..) or a
+// block tile (the request's own packed rows).  Each producer thread issues
+// CHUNKS_PER_THREAD 16-byte copies; consecutive threads take consecutive chunks
+// of a row, so every warp-wide copy reads whole 256-byte (or 1152-byte) rows.
+template <class C>
+__device__ __forceinline__ void produce_tile(const Params& prm, const AttnItem& item, int t, int ct,
+                                             int ctx, int c0, int n_r, const int (&pg)[C::NK / 16],
+                                             uint32_t kdst, int pt) {
+  constexpr int KCH = C::D_QK / 8;   // chunks per K row
+  constexpr int VCH = C::DV / 8;     // chunks per V row (GQA)
+  const long long rs = C::MLA ? C::D_QK : (long long)prm.Hkv * C::D_QK;  // row stride (elements)
+  const int lp = prm.log2_page;
+  const bool cache = t < ct;
+  const __nv_bfloat16* kbase;
+  const __nv_bfloat16* vbase;
+  int valid;                         // rows [0, valid) of this tile exist
+  if (cache) {
+    kbase = prm.k_cache + (C::MLA ? 0 : (long long)item.kvh * C::D_QK);
+    vbase = C::MLA ? nullptr : prm.v_cache + (long long)item.kvh * C::D_QK;
+    valid = ctx - t * C::NK;
+  } else {
+    const int b0 = (t - ct) * C::NK;
+    const long long off = (long long)(c0 + b0) * rs + (C::MLA ? 0 : (long long)item.kvh * C::D_QK);
+    kbase = prm.k_new + off;
+    vbase = C::MLA ? nullptr : prm.v_new + off;
+    valid = n_r - b0;
+  }
+  const int slot0 = (t * C::NK) >> lp;
+  const uint32_t vdst = kdst + C::K_BYTES;
+#pragma unroll
+  for (int k = 0; k < C::CHUNKS_PER_THREAD; ++k) {
+    const int c = pt + k * kProducerThreads;
+    const bool is_v = !C::MLA && c >= C::K_CHUNKS;
+    const int cc = is_v ? c - C::K_CHUNKS : c;
+    const int row = is_v ? cc / VCH : cc / KCH;
+    const int q = is_v ? cc % VCH : cc % KCH;
+    const __nv_bfloat16* base = is_v ? vbase : kbase;
+    bool ok = row < valid;
+    long long src_row = row;
+    if (cache) {
+      const int key = t * C::NK + row;
+      const int j = (key >> lp) - slot0;
+      int p = pg[0];
+#pragma unroll
+      for (int jj = 1; jj < C::NK / 16; ++jj) p = (j == jj) ? pg[jj] : p;
+      ok = ok && p >= 0;
+      src_row = ((long long)(ok ? p : 0) << lp) + (key & ((1 << lp) - 1));
+    }
+    const __nv_bfloat16* src = ok ? base + src_row * rs + q * 8 : prm.k_cache;
+    const uint32_t dst = (is_v ? vdst : kdst) + (q >> 3) * C::KV_CB_BYTES + sw128_off(row, q & 7);
+    cp_async16(dst, src, ok ? 16u : 0u);
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params prm) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -225,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(L.kv_full(s), 1);
+      mbar_init(L.kv_full(s), kProducerWarps);
       mbar_init(L.kv_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -239,11 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(L.q_full(), 1);
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&tm_k);
-    if (!C::MLA) prefetch_tensormap(&tm_v);
-  }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -254,14 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_items = *prm.n_items;
   const int G = C::MLA ? kRows : prm.Hq / prm.Hkv;  // query rows per block row
-  const int P = prm.page_size;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------- producer
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------- producers
+    const int pt = threadIdx.x;  // 0..127
     int g = 0;
     bool ok = true;
-    const int box_rows = P < C::NK ? P : C::NK;
-    const uint32_t box_bytes = box_rows * 128;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const AttnItem item = prm.items[it];
       const int r = item.r;
@@ -270,6 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_r = prm.cu_seqlens[r + 1] - c0;
       const int ct = ceil_div(ctx, C::NK);
       const int32_t* ptab = prm.page_table + (long long)r * prm.max_pages;
+      int pg[C::NK / 16];
+      load_tile_pages<C>(prm, ptab, item.tb, ct, ctx, pg);
       for (int t = item.tb; t < item.te; ++t, ++g) {
         const int s = g % C::STAGES;
         if (g >= C::STAGES) {
@@ -277,94 +348,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
         }
-        const uint32_t kdst = L.stage(s);
-        const uint32_t vdst = kdst + C::K_BYTES;
-        if (t < ct) {
-          // cache tile: keys [t*NK, t*NK + NK) of the committed context
-          uint32_t tx = 0;
-          const int nbox = C::NK / box_rows;
-          for (int bx = 0; bx < nbox; ++bx) {
-            const int kg = t * C::NK + bx * box_rows;
-            if (kg + box_rows <= ctx) tx += box_bytes * (C::QK_CB + (C::MLA ? 0 : C::DV / 64));
-          }
-          if (lane == 0 && tx > 0) mbar_expect_tx(L.kv_full(s), tx);
-          for (int bx = 0; bx < nbox; ++bx) {
-            const int kg = t * C::NK + bx * box_rows;
-            int page = kg < ctx ? ptab[kg / P] : 0;
-            if (page < 0 || page >= prm.n_pages) {
-              // a corrupt page-table entry: read nothing (zeros), report it
-              if (lane == 0) raise_error(prm.err, DSPARK_DEVERR_BAD_INPUT);
-              page = kg < ctx ? -1 : 0;
-            }
-            const int in_page = kg % P;
-            const int row0 = bx * box_rows;
-            if (kg + box_rows <= ctx) {
-              if (lane == 0) {
-                for (int cb = 0; cb < C::QK_CB; ++cb) {
-                  const uint32_t dst = kdst + cb * C::KV_CB_BYTES + row0 * 128;
-                  if (C::MLA)
-                    tma_load_3d(dst, &tm_k, L.kv_full(s), cb * 64, in_page, page);
-                  else
-                    tma_load_4d(dst, &tm_k, L.kv_full(s), cb * 64, item.kvh, in_page, page);
-                }
-                if (!C::MLA) {
-                  for (int cb = 0; cb < C::DV / 64; ++cb) {
-                    const uint32_t dst = vdst + cb * C::KV_CB_BYTES + row0 * 128;
-                    tma_load_4d(dst, &tm_v, L.kv_full(s), cb * 64, item.kvh, in_page, page);
-                  }
-                }
-              }
-            } else {
-              // partial or empty box: plain loads of the valid rows, zeros elsewhere
-              const int valid = (kg < ctx && page >= 0) ? ctx - kg : 0;
-              const long long rs = C::MLA ? C::D_QK : (long long)prm.Hkv * C::D_QK;
-              const long long off =
-                  ((long long)(valid > 0 ? page : 0) * P + in_page) * rs +
-                  (C::MLA ? 0 : (long long)item.kvh * C::D_QK);
-              // rows of this box land at tile rows row0 .. row0+box_rows-1
-              constexpr int CH = C::D_QK / 8;
-              for (int idx = lane; idx < box_rows * CH; idx += 32) {
-                const int rr = idx / CH, q = idx % CH;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (rr < valid) v = ldg_nc_v4(prm.k_cache + off + rr * rs + q * 8);
-                st_shared_v4(kdst + (q >> 3) * C::KV_CB_BYTES + sw128_off(row0 + rr, q & 7), v);
-              }
-              if (!C::MLA) {
-                constexpr int CHV = C::DV / 8;
-                for (int idx = lane; idx < box_rows * CHV; idx += 32) {
-                  const int rr = idx / CHV, q = idx % CHV;
-                  uint4 v = make_uint4(0, 0, 0, 0);
-                  if (rr < valid) v = ldg_nc_v4(prm.v_cache + off + rr * rs + q * 8);
-                  st_shared_v4(vdst + (q >> 3) * C::KV_CB_BYTES + sw128_off(row0 + rr, q & 7), v);
-                }
-              }
-            }
-          }
-        } else {
-          // block tile: the request's own packed rows (anchor + drafts), from k_new/v_new
-          const int b0 = (t - ct) * C::NK;
-          const int valid = n_r - b0 < C::NK ? n_r - b0 : C::NK;
-          if (C::MLA) {
-            warp_fill_tile<C::D_QK, C::NK>(kdst, prm.k_new + (long long)(c0 + b0) * C::D_QK, C::D_QK,
-                                           valid, lane);
-          } else {
-            const long long rs = (long long)prm.Hkv * C::D_QK;
-            const long long off = (long long)(c0 + b0) * rs + (long long)item.kvh * C::D_QK;
-            warp_fill_tile<C::D_QK, C::NK>(kdst, prm.k_new + off, rs, valid, lane);
-            warp_fill_tile<C::DV, C::NK>(vdst, prm.v_new + off, rs, valid, lane);
-          }
+        produce_tile<C>(prm, item, t, ct, ctx, c0, n_r, pg, L.stage(s), pt);
+        cp_async_commit();
+        if (t + 1 < item.te) load_tile_pages<C>(prm, ptab, t + 1, ct, ctx, pg);
+        if (g >= C::LAG) {
+          // tile g - LAG has landed for this thread: publish it to the tensor cores
+          cp_async_wait<C::LAG>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(L.kv_full((g - C::LAG) % C::STAGES));
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(L.kv_full(s));
       }
     }
-    // Make sure no copy of ours is still in flight before the CTA exits.
+    // publish the last tiles (and never leave copies in flight)
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
     if (lane == 0) {
-      const int first = g - C::STAGES > 0 ? g - C::STAGES : 0;
-      for (int gg = first; gg < g; ++gg) drain_bar(L.kv_full(gg % C::STAGES), (gg / C::STAGES) & 1, prm.err);
+      const int first = g - C::LAG > 0 ? g - C::LAG : 0;
+      for (int gg = first; gg < g; ++gg) mbar_arrive(L.kv_full(gg % C::STAGES));
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(kRows, C::NK, 0, 0);
@@ -419,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sw = warp & 3;                 // TMEM lane quadrant of this warp
     const int m = sw * 32 + lane;            // query row of this thread
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
-    const int stid = threadIdx.x - 64;       // 0..127
+    const int stid = threadIdx.x - kSoftmaxWarp0 * 32;  // 0..127
+    const float sl2 = prm.scale_log2;
     int g = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -453,9 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = m < rows_valid;
       const bool warp_active = __any_sync(0xffffffffu, row_ok);
       const int bi = C::MLA ? item.i0 : item.i0 + m / G;   // block index of this row
-      // l_sum: sum of the bf16 P fed to the MMA (normalises O consistently);
-      // l_lse: the same sum in fp32 before rounding (for the log-sum-exp)
-      float m_used = -INFINITY, l_sum = 0.f, l_lse = 0.f;
+      // m_used: reference max (log2 domain, scaled); l_sum: sum of exp2(s*sl2 - m_used)
+      float m_used = -INFINITY, l_sum = 0.f;
       const int ntiles = item.te - item.tb;
       for (int l = 0; l < ntiles; ++l, ++g) {
         const int t = item.tb + l;
@@ -487,22 +491,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!w_ok) { ok = false; break; }
         }
         if (warp_active) {
-          // ---- mask + scale + tile max
+          // ---- mask (only the last cache tile and the block tile need it) + tile max
           // Keys [0, lim) of this tile are visible to this row: the committed
-          // context for a cache tile, block rows 0..bi for the block tile.  One
-          // compare-select per key (no per-key branch: lanes differ in bi).
-          float mt = -INFINITY;
+          // context for a cache tile, block rows 0..bi for the block tile.
           const bool block_tile = t >= ct;
           const int lim = block_tile ? min(bi + 1, n_r) - (t - ct) * C::NK : ctx - t * C::NK;
+          if (__any_sync(0xffffffffu, lim < C::NK)) {
 #pragma unroll
-          for (int k = 0; k < C::NK; ++k) {
-            s[k] = (k < lim) ? s[k] * prm.scale_log2 : -INFINITY;
-            mt = fmaxf(mt, s[k]);
+            for (int k = 0; k < C::NK; ++k) s[k] = (k < lim) ? s[k] : -INFINITY;
           }
+          float mx[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mx[j] = s[j];
+#pragma unroll
+          for (int k = 8; k < C::NK; ++k) mx[k & 7] = fmaxf(mx[k & 7], s[k]);
+          const float mt =
+              fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
           // ---- lazy rescale of O when the running max grows by more than 2^8
           const bool need = row_ok && (mt > m_used + 8.0f);
-          const bool any_need = __any_sync(0xffffffffu, need) && l > 0;
-          if (any_need) {
+          if (__any_sync(0xffffffffu, need) && l > 0) {
             // O must hold PV(g-1): wait for it (its P buffer's barrier)
             const int gq = g - 1;
             if (C::P_BUFS > 1) {
@@ -511,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!w_ok) { ok = false; break; }
             }
             tc_fence_after();
-            const float alpha = need ? exp2f(m_used - mt) : 1.0f;
+            const float alpha = need ? fast_exp2(m_used - mt) : 1.0f;
 #pragma unroll 1
             for (int c = 0; c < C::DV / 32; ++c) {
               float o[32];
@@ -524,34 +532,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
           }
           if (need) {
-            const float a_res = (l > 0) ? exp2f(m_used - mt) : 0.f;
-            l_sum *= a_res;
-            l_lse *= a_res;
+            l_sum *= (l > 0) ? fast_exp2(m_used - mt) : 0.f;
             m_used = mt;
           }
-          // ---- P = exp2(s - m_used), bf16, swizzled K-major row m
+          // ---- P = exp2(s*scale - m_used), bf16, swizzled K-major row m.  Rows
+          // past rows_valid compute harmless values: they only feed their own O
+          // rows, which are never stored.
           const uint32_t prow = L.pbuf(pb);
           const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-          float psum = 0.f, psum32 = 0.f;
+          float psum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int q = 0; q < C::NK / 8; ++q) {
             uint32_t w[4];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-              // rows past rows_valid compute harmless values: they only feed their
-              // own O rows, which are never stored
-              const float p0 = fast_exp2(s[q * 8 + 2 * h] - mref);
-              const float p1 = fast_exp2(s[q * 8 + 2 * h + 1] - mref);
+              const float p0 = fast_exp2(fmaf(s[q * 8 + 2 * h], sl2, -mref));
+              const float p1 = fast_exp2(fmaf(s[q * 8 + 2 * h + 1], sl2, -mref));
+              psum[h] += p0 + p1;
               __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-              psum += __low2float(b2) + __high2float(b2);
-              psum32 += p0 + p1;
               w[h] = *reinterpret_cast<uint32_t*>(&b2);
             }
             const uint32_t off = (C::NK == 64) ? sw128_off(m, q) : sw64_off(m, q);
             st_shared_v4(prow + off, make_uint4(w[0], w[1], w[2], w[3]));
           }
-          l_sum += psum;
-          l_lse += psum32;
+          l_sum += (psum[0] + psum[1]) + (psum[2] + psum[3]);
           tc_fence_before();
           fence_proxy_async_smem();
         }
@@ -592,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (row_ok && item.part == 0) {
-            const float lse_v = (m_used + log2f(l_lse)) * 0.69314718055994530942f;
+            const float lse_v = (m_used + log2f(l_sum)) * 0.69314718055994530942f;
             if (split)
               prm.ws_lse[((long long)item.split * prm.max_rows + row_g) * prm.Hq + head] = lse_v;
             else
@@ -608,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- work list
@@ -739,38 +743,6 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------- host side
 namespace {
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                              CUtensorMapFloatOOBfill);
-
-EncodeFn get_encode() {
-  static EncodeFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(p);
-  }
-  return fn;
-}
-
-bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-              const cuuint64_t* strides_bytes, const cuuint32_t* box) {
-  EncodeFn enc = get_encode();
-  if (!enc) return false;
-  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult rc = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
-                    strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return rc == CUDA_SUCCESS;
-}
-
 template <class C>
 bool configure_smem() {
   static bool done = false, okv = false;
@@ -786,13 +758,15 @@ constexpr int kItemsPerSm = 2;
 
 }  // namespace
 
-Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_splits) {
+Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_splits,
+          int max_block_rows) {
   Plan p{};
   p.mla = (d_qk == 576);
   const int G = p.mla ? Hq : Hq / Hkv;
   p.parts = p.mla ? 2 : 1;
-  p.rows_per_tile = p.mla ? 1 : (kRows / G);
-  p.nk = p.mla ? CfgMLA::NK : CfgGQA::NK;
+  p.nt = p.mla ? kRows : gqa::query_tile(Hq, Hkv, max_block_rows);
+  p.rows_per_tile = p.mla ? 1 : (p.nt / G);
+  p.nk = p.mla ? CfgMLA::NK : gqa::kKeyTile;
   const long long tiles_rows = (long long)max_rows / (p.rows_per_tile > 0 ? p.rows_per_tile : 1) + B;
   p.max_items = (long long)Hkv * p.parts * max_splits * tiles_rows;
   size_t off = 0;
@@ -852,33 +826,24 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
   prm.Hq = Hq;
   prm.Hkv = Hkv;
   prm.page_size = page_size;
+  prm.log2_page = 0;
+  while ((1 << prm.log2_page) < page_size) ++prm.log2_page;
   prm.max_rows = max_rows;
   prm.d_v_total = d_v;
   prm.n_pages = n_pages;
   prm.scale_log2 = scale * 1.4426950408889634f;
 
-  CUtensorMap tk, tv;
   if (pl.mla) {
-    const int box_rows = page_size < CfgMLA::NK ? page_size : CfgMLA::NK;
-    cuuint64_t dims[3] = {(cuuint64_t)d_qk, (cuuint64_t)page_size, (cuuint64_t)n_pages};
-    cuuint64_t str[2] = {(cuuint64_t)d_qk * 2, (cuuint64_t)page_size * d_qk * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-    if (!make_map(&tk, k_cache, 3, dims, str, box)) return DSPARK_ECUDA;
-    tv = tk;
     if (!configure_smem<CfgMLA>()) return DSPARK_ECUDA;
-    verify_attn_kernel<CfgMLA><<<sms, kThreads, CfgMLA::SMEM_BYTES, stream>>>(tk, tv, prm);
+    verify_attn_kernel<CfgMLA><<<sms, kThreads, CfgMLA::SMEM_BYTES, stream>>>(prm);
+    DSPARK_LAUNCH_CHECK();
   } else {
-    const int box_rows = page_size < CfgGQA::NK ? page_size : CfgGQA::NK;
-    cuuint64_t dims[4] = {(cuuint64_t)d_qk, (cuuint64_t)Hkv, (cuuint64_t)page_size, (cuuint64_t)n_pages};
-    cuuint64_t str[3] = {(cuuint64_t)d_qk * 2, (cuuint64_t)Hkv * d_qk * 2,
-                         (cuuint64_t)page_size * Hkv * d_qk * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
-    if (!make_map(&tk, k_cache, 4, dims, str, box)) return DSPARK_ECUDA;
-    if (!make_map(&tv, v_cache, 4, dims, str, box)) return DSPARK_ECUDA;
-    if (!configure_smem<CfgGQA>()) return DSPARK_ECUDA;
-    verify_attn_kernel<CfgGQA><<<sms, kThreads, CfgGQA::SMEM_BYTES, stream>>>(tk, tv, prm);
+    const int rc = gqa::launch_kernel(pl.nt, q, k_new, v_new, k_cache, v_cache, n_pages, page_table,
+                                      max_pages, ctx_len, cu_seqlens, B, max_rows, Hq, Hkv,
+                                      page_size, scale, items, n_items, out, lse, ws_o, ws_lse,
+                                      stream);
+    if (rc != DSPARK_OK) return rc;
   }
-  DSPARK_LAUNCH_CHECK();
   const long long warps = (long long)max_rows * Hq;
   const int blocks = (int)((warps * 32 + 255) / 256);
   combine_kernel<<<blocks, 256, 0, stream>>>(cu_seqlens, B, Hq, d_v, nsplit, ws_o, ws_lse, max_rows,

@@ -1,0 +1,753 @@
+// Varlen verify attention, GQA shape (head dim 128), keys on the MMA's M side.
+//
+// What it computes ("DFlash 到 DSpark in SGLang", section "Ragged verify under
+// full CUDA graphs": each packed verify token attends only to its own request's
+// KV, causal inside the block): for packed row cu_seqlens[r] + i and query head
+// h of KV group kvh, o = softmax(scale q.K^T) V over the ctx_len[r] committed keys
+// (paged) followed by block rows 0..i; lse = log-sum-exp.
+//
+// Why transposed: a verify step has few query rows per (request, KV head) -- the
+// window's 1 + w rows times the group's G heads, typically 10-40 -- against
+// thousands of keys.  With keys on the M side (128 TMEM lanes) and the query rows
+// on N (NT = 32, 64 or 128 columns), every tensor-core row and every softmax
+// thread does useful work, and the exp count per key scales with the real row
+// count instead of a padded 128.
+//
+//   S^T [128 keys x NT rows] = K_tile [128 x 128] . Q^T           (tcgen05, TMEM)
+//   O^T [128 d    x NT rows] += V_tile^T . P^T                    (tcgen05, TMEM)
+//
+// Warp roles (one CTA per SM, persistent over the work list):
+//   warps 0-2  producers: TMA tiled loads of 16-token pages (128-byte swizzle,
+//              no multicast), 3 issuing warps; the partial last page and the
+//              block's own rows by plain loads into the same layout
+//   warp 3     MMA issuer (one lane) + TMEM owner
+//   warps 4-7  softmax: thread = key (TMEM lane).  Per tile: per-row max by a
+//              warp transpose-reduction and one cross-warp exchange through an
+//              mbarrier, lazy rescale of O^T when a row's max grows by > 2^8,
+//              exp2 on the SFU, P^T to shared memory in bf16, per-row sums by a
+//              second transpose-reduction.  Epilogue: O / l, lse.
+// Every wait is bounded in time (DSPARK_DEVERR_WAIT_TIMEOUT on expiry).
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dspark {
+namespace attn {
+namespace gqa {
+
+using namespace ptx;
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kKT = 128;              // keys per tile (MMA M)
+constexpr int kD = 128;               // head dim
+constexpr int kStages = 2;
+constexpr int kProducerWarps = 3;
+constexpr int kMmaWarp = 3;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kThreads = 8 * 32;
+constexpr int kTileHalf = kKT * 128;  // one 64-wide column block of a [128 x 128] bf16 tile
+constexpr int kKVBytes = 2 * kTileHalf;
+constexpr int kStageBytes = 2 * kKVBytes;  // K and V
+
+template <int NT_>
+struct Cfg {
+  static constexpr int NT = NT_;                         // query rows (N)
+  static constexpr int Q_CB = NT * 128;                  // one 64-wide column block of Q
+  static constexpr int Q_BYTES = 2 * Q_CB;
+  static constexpr int P_ROW = NT <= 64 ? NT * 2 : 128;  // bytes per key row of one P block
+  static constexpr int P_BLOCKS = NT <= 64 ? 1 : NT / 64;
+  static constexpr int P_BYTES = kKT * NT * 2;
+  static constexpr int P_BUFS = NT <= 64 ? 2 : 1;
+  static constexpr SwizzleMode P_SW = NT == 32 ? SW_64B : SW_128B;
+  static constexpr int G32 = NT / 32;                    // 32-row groups
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_STAGE = OFF_Q + Q_BYTES;
+  static constexpr int OFF_P = OFF_STAGE + kStages * kStageBytes;
+  static constexpr int OFF_RED = OFF_P + P_BUFS * P_BYTES;         // float wmax[2][4][NT]
+  static constexpr int OFF_REF = OFF_RED + 2 * 4 * NT * 4;         // float mref[4][NT], alpha[4][NT]
+  static constexpr int OFF_LS = OFF_REF + 2 * 4 * NT * 4;          // float lsum[4][NT], ltot[NT]
+  static constexpr int OFF_BAR = OFF_LS + 5 * NT * 4;
+  // kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[PB], p_empty[PB], q_full, xw[2], ep[2]
+  static constexpr int N_BARS = 8 + 2 * P_BUFS + 1 + 4;
+  static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
+  static constexpr int TMEM_S = 0;
+  static constexpr int TMEM_O = 2 * NT;
+  static constexpr int TMEM_COLS = 3 * NT <= 128 ? 128 : (3 * NT <= 256 ? 256 : 512);
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(NT == 32 || NT == 64 || NT == 128, "query tile");
+};
+
+struct Ctx {
+  volatile int* abort_flag;
+  unsigned int* err;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctx& cx) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++n & 31u) == 0) {
+      if (*cx.abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *cx.abort_flag = 1;
+        raise_error(cx.err, DSPARK_DEVERR_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned int* err) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      raise_error(err, DSPARK_DEVERR_WAIT_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// warp-uniform bounded wait (every lane polls; all agree on the outcome)
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctx& cx) {
+  bool ok = wait_bar(bar, parity, cx);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
+  return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Warp transpose-reduction: lane l holds v[0..31] (one value per query row for
+// its key); returns op over all 32 lanes of v[l], i.e. the reduction for row l.
+template <bool MAX, int W>
+__device__ __forceinline__ void transpose_step(float (&v)[32], int lane) {
+  const bool hi = (lane & W) != 0;
+#pragma unroll
+  for (int i = 0; i < W; ++i) {
+    const float send = hi ? v[i] : v[i + W];
+    const float keep = hi ? v[i + W] : v[i];
+    const float got = __shfl_xor_sync(0xffffffffu, send, W);
+    v[i] = MAX ? fmaxf(keep, got) : keep + got;
+  }
+}
+template <bool MAX>
+__device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
+  transpose_step<MAX, 16>(v, lane);
+  transpose_step<MAX, 8>(v, lane);
+  transpose_step<MAX, 4>(v, lane);
+  transpose_step<MAX, 2>(v, lane);
+  transpose_step<MAX, 1>(v, lane);
+  return v[0];
+}
+
+template <int NT>
+struct Layout {
+  uint32_t base;
+  __device__ uint32_t q() const { return base + Cfg<NT>::OFF_Q; }
+  __device__ uint32_t stage(int s) const { return base + Cfg<NT>::OFF_STAGE + s * kStageBytes; }
+  __device__ uint32_t pbuf(int b) const { return base + Cfg<NT>::OFF_P + b * Cfg<NT>::P_BYTES; }
+  __device__ uint32_t bar(int i) const { return base + Cfg<NT>::OFF_BAR + 8 * i; }
+  __device__ uint32_t kv_full(int s) const { return bar(s); }
+  __device__ uint32_t kv_empty(int s) const { return bar(2 + s); }
+  __device__ uint32_t s_full(int b) const { return bar(4 + b); }
+  __device__ uint32_t s_free(int b) const { return bar(6 + b); }
+  __device__ uint32_t p_full(int b) const { return bar(8 + b); }
+  __device__ uint32_t p_empty(int b) const { return bar(8 + Cfg<NT>::P_BUFS + b); }
+  __device__ uint32_t q_full() const { return bar(8 + 2 * Cfg<NT>::P_BUFS); }
+  __device__ uint32_t xw(int b) const { return bar(9 + 2 * Cfg<NT>::P_BUFS + b); }
+  __device__ uint32_t ep(int b) const { return bar(11 + 2 * Cfg<NT>::P_BUFS + b); }
+};
+
+struct Params {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
+  const int32_t* page_table;
+  const int32_t* ctx_len;
+  const int32_t* cu_seqlens;
+  const AttnItem* items;
+  const int* n_items;
+  float* out;
+  float* lse;
+  float* ws_o;
+  float* ws_lse;
+  unsigned int* err;
+  int max_pages, B, Hq, Hkv, page_size, log2_page, max_rows, n_pages;
+  float scale_log2;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    verify_attn_gqa_kernel(const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+  using C = Cfg<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* bp = smem_raw + (base - raw);
+  const Layout<NT> L{base};
+  float* s_wmax = reinterpret_cast<float*>(bp + C::OFF_RED);       // [2][4][NT]
+  float* s_mref = reinterpret_cast<float*>(bp + C::OFF_REF);       // [4][NT]
+  float* s_alpha = s_mref + 4 * NT;                                 // [4][NT]
+  float* s_lsum = reinterpret_cast<float*>(bp + C::OFF_LS);        // [4][NT]
+  float* s_ltot = s_lsum + 4 * NT;                                  // [NT]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + C::OFF_MISC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bp + C::OFF_MISC + 16);
+  const Ctx cx{abort_flag, prm.err};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(L.kv_full(s), kProducerWarps);
+      mbar_init(L.kv_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(L.s_full(b), 1);
+      mbar_init(L.s_free(b), 4);
+      mbar_init(L.xw(b), 4);
+      mbar_init(L.ep(b), 4);
+    }
+    for (int b = 0; b < C::P_BUFS; ++b) {
+      mbar_init(L.p_full(b), 4);
+      mbar_init(L.p_empty(b), 1);
+    }
+    mbar_init(L.q_full(), 4);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_items = *prm.n_items;
+  const int G = prm.Hq / prm.Hkv;
+  const int P = prm.page_size;
+  const int lp = prm.log2_page;
+
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------- producers
+    // warp w owns the boxes (16-row pieces) w, w+4, ... of every tile; lane j of
+    // the warp holds page-table slot win_base + j of the current request.
+    const int box_rows = P < kKT ? P : kKT;
+    const int nbox = kKT / box_rows;
+    const uint32_t box_bytes = box_rows * 128;
+    int g = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const AttnItem item = prm.items[it];
+      const int r = item.r;
+      const int ctx = prm.ctx_len[r];
+      const int c0 = prm.cu_seqlens[r];
+      const int n_r = prm.cu_seqlens[r + 1] - c0;
+      const int ct = ceil_div(ctx, kKT);
+      const int32_t* ptab = prm.page_table + (long long)r * prm.max_pages;
+      const long long rs = (long long)prm.Hkv * kD;
+      int win_base = -1, win_page = 0;
+      for (int t = item.tb; t < item.te; ++t, ++g) {
+        const int s = g % kStages;
+        if (g >= kStages) {
+          ok = wait_warp(L.kv_empty(s), ((g / kStages) - 1) & 1, cx);
+          if (!ok) break;
+        }
+        const uint32_t kdst = L.stage(s);
+        const uint32_t vdst = kdst + kKVBytes;
+        bool manual = false;
+        if (t < ct) {
+          const int slot0 = (t * kKT) >> lp;
+          const int nslot = ceil_div(kKT, P);
+          if (win_base < 0 || slot0 + nslot > win_base + 32) {
+            win_base = slot0;
+            const int sl = win_base + lane;
+            int pg = (sl << lp) < ctx ? ptab[sl] : 0;
+            if ((sl << lp) < ctx && (pg < 0 || pg >= prm.n_pages)) {
+              raise_error(prm.err, DSPARK_DEVERR_BAD_INPUT);
+              pg = -1;
+            }
+            win_page = pg;
+          }
+          uint32_t tx = 0;
+          for (int bx = warp; bx < nbox; bx += kProducerWarps) {
+            const int kg = t * kKT + bx * box_rows;
+            if (kg + box_rows <= ctx) tx += 4 * box_bytes;
+          }
+          if (lane == 0 && tx > 0) mbar_expect_tx(L.kv_full(s), tx);
+          __syncwarp();
+          // full boxes: lanes 0..(4 * owned boxes - 1) issue one copy each
+          {
+            const int ob = lane >> 2;             // owned box ordinal
+            const int cp = lane & 3;              // K cb0, K cb1, V cb0, V cb1
+            const int bx = warp + ob * kProducerWarps;
+            const int src_lane = bx < nbox ? (((t * kKT + bx * box_rows) >> lp) - win_base) & 31 : 0;
+            const int page = __shfl_sync(0xffffffffu, win_page, src_lane);  // all lanes, converged
+            if (bx < nbox) {
+              const int kg = t * kKT + bx * box_rows;
+              if (kg + box_rows <= ctx) {
+                const uint32_t dst = (cp < 2 ? kdst : vdst) + (cp & 1) * kTileHalf + bx * box_rows * 128;
+                tma_load_4d(dst, cp < 2 ? &tm_k : &tm_v, L.kv_full(s), (cp & 1) * 64, item.kvh,
+                            kg & (P - 1), page);
+              }
+            }
+          }
+          // partial / empty boxes of this warp: plain loads, zeros past the context
+          for (int bx = warp; bx < nbox; bx += kProducerWarps) {
+            const int kg = t * kKT + bx * box_rows;
+            if (kg + box_rows <= ctx) continue;
+            manual = true;
+            const int page = __shfl_sync(0xffffffffu, win_page, ((kg >> lp) - win_base) & 31);
+            const int valid = (kg < ctx && page >= 0) ? ctx - kg : 0;
+            const long long off =
+                ((long long)(valid > 0 ? page : 0) * P + (kg & (P - 1))) * rs + (long long)item.kvh * kD;
+            const int row0 = bx * box_rows;
+            for (int idx = lane; idx < box_rows * 32; idx += 32) {
+              const int rr = idx >> 5, q = idx & 31;   // q: 16 K chunks then 16 V chunks
+              const bool isv = q >= 16;
+              const int qq = q & 15;
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (rr < valid)
+                v = ldg_nc_v4((isv ? prm.v_cache : prm.k_cache) + off + rr * rs + qq * 8);
+              st_shared_v4((isv ? vdst : kdst) + (qq >> 3) * kTileHalf + sw128_off(row0 + rr, qq & 7), v);
+            }
+          }
+        } else {
+          // block tile: the request's own rows b0..b0+127 (zeros past n_r); warp w
+          // fills tile rows w, w + kProducerWarps, ...; lane = 16-byte chunk (16 K + 16 V)
+          manual = true;
+          const int b0 = (t - ct) * kKT;
+          const long long off = (long long)(c0 + b0) * rs + (long long)item.kvh * kD;
+          for (int rr = warp; rr < kKT; rr += kProducerWarps) {
+            const int q = lane;
+            const bool isv = q >= 16;
+            const int qq = q & 15;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (b0 + rr < n_r) v = ldg_nc_v4((isv ? prm.v_new : prm.k_new) + off + rr * rs + qq * 8);
+            st_shared_v4((isv ? vdst : kdst) + (qq >> 3) * kTileHalf + sw128_off(rr, qq & 7), v);
+          }
+        }
+        if (manual) fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.kv_full(s));
+      }
+    }
+    if (lane == 0) {
+      const int first = g - kStages > 0 ? g - kStages : 0;
+      for (int gg = first; gg < g; ++gg) drain_bar(L.kv_full(gg % kStages), (gg / kStages) & 1, prm.err);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(kKT, NT, 0, 0);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(kD, NT, 1, 1);
+      int g = 0, n_it = 0, last_pv = -1;
+      bool ok = true;
+      auto issue_pv = [&](int gp, int local) -> bool {
+        const int pb = gp % C::P_BUFS;
+        if (!wait_bar(L.p_full(pb), (gp / C::P_BUFS) & 1, cx)) return false;
+        tc_fence_after();
+        const int s = gp % kStages;
+        const uint32_t vb = L.stage(s) + kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < kKT / 16; ++kk) {
+          // A = V^T (M = d, MN-major), B = P^T (N = query rows, MN-major); K = 16 keys
+          const uint64_t a = smem_desc(vb + kk * 2048, kTileHalf, 1024, SW_128B);
+          const uint64_t b = smem_desc(L.pbuf(pb) + kk * 16 * C::P_ROW, kKT * 128, 8 * C::P_ROW, C::P_SW);
+          umma_bf16(tmem + C::TMEM_O, a, b, IDESC_PV, (local > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(L.p_empty(pb));
+        umma_commit(L.kv_empty(s));
+        last_pv = gp;
+        return true;
+      };
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n_it) {
+        const AttnItem item = prm.items[it];
+        if (!wait_bar(L.q_full(), n_it & 1, cx)) { ok = false; break; }
+        const int ntiles = item.te - item.tb;
+        for (int l = 0; l < ntiles; ++l, ++g) {
+          const int s = g % kStages;
+          const int sb = g & 1;
+          if (!wait_bar(L.kv_full(s), (g / kStages) & 1, cx)) { ok = false; break; }
+          if (g >= 2 && !wait_bar(L.s_free(sb), ((g >> 1) - 1) & 1, cx)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            // A = K tile (M = 128 keys, K-major), B = Q (N = query rows, K-major); K = 16 dims
+            const uint64_t a = smem_desc(L.stage(s) + (kk >> 2) * kTileHalf + (kk & 3) * 32, 16, 1024, SW_128B);
+            const uint64_t b = smem_desc(L.q() + (kk >> 2) * C::Q_CB + (kk & 3) * 32, 16, 1024, SW_128B);
+            umma_bf16(tmem + C::TMEM_S + sb * NT, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(L.s_full(sb));
+          if (l >= 1 && !issue_pv(g - 1, l - 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!issue_pv(g - 1, ntiles - 1)) { ok = false; break; }
+      }
+      if (last_pv >= 0) drain_bar(L.p_empty(last_pv % C::P_BUFS), (last_pv / C::P_BUFS) & 1, prm.err);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax / epilogue
+    const int sw = warp & 3;                          // TMEM lane quadrant
+    const int kl = sw * 32 + lane;                    // key of this thread within a tile (= d in O^T)
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
+    const int stid = threadIdx.x - kSoftmaxWarp0 * 32;
+    const float sl2 = prm.scale_log2;
+    float* my_mref = s_mref + sw * NT;
+    float* my_alpha = s_alpha + sw * NT;
+    int g = 0, n_it = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n_it) {
+      const AttnItem item = prm.items[it];
+      const int r = item.r;
+      const int ctx = prm.ctx_len[r];
+      const int c0 = prm.cu_seqlens[r];
+      const int n_r = prm.cu_seqlens[r + 1] - c0;
+      const int ct = ceil_div(ctx, kKT);
+      const int nq = item.ni * G;                     // valid query rows (columns)
+      // ---- Q tile: row n = (block row n / G, head kvh*G + n % G); rows >= nq zero
+      for (int idx = stid; idx < NT * 16; idx += 128) {
+        const int row = idx >> 4, q = idx & 15;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < nq) {
+          const long long src =
+              ((long long)(c0 + item.i0 + row / G) * prm.Hq + item.kvh * G + row % G) * kD;
+          v = ldg_nc_v4(prm.q + src + q * 8);
+        }
+        st_shared_v4(L.q() + (q >> 3) * C::Q_CB + sw128_off(row, q & 7), v);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(L.q_full());
+      // per-row state, lane-distributed: row = gi*32 + lane
+      float mref[C::G32], lacc[C::G32];
+#pragma unroll
+      for (int gi = 0; gi < C::G32; ++gi) { mref[gi] = -INFINITY; lacc[gi] = 0.f; }
+      const int ntiles = item.te - item.tb;
+      for (int l = 0; l < ntiles; ++l, ++g) {
+        const int t = item.tb + l;
+        const int sb = g & 1;
+        if (!wait_warp(L.s_full(sb), (g >> 1) & 1, cx)) { ok = false; break; }
+        tc_fence_after();
+        float s[NT];
+#pragma unroll
+        for (int c = 0; c < NT / 32; ++c) {
+          float tmp[32];
+          tmem_ld32(t_lane + C::TMEM_S + sb * NT + c * 32, tmp);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) s[c * 32 + k] = tmp[k];
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.s_free(sb));
+        // ---- visibility: cache tile -> key < ctx; block tile -> block row b <= bi(row)
+        if (t < ct) {
+          if (t * kKT + kl >= ctx) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) s[n] = -INFINITY;
+          }
+        } else {
+          const int b = (t - ct) * kKT + kl;          // block row of this key
+          // row n sees key b iff b < n_r and b <= i0 + n / G  <=>  n >= (b - i0) * G
+          const int nmin = b < n_r ? (b - item.i0) * G : 0x7fffffff;
+#pragma unroll
+          for (int n = 0; n < NT; ++n) s[n] = (n >= nmin) ? s[n] : -INFINITY;
+        }
+        // ---- tile max per row: warp transpose-reduce, then across the 4 warps
+        float* wmax = s_wmax + (g & 1) * 4 * NT;
+#pragma unroll
+        for (int gi = 0; gi < C::G32; ++gi) {
+          float v[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = s[gi * 32 + k];
+          wmax[sw * NT + gi * 32 + lane] = transpose_reduce<true>(v, lane) * sl2;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.xw(g & 1));
+        if (!wait_warp(L.xw(g & 1), (g >> 1) & 1, cx)) { ok = false; break; }
+        bool need_any = false;
+#pragma unroll
+        for (int gi = 0; gi < C::G32; ++gi) {
+          const int n = gi * 32 + lane;
+          const float tm = fmaxf(fmaxf(wmax[n], wmax[NT + n]), fmaxf(wmax[2 * NT + n], wmax[3 * NT + n]));
+          float alpha = 1.f;
+          if (tm > mref[gi] + 8.0f) {        // lazy: move the reference only on a 2^8 jump
+            alpha = (mref[gi] == -INFINITY) ? 0.f : fast_exp2(mref[gi] - tm);
+            mref[gi] = tm;
+            lacc[gi] *= alpha;
+            need_any = true;
+          }
+          my_mref[n] = mref[gi] == -INFINITY ? 0.f : mref[gi];
+          my_alpha[n] = alpha;
+        }
+        const bool rescale = __any_sync(0xffffffffu, need_any) && l > 0;
+        __syncwarp();
+        // P buffer of this tile must be free: PV(g - P_BUFS) done
+        const int pb = g % C::P_BUFS;
+        if (g >= C::P_BUFS &&
+            !wait_warp(L.p_empty((g - C::P_BUFS) % C::P_BUFS), ((g - C::P_BUFS) / C::P_BUFS) & 1, cx)) {
+          ok = false;
+          break;
+        }
+        if (rescale) {
+          // O^T must hold PV(g-1) before its columns are rescaled
+          if (C::P_BUFS > 1 &&
+              !wait_warp(L.p_empty((g - 1) % C::P_BUFS), ((g - 1) / C::P_BUFS) & 1, cx)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < NT / 32; ++c) {
+            float o[32];
+            tmem_ld32(t_lane + C::TMEM_O + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= my_alpha[c * 32 + k];
+            tmem_st32(t_lane + C::TMEM_O + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        // ---- P^T row of this key: exp2(s * scale - mref[n]) in bf16
+        const uint32_t prow = L.pbuf(pb);
+#pragma unroll
+        for (int n8 = 0; n8 < NT / 8; ++n8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int n = n8 * 8 + 2 * h;
+            const float p0 = fast_exp2(fmaf(s[n], sl2, -my_mref[n]));
+            const float p1 = fast_exp2(fmaf(s[n + 1], sl2, -my_mref[n + 1]));
+            s[n] = p0;
+            s[n + 1] = p1;
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            w[h] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          uint32_t off;
+          if (NT == 32) off = sw64_off(kl, n8);
+          else off = (n8 >> 3) * (kKT * 128) + sw128_off(kl, n8 & 7);
+          st_shared_v4(prow + off, make_uint4(w[0], w[1], w[2], w[3]));
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.p_full(pb));
+        // ---- per-row partial sums over this warp's 32 keys
+#pragma unroll
+        for (int gi = 0; gi < C::G32; ++gi) {
+          float v[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = s[gi * 32 + k];
+          lacc[gi] += transpose_reduce<false>(v, lane);
+        }
+      }
+      if (!ok) break;
+      // ---- epilogue: l across warps, then O^T / l for the valid rows
+      {
+        float* lsum = s_lsum;
+#pragma unroll
+        for (int gi = 0; gi < C::G32; ++gi) lsum[sw * NT + gi * 32 + lane] = lacc[gi];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.ep(n_it & 1));
+        if (!wait_warp(L.ep(n_it & 1), (n_it >> 1) & 1, cx)) { ok = false; break; }
+        const int gl = g - 1;
+        if (!wait_warp(L.p_empty(gl % C::P_BUFS), (gl / C::P_BUFS) & 1, cx)) { ok = false; break; }
+        tc_fence_after();
+        const bool split = item.nsplit > 1;
+        // lse for rows lane + 32*gi (warp 0 of the group writes it)
+        if (sw == 0) {
+#pragma unroll
+          for (int gi = 0; gi < C::G32; ++gi) {
+            const int n = gi * 32 + lane;
+            if (n < nq) {
+              const float lt = lsum[n] + lsum[NT + n] + lsum[2 * NT + n] + lsum[3 * NT + n];
+              const int row_g = c0 + item.i0 + n / G;
+              const int head = item.kvh * G + n % G;
+              const float lse_v = (mref[gi] + log2f(lt)) * 0.69314718055994530942f;
+              if (split)
+                prm.ws_lse[((long long)item.split * prm.max_rows + row_g) * prm.Hq + head] = lse_v;
+              else
+                prm.lse[(long long)row_g * prm.Hq + head] = lse_v;
+            }
+          }
+        }
+#pragma unroll 1
+        for (int c = 0; c < NT / 32; ++c) {
+          float o[32];
+          tmem_ld32(t_lane + C::TMEM_O + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int n = c * 32 + k;
+            if (n < nq) {
+              const float lt = lsum[n] + lsum[NT + n] + lsum[2 * NT + n] + lsum[3 * NT + n];
+              const int row_g = c0 + item.i0 + n / G;
+              const int head = item.kvh * G + n % G;
+              float* dst = split ? prm.ws_o + (((long long)item.split * prm.max_rows + row_g) * prm.Hq + head) * kD
+                                 : prm.out + ((long long)row_g * prm.Hq + head) * kD;
+              dst[kl] = lt > 0.f ? o[k] / lt : 0.f;
+            }
+          }
+        }
+        tc_fence_before();
+        // lsum is rewritten by the next item only after every warp passed its ep barrier
+        // and the next tile's cross-warp barrier; the latter orders it.
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+// 4-D map over a [n_pages, P, Hkv, 128] bf16 cache; box = 64 dims x 1 head x box_rows tokens.
+bool make_cache_map(CUtensorMap* m, const void* base, int n_pages, int P, int Hkv) {
+  EncodeFn enc = get_encode();
+  if (!enc) return false;
+  const int box_rows = P < kKT ? P : kKT;
+  cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)Hkv, (cuuint64_t)P, (cuuint64_t)n_pages};
+  cuuint64_t str[3] = {(cuuint64_t)kD * 2, (cuuint64_t)Hkv * kD * 2, (cuuint64_t)P * Hkv * kD * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, str, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NT>
+bool configure() {
+  static bool done = false, okv = false;
+  if (!done) {
+    done = true;
+    okv = cudaFuncSetAttribute(verify_attn_gqa_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<NT>::SMEM_BYTES) == cudaSuccess;
+  }
+  return okv;
+}
+
+}  // namespace
+
+int query_tile(int Hq, int Hkv, int max_block_rows) {
+  const int G = Hq / Hkv;
+  const long long rows = (long long)G * (max_block_rows > 0 ? max_block_rows : 1);
+  if (rows <= 32) return 32;
+  if (rows <= 64) return 64;
+  return 128;
+}
+
+int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                  const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
+                  const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq,
+                  int Hkv, int page_size, float scale, const AttnItem* items, const int* n_items,
+                  float* out, float* lse, float* ws_o, float* ws_lse, cudaStream_t stream) {
+  Params prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  prm.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  prm.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  prm.page_table = page_table;
+  prm.ctx_len = ctx_len;
+  prm.cu_seqlens = cu_seqlens;
+  prm.items = items;
+  prm.n_items = n_items;
+  prm.out = out;
+  prm.lse = lse;
+  prm.ws_o = ws_o;
+  prm.ws_lse = ws_lse;
+  prm.err = device_error_word();
+  prm.max_pages = max_pages;
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.page_size = page_size;
+  prm.log2_page = 0;
+  while ((1 << prm.log2_page) < page_size) ++prm.log2_page;
+  prm.max_rows = max_rows;
+  prm.n_pages = n_pages;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  CUtensorMap tk, tv;
+  if (!make_cache_map(&tk, k_cache, n_pages, page_size, Hkv)) return DSPARK_ECUDA;
+  if (!make_cache_map(&tv, v_cache, n_pages, page_size, Hkv)) return DSPARK_ECUDA;
+  const int sms = num_sms_cached();
+  switch (nt) {
+    case 32:
+      if (!configure<32>()) return DSPARK_ECUDA;
+      verify_attn_gqa_kernel<32><<<sms, kThreads, Cfg<32>::SMEM_BYTES, stream>>>(tk, tv, prm);
+      break;
+    case 64:
+      if (!configure<64>()) return DSPARK_ECUDA;
+      verify_attn_gqa_kernel<64><<<sms, kThreads, Cfg<64>::SMEM_BYTES, stream>>>(tk, tv, prm);
+      break;
+    default:
+      if (!configure<128>()) return DSPARK_ECUDA;
+      verify_attn_gqa_kernel<128><<<sms, kThreads, Cfg<128>::SMEM_BYTES, stream>>>(tk, tv, prm);
+      break;
+  }
+  DSPARK_LAUNCH_CHECK();
+  return DSPARK_OK;
+}
+
+}  // namespace gqa
+}  // namespace attn
+}  // namespace dspark

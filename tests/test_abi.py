@@ -49,7 +49,7 @@ def test_host_validation_without_device(lib):
                            nul) == -1
     # unsupported attention shape (head dim 96)
     assert lib.dspark_verify_attn(nul, nul, nul, nul, nul, 1, nul, 1, nul, nul, 1, 8, 8, 2, 96, 96,
-                                  16, ctypes.c_float(0.1), 4, nul, nul, nul, 0, nul) == -2
+                                  16, ctypes.c_float(0.1), 4, 9, nul, nul, nul, 0, nul) == -2
     # vocabulary not a multiple of 8
     fake = ctypes.c_void_p(4096)
     assert lib.dspark_accept(fake, fake, 0, 1001, fake, fake, fake, fake, fake, 0, 4, 6, 8, fake,
@@ -57,9 +57,9 @@ def test_host_validation_without_device(lib):
 
 
 def test_workspace_sizes_are_host_computable(lib):
-    s = lib.dspark_verify_attn_workspace_size(32, 512, 32, 8, 128, 128, 8)
+    s = lib.dspark_verify_attn_workspace_size(32, 512, 32, 8, 128, 128, 8, 9)
     assert s > 0
-    assert lib.dspark_verify_attn_workspace_size(64, 1024, 128, 1, 576, 512, 8) > 0
-    assert lib.dspark_verify_attn_workspace_size(32, 512, 32, 8, 96, 96, 8) == 0
+    assert lib.dspark_verify_attn_workspace_size(64, 1024, 128, 1, 576, 512, 8, 9) > 0
+    assert lib.dspark_verify_attn_workspace_size(32, 512, 32, 8, 96, 96, 8, 9) == 0
     assert lib.dspark_accept_workspace_size(32, 8, 512, 151936) > 0
     assert lib.dspark_compact_workspace_size(32) > 0
