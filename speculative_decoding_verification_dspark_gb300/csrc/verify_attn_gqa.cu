@@ -17,9 +17,10 @@
 //   O^T [128 d    x NT rows] += V_tile^T . P^T                    (tcgen05, TMEM)
 //
 // Warp roles (one CTA per SM, persistent over the work list):
-//   warps 0-2  producers: TMA tiled loads of 16-token pages (128-byte swizzle,
-//              no multicast), 3 issuing warps; the partial last page and the
-//              block's own rows by plain loads into the same layout
+//   warps 0-1  producers, K and V streams with separate two-slot rings: TMA tiled
+//              loads of 16-token pages (128-byte swizzle, no multicast); the
+//              partial last page and the block's own rows by plain loads into the
+//              same layout (warp 2 idles)
 //   warp 3     MMA issuer (one lane) + TMEM owner
 //   warps 4-7  softmax: thread = key (TMEM lane).  Per tile: per-row max by a
 //              warp transpose-reduction and one cross-warp exchange through an
@@ -47,7 +48,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kKT = 128;              // keys per tile (MMA M)
 constexpr int kD = 128;               // head dim
 constexpr int kStages = 2;
-constexpr int kProducerWarps = 3;
+constexpr int kProducerWarps = 2;  // warp 0 streams K, warp 1 V; warp 2 has no role
 constexpr int kMmaWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kThreads = 8 * 32;
@@ -73,8 +74,9 @@ struct Cfg {
   static constexpr int OFF_REF = OFF_RED + 2 * 4 * NT * 4;         // float mref[4][NT], alpha[4][NT]
   static constexpr int OFF_LS = OFF_REF + 2 * 4 * NT * 4;          // float lsum[4][NT], ltot[NT]
   static constexpr int OFF_BAR = OFF_LS + 5 * NT * 4;
-  // kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[PB], p_empty[PB], q_full, xw[2], ep[2]
-  static constexpr int N_BARS = 8 + 2 * P_BUFS + 1 + 4;
+  // k_full[2], k_empty[2], s_full[2], s_free[2], p_full[PB], p_empty[PB], q_full, xw[2], ep[2],
+  // v_full[2], v_empty[2]
+  static constexpr int N_BARS = 8 + 2 * P_BUFS + 1 + 4 + 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
   static constexpr int TMEM_S = 0;
@@ -179,8 +181,8 @@ struct Layout {
   __device__ uint32_t stage(int s) const { return base + Cfg<NT>::OFF_STAGE + s * kStageBytes; }
   __device__ uint32_t pbuf(int b) const { return base + Cfg<NT>::OFF_P + b * Cfg<NT>::P_BYTES; }
   __device__ uint32_t bar(int i) const { return base + Cfg<NT>::OFF_BAR + 8 * i; }
-  __device__ uint32_t kv_full(int s) const { return bar(s); }
-  __device__ uint32_t kv_empty(int s) const { return bar(2 + s); }
+  __device__ uint32_t k_full(int s) const { return bar(s); }
+  __device__ uint32_t k_empty(int s) const { return bar(2 + s); }
   __device__ uint32_t s_full(int b) const { return bar(4 + b); }
   __device__ uint32_t s_free(int b) const { return bar(6 + b); }
   __device__ uint32_t p_full(int b) const { return bar(8 + b); }
@@ -188,6 +190,8 @@ struct Layout {
   __device__ uint32_t q_full() const { return bar(8 + 2 * Cfg<NT>::P_BUFS); }
   __device__ uint32_t xw(int b) const { return bar(9 + 2 * Cfg<NT>::P_BUFS + b); }
   __device__ uint32_t ep(int b) const { return bar(11 + 2 * Cfg<NT>::P_BUFS + b); }
+  __device__ uint32_t v_full(int s) const { return bar(13 + 2 * Cfg<NT>::P_BUFS + s); }
+  __device__ uint32_t v_empty(int s) const { return bar(15 + 2 * Cfg<NT>::P_BUFS + s); }
 };
 
 struct Params {
@@ -233,8 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(L.kv_full(s), kProducerWarps);
-      mbar_init(L.kv_empty(s), 1);
+      mbar_init(L.k_full(s), 1);
+      mbar_init(L.k_empty(s), 1);
+      mbar_init(L.v_full(s), 1);
+      mbar_init(L.v_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(L.s_full(b), 1);
@@ -264,8 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------- producers
-    // warp w owns the boxes (16-row pieces) w, w+4, ... of every tile; lane j of
-    // the warp holds page-table slot win_base + j of the current request.
+    // warp 0 streams K tiles, warp 1 V tiles, each through its own two-slot ring:
+    // a K slot is released as soon as QK^T of its tile completes, so the next K
+    // tiles (and with them QK^T and the softmax) run ahead of the V stream.
+    // Lane j of a warp holds page-table slot win_base + j of the current request.
+    const bool is_v = warp == 1;
+    const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
+    const __nv_bfloat16* cache = is_v ? prm.v_cache : prm.k_cache;
+    const __nv_bfloat16* fresh = is_v ? prm.v_new : prm.k_new;
     const int box_rows = P < kKT ? P : kKT;
     const int nbox = kKT / box_rows;
     const uint32_t box_bytes = box_rows * 128;
@@ -283,12 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int win_base = -1, win_page = 0;
       for (int t = item.tb; t < item.te; ++t, ++g) {
         const int s = g % kStages;
+        const uint32_t full = is_v ? L.v_full(s) : L.k_full(s);
         if (g >= kStages) {
-          ok = wait_warp(L.kv_empty(s), ((g / kStages) - 1) & 1, cx);
+          ok = wait_warp(is_v ? L.v_empty(s) : L.k_empty(s), ((g / kStages) - 1) & 1, cx);
           if (!ok) break;
         }
-        const uint32_t kdst = L.stage(s);
-        const uint32_t vdst = kdst + kKVBytes;
+        const uint32_t dst0 = L.stage(s) + (is_v ? kKVBytes : 0);
         bool manual = false;
         if (t < ct) {
           const int slot0 = (t * kKT) >> lp;
@@ -303,72 +315,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             win_page = pg;
           }
-          uint32_t tx = 0;
-          for (int bx = warp; bx < nbox; bx += kProducerWarps) {
-            const int kg = t * kKT + bx * box_rows;
-            if (kg + box_rows <= ctx) tx += 4 * box_bytes;
-          }
-          if (lane == 0 && tx > 0) mbar_expect_tx(L.kv_full(s), tx);
+          const int full_boxes = min(nbox, max(0, (ctx - t * kKT) / box_rows));
+          if (lane == 0 && full_boxes > 0) mbar_expect_tx(full, full_boxes * 2 * box_bytes);
           __syncwarp();
-          // full boxes: lanes 0..(4 * owned boxes - 1) issue one copy each
-          {
-            const int ob = lane >> 2;             // owned box ordinal
-            const int cp = lane & 3;              // K cb0, K cb1, V cb0, V cb1
-            const int bx = warp + ob * kProducerWarps;
+          // full boxes: lane = (box, column block), one copy each
+          for (int base_l = 0; base_l < 2 * nbox; base_l += 32) {
+            const int o = base_l + lane;
+            const int bx = o >> 1, cb = o & 1;
             const int src_lane = bx < nbox ? (((t * kKT + bx * box_rows) >> lp) - win_base) & 31 : 0;
             const int page = __shfl_sync(0xffffffffu, win_page, src_lane);  // all lanes, converged
-            if (bx < nbox) {
-              const int kg = t * kKT + bx * box_rows;
-              if (kg + box_rows <= ctx) {
-                const uint32_t dst = (cp < 2 ? kdst : vdst) + (cp & 1) * kTileHalf + bx * box_rows * 128;
-                tma_load_4d(dst, cp < 2 ? &tm_k : &tm_v, L.kv_full(s), (cp & 1) * 64, item.kvh,
-                            kg & (P - 1), page);
-              }
-            }
+            if (bx < full_boxes)
+              tma_load_4d(dst0 + cb * kTileHalf + bx * box_rows * 128, tm, full, cb * 64, item.kvh,
+                          (t * kKT + bx * box_rows) & (P - 1), page);
           }
-          // partial / empty boxes of this warp: plain loads, zeros past the context
-          for (int bx = warp; bx < nbox; bx += kProducerWarps) {
-            const int kg = t * kKT + bx * box_rows;
-            if (kg + box_rows <= ctx) continue;
+          // partial / empty boxes (last cache tile): plain loads, zeros past the context
+          for (int bx = full_boxes; bx < nbox; ++bx) {
             manual = true;
+            const int kg = t * kKT + bx * box_rows;
             const int page = __shfl_sync(0xffffffffu, win_page, ((kg >> lp) - win_base) & 31);
             const int valid = (kg < ctx && page >= 0) ? ctx - kg : 0;
             const long long off =
                 ((long long)(valid > 0 ? page : 0) * P + (kg & (P - 1))) * rs + (long long)item.kvh * kD;
             const int row0 = bx * box_rows;
-            for (int idx = lane; idx < box_rows * 32; idx += 32) {
-              const int rr = idx >> 5, q = idx & 31;   // q: 16 K chunks then 16 V chunks
-              const bool isv = q >= 16;
-              const int qq = q & 15;
+            for (int idx = lane; idx < box_rows * 16; idx += 32) {
+              const int rr = idx >> 4, q = idx & 15;
               uint4 v = make_uint4(0, 0, 0, 0);
-              if (rr < valid)
-                v = ldg_nc_v4((isv ? prm.v_cache : prm.k_cache) + off + rr * rs + qq * 8);
-              st_shared_v4((isv ? vdst : kdst) + (qq >> 3) * kTileHalf + sw128_off(row0 + rr, qq & 7), v);
+              if (rr < valid) v = ldg_nc_v4(cache + off + rr * rs + q * 8);
+              st_shared_v4(dst0 + (q >> 3) * kTileHalf + sw128_off(row0 + rr, q & 7), v);
             }
           }
         } else {
-          // block tile: the request's own rows b0..b0+127 (zeros past n_r); warp w
-          // fills tile rows w, w + kProducerWarps, ...; lane = 16-byte chunk (16 K + 16 V)
+          // block tile: the request's own rows b0..b0+127, zeros past n_r
           manual = true;
           const int b0 = (t - ct) * kKT;
           const long long off = (long long)(c0 + b0) * rs + (long long)item.kvh * kD;
-          for (int rr = warp; rr < kKT; rr += kProducerWarps) {
-            const int q = lane;
-            const bool isv = q >= 16;
-            const int qq = q & 15;
+          for (int idx = lane; idx < kKT * 16; idx += 32) {
+            const int rr = idx >> 4, q = idx & 15;
             uint4 v = make_uint4(0, 0, 0, 0);
-            if (b0 + rr < n_r) v = ldg_nc_v4((isv ? prm.v_new : prm.k_new) + off + rr * rs + qq * 8);
-            st_shared_v4((isv ? vdst : kdst) + (qq >> 3) * kTileHalf + sw128_off(rr, qq & 7), v);
+            if (b0 + rr < n_r) v = ldg_nc_v4(fresh + off + rr * rs + q * 8);
+            st_shared_v4(dst0 + (q >> 3) * kTileHalf + sw128_off(rr, q & 7), v);
           }
         }
         if (manual) fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(L.kv_full(s));
+        if (lane == 0) mbar_arrive(full);
       }
     }
     if (lane == 0) {
       const int first = g - kStages > 0 ? g - kStages : 0;
-      for (int gg = first; gg < g; ++gg) drain_bar(L.kv_full(gg % kStages), (gg / kStages) & 1, prm.err);
+      for (int gg = first; gg < g; ++gg)
+        drain_bar(is_v ? L.v_full(gg % kStages) : L.k_full(gg % kStages), (gg / kStages) & 1, prm.err);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
@@ -382,6 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(L.p_full(pb), (gp / C::P_BUFS) & 1, cx)) return false;
         tc_fence_after();
         const int s = gp % kStages;
+        if (!wait_bar(L.v_full(s), (gp / kStages) & 1, cx)) return false;
+        tc_fence_after();
         const uint32_t vb = L.stage(s) + kKVBytes;
 #pragma unroll
         for (int kk = 0; kk < kKT / 16; ++kk) {
@@ -391,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16(tmem + C::TMEM_O, a, b, IDESC_PV, (local > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(L.p_empty(pb));
-        umma_commit(L.kv_empty(s));
+        umma_commit(L.v_empty(s));
         last_pv = gp;
         return true;
       };
@@ -402,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int l = 0; l < ntiles; ++l, ++g) {
           const int s = g % kStages;
           const int sb = g & 1;
-          if (!wait_bar(L.kv_full(s), (g / kStages) & 1, cx)) { ok = false; break; }
+          if (!wait_bar(L.k_full(s), (g / kStages) & 1, cx)) { ok = false; break; }
           if (g >= 2 && !wait_bar(L.s_free(sb), ((g >> 1) - 1) & 1, cx)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -413,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16(tmem + C::TMEM_S + sb * NT, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
           }
           umma_commit(L.s_full(sb));
+          umma_commit(L.k_empty(s));
           if (l >= 1 && !issue_pv(g - 1, l - 1)) { ok = false; break; }
         }
         if (!ok) break;
@@ -420,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (last_pv >= 0) drain_bar(L.p_empty(last_pv % C::P_BUFS), (last_pv / C::P_BUFS) & 1, prm.err);
     }
-  } else {
+  } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------- softmax / epilogue
     const int sw = warp & 3;                          // TMEM lane quadrant
     const int kl = sw * 32 + lane;                    // key of this thread within a tile (= d in O^T)
@@ -439,6 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_r = prm.cu_seqlens[r + 1] - c0;
       const int ct = ceil_div(ctx, kKT);
       const int nq = item.ni * G;                     // valid query rows (columns)
+      const int ng = (nq + 31) >> 5;                  // 32-row groups holding valid rows
+      const int nc8 = (nq + 7) >> 3;                  // 8-row chunks holding valid rows
       // ---- Q tile: row n = (block row n / G, head kvh*G + n % G); rows >= nq zero
       for (int idx = stid; idx < NT * 16; idx += 128) {
         const int row = idx >> 4, q = idx & 15;
@@ -492,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* wmax = s_wmax + (g & 1) * 4 * NT;
 #pragma unroll
         for (int gi = 0; gi < C::G32; ++gi) {
+          if (gi >= ng) break;                        // groups of padding rows only
           float v[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = s[gi * 32 + k];
@@ -503,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool need_any = false;
 #pragma unroll
         for (int gi = 0; gi < C::G32; ++gi) {
+          if (gi >= ng) break;
           const int n = gi * 32 + lane;
           const float tm = fmaxf(fmaxf(wmax[n], wmax[NT + n]), fmaxf(wmax[2 * NT + n], wmax[3 * NT + n]));
           float alpha = 1.f;
@@ -545,8 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- P^T row of this key: exp2(s * scale - mref[n]) in bf16
         const uint32_t prow = L.pbuf(pb);
+        // only the chunks holding valid rows: padding columns of P^T are left as they
+        // are -- they only reach their own columns of O^T, which are never stored
 #pragma unroll
         for (int n8 = 0; n8 < NT / 8; ++n8) {
+          if (n8 >= nc8) break;
           uint32_t w[4];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
@@ -570,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- per-row partial sums over this warp's 32 keys
 #pragma unroll
         for (int gi = 0; gi < C::G32; ++gi) {
+          if (gi >= ng) break;
           float v[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = s[gi * 32 + k];
