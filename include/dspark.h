@@ -104,7 +104,8 @@ int dspark_num_sms(void);
  * a_hat_j = fp32(1/(1+exp(-(log a - log1p(-a))/T_j))) in fp64, then the running
  * minimum over j.  Candidates sort by a_hat descending, ties by request then
  * position ascending.  E starts at B and M at B; candidate k is accepted iff
- * B + k + 1 <= max_tokens and (E_k + a_k)/T[M_k+1] > E_k/T[M_k] in fp64.
+ * B + k + 1 <= max_tokens and (E_k + a_k)/T[M_k+1] > E_k/T[M_k], evaluated in
+ * fp64 cross-multiplied: (E_k + a_k) * T[M_k] > E_k * T[M_k+1] (T > 0).
  * Limits: 1 <= B <= 1024, 1 <= gamma <= 32, B*gamma <= 4096.
  * ------------------------------------------------------------------------- */
 int dspark_schedule(const float* conf, int conf_is_logit, const float* sts_temp,

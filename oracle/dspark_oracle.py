@@ -140,8 +140,9 @@ def schedule(conf, conf_is_logit, sts_temp, cost_table, max_tokens, mode) -> Sch
     candidate that does not raise it, or when M + 1 would exceed the largest
     captured tier.  T is the profiled step-cost table indexed by M.
 
-    E and the two ratios are fp64 (E summed in sorted order).  Every decision
-    whose relative margin |lhs - rhs| / rhs is below 1e-5, and a near-tie
+    E and the comparison are fp64 (E summed in sorted order; the two ratios
+    compared cross-multiplied, T > 0).  Every decision whose relative margin
+    |lhs - rhs| / rhs is below 1e-5, and a near-tie
     between the stopping candidate and the last accepted one of another
     request, is recorded in ``listed``.
 
@@ -167,8 +168,10 @@ def schedule(conf, conf_is_logit, sts_temp, cost_table, max_tokens, mode) -> Sch
         if M + 1 > max_tokens:
             stop = "budget"
             break
-        lhs = (E + v) / float(cost[M + 1])
-        rhs = E / float(cost[M])
+        # throughput rises iff (E + v) / T[M+1] > E / T[M]; with T > 0 this is
+        # (E + v) * T[M] > E * T[M+1], evaluated in fp64 without a division
+        lhs = (E + v) * float(cost[M])
+        rhs = E * float(cost[M + 1])
         rel = abs(lhs - rhs) / rhs
         if lhs > rhs:
             if rel < MARGIN_LIST_REL:
