@@ -7,9 +7,10 @@
 // scheduler 与 verify 模式" (cap-accept verifies the block, commits to the window).
 //
 // Three kernels:
-//   accept_test_kernel   one thread per request: the fp32 test u*p_d(d_j) <= p_t(d_j)
-//                        over the verified positions -> committed length, cap, and
-//                        which packed row is sampled (residual or target).
+//   accept_test_kernel   one warp per request, one lane per position: the fp32 test
+//                        u*p_d(d_j) <= p_t(d_j) over the verified positions ->
+//                        committed length, cap, and which packed row is sampled
+//                        (residual or target).
 //   accept_vocab_kernel  persistent grid over (packed row, vocab chunk): one pass of
 //                        128-bit coalesced loads of p_t and p_d computes the partial
 //                        L1 distance for c*, and on the sampled row the partial
@@ -83,6 +84,8 @@ __device__ __forceinline__ void better(float& k, int& i, float k2, int i2) {
 
 }  // namespace
 
+// One warp per request, lane j = draft position j+1: every test's two gathers are
+// issued at once; the accepted prefix is the run of set bits from lane 0.
 template <class T>
 __global__ void __launch_bounds__(128)
     accept_test_kernel(const T* __restrict__ p_t, const T* __restrict__ p_d, int V,
@@ -91,36 +94,40 @@ __global__ void __launch_bounds__(128)
                        int mode, int B, int gamma, int32_t* __restrict__ accept_len,
                        int32_t* __restrict__ cap_len, RowInfo* __restrict__ info,
                        unsigned int* __restrict__ err) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= B) return;
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= B) return;  // warp-uniform
   const int w = windows[r];
   const int base = cu[r];
   const int n_rows = cu[r + 1] - base;
   int test_len = (mode == DSPARK_CAP_ACCEPT) ? gamma : w;
   if (test_len > n_rows - 1) test_len = n_rows - 1;
-  int L = 0;
-  for (int j = 1; j <= test_len; ++j) {
-    int x = draft_tok[r * gamma + j - 1];
+  bool acc = false;
+  if (lane < test_len) {
+    const int x = draft_tok[r * gamma + lane];
     if (x < 0 || x >= V) {
-      raise_error(err, DSPARK_DEVERR_BAD_INPUT);
-      break;
+      raise_error(err, DSPARK_DEVERR_BAD_INPUT);  // an out-of-range draft is rejected
+    } else {
+      const float pt = ld_p(p_t, (long long)(base + lane) * V + x);
+      const float pd = ld_p(p_d, ((long long)r * gamma + lane) * V + x);
+      acc = __fmul_rn(uniforms[r * gamma + lane], pd) <= pt;
     }
-    const float pt = ld_p(p_t, (long long)(base + j - 1) * V + x);
-    const float pd = ld_p(p_d, ((long long)r * gamma + j - 1) * V + x);
-    if (__fmul_rn(uniforms[r * gamma + j - 1], pd) <= pt)
-      ++L;
-    else
-      break;
   }
-  const int commit = L < w ? L : w;
-  RowInfo ri;
-  ri.commit = commit;
-  ri.cap = L;
-  ri.sample_row = commit;
-  ri.residual = commit < w ? 1 : 0;
-  info[r] = ri;
-  accept_len[r] = commit;
-  cap_len[r] = L;
+  const unsigned ok = __ballot_sync(0xffffffffu, acc);
+  const unsigned in_range = test_len >= 32 ? 0xffffffffu : ((1u << test_len) - 1u);
+  const unsigned rejected = ~ok & in_range;
+  const int L = rejected ? __ffs(rejected) - 1 : test_len;
+  if (lane == 0) {
+    const int commit = L < w ? L : w;
+    RowInfo ri;
+    ri.commit = commit;
+    ri.cap = L;
+    ri.sample_row = commit;
+    ri.residual = commit < w ? 1 : 0;
+    info[r] = ri;
+    accept_len[r] = commit;
+    cap_len[r] = L;
+  }
 }
 
 template <class T>
@@ -275,7 +282,7 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
   if (pdt == DSPARK_F32) {
     const float* t = static_cast<const float*>(p_t);
     const float* d = static_cast<const float*>(p_d);
-    accept_test_kernel<float><<<ceil_div(B, 128), 128, 0, stream>>>(
+    accept_test_kernel<float><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
         t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, accept_len, cap_len, info, err);
     DSPARK_LAUNCH_CHECK();
     accept_vocab_kernel<float><<<(int)grid, kVocabThreads, 0, stream>>>(t, d, exp_noise, V, n_chunks,
@@ -283,7 +290,7 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
   } else {
     const __nv_bfloat16* t = static_cast<const __nv_bfloat16*>(p_t);
     const __nv_bfloat16* d = static_cast<const __nv_bfloat16*>(p_d);
-    accept_test_kernel<__nv_bfloat16><<<ceil_div(B, 128), 128, 0, stream>>>(
+    accept_test_kernel<__nv_bfloat16><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
         t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, accept_len, cap_len, info, err);
     DSPARK_LAUNCH_CHECK();
     accept_vocab_kernel<__nv_bfloat16><<<(int)grid, kVocabThreads, 0, stream>>>(

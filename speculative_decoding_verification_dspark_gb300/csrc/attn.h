@@ -8,18 +8,25 @@
 namespace dspark {
 namespace attn {
 
-// One unit of work: a tile of query rows of one request against a range of its key tiles.
+// One unit of work: a tile of query rows of one request against a range of its key tiles;
+// split = which piece of its group, nsplit = the group's piece count (1: not split).
 struct __align__(16) AttnItem {
   int r, kvh, i0, ni;        // request, KV head, first block row, block rows in the tile
   int part, split, tb, te;   // value-column part, split index, key-tile range [tb, te)
   int nsplit, pad0, pad1, pad2;
 };
 
+// A (request, row tile, part, KV head) group whose key range was cut into pieces.
+struct __align__(16) SplitGroup {
+  int r, kvh, part, i0;
+  int ni, c_first, nsplit, pad;
+};
+
 struct Plan {
   bool mla;
-  int parts, rows_per_tile, nk, nt;
+  int parts, rows_per_tile, nk, nt, d_part, ncta;
   long long max_items;
-  size_t off_items, off_nitems, off_nsplit, off_o, off_lse, bytes;
+  size_t off_items, off_begin, off_groups, off_ngroups, off_o, off_lse, bytes;
 };
 
 Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_splits,
@@ -38,8 +45,9 @@ int query_tile(int Hq, int Hkv, int max_block_rows);
 int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, const void* k_cache,
                   const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
                   const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq,
-                  int Hkv, int page_size, float scale, const AttnItem* items, const int* n_items,
-                  float* out, float* lse, float* ws_o, float* ws_lse, cudaStream_t stream);
+                  int Hkv, int page_size, float scale, const AttnItem* items,
+                  const int* item_begin, float* out, float* lse, float* ws_o, float* ws_lse,
+                  cudaStream_t stream);
 constexpr int kKeyTile = 128;
 }  // namespace gqa
 

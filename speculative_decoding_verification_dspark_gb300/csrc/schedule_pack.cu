@@ -1,18 +1,19 @@
 // Confidence scheduling and ragged packing.
 //
-// schedule_kernel (one CTA of 1024 threads):
-//   * one thread per request: c_k (sigmoid of the confidence logit, fp64 then one
-//     fp32 rounding), prefix survival a_j = prod_{i<=j} c_i as an fp32 running
-//     product, Sequential Temperature Scaling a_hat_j = sigmoid(logit(a_j)/T_j)
-//     in fp64 rounded to fp32, clamped non-increasing in j
-//     ("DSpark：投机解码与生产级 Serving 学习笔记", section 07 Confidence Head);
-//   * a bitonic sort of the <= 4096 (a_hat, request, position) keys in shared
-//     memory, survival descending, ties by request then position;
-//   * the greedy of section 08.3 (add candidates while expected throughput
-//     E / T(M) rises, stop at the first that does not; M = bs + K as in the
-//     CSDN article's additive cost model): fp64 block-wide prefix sums give E
-//     before every candidate, each candidate's decision is evaluated in
-//     parallel, and the first failing index is a block-wide minimum.
+// calibrate_kernel (one warp per request, many CTAs): c_k (sigmoid of the
+//   confidence logit, fp64 then one fp32 rounding), prefix survival
+//   a_j = prod_{i<=j} c_i as fp32 products in left-to-right order, Sequential
+//   Temperature Scaling a_hat_j = sigmoid(logit(a_j)/T_j) in fp64 rounded to fp32,
+//   clamped non-increasing in j ("DSpark：投机解码与生产级 Serving 学习笔记",
+//   section 07 Confidence Head).  FP64 is slow on this part, so these run spread
+//   over the whole GPU rather than in the sorting CTA.
+// greedy_kernel (one CTA of 1024 threads): a bitonic sort of the <= 4096
+//   (a_hat, request, position) keys, survival descending, ties by request then
+//   position; the greedy of section 08.3 (add candidates while expected
+//   throughput E / T(M) rises, stop at the first that does not; M = bs + K as in
+//   the CSDN article's additive cost model): fp64 block-wide prefix sums give E
+//   before every candidate, each candidate's test is evaluated in parallel, and
+//   the first failing index is a block-wide minimum.
 // pack_kernel (one CTA): exclusive scan of the per-request row counts
 //   (cu_seqlens), tier selection, and per-row request / position / token
 //   ("DFlash 到 DSpark in SGLang", section "Ragged verify under full CUDA graphs").
@@ -53,12 +54,60 @@ __device__ __forceinline__ int warp_incl_scan_i(int v) {
 
 }  // namespace
 
+// Calibration: one warp per request, lane j = position j (gamma <= 32).  The fp64
+// transcendentals of every position run in parallel across warps and CTAs;
+// lane j forms a_j = ((c_0 c_1) c_2 ... c_j) with the fp32 products taken in that
+// left-to-right order; the clamp to a non-increasing sequence is an (exact)
+// inclusive min-scan over the lanes.
+__global__ void __launch_bounds__(64)
+    calibrate_kernel(const float* __restrict__ conf, int conf_is_logit,
+                     const float* __restrict__ sts_temp, int B, int gamma,
+                     float* __restrict__ a_hat) {
+  const int r = blockIdx.x * 2 + (threadIdx.x >> 5);
+  const int j = threadIdx.x & 31;
+  if (r >= B) return;  // warp-uniform
+  float c = 1.f;
+  if (j < gamma) {
+    const float x = conf[r * gamma + j];
+    c = x;
+    if (conf_is_logit) c = __double2float_rn(1.0 / (1.0 + exp(-static_cast<double>(x))));
+  }
+  float a = 0.f;
+  for (int i = 0; i < gamma; ++i) {
+    const float ci = __shfl_sync(0xffffffffu, c, i);
+    if (i == 0) a = ci;
+    else if (i <= j) a = __fmul_rn(a, ci);
+  }
+  float v = 1.f;
+  if (j < gamma) {
+    const double ad = static_cast<double>(a);
+    double y;
+    if (ad <= 0.0) {
+      y = 0.0;
+    } else if (ad >= 1.0) {
+      y = 1.0;
+    } else {
+      const double t = (log(ad) - log1p(-ad)) / static_cast<double>(sts_temp[j]);
+      y = 1.0 / (1.0 + exp(-t));
+    }
+    v = __double2float_rn(y);
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float u = __shfl_up_sync(0xffffffffu, v, o);
+    if (j >= o) v = fminf(v, u);
+  }
+  if (j < gamma) a_hat[r * gamma + j] = v;
+}
+
+// Greedy window choice over the calibrated survival (one CTA of 1024 threads):
+// bitonic sort of the <= 4096 (a_hat, request, position) keys, fp64 block-wide
+// prefix sums of a_hat in sorted order (E before each candidate), every
+// candidate's throughput test in parallel, first failure by a block minimum.
 __global__ void __launch_bounds__(kSchedThreads)
-    schedule_kernel(const float* __restrict__ conf, int conf_is_logit,
-                    const float* __restrict__ sts_temp, const float* __restrict__ cost, int B,
-                    int gamma, int max_tokens, int mode, int32_t* __restrict__ windows,
-                    float* __restrict__ a_hat, int32_t* __restrict__ M_out,
-                    double* __restrict__ E_out) {
+    greedy_kernel(const float* __restrict__ a_hat, const float* __restrict__ cost, int B,
+                  int gamma, int max_tokens, int mode, int32_t* __restrict__ windows,
+                  int32_t* __restrict__ M_out, double* __restrict__ E_out) {
   __shared__ unsigned long long keys[DSPARK_MAX_CANDS];
   __shared__ double s_warp[32];
   __shared__ int s_first;
@@ -69,36 +118,16 @@ __global__ void __launch_bounds__(kSchedThreads)
   while (npow < n) npow <<= 1;
 
   if (tid == 0) s_first = n;
-  for (int r = tid; r < B; r += blockDim.x) {
-    float acc = 0.f, prev = 0.f;
-    for (int j = 0; j < gamma; ++j) {
-      const float x = conf[r * gamma + j];
-      float c = x;
-      if (conf_is_logit) {
-        const double z = static_cast<double>(x);
-        c = __double2float_rn(1.0 / (1.0 + exp(-z)));
-      }
-      acc = (j == 0) ? c : __fmul_rn(acc, c);
-      const double a = static_cast<double>(acc);
-      double y;
-      if (a <= 0.0) {
-        y = 0.0;
-      } else if (a >= 1.0) {
-        y = 1.0;
-      } else {
-        const double t = (log(a) - log1p(-a)) / static_cast<double>(sts_temp[j]);
-        y = 1.0 / (1.0 + exp(-t));
-      }
-      float v = __double2float_rn(y);
-      if (j > 0 && v > prev) v = prev;
-      prev = v;
-      a_hat[r * gamma + j] = v;
-      keys[r * gamma + j] = (static_cast<unsigned long long>(~__float_as_uint(v)) << 32) |
-                            (static_cast<unsigned>(r) << 16) | static_cast<unsigned>(j);
+  for (int k = tid; k < npow; k += blockDim.x) {
+    unsigned long long key = ~0ull;
+    if (k < n) {
+      const int r = k / gamma, j = k - r * gamma;
+      key = (static_cast<unsigned long long>(~__float_as_uint(a_hat[k])) << 32) |
+            (static_cast<unsigned>(r) << 16) | static_cast<unsigned>(j);
     }
-    s_win[r] = 0;
+    keys[k] = key;
   }
-  for (int i = n + tid; i < npow; i += blockDim.x) keys[i] = ~0ull;
+  for (int r = tid; r < B; r += blockDim.x) s_win[r] = 0;
   __syncthreads();
 
   // bitonic sort, ascending keys = survival descending
@@ -129,17 +158,18 @@ __global__ void __launch_bounds__(kSchedThreads)
                    : 0.0;
     local += v[q];
   }
+  const int nwarps = blockDim.x >> 5;
   double incl = warp_incl_scan(local);
   if ((tid & 31) == 31) s_warp[tid >> 5] = incl;
   __syncthreads();
   if (tid < 32) {
-    double w = s_warp[tid];
+    double w = tid < nwarps ? s_warp[tid] : 0.0;
     w = warp_incl_scan(w);
     s_warp[tid] = w;
   }
   __syncthreads();
   const double warp_off = (tid >> 5) ? s_warp[(tid >> 5) - 1] : 0.0;
-  const double total = s_warp[31];
+  const double total = s_warp[nwarps - 1];
   double E = static_cast<double>(B) + warp_off + (incl - local);
 
   const bool greedy = (mode != DSPARK_STATIC);
@@ -151,8 +181,9 @@ __global__ void __launch_bounds__(kSchedThreads)
       const int M = B + k;
       bool ok = (M + 1 <= max_tokens);
       if (ok) {
-        const double lhs = (E + v[q]) / static_cast<double>(cost[M + 1]);
-        const double rhs = E / static_cast<double>(cost[M]);
+        // throughput E/T(M) rises iff (E + a) T[M] > E T[M+1]  (T > 0)
+        const double lhs = __dmul_rn(E + v[q], static_cast<double>(cost[M]));
+        const double rhs = __dmul_rn(E, static_cast<double>(cost[M + 1]));
         ok = lhs > rhs;
       }
       if (!ok) first_fail = k;
@@ -249,9 +280,16 @@ int launch_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
                     const float* cost_table, int B, int gamma, int max_tokens, int mode,
                     int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
                     cudaStream_t stream) {
-  schedule_kernel<<<1, kSchedThreads, 0, stream>>>(conf, conf_is_logit, sts_temp, cost_table, B,
-                                                   gamma, max_tokens, mode, windows, a_hat, M_out,
-                                                   E_out);
+  calibrate_kernel<<<ceil_div(B, 2), 64, 0, stream>>>(conf, conf_is_logit, sts_temp, B, gamma, a_hat);
+  DSPARK_LAUNCH_CHECK();
+  // kPerThread candidates per thread, no more warps than the candidates need:
+  // the fp64 scan and tests run at the part's (low) fp64 rate.
+  int npow = 1;
+  while (npow < B * gamma) npow <<= 1;
+  int threads = ceil_div(ceil_div(npow, kPerThread), 32) * 32;
+  threads = threads < 32 ? 32 : (threads > kSchedThreads ? kSchedThreads : threads);
+  greedy_kernel<<<1, threads, 0, stream>>>(a_hat, cost_table, B, gamma, max_tokens, mode, windows,
+                                           M_out, E_out);
   DSPARK_LAUNCH_CHECK();
   return DSPARK_OK;
 }

@@ -199,7 +199,7 @@ struct Params {
   const int32_t* ctx_len;
   const int32_t* cu_seqlens;
   const AttnItem* items;
-  const int* n_items;
+  const int* item_begin;  // [gridDim.x + 1]: CTA c runs items [item_begin[c], item_begin[c+1])
   float* out;
   float* lse;
   float* ws_o;
@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int n_items = *prm.n_items;
+  const int it_begin = prm.item_begin[blockIdx.x];
+  const int it_end = prm.item_begin[blockIdx.x + 1];
   const int G = C::MLA ? kRows : prm.Hq / prm.Hkv;  // query rows per block row
 
   if (warp < kProducerWarps) {
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
     const int pt = threadIdx.x;  // 0..127
     int g = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int it = it_begin; it < it_end && ok; ++it) {
       const AttnItem item = prm.items[it];
       const int r = item.r;
       const int ctx = prm.ctx_len[r];
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
         last_pv = gp;
         return true;
       };
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n_it) {
+      for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
         const AttnItem item = prm.items[it];
         if (!wait_bar(L.q_full(), n_it & 1, cx)) { ok = false; break; }
         const int ntiles = item.te - item.tb;
@@ -427,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
     const float sl2 = prm.scale_log2;
     int g = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int it = it_begin; it < it_end && ok; ++it) {
       const AttnItem item = prm.items[it];
       const int r = item.r;
       const int ctx = prm.ctx_len[r];
@@ -576,12 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
           const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
           const bool split = item.nsplit > 1;
           float* obase;
+          // a piece of a split context writes its partial rows into its own slot
           if (split)
-            obase = prm.ws_o + (((long long)item.split * prm.max_rows + row_g) * prm.Hq + head) *
-                                   prm.d_v_total;
+            obase = prm.ws_o + ((long long)it * kRows + m) * C::DV;
           else
-            obase = prm.out + ((long long)row_g * prm.Hq + head) * prm.d_v_total;
-          obase += item.part * C::DV;
+            obase = prm.out + ((long long)row_g * prm.Hq + head) * prm.d_v_total + item.part * C::DV;
 #pragma unroll 1
           for (int c = 0; c < C::DV / 32; ++c) {
             float o[32];
@@ -595,11 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
                                      o[4 * k + 3] * inv_l);
             }
           }
-          if (row_ok && item.part == 0) {
+          if (row_ok) {
             const float lse_v = (m_used + log2f(l_sum)) * 0.69314718055994530942f;
             if (split)
-              prm.ws_lse[((long long)item.split * prm.max_rows + row_g) * prm.Hq + head] = lse_v;
-            else
+              prm.ws_lse[(long long)it * kRows + m] = lse_v;
+            else if (item.part == 0)
               prm.lse[(long long)row_g * prm.Hq + head] = lse_v;
           }
         }
@@ -616,128 +616,213 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
 }
 
 // ---------------------------------------------------------------- work list
-// One CTA.  Splits each request's key range so that the item count is near
-// `target_items` and no request is cut into more than `max_splits` pieces.
+// One CTA.  Stream-K style split: the key tiles of every (request, row tile,
+// value part, KV head) group are laid end to end (U units) and CTA c of the
+// persistent grid receives units [c*U/n, (c+1)*U/n) -- the same number of tiles
+// for every CTA, whatever the context-length mix.  A group cut by CTA boundaries
+// becomes pieces; each piece writes partial (o, lse) rows into the slot of its
+// own item, and the group is listed for the combine.  Piece s of a group is the
+// last item of CTA c_first (s = 0) or the first item of CTA c_first + s.
+__device__ __forceinline__ int cta_of_unit(long long x, long long U, int ncta) {
+  return static_cast<int>(((x + 1) * ncta - 1) / U);  // largest c with c*U/ncta <= x
+}
+
 __global__ void __launch_bounds__(1024)
     worklist_kernel(const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ cu_seqlens,
-                    int B, int Hkv, int parts, int rows_per_tile, int NK, int max_splits,
-                    int target_items, int max_items, AttnItem* __restrict__ items,
-                    int* __restrict__ n_items, int* __restrict__ nsplit_r,
+                    int B, int max_rows, int Hkv, int parts, int rows_per_tile, int NK, int ncta,
+                    int max_splits, int max_items, AttnItem* __restrict__ items, int* __restrict__ item_begin,
+                    SplitGroup* __restrict__ groups, int* __restrict__ n_groups,
                     unsigned int* __restrict__ err) {
+  __shared__ long long s_off[DSPARK_MAX_B + 1];
+  __shared__ int s_tt[DSPARK_MAX_B];
+  __shared__ int s_n[DSPARK_MAX_B];
   __shared__ long long s_red[32];
-  __shared__ int s_scan[32];
-  const int r = threadIdx.x;
-  int n = 0, ctx = 0, tt = 0, rt = 0;
-  if (r < B) {
-    n = cu_seqlens[r + 1] - cu_seqlens[r];
-    ctx = ctx_len[r];
-    tt = ceil_div(ctx, NK) + ceil_div(n, NK);
-    rt = ceil_div(n, rows_per_tile);
+  __shared__ int s_cnt[1025];
+  __shared__ int s_ngroups;
+  __shared__ int s_ok;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int ng_per_tile = parts * Hkv;
+  long long units = 0;
+  int tt = 0;
+  if (tid < B) {
+    const int n = cu_seqlens[tid + 1] - cu_seqlens[tid];
+    tt = ceil_div(ctx_len[tid], NK) + ceil_div(n, NK);
+    const int rt = ceil_div(n, rows_per_tile);
+    units = (long long)tt * rt * ng_per_tile;
+    s_tt[tid] = tt;
+    s_n[tid] = n;
   }
-  long long units = (long long)tt * rt * Hkv * parts;
-  // block sum of units
-  for (int o = 16; o > 0; o >>= 1) units += __shfl_xor_sync(0xffffffffu, units, o);
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = units;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    long long v = threadIdx.x < (blockDim.x >> 5) ? s_red[threadIdx.x] : 0;
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (threadIdx.x == 0) s_red[0] = v;
+  if (tid == 0) {
+    s_ngroups = 0;
+    s_ok = 1;
+    // packed rows beyond the caller's buffers: report and run nothing
+    if (cu_seqlens[B] > max_rows) {
+      raise_error(err, DSPARK_DEVERR_ROWS_OVERFLOW);
+      s_ok = 0;
+    }
   }
-  __syncthreads();
-  const long long U = s_red[0];
-  const long long chunk = U / target_items + ((U % target_items) ? 1 : 0);
-  int ns = 0, per = 1;
-  if (r < B) {
-    long long want = chunk > 0 ? (tt + chunk - 1) / chunk : 1;
-    ns = (int)(want < 1 ? 1 : (want > max_splits ? max_splits : want));
-    per = ceil_div(tt, ns);
-    ns = ceil_div(tt, per);
-  }
-  int cnt = (r < B) ? rt * Hkv * parts * ns : 0;
-  // exclusive scan of cnt
-  int v = cnt;
+  // exclusive scan of units, and the largest group (in tiles)
+  long long v = units;
+  int tmax = tt;
   for (int o = 1; o < 32; o <<= 1) {
-    int u = __shfl_up_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) >= o) v += u;
+    const long long u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
   }
-  if ((threadIdx.x & 31) == 31) s_scan[threadIdx.x >> 5] = v;
+  if (lane == 31) s_red[wid] = v;
+  __shared__ int s_tmax[32];
+  if (lane == 0) s_tmax[wid] = tmax;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    int w = threadIdx.x < (blockDim.x >> 5) ? s_scan[threadIdx.x] : 0;
+  if (tid < 32) {
+    long long w = tid < (int)(blockDim.x >> 5) ? s_red[tid] : 0;
+    int tm = tid < (int)(blockDim.x >> 5) ? s_tmax[tid] : 0;
     for (int o = 1; o < 32; o <<= 1) {
-      int u = __shfl_up_sync(0xffffffffu, w, o);
-      if (threadIdx.x >= o) w += u;
+      const long long u = __shfl_up_sync(0xffffffffu, w, o);
+      if (tid >= o) w += u;
+      tm = max(tm, __shfl_xor_sync(0xffffffffu, tm, o));
     }
-    s_scan[threadIdx.x] = w;
+    s_red[tid] = w;
+    if (tid == 0) s_tmax[0] = tm;
   }
   __syncthreads();
-  const int warp_off = (threadIdx.x >> 5) ? s_scan[(threadIdx.x >> 5) - 1] : 0;
-  const int off = warp_off + v - cnt;
-  const int total = s_scan[(blockDim.x >> 5) - 1];
-  if (threadIdx.x == 0) {
-    if (total > max_items) {
-      raise_error(err, DSPARK_DEVERR_WORK_OVERFLOW);
-      *n_items = 0;
-    } else {
-      *n_items = total;
-    }
+  const long long U = s_red[(blockDim.x >> 5) - 1];
+  if (tid < B) s_off[tid] = ((wid > 0) ? s_red[wid - 1] : 0) + v - units;
+  if (tid == 0) s_off[B] = U;
+  // No group may be cut into more than max_splits pieces.  Every CTA range holds at
+  // least L = floor(U/n) units, and a group of T units meets at most
+  // ceil((T-1)/L) + 1 ranges, so L >= ceil((T_max-1)/(max_splits-1)) suffices:
+  // n <= U / that.  Then n <= U too, so no CTA range is empty, the pieces of a
+  // group sit in consecutive CTAs and piece s is found from c_first alone.
+  int n_eff = ncta;
+  {
+    const long long t_max = s_tmax[0];
+    long long l_req = t_max > 1 ? (t_max - 1 + max_splits - 2) / (max_splits - 1) : 1;
+    if (l_req < 1) l_req = 1;
+    const long long cap = U / l_req;
+    if (cap < n_eff) n_eff = cap > 0 ? static_cast<int>(cap) : 1;
   }
-  if (r < B) nsplit_r[r] = ns;
-  if (r < B && total <= max_items) {
-    int k = off;
-    for (int s = 0; s < ns; ++s) {
-      const int tb = s * per;
-      const int te = (tb + per < tt) ? tb + per : tt;
-      for (int t = 0; t < rt; ++t) {
+  __syncthreads();
+  // walk one CTA's unit range: count (pass 0) or emit (pass 1) its pieces
+  auto walk = [&](int c, bool emit, int base) -> int {
+    if (c >= n_eff || U == 0) return 0;
+    const long long lo = (long long)c * U / n_eff, hi = (long long)(c + 1) * U / n_eff;
+    long long u = lo;
+    int k = 0;
+    while (u < hi) {
+      int a = 0, b = B;  // request: s_off[a] <= u < s_off[a + 1]
+      while (b - a > 1) {
+        const int mid = (a + b) >> 1;
+        if (s_off[mid] <= u) a = mid; else b = mid;
+      }
+      const int r = a;
+      const int t_r = s_tt[r];
+      const long long lu = u - s_off[r];
+      const int lg = static_cast<int>(lu / t_r);          // group within the request
+      const long long gstart = s_off[r] + (long long)lg * t_r;
+      const long long gend = gstart + t_r;
+      const long long next = gend < hi ? gend : hi;
+      if (emit) {
+        const int c_first = cta_of_unit(gstart, U, n_eff);
+        const int c_last = cta_of_unit(gend - 1, U, n_eff);
+        const int t = lg / ng_per_tile, p = (lg / Hkv) % parts, h = lg % Hkv;
         const int i0 = t * rows_per_tile;
-        const int ni = (n - i0 < rows_per_tile) ? n - i0 : rows_per_tile;
-        for (int p = 0; p < parts; ++p) {
-          for (int h = 0; h < Hkv; ++h) {
-            AttnItem it;
-            it.r = r; it.kvh = h; it.i0 = i0; it.ni = ni;
-            it.part = p; it.split = s; it.tb = tb; it.te = te;
-            it.nsplit = ns; it.pad0 = 0; it.pad1 = 0; it.pad2 = 0;
-            items[k++] = it;
-          }
+        const int ni = min(rows_per_tile, s_n[r] - i0);
+        AttnItem it;
+        it.r = r; it.kvh = h; it.i0 = i0; it.ni = ni;
+        it.part = p; it.split = c - c_first;
+        it.tb = static_cast<int>(lu - (long long)lg * t_r);
+        it.te = it.tb + static_cast<int>(next - u);
+        it.nsplit = c_last - c_first + 1;
+        it.pad0 = 0; it.pad1 = 0; it.pad2 = 0;
+        items[base + k] = it;
+        if (it.split == 0 && it.nsplit > 1) {
+          const int gi = atomicAdd(&s_ngroups, 1);
+          SplitGroup sg;
+          sg.r = r; sg.kvh = h; sg.part = p; sg.i0 = i0;
+          sg.ni = ni; sg.c_first = c_first; sg.nsplit = it.nsplit; sg.pad = 0;
+          groups[gi] = sg;
         }
       }
+      ++k;
+      u = next;
+    }
+    return k;
+  };
+  for (int c = tid; c <= 1024; c += blockDim.x) s_cnt[c] = 0;
+  __syncthreads();
+  for (int c = tid; c < ncta; c += blockDim.x) s_cnt[c] = walk(c, false, 0);
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int c = 0; c < ncta; ++c) {
+      const int k = s_cnt[c];
+      s_cnt[c] = acc;
+      acc += k;
+    }
+    s_cnt[ncta] = acc;
+    if (s_ok && acc > max_items) {
+      raise_error(err, DSPARK_DEVERR_WORK_OVERFLOW);
+      s_ok = 0;
     }
   }
+  __syncthreads();
+  const bool fits = s_ok != 0;
+  for (int c = tid; c <= ncta; c += blockDim.x) item_begin[c] = fits ? s_cnt[c] : 0;
+  if (fits)
+    for (int c = tid; c < ncta; c += blockDim.x) walk(c, true, s_cnt[c]);
+  __syncthreads();
+  if (tid == 0) *n_groups = fits ? s_ngroups : 0;
 }
 
 // ---------------------------------------------------------------- split combine
-// One warp per (packed row, query head) of a request that was split.
+// One warp per (split group, query row): o = sum_s e^{lse_s - lse} o_s / ...,
+// lse = log sum_s e^{lse_s}, over the group's pieces' slots.
 __global__ void __launch_bounds__(256)
-    combine_kernel(const int32_t* __restrict__ cu_seqlens, int B, int Hq, int d_v,
-                   const int* __restrict__ nsplit_r, const float* __restrict__ ws_o,
-                   const float* __restrict__ ws_lse, int max_rows, float* __restrict__ out,
-                   float* __restrict__ lse) {
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    combine_kernel(const int32_t* __restrict__ cu_seqlens, const SplitGroup* __restrict__ groups,
+                   const int* __restrict__ n_groups, const int* __restrict__ item_begin, int G,
+                   int Hq, int rows_per_slot, int d_part, int d_v_total, const float* __restrict__ ws_o,
+                   const float* __restrict__ ws_lse, float* __restrict__ out,
+                   float* __restrict__ lse, int mla) {
   const int lane = threadIdx.x & 31;
-  const int M = cu_seqlens[B];
-  const int row = wid / Hq, head = wid % Hq;
-  if (row >= M || row >= max_rows) return;
-  const int r = upper_segment(cu_seqlens, B, row);
-  const int ns = nsplit_r[r];
-  if (ns <= 1) return;
-  float my = -INFINITY;
-  if (lane < ns) my = ws_lse[((long long)lane * max_rows + row) * Hq + head];
-  float mx = my;
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  const float w = lane < ns ? expf(my - mx) : 0.f;
-  float sum = w;
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float inv = 1.f / sum;
-  for (int c = lane; c < d_v; c += 32) {
-    float acc = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w, s);
-      acc += ws * ws_o[(((long long)s * max_rows + row) * Hq + head) * d_v + c];
+  const int ng = *n_groups;
+  const int warps_per_cta = blockDim.x >> 5;
+  for (int e = blockIdx.x; e < ng; e += gridDim.x) {
+    const SplitGroup sg = groups[e];
+    const int nq = mla ? Hq : sg.ni * G;
+    const int ns = sg.nsplit;
+    // item index of piece `lane`
+    int piece = 0;
+    if (lane < ns)
+      piece = lane == 0 ? item_begin[sg.c_first + 1] - 1 : item_begin[sg.c_first + lane];
+    const int c0 = cu_seqlens[sg.r];
+    for (int n = threadIdx.x >> 5; n < nq; n += warps_per_cta) {
+      float my = -INFINITY;
+      if (lane < ns) my = ws_lse[(long long)piece * rows_per_slot + n];
+      float mx = my;
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float wgt = lane < ns ? expf(my - mx) : 0.f;
+      float sum = wgt;
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      const float inv = 1.f / sum;
+      int row_g, head;
+      if (mla) { row_g = c0 + sg.i0; head = n; }
+      else { row_g = c0 + sg.i0 + n / G; head = sg.kvh * G + n % G; }
+      float4* dst = reinterpret_cast<float4*>(out + ((long long)row_g * Hq + head) * d_v_total +
+                                              sg.part * d_part);
+      for (int d4 = lane; d4 < (d_part >> 2); d4 += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < ns; ++sp) {
+          const float ws = __shfl_sync(0xffffffffu, wgt, sp);
+          const int pc = __shfl_sync(0xffffffffu, piece, sp);
+          const float4 v = reinterpret_cast<const float4*>(
+              ws_o + ((long long)pc * rows_per_slot + n) * d_part)[d4];
+          acc.x += ws * v.x; acc.y += ws * v.y; acc.z += ws * v.z; acc.w += ws * v.w;
+        }
+        dst[d4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      }
+      if (lane == 0 && sg.part == 0) lse[(long long)row_g * Hq + head] = mx + logf(sum);
     }
-    out[((long long)row * Hq + head) * d_v + c] = acc * inv;
   }
-  if (lane == 0) lse[(long long)row * Hq + head] = mx + logf(sum);
 }
 
 // ---------------------------------------------------------------- host side
@@ -754,8 +839,6 @@ bool configure_smem() {
   return okv;
 }
 
-constexpr int kItemsPerSm = 2;
-
 }  // namespace
 
 Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_splits,
@@ -767,8 +850,11 @@ Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_split
   p.nt = p.mla ? kRows : gqa::query_tile(Hq, Hkv, max_block_rows);
   p.rows_per_tile = p.mla ? 1 : (p.nt / G);
   p.nk = p.mla ? CfgMLA::NK : gqa::kKeyTile;
-  const long long tiles_rows = (long long)max_rows / (p.rows_per_tile > 0 ? p.rows_per_tile : 1) + B;
-  p.max_items = (long long)Hkv * p.parts * max_splits * tiles_rows;
+  p.d_part = p.mla ? CfgMLA::DV : d_v;
+  p.ncta = num_sms_cached();
+  if (p.ncta > 1024) p.ncta = 1024;  // the work list keeps one counter per CTA in shared memory
+  const long long groups = (long long)Hkv * p.parts * ((long long)max_rows / p.rows_per_tile + B);
+  p.max_items = groups + p.ncta;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -776,11 +862,13 @@ Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_split
     return o;
   };
   p.off_items = take(sizeof(AttnItem) * (size_t)p.max_items);
-  p.off_nitems = take(sizeof(int));
-  p.off_nsplit = take(sizeof(int) * (size_t)B);
-  p.off_o = take(sizeof(float) * (size_t)max_splits * max_rows * Hq * d_v);
-  p.off_lse = take(sizeof(float) * (size_t)max_splits * max_rows * Hq);
+  p.off_begin = take(sizeof(int) * (size_t)(p.ncta + 1));
+  p.off_groups = take(sizeof(SplitGroup) * (size_t)groups);
+  p.off_ngroups = take(sizeof(int));
+  p.off_o = take(sizeof(float) * (size_t)p.max_items * kRows * p.d_part);
+  p.off_lse = take(sizeof(float) * (size_t)p.max_items * kRows);
   p.bytes = off;
+  (void)max_splits;
   return p;
 }
 
@@ -791,63 +879,64 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
            void* ws, const Plan& pl, cudaStream_t stream) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   AttnItem* items = reinterpret_cast<AttnItem*>(w + pl.off_items);
-  int* n_items = reinterpret_cast<int*>(w + pl.off_nitems);
-  int* nsplit = reinterpret_cast<int*>(w + pl.off_nsplit);
+  int* item_begin = reinterpret_cast<int*>(w + pl.off_begin);
+  SplitGroup* groups = reinterpret_cast<SplitGroup*>(w + pl.off_groups);
+  int* n_groups = reinterpret_cast<int*>(w + pl.off_ngroups);
   float* ws_o = reinterpret_cast<float*>(w + pl.off_o);
   float* ws_lse = reinterpret_cast<float*>(w + pl.off_lse);
   unsigned int* err = device_error_word();
-  const int sms = num_sms_cached();
-  const int target = sms * kItemsPerSm;
+  const int ncta = pl.ncta;
   const int max_items = pl.max_items > 0x7fffffff ? 0x7fffffff : (int)pl.max_items;
+  const int splits = max_splits < 2 ? 2 : (max_splits > 32 ? 32 : max_splits);
 
-  worklist_kernel<<<1, 1024, 0, stream>>>(ctx_len, cu_seqlens, B, Hkv, pl.parts, pl.rows_per_tile,
-                                           pl.nk, max_splits, target, max_items, items, n_items,
-                                           nsplit, err);
+  worklist_kernel<<<1, 1024, 0, stream>>>(ctx_len, cu_seqlens, B, max_rows, Hkv, pl.parts,
+                                           pl.rows_per_tile,
+                                           pl.nk, ncta, splits, max_items, items, item_begin, groups,
+                                           n_groups, err);
   DSPARK_LAUNCH_CHECK();
 
-  Params prm;
-  prm.q = static_cast<const __nv_bfloat16*>(q);
-  prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
-  prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
-  prm.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
-  prm.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
-  prm.page_table = page_table;
-  prm.ctx_len = ctx_len;
-  prm.cu_seqlens = cu_seqlens;
-  prm.items = items;
-  prm.n_items = n_items;
-  prm.out = out;
-  prm.lse = lse;
-  prm.ws_o = ws_o;
-  prm.ws_lse = ws_lse;
-  prm.err = err;
-  prm.max_pages = max_pages;
-  prm.B = B;
-  prm.Hq = Hq;
-  prm.Hkv = Hkv;
-  prm.page_size = page_size;
-  prm.log2_page = 0;
-  while ((1 << prm.log2_page) < page_size) ++prm.log2_page;
-  prm.max_rows = max_rows;
-  prm.d_v_total = d_v;
-  prm.n_pages = n_pages;
-  prm.scale_log2 = scale * 1.4426950408889634f;
-
   if (pl.mla) {
+    Params prm;
+    prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    prm.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+    prm.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+    prm.page_table = page_table;
+    prm.ctx_len = ctx_len;
+    prm.cu_seqlens = cu_seqlens;
+    prm.items = items;
+    prm.item_begin = item_begin;
+    prm.out = out;
+    prm.lse = lse;
+    prm.ws_o = ws_o;
+    prm.ws_lse = ws_lse;
+    prm.err = err;
+    prm.max_pages = max_pages;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.page_size = page_size;
+    prm.log2_page = 0;
+    while ((1 << prm.log2_page) < page_size) ++prm.log2_page;
+    prm.max_rows = max_rows;
+    prm.d_v_total = d_v;
+    prm.n_pages = n_pages;
+    prm.scale_log2 = scale * 1.4426950408889634f;
     if (!configure_smem<CfgMLA>()) return DSPARK_ECUDA;
-    verify_attn_kernel<CfgMLA><<<sms, kThreads, CfgMLA::SMEM_BYTES, stream>>>(prm);
+    verify_attn_kernel<CfgMLA><<<ncta, kThreads, CfgMLA::SMEM_BYTES, stream>>>(prm);
     DSPARK_LAUNCH_CHECK();
   } else {
     const int rc = gqa::launch_kernel(pl.nt, q, k_new, v_new, k_cache, v_cache, n_pages, page_table,
                                       max_pages, ctx_len, cu_seqlens, B, max_rows, Hq, Hkv,
-                                      page_size, scale, items, n_items, out, lse, ws_o, ws_lse,
+                                      page_size, scale, items, item_begin, out, lse, ws_o, ws_lse,
                                       stream);
     if (rc != DSPARK_OK) return rc;
   }
-  const long long warps = (long long)max_rows * Hq;
-  const int blocks = (int)((warps * 32 + 255) / 256);
-  combine_kernel<<<blocks, 256, 0, stream>>>(cu_seqlens, B, Hq, d_v, nsplit, ws_o, ws_lse, max_rows,
-                                             out, lse);
+  const int G = pl.mla ? Hq : Hq / Hkv;
+  combine_kernel<<<ncta * 2, 256, 0, stream>>>(cu_seqlens, groups, n_groups, item_begin, G, Hq,
+                                               kRows, pl.d_part, d_v, ws_o, ws_lse, out, lse,
+                                               pl.mla ? 1 : 0);
   DSPARK_LAUNCH_CHECK();
   return DSPARK_OK;
 }

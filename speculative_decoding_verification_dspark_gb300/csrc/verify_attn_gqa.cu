@@ -204,7 +204,7 @@ struct Params {
   const int32_t* ctx_len;
   const int32_t* cu_seqlens;
   const AttnItem* items;
-  const int* n_items;
+  const int* item_begin;  // [gridDim.x + 1]: CTA c runs items [item_begin[c], item_begin[c+1])
   float* out;
   float* lse;
   float* ws_o;
@@ -228,7 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_mref = reinterpret_cast<float*>(bp + C::OFF_REF);       // [4][NT]
   float* s_alpha = s_mref + 4 * NT;                                 // [4][NT]
   float* s_lsum = reinterpret_cast<float*>(bp + C::OFF_LS);        // [4][NT]
-  float* s_ltot = s_lsum + 4 * NT;                                  // [NT]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + C::OFF_MISC);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bp + C::OFF_MISC + 16);
   const Ctx cx{abort_flag, prm.err};
@@ -263,7 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_items = *prm.n_items;
+  const int it_begin = prm.item_begin[blockIdx.x];
+  const int it_end = prm.item_begin[blockIdx.x + 1];
   const int G = prm.Hq / prm.Hkv;
   const int P = prm.page_size;
   const int lp = prm.log2_page;
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t box_bytes = box_rows * 128;
     int g = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int it = it_begin; it < it_end && ok; ++it) {
       const AttnItem item = prm.items[it];
       const int r = item.r;
       const int ctx = prm.ctx_len[r];
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         last_pv = gp;
         return true;
       };
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n_it) {
+      for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
         const AttnItem item = prm.items[it];
         if (!wait_bar(L.q_full(), n_it & 1, cx)) { ok = false; break; }
         const int ntiles = item.te - item.tb;
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* my_alpha = s_alpha + sw * NT;
     int g = 0, n_it = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n_it) {
+    for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
       const AttnItem item = prm.items[it];
       const int r = item.r;
       const int ctx = prm.ctx_len[r];
@@ -596,39 +596,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(L.p_empty(gl % C::P_BUFS), (gl / C::P_BUFS) & 1, cx)) { ok = false; break; }
         tc_fence_after();
         const bool split = item.nsplit > 1;
-        // lse for rows lane + 32*gi (warp 0 of the group writes it)
-        if (sw == 0) {
+        // Row n = gi*32 + lane: 1/l and the destination row (in units of kD floats) are
+        // computed once per row, lane-distributed, and broadcast in the store loop.
+        float inv_l[C::G32];
+        int dst_row[C::G32];
 #pragma unroll
-          for (int gi = 0; gi < C::G32; ++gi) {
-            const int n = gi * 32 + lane;
-            if (n < nq) {
-              const float lt = lsum[n] + lsum[NT + n] + lsum[2 * NT + n] + lsum[3 * NT + n];
-              const int row_g = c0 + item.i0 + n / G;
-              const int head = item.kvh * G + n % G;
+        for (int gi = 0; gi < C::G32; ++gi) {
+          const int n = gi * 32 + lane;
+          inv_l[gi] = 0.f;
+          dst_row[gi] = 0;
+          if (gi < ng && n < nq) {
+            const float lt = lsum[n] + lsum[NT + n] + lsum[2 * NT + n] + lsum[3 * NT + n];
+            const int row_g = c0 + item.i0 + n / G;
+            const int head = item.kvh * G + n % G;
+            inv_l[gi] = lt > 0.f ? 1.f / lt : 0.f;
+            dst_row[gi] = split ? it * kKT + n : row_g * prm.Hq + head;
+            if (sw == 0) {  // warp 0 of the group writes the lse
               const float lse_v = (mref[gi] + log2f(lt)) * 0.69314718055994530942f;
               if (split)
-                prm.ws_lse[((long long)item.split * prm.max_rows + row_g) * prm.Hq + head] = lse_v;
+                prm.ws_lse[(long long)it * kKT + n] = lse_v;  // this piece's slot
               else
                 prm.lse[(long long)row_g * prm.Hq + head] = lse_v;
             }
           }
         }
-#pragma unroll 1
-        for (int c = 0; c < NT / 32; ++c) {
+        float* const obase = split ? prm.ws_o : prm.out;
+#pragma unroll
+        for (int c = 0; c < C::G32; ++c) {
+          if (c >= ng) break;
           float o[32];
           tmem_ld32(t_lane + C::TMEM_O + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            const int n = c * 32 + k;
-            if (n < nq) {
-              const float lt = lsum[n] + lsum[NT + n] + lsum[2 * NT + n] + lsum[3 * NT + n];
-              const int row_g = c0 + item.i0 + n / G;
-              const int head = item.kvh * G + n % G;
-              float* dst = split ? prm.ws_o + (((long long)item.split * prm.max_rows + row_g) * prm.Hq + head) * kD
-                                 : prm.out + ((long long)row_g * prm.Hq + head) * kD;
-              dst[kl] = lt > 0.f ? o[k] / lt : 0.f;
-            }
+            const float il = __shfl_sync(0xffffffffu, inv_l[c], k);
+            const int dr = __shfl_sync(0xffffffffu, dst_row[c], k);
+            if (c * 32 + k < nq) obase[(long long)dr * kD + kl] = o[k] * il;
           }
         }
         tc_fence_before();
@@ -705,8 +708,9 @@ int query_tile(int Hq, int Hkv, int max_block_rows) {
 int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, const void* k_cache,
                   const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
                   const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq,
-                  int Hkv, int page_size, float scale, const AttnItem* items, const int* n_items,
-                  float* out, float* lse, float* ws_o, float* ws_lse, cudaStream_t stream) {
+                  int Hkv, int page_size, float scale, const AttnItem* items,
+                  const int* item_begin, float* out, float* lse, float* ws_o, float* ws_lse,
+                  cudaStream_t stream) {
   Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
@@ -717,7 +721,7 @@ int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, c
   prm.ctx_len = ctx_len;
   prm.cu_seqlens = cu_seqlens;
   prm.items = items;
-  prm.n_items = n_items;
+  prm.item_begin = item_begin;
   prm.out = out;
   prm.lse = lse;
   prm.ws_o = ws_o;
