@@ -158,8 +158,11 @@ int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* a
  *   lse         fp32 [max_rows, Hq]       out, natural log
  *   workspace   >= dspark_verify_attn_workspace_size(...) bytes, 256-B aligned
  * page_size must be a power of two >= 16.  All base pointers 16-byte aligned.
- * Long contexts are split across CTAs (at most max_splits pieces per request,
- * head and row tile) and merged by a log-sum-exp combine.  max_block_rows is a
+ * Work is divided stream-K style: the key tiles of all (request, row tile, KV
+ * head) groups are cut into equal per-CTA ranges; a group cut by a range
+ * boundary (into at most max_splits pieces, 2..32) is merged by a log-sum-exp
+ * combine.  If cu_seqlens[B] > max_rows the device sets
+ * DSPARK_DEVERR_ROWS_OVERFLOW and nothing is computed.  max_block_rows is a
  * hint: the largest row count of one request's segment (gamma + 1), used to size
  * the query tile of the GQA kernel (<= 0: unknown); any segment length is
  * handled correctly whatever its value.
@@ -192,6 +195,8 @@ int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, cons
  *              exists for the position, NaN elsewhere
  *   fallback   int32 [B] out (nullable): 1 if an all-zero residual forced the
  *              draw from p_target
+ * If cu_seqlens[B] > max_rows the device sets DSPARK_DEVERR_ROWS_OVERFLOW and no
+ * output is written.
  * Test: accept d_j iff fp32(u_j * p_d(d_j)) <= p_t(d_j).  Draws: argmax over v of
  * w_v / e_v in fp32 (w = max(0, p_t - p_d) after a rejection, p_t for the bonus),
  * lowest index on ties.
@@ -215,16 +220,21 @@ int dspark_accept(const void* p_target, const void* p_draft, int pdt, int V,
  * ctx_len[r] += L_r + 1; anchor[r] = out_tok[r]; committed[r] = d_1..d_L, out_tok
  * (-1 beyond), n_committed[r] = L_r + 1.  Rejected rows are never written.
  *   row_bytes   bytes of one K row (GQA: Hkv*128*2, MLA: 576*2); V rows the same
+ *   max_rows    rows of k_new/v_new
  *   k_new/v_new [max_rows, row] packed block rows; v_new/v_cache NULL for MLA
  *   k_cache/v_cache [n_pages, page_size, row]
  *   page_table  int32 [B, max_pages] in/out; ctx_len, anchor int32 [B] in/out
  *   free_pages  int32 [n_free]; free_top int32 [1] in/out
  *   committed   int32 [B, gamma+1] out; n_committed int32 [B] out
  * If the free stack or a page-table row is too short the device sets
- * DSPARK_DEVERR_NO_FREE_PAGE / _PAGE_ROW_FULL and changes nothing.
+ * DSPARK_DEVERR_NO_FREE_PAGE / _PAGE_ROW_FULL, if cu_seqlens[B] > max_rows it sets
+ * DSPARK_DEVERR_ROWS_OVERFLOW, and if accept_len[r] is outside 0..gamma or keeps
+ * more rows than request r's packed segment holds it sets DSPARK_DEVERR_BAD_INPUT;
+ * in each of these cases it changes nothing.
  * ------------------------------------------------------------------------- */
 size_t dspark_compact_workspace_size(int B);
-int dspark_compact(const void* k_new, const void* v_new, int row_bytes, const int32_t* cu_seqlens,
+int dspark_compact(const void* k_new, const void* v_new, int row_bytes, int max_rows,
+                   const int32_t* cu_seqlens,
                    const int32_t* accept_len, const int32_t* out_tok, const int32_t* draft_tok,
                    int B, int gamma, int page_size, int max_pages, int n_pages,
                    int32_t* page_table, int32_t* ctx_len, int32_t* anchor,

@@ -48,7 +48,7 @@ _SIGNATURES = {
     "dspark_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                            _P, _Z, _P]),
     "dspark_compact_workspace_size": (_Z, [_I]),
-    "dspark_compact": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+    "dspark_compact": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                             _P, _P, _P, _P, _Z, _P]),
 }
 
@@ -178,7 +178,7 @@ def compact(k_new, v_new, cu_seqlens, accept_len, out_tok, draft_tok, page_table
     B, gamma = draft_tok.shape
     row_bytes = k_new[0].numel() * k_new.element_size()
     _check("dspark_compact", lib().dspark_compact(
-        _ptr(k_new), _ptr(v_new), row_bytes, _ptr(cu_seqlens), _ptr(accept_len), _ptr(out_tok),
+        _ptr(k_new), _ptr(v_new), row_bytes, k_new.shape[0], _ptr(cu_seqlens), _ptr(accept_len), _ptr(out_tok),
         _ptr(draft_tok), B, gamma, k_cache.shape[1], page_table.shape[1], k_cache.shape[0],
         _ptr(page_table), _ptr(ctx_len), _ptr(anchor), _ptr(free_pages), _ptr(free_top),
         _ptr(k_cache), _ptr(v_cache), _ptr(committed), _ptr(n_committed), _ptr(workspace),

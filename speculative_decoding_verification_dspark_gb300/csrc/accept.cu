@@ -91,11 +91,15 @@ __global__ void __launch_bounds__(128)
     accept_test_kernel(const T* __restrict__ p_t, const T* __restrict__ p_d, int V,
                        const int32_t* __restrict__ draft_tok, const float* __restrict__ uniforms,
                        const int32_t* __restrict__ windows, const int32_t* __restrict__ cu,
-                       int mode, int B, int gamma, int32_t* __restrict__ accept_len,
+                       int mode, int B, int gamma, int max_rows, int32_t* __restrict__ accept_len,
                        int32_t* __restrict__ cap_len, RowInfo* __restrict__ info,
                        unsigned int* __restrict__ err) {
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  if (cu[B] > max_rows) {  // packed rows beyond the caller's buffers: report, touch nothing
+    if (r == 0 && lane == 0) raise_error(err, DSPARK_DEVERR_ROWS_OVERFLOW);
+    return;
+  }
   if (r >= B) return;  // warp-uniform
   const int w = windows[r];
   const int base = cu[r];
@@ -134,12 +138,13 @@ template <class T>
 __global__ void __launch_bounds__(kVocabThreads)
     accept_vocab_kernel(const T* __restrict__ p_t, const T* __restrict__ p_d,
                         const float* __restrict__ exp_noise, int V, int n_chunks,
-                        const int32_t* __restrict__ cu, int B, int gamma,
+                        const int32_t* __restrict__ cu, int B, int gamma, int max_rows,
                         const RowInfo* __restrict__ info, Partial* __restrict__ part) {
   __shared__ double s_l1[kVocabThreads / 32];
   __shared__ float s_kr[kVocabThreads / 32], s_kt[kVocabThreads / 32];
   __shared__ int s_ir[kVocabThreads / 32], s_it[kVocabThreads / 32];
   const int M = cu[B];
+  if (M > max_rows) return;  // reported by the test kernel
   const long long n_items = (long long)M * n_chunks;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -220,13 +225,13 @@ __global__ void __launch_bounds__(kVocabThreads)
 }
 
 __global__ void __launch_bounds__(128)
-    accept_final_kernel(const int32_t* __restrict__ cu, int B, int gamma, int n_chunks,
-                        const RowInfo* __restrict__ info, const Partial* __restrict__ part,
-                        int32_t* __restrict__ out_tok, float* __restrict__ cstar,
-                        int32_t* __restrict__ fallback) {
+    accept_final_kernel(const int32_t* __restrict__ cu, int B, int gamma, int max_rows,
+                        int n_chunks, const RowInfo* __restrict__ info,
+                        const Partial* __restrict__ part, int32_t* __restrict__ out_tok,
+                        float* __restrict__ cstar, int32_t* __restrict__ fallback) {
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (r >= B) return;
+  if (r >= B || cu[B] > max_rows) return;
   const int base = cu[r];
   const int n_rows = cu[r + 1] - base;
   const RowInfo ri = info[r];
@@ -283,22 +288,25 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
     const float* t = static_cast<const float*>(p_t);
     const float* d = static_cast<const float*>(p_d);
     accept_test_kernel<float><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
-        t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, accept_len, cap_len, info, err);
+        t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, max_rows, accept_len, cap_len, info,
+        err);
     DSPARK_LAUNCH_CHECK();
     accept_vocab_kernel<float><<<(int)grid, kVocabThreads, 0, stream>>>(t, d, exp_noise, V, n_chunks,
-                                                                        cu, B, gamma, info, part);
+                                                                        cu, B, gamma, max_rows, info,
+                                                                        part);
   } else {
     const __nv_bfloat16* t = static_cast<const __nv_bfloat16*>(p_t);
     const __nv_bfloat16* d = static_cast<const __nv_bfloat16*>(p_d);
     accept_test_kernel<__nv_bfloat16><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
-        t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, accept_len, cap_len, info, err);
+        t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, max_rows, accept_len, cap_len, info,
+        err);
     DSPARK_LAUNCH_CHECK();
     accept_vocab_kernel<__nv_bfloat16><<<(int)grid, kVocabThreads, 0, stream>>>(
-        t, d, exp_noise, V, n_chunks, cu, B, gamma, info, part);
+        t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows, info, part);
   }
   DSPARK_LAUNCH_CHECK();
-  accept_final_kernel<<<ceil_div(B * 32, 128), 128, 0, stream>>>(cu, B, gamma, n_chunks, info, part,
-                                                                 out_tok, cstar, fallback);
+  accept_final_kernel<<<ceil_div(B * 32, 128), 128, 0, stream>>>(cu, B, gamma, max_rows, n_chunks,
+                                                                 info, part, out_tok, cstar, fallback);
   DSPARK_LAUNCH_CHECK();
   return DSPARK_OK;
 }

@@ -220,7 +220,8 @@ size_t dspark_compact_workspace_size(int B) {
   return compact_workspace(B);
 }
 
-int dspark_compact(const void* k_new, const void* v_new, int row_bytes, const int32_t* cu_seqlens,
+int dspark_compact(const void* k_new, const void* v_new, int row_bytes, int max_rows,
+                   const int32_t* cu_seqlens,
                    const int32_t* accept_len, const int32_t* out_tok, const int32_t* draft_tok,
                    int B, int gamma, int page_size, int max_pages, int n_pages,
                    int32_t* page_table, int32_t* ctx_len, int32_t* anchor,
@@ -232,6 +233,7 @@ int dspark_compact(const void* k_new, const void* v_new, int row_bytes, const in
         DSPARK_EINVAL);
   CHECK((v_new == nullptr) == (v_cache == nullptr), DSPARK_EINVAL);
   CHECK(row_bytes >= 16 && row_bytes % 16 == 0, DSPARK_EINVAL);
+  CHECK(max_rows >= 1, DSPARK_EINVAL);
   CHECK(aligned16(k_new) && aligned16(k_cache) && (!v_new || (aligned16(v_new) && aligned16(v_cache))),
         DSPARK_EINVAL);
   CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
@@ -240,7 +242,7 @@ int dspark_compact(const void* k_new, const void* v_new, int row_bytes, const in
   int rc = device_ok();
   if (rc != DSPARK_OK) return rc;
   CHECK(ws_bytes >= compact_workspace(B), DSPARK_ENOSPACE);
-  return launch_compact(k_new, v_new, row_bytes, cu_seqlens, accept_len, out_tok, draft_tok, B,
+  return launch_compact(k_new, v_new, row_bytes, max_rows, cu_seqlens, accept_len, out_tok, draft_tok, B,
                         gamma, page_size, max_pages, n_pages, page_table, ctx_len, anchor,
                         free_pages, free_top, k_cache, v_cache, committed, n_committed, workspace,
                         static_cast<cudaStream_t>(stream));

@@ -39,7 +39,8 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 }  // namespace
 
 __global__ void __launch_bounds__(1024)
-    compact_alloc_kernel(const int32_t* __restrict__ accept_len, const int32_t* __restrict__ out_tok,
+    compact_alloc_kernel(const int32_t* __restrict__ cu, int max_rows,
+                         const int32_t* __restrict__ accept_len, const int32_t* __restrict__ out_tok,
                          const int32_t* __restrict__ draft_tok, int B, int gamma, int page_size,
                          int max_pages, int n_pages, int32_t* __restrict__ page_table,
                          int32_t* __restrict__ ctx_len, int32_t* __restrict__ anchor,
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(1024)
   const int tid = threadIdx.x;
   if (tid == 0) {
     cws->ok = 0;
-    s_flags = 0;
+    s_flags = cu[B] > max_rows ? DSPARK_DEVERR_ROWS_OVERFLOW : 0;
     s_top = *free_top;
   }
   __syncthreads();
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(1024)
       L = L < 0 ? 0 : gamma;
     }
     keep = L + 1;
+    if (keep > cu[tid + 1] - cu[tid]) atomicOr(&s_flags, DSPARK_DEVERR_BAD_INPUT);  // unverified rows
     c0 = ctx_len[tid];
     have = ceil_div(c0, page_size);
     need = ceil_div(c0 + keep, page_size);
@@ -145,7 +147,8 @@ __global__ void __launch_bounds__(128)
 
 size_t compact_workspace(int B) { return sizeof(CompactWs) + (((size_t)B * sizeof(int) + 255) & ~size_t(255)); }
 
-int launch_compact(const void* k_new, const void* v_new, int row_bytes, const int32_t* cu,
+int launch_compact(const void* k_new, const void* v_new, int row_bytes, int max_rows,
+                   const int32_t* cu,
                    const int32_t* accept_len, const int32_t* out_tok, const int32_t* draft_tok,
                    int B, int gamma, int page_size, int max_pages, int n_pages, int32_t* page_table,
                    int32_t* ctx_len, int32_t* anchor, const int32_t* free_pages, int32_t* free_top,
@@ -153,7 +156,8 @@ int launch_compact(const void* k_new, const void* v_new, int row_bytes, const in
                    cudaStream_t stream) {
   CompactWs* cws = static_cast<CompactWs*>(ws);
   int* old_ctx = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + sizeof(CompactWs));
-  compact_alloc_kernel<<<1, 1024, 0, stream>>>(accept_len, out_tok, draft_tok, B, gamma, page_size,
+  compact_alloc_kernel<<<1, 1024, 0, stream>>>(cu, max_rows, accept_len, out_tok, draft_tok, B, gamma,
+                                               page_size,
                                                max_pages, n_pages, page_table, ctx_len, anchor,
                                                free_pages, free_top, committed, n_committed, cws,
                                                old_ctx, device_error_word());

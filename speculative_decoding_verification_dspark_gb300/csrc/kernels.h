@@ -25,7 +25,8 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
                   cudaStream_t stream);
 
 size_t compact_workspace(int B);
-int launch_compact(const void* k_new, const void* v_new, int row_bytes, const int32_t* cu,
+int launch_compact(const void* k_new, const void* v_new, int row_bytes, int max_rows,
+                   const int32_t* cu,
                    const int32_t* accept_len, const int32_t* out_tok, const int32_t* draft_tok,
                    int B, int gamma, int page_size, int max_pages, int n_pages, int32_t* page_table,
                    int32_t* ctx_len, int32_t* anchor, const int32_t* free_pages, int32_t* free_top,

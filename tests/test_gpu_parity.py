@@ -340,3 +340,19 @@ def test_rows_overflow_is_reported():
     step.schedule(d, O.STATIC)
     step.pack(d, O.STATIC)
     assert dspark.read_device_error() & 0x1
+    # the later stages see packed rows beyond their 4-row buffers: each one reports
+    # the overflow and reads or writes no row (the state is left as it was)
+    assert int(step.cu_seqlens[-1]) > 4
+    dev = torch.device("cuda")
+    d["q"] = torch.zeros(4, wl.Hq, wl.d_qk, dtype=torch.bfloat16, device=dev)
+    d["k_new"] = torch.zeros(4, wl.Hkv, wl.d_qk, dtype=torch.bfloat16, device=dev)
+    d["v_new"] = torch.zeros(4, wl.Hkv, wl.d_v, dtype=torch.bfloat16, device=dev)
+    d["p_target"] = torch.zeros(4, wl.vocab, dtype=torch.float32, device=dev)
+    before = harness.snapshot_state(d)
+    for run in (lambda: step.attention(d), lambda: step.accept(d, O.STATIC),
+                lambda: step.compact(d)):
+        run()
+        assert dspark.read_device_error() & 0x1
+    for k, v in before.items():
+        if isinstance(v, torch.Tensor):
+            assert torch.equal(d[k], v), k
