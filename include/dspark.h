@@ -210,6 +210,38 @@ int dspark_accept(const void* p_target, const void* p_draft, int pdt, int V,
                   void* stream);
 
 /* ---------------------------------------------------------------------------
+ * dspark_accept_noalloc -- dspark_accept without a caller-provided workspace.
+ *
+ * The paper has no counterpart: this is a library convenience.  It is meant for
+ * callers that cannot hand over device memory of their own -- a plain C host that
+ * links only this library and owns no CUDA allocator, or a serving engine whose
+ * device memory pool is sized and frozen before serving starts, so that no
+ * allocation may happen while it runs.  The call allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library routine); its scratch is one fixed array of
+ * DSPARK_ACCEPT_NOALLOC_SCRATCH_BYTES compiled into the library, one per device.
+ *
+ * Arguments, outputs, error handling and results are those of dspark_accept.
+ * Limit: the call returns DSPARK_ENOSPACE, launching nothing, when
+ * dspark_accept_workspace_size(B, gamma, max_rows, V) exceeds the scratch size
+ * (about max_rows * ceil(V / 8192) * 32 bytes; the 8 MiB hold max_rows = 8192,
+ * i.e. B = 256 requests of 32 rows, at V = 151936).  No part of the scratch needs to start at zero: every entry read
+ * is written earlier in the same call.
+ * The first call on a device looks up the scratch address with that device
+ * current (DSPARK_ECUDA if the lookup fails); make that first call before any
+ * stream capture begins.  All calls on one device share the one array, so two
+ * calls that may run at the same time (on different streams, or from host threads
+ * without ordering between them) race on it and give undefined results: order
+ * them on one stream.
+ * ------------------------------------------------------------------------- */
+#define DSPARK_ACCEPT_NOALLOC_SCRATCH_BYTES (8u << 20)
+int dspark_accept_noalloc(const void* p_target, const void* p_draft, int pdt, int V,
+                          const int32_t* draft_tok, const float* uniforms,
+                          const float* exp_noise, const int32_t* windows,
+                          const int32_t* cu_seqlens, int mode, int B, int gamma, int max_rows,
+                          int32_t* accept_len, int32_t* cap_len, int32_t* out_tok, float* cstar,
+                          int32_t* fallback, void* stream);
+
+/* ---------------------------------------------------------------------------
  * dspark_compact -- commit the step ([lesson] "Zero-overhead scheduling 与
  * kernel": compact scatter, device-resident page table).
  *

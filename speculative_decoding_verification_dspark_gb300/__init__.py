@@ -15,7 +15,7 @@ import torch
 
 __all__ = [
     "COMPACT", "STATIC", "CAP_ACCEPT", "F32", "BF16", "DSparkError", "lib", "load",
-    "schedule", "pack", "verify_attn", "accept", "compact", "read_device_error",
+    "schedule", "pack", "verify_attn", "accept", "accept_noalloc", "compact", "read_device_error",
     "verify_attn_workspace_size", "accept_workspace_size", "compact_workspace_size",
     "VerifyStep", "DEVERR",
 ]
@@ -47,6 +47,8 @@ _SIGNATURES = {
     "dspark_accept_workspace_size": (_Z, [_I, _I, _I, _I]),
     "dspark_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                            _P, _Z, _P]),
+    "dspark_accept_noalloc": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P,
+                                   _P, _P, _P]),
     "dspark_compact_workspace_size": (_Z, [_I]),
     "dspark_compact": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                             _P, _P, _P, _P, _Z, _P]),
@@ -167,6 +169,17 @@ def accept(p_target, p_draft, draft_tok, uniforms, exp_noise, windows, cu_seqlen
         _ptr(windows), _ptr(cu_seqlens), int(mode), B, gamma, p_target.shape[0], _ptr(accept_len),
         _ptr(cap_len), _ptr(out_tok), _ptr(cstar), _ptr(fallback), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def accept_noalloc(p_target, p_draft, draft_tok, uniforms, exp_noise, windows, cu_seqlens, mode,
+                   accept_len, cap_len, out_tok, cstar, fallback, stream=None):
+    """``accept`` with the library's fixed scratch instead of a workspace argument."""
+    B, gamma, V = p_draft.shape
+    pdt = BF16 if p_target.dtype == torch.bfloat16 else F32
+    _check("dspark_accept_noalloc", lib().dspark_accept_noalloc(
+        _ptr(p_target), _ptr(p_draft), pdt, V, _ptr(draft_tok), _ptr(uniforms), _ptr(exp_noise),
+        _ptr(windows), _ptr(cu_seqlens), int(mode), B, gamma, p_target.shape[0], _ptr(accept_len),
+        _ptr(cap_len), _ptr(out_tok), _ptr(cstar), _ptr(fallback), _stream(stream)))
 
 
 def compact_workspace_size(B) -> int:

@@ -24,6 +24,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -267,6 +269,23 @@ size_t accept_workspace(int B, int max_rows, int V) {
   const int n_chunks = ceil_div(V, kChunk);
   size_t a = ((size_t)B * sizeof(RowInfo) + 255) & ~size_t(255);
   return a + (size_t)max_rows * n_chunks * sizeof(Partial);
+}
+
+// Scratch of dspark_accept_noalloc: a fixed array in the library image, one per
+// device.  Its address is looked up once per device, with that device current.
+static __device__ __align__(256) unsigned char g_accept_scratch[DSPARK_ACCEPT_NOALLOC_SCRATCH_BYTES];
+
+void* accept_fixed_scratch() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<void*> addr[kMaxDevices];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  void* p = addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess) return nullptr;
+    addr[dev].store(p, std::memory_order_release);
+  }
+  return p;
 }
 
 int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_t* draft_tok,

@@ -215,6 +215,31 @@ int dspark_accept(const void* p_target, const void* p_draft, int pdt, int V,
                        fallback, workspace, static_cast<cudaStream_t>(stream));
 }
 
+int dspark_accept_noalloc(const void* p_target, const void* p_draft, int pdt, int V,
+                          const int32_t* draft_tok, const float* uniforms,
+                          const float* exp_noise, const int32_t* windows,
+                          const int32_t* cu_seqlens, int mode, int B, int gamma, int max_rows,
+                          int32_t* accept_len, int32_t* cap_len, int32_t* out_tok, float* cstar,
+                          int32_t* fallback, void* stream) {
+  CHECK(p_target && p_draft && draft_tok && uniforms && exp_noise && windows && cu_seqlens &&
+            accept_len && cap_len && out_tok && cstar,
+        DSPARK_EINVAL);
+  CHECK(pdt == DSPARK_F32 || pdt == DSPARK_BF16, DSPARK_EINVAL);
+  CHECK(V >= 8 && V % 8 == 0, DSPARK_EUNSUPPORTED);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
+  CHECK(mode >= DSPARK_COMPACT && mode <= DSPARK_CAP_ACCEPT, DSPARK_EINVAL);
+  CHECK(max_rows >= 1, DSPARK_EINVAL);
+  CHECK(aligned16(p_target) && aligned16(p_draft) && aligned16(exp_noise), DSPARK_EINVAL);
+  CHECK(accept_workspace(B, max_rows, V) <= DSPARK_ACCEPT_NOALLOC_SCRATCH_BYTES, DSPARK_ENOSPACE);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  void* scratch = accept_fixed_scratch();
+  CHECK(scratch != nullptr, DSPARK_ECUDA);
+  return launch_accept(p_target, p_draft, pdt, V, draft_tok, uniforms, exp_noise, windows,
+                       cu_seqlens, mode, B, gamma, max_rows, accept_len, cap_len, out_tok, cstar,
+                       fallback, scratch, static_cast<cudaStream_t>(stream));
+}
+
 size_t dspark_compact_workspace_size(int B) {
   if (B < 1) return 0;
   return compact_workspace(B);

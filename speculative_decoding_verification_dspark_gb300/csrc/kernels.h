@@ -24,6 +24,10 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
                   int32_t* cap_len, int32_t* out_tok, float* cstar, int32_t* fallback, void* ws,
                   cudaStream_t stream);
 
+// Address of the fixed scratch array on the current device (looked up once per
+// device); nullptr if the lookup fails.
+void* accept_fixed_scratch();
+
 size_t compact_workspace(int B);
 int launch_compact(const void* k_new, const void* v_new, int row_bytes, int max_rows,
                    const int32_t* cu,

@@ -54,6 +54,12 @@ def test_host_validation_without_device(lib):
     fake = ctypes.c_void_p(4096)
     assert lib.dspark_accept(fake, fake, 0, 1001, fake, fake, fake, fake, fake, 0, 4, 6, 8, fake,
                              fake, fake, fake, nul, fake, 1 << 20, nul) == -2
+    # the fixed-scratch variant: a problem larger than its scratch is refused (ENOSPACE)
+    # on the host, and a small one passes validation up to the device check
+    assert lib.dspark_accept_noalloc(fake, fake, 0, 151936, fake, fake, fake, fake, fake, 0, 4, 6,
+                                     16384, fake, fake, fake, fake, nul, nul) == -4
+    assert lib.dspark_accept_noalloc(fake, fake, 0, 1001, fake, fake, fake, fake, fake, 0, 4, 6, 8,
+                                     fake, fake, fake, fake, nul, nul) == -2
 
 
 def test_workspace_sizes_are_host_computable(lib):
