@@ -46,8 +46,8 @@ int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, c
                   const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
                   const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq,
                   int Hkv, int page_size, float scale, const AttnItem* items,
-                  const int* item_begin, float* out, float* lse, float* ws_o, float* ws_lse,
-                  cudaStream_t stream);
+                  const int* item_begin, int grid, float* out, float* lse, float* ws_o,
+                  float* ws_lse, cudaStream_t stream);
 constexpr int kKeyTile = 128;
 }  // namespace gqa
 

@@ -929,8 +929,8 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
   } else {
     const int rc = gqa::launch_kernel(pl.nt, q, k_new, v_new, k_cache, v_cache, n_pages, page_table,
                                       max_pages, ctx_len, cu_seqlens, B, max_rows, Hq, Hkv,
-                                      page_size, scale, items, item_begin, out, lse, ws_o, ws_lse,
-                                      stream);
+                                      page_size, scale, items, item_begin, ncta, out, lse, ws_o,
+                                      ws_lse, stream);
     if (rc != DSPARK_OK) return rc;
   }
   const int G = pl.mla ? Hq : Hq / Hkv;

@@ -16,12 +16,20 @@
 //   S^T [128 keys x NT rows] = K_tile [128 x 128] . Q^T           (tcgen05, TMEM)
 //   O^T [128 d    x NT rows] += V_tile^T . P^T                    (tcgen05, TMEM)
 //
-// Warp roles (one CTA per SM, persistent over the work list):
-//   warps 0-1  producers, K and V streams with separate two-slot rings: TMA tiled
-//              loads of 16-token pages (128-byte swizzle, no multicast); the
-//              partial last page and the block's own rows by plain loads into the
-//              same layout (warp 2 idles)
-//   warp 3     MMA issuer (one lane) + TMEM owner
+// Warp roles (one CTA per SM, persistent over its stream-K range of the work list):
+//   warp 0     K producer: TMA tiled loads (128-byte swizzle, no multicast) of the
+//              context pages holding at least one visible key and of the block's
+//              own rows; keys past the visible range are left as they are (the
+//              softmax masks them by index)
+//   warp 1     V producer: TMA for every full 16-key chunk; the one partial chunk
+//              of a tile by plain loads with zeros past the visible keys.  Chunks
+//              past the visible keys are neither loaded nor multiplied (PV skips
+//              them), so no stale value reaches O
+//   warp 2     Q loader: the next item's query tile into the second Q buffer
+//              while the current item runs
+//   warp 3     MMA issuer (one lane) + TMEM owner.  O^T is double-buffered in
+//              TMEM, so the next item's products start while the epilogue of the
+//              last one still reads its O^T
 //   warps 4-7  softmax: thread = key (TMEM lane).  Per tile: per-row max by a
 //              warp transpose-reduction and one cross-warp exchange through an
 //              mbarrier, lazy rescale of O^T when a row's max grows by > 2^8,
@@ -48,19 +56,23 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kKT = 128;              // keys per tile (MMA M)
 constexpr int kD = 128;               // head dim
 constexpr int kStages = 2;
-constexpr int kProducerWarps = 2;  // warp 0 streams K, warp 1 V; warp 2 has no role
+constexpr int kKWarp = 0;
+constexpr int kVWarp = 1;
+constexpr int kQWarp = 2;
 constexpr int kMmaWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kThreads = 8 * 32;
 constexpr int kTileHalf = kKT * 128;  // one 64-wide column block of a [128 x 128] bf16 tile
 constexpr int kKVBytes = 2 * kTileHalf;
 constexpr int kStageBytes = 2 * kKVBytes;  // K and V
+constexpr int kChunkRows = 16;             // V chunk = PV k-step; also the block-row box
 
 template <int NT_>
 struct Cfg {
   static constexpr int NT = NT_;                         // query rows (N)
   static constexpr int Q_CB = NT * 128;                  // one 64-wide column block of Q
   static constexpr int Q_BYTES = 2 * Q_CB;
+  static constexpr int Q_BUFS = NT <= 64 ? 2 : 1;
   static constexpr int P_ROW = NT <= 64 ? NT * 2 : 128;  // bytes per key row of one P block
   static constexpr int P_BLOCKS = NT <= 64 ? 1 : NT / 64;
   static constexpr int P_BYTES = kKT * NT * 2;
@@ -68,20 +80,20 @@ struct Cfg {
   static constexpr SwizzleMode P_SW = NT == 32 ? SW_64B : SW_128B;
   static constexpr int G32 = NT / 32;                    // 32-row groups
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_STAGE = OFF_Q + Q_BYTES;
+  static constexpr int OFF_STAGE = OFF_Q + Q_BUFS * Q_BYTES;
   static constexpr int OFF_P = OFF_STAGE + kStages * kStageBytes;
   static constexpr int OFF_RED = OFF_P + P_BUFS * P_BYTES;         // float wmax[2][4][NT]
   static constexpr int OFF_REF = OFF_RED + 2 * 4 * NT * 4;         // float mref[4][NT], alpha[4][NT]
-  static constexpr int OFF_LS = OFF_REF + 2 * 4 * NT * 4;          // float lsum[4][NT], ltot[NT]
-  static constexpr int OFF_BAR = OFF_LS + 5 * NT * 4;
-  // k_full[2], k_empty[2], s_full[2], s_free[2], p_full[PB], p_empty[PB], q_full, xw[2], ep[2],
-  // v_full[2], v_empty[2]
-  static constexpr int N_BARS = 8 + 2 * P_BUFS + 1 + 4 + 4;
+  static constexpr int OFF_LS = OFF_REF + 2 * 4 * NT * 4;          // float lsum[4][NT]
+  static constexpr int OFF_BAR = OFF_LS + 4 * NT * 4;
+  // k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], xw[2], ep[2],
+  // o_free[2], p_full[PB], p_empty[PB], q_full[QB], q_empty[QB]
+  static constexpr int N_BARS = 18 + 2 * P_BUFS + 2 * Q_BUFS;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
-  static constexpr int TMEM_S = 0;
-  static constexpr int TMEM_O = 2 * NT;
-  static constexpr int TMEM_COLS = 3 * NT <= 128 ? 128 : (3 * NT <= 256 ? 256 : 512);
+  static constexpr int TMEM_S = 0;          // S^T, two buffers of NT columns
+  static constexpr int TMEM_O = 2 * NT;     // O^T, two buffers of NT columns
+  static constexpr int TMEM_COLS = 4 * NT <= 128 ? 128 : (4 * NT <= 256 ? 256 : 512);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(NT == 32 || NT == 64 || NT == 128, "query tile");
 };
@@ -177,22 +189,33 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
 template <int NT>
 struct Layout {
   uint32_t base;
-  __device__ uint32_t q() const { return base + Cfg<NT>::OFF_Q; }
+  __device__ uint32_t q(int b) const { return base + Cfg<NT>::OFF_Q + b * Cfg<NT>::Q_BYTES; }
   __device__ uint32_t stage(int s) const { return base + Cfg<NT>::OFF_STAGE + s * kStageBytes; }
   __device__ uint32_t pbuf(int b) const { return base + Cfg<NT>::OFF_P + b * Cfg<NT>::P_BYTES; }
   __device__ uint32_t bar(int i) const { return base + Cfg<NT>::OFF_BAR + 8 * i; }
   __device__ uint32_t k_full(int s) const { return bar(s); }
   __device__ uint32_t k_empty(int s) const { return bar(2 + s); }
-  __device__ uint32_t s_full(int b) const { return bar(4 + b); }
-  __device__ uint32_t s_free(int b) const { return bar(6 + b); }
-  __device__ uint32_t p_full(int b) const { return bar(8 + b); }
-  __device__ uint32_t p_empty(int b) const { return bar(8 + Cfg<NT>::P_BUFS + b); }
-  __device__ uint32_t q_full() const { return bar(8 + 2 * Cfg<NT>::P_BUFS); }
-  __device__ uint32_t xw(int b) const { return bar(9 + 2 * Cfg<NT>::P_BUFS + b); }
-  __device__ uint32_t ep(int b) const { return bar(11 + 2 * Cfg<NT>::P_BUFS + b); }
-  __device__ uint32_t v_full(int s) const { return bar(13 + 2 * Cfg<NT>::P_BUFS + s); }
-  __device__ uint32_t v_empty(int s) const { return bar(15 + 2 * Cfg<NT>::P_BUFS + s); }
+  __device__ uint32_t v_full(int s) const { return bar(4 + s); }
+  __device__ uint32_t v_empty(int s) const { return bar(6 + s); }
+  __device__ uint32_t s_full(int b) const { return bar(8 + b); }
+  __device__ uint32_t s_free(int b) const { return bar(10 + b); }
+  __device__ uint32_t xw(int b) const { return bar(12 + b); }
+  __device__ uint32_t ep(int b) const { return bar(14 + b); }
+  __device__ uint32_t o_free(int b) const { return bar(16 + b); }
+  __device__ uint32_t p_full(int b) const { return bar(18 + b); }
+  __device__ uint32_t p_empty(int b) const { return bar(18 + Cfg<NT>::P_BUFS + b); }
+  __device__ uint32_t q_full(int b) const { return bar(18 + 2 * Cfg<NT>::P_BUFS + b); }
+  __device__ uint32_t q_empty(int b) const {
+    return bar(18 + 2 * Cfg<NT>::P_BUFS + Cfg<NT>::Q_BUFS + b);
+  }
 };
+
+// Keys of tile t of a request that a query row can see at all: the cache tile's
+// keys below ctx, or the block tile's rows below n_r.
+__device__ __forceinline__ int visible_keys(int t, int ct, int ctx, int n_r) {
+  const int v = t < ct ? ctx - t * kKT : n_r - (t - ct) * kKT;
+  return v < kKT ? v : kKT;
+}
 
 struct Params {
   const __nv_bfloat16* q;
@@ -217,7 +240,9 @@ struct Params {
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_attn_gqa_kernel(const __grid_constant__ CUtensorMap tm_k,
-                           const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ CUtensorMap tm_kn,
+                           const __grid_constant__ CUtensorMap tm_vn, const Params prm) {
   using C = Cfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -235,24 +260,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(L.k_full(s), 1);
-      mbar_init(L.k_empty(s), 1);
-      mbar_init(L.v_full(s), 1);
-      mbar_init(L.v_empty(s), 1);
-    }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(L.k_full(b), 1);
+      mbar_init(L.k_empty(b), 1);
+      mbar_init(L.v_full(b), 1);
+      mbar_init(L.v_empty(b), 1);
       mbar_init(L.s_full(b), 1);
       mbar_init(L.s_free(b), 4);
       mbar_init(L.xw(b), 4);
       mbar_init(L.ep(b), 4);
+      mbar_init(L.o_free(b), 4);
     }
     for (int b = 0; b < C::P_BUFS; ++b) {
       mbar_init(L.p_full(b), 4);
       mbar_init(L.p_empty(b), 1);
     }
-    mbar_init(L.q_full(), 4);
+    for (int b = 0; b < C::Q_BUFS; ++b) {
+      mbar_init(L.q_full(b), 1);
+      mbar_init(L.q_empty(b), 1);
+    }
     fence_mbar_init();
+  }
+  if (warp == kKWarp && lane == 0) {
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_kn);
+  }
+  if (warp == kVWarp && lane == 0) {
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_vn);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
@@ -268,19 +303,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int P = prm.page_size;
   const int lp = prm.log2_page;
 
-  if (warp < kProducerWarps) {
+  if (warp == kKWarp || warp == kVWarp) {
     // ------------------------------------------------------------- producers
-    // warp 0 streams K tiles, warp 1 V tiles, each through its own two-slot ring:
-    // a K slot is released as soon as QK^T of its tile completes, so the next K
-    // tiles (and with them QK^T and the softmax) run ahead of the V stream.
-    // Lane j of a warp holds page-table slot win_base + j of the current request.
-    const bool is_v = warp == 1;
-    const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
-    const __nv_bfloat16* cache = is_v ? prm.v_cache : prm.k_cache;
-    const __nv_bfloat16* fresh = is_v ? prm.v_new : prm.k_new;
-    const int box_rows = P < kKT ? P : kKT;
-    const int nbox = kKT / box_rows;
-    const uint32_t box_bytes = box_rows * 128;
+    // Each stream has its own two-slot ring: a K slot is released as soon as QK^T of
+    // its tile completes, so the next K tiles (and with them QK^T and the softmax)
+    // run ahead of the V stream.  Lane j holds page-table slot win_base + j of the
+    // current request.
+    const bool is_v = warp == kVWarp;
+    const CUtensorMap* tm_c = is_v ? &tm_v : &tm_k;
+    const CUtensorMap* tm_n = is_v ? &tm_vn : &tm_kn;
+    const __nv_bfloat16* cache = prm.v_cache;
+    const __nv_bfloat16* fresh = prm.v_new;
+    // K boxes follow the page (up to a tile); V boxes are 16-key chunks
+    const int box_rows = is_v ? kChunkRows : (P < kKT ? P : kKT);
     int g = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it) {
@@ -301,7 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         const uint32_t dst0 = L.stage(s) + (is_v ? kKVBytes : 0);
-        bool manual = false;
+        const int vis = visible_keys(t, ct, ctx, n_r);  // >= 1
+        // boxes copied whole by TMA: K every box with a visible key, V the full chunks;
+        // cache boxes are box_rows keys, block-row boxes kChunkRows rows
+        const int rows_box = t < ct ? box_rows : kChunkRows;
+        const int nb = is_v ? (vis >> 4) : ceil_div(vis, rows_box);
+        const int rem = is_v ? (vis & 15) : 0;            // V rows of the partial chunk
+        if (lane == 0 && nb > 0) mbar_expect_tx(full, nb * 2 * rows_box * 128);
+        __syncwarp();
         if (t < ct) {
           const int slot0 = (t * kKT) >> lp;
           const int nslot = ceil_div(kKT, P);
@@ -315,48 +357,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             win_page = pg;
           }
-          const int full_boxes = min(nbox, max(0, (ctx - t * kKT) / box_rows));
-          if (lane == 0 && full_boxes > 0) mbar_expect_tx(full, full_boxes * 2 * box_bytes);
-          __syncwarp();
-          // full boxes: lane = (box, column block), one copy each
-          for (int base_l = 0; base_l < 2 * nbox; base_l += 32) {
+          // lane = (box, column block), one copy each; every copied box starts at a
+          // visible key, so its page-table slot is a valid one
+          for (int base_l = 0; base_l < 2 * nb; base_l += 32) {
             const int o = base_l + lane;
             const int bx = o >> 1, cb = o & 1;
-            const int src_lane = bx < nbox ? (((t * kKT + bx * box_rows) >> lp) - win_base) & 31 : 0;
-            const int page = __shfl_sync(0xffffffffu, win_page, src_lane);  // all lanes, converged
-            if (bx < full_boxes)
-              tma_load_4d(dst0 + cb * kTileHalf + bx * box_rows * 128, tm, full, cb * 64, item.kvh,
-                          (t * kKT + bx * box_rows) & (P - 1), page);
-          }
-          // partial / empty boxes (last cache tile): plain loads, zeros past the context
-          for (int bx = full_boxes; bx < nbox; ++bx) {
-            manual = true;
             const int kg = t * kKT + bx * box_rows;
+            const int src_lane = bx < nb ? ((kg >> lp) - win_base) & 31 : 0;
+            const int page = __shfl_sync(0xffffffffu, win_page, src_lane);  // converged
+            if (bx < nb)
+              tma_load_4d(dst0 + cb * kTileHalf + bx * box_rows * 128, tm_c, full, cb * 64,
+                          item.kvh, kg & (P - 1), page);
+          }
+          if (rem > 0) {
+            // V: the partial chunk, all loads in flight at once, zeros past ctx
+            const int kg = t * kKT + nb * kChunkRows;
             const int page = __shfl_sync(0xffffffffu, win_page, ((kg >> lp) - win_base) & 31);
-            const int valid = (kg < ctx && page >= 0) ? ctx - kg : 0;
             const long long off =
-                ((long long)(valid > 0 ? page : 0) * P + (kg & (P - 1))) * rs + (long long)item.kvh * kD;
-            const int row0 = bx * box_rows;
-            for (int idx = lane; idx < box_rows * 16; idx += 32) {
-              const int rr = idx >> 4, q = idx & 15;
-              uint4 v = make_uint4(0, 0, 0, 0);
-              if (rr < valid) v = ldg_nc_v4(cache + off + rr * rs + q * 8);
-              st_shared_v4(dst0 + (q >> 3) * kTileHalf + sw128_off(row0 + rr, q & 7), v);
+                ((long long)(page >= 0 ? page : 0) * P + (kg & (P - 1))) * rs + (long long)item.kvh * kD;
+            uint4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int idx = i * 32 + lane, rr = idx >> 4, q = idx & 15;
+              v[i] = make_uint4(0, 0, 0, 0);
+              if (rr < rem && page >= 0) v[i] = ldg_nc_v4(cache + off + rr * rs + q * 8);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int idx = i * 32 + lane, rr = idx >> 4, q = idx & 15;
+              st_shared_v4(dst0 + (q >> 3) * kTileHalf + sw128_off(nb * kChunkRows + rr, q & 7), v[i]);
             }
           }
         } else {
-          // block tile: the request's own rows b0..b0+127, zeros past n_r
-          manual = true;
+          // block tile: the request's own rows b0.., 16-row boxes of the packed buffer
           const int b0 = (t - ct) * kKT;
-          const long long off = (long long)(c0 + b0) * rs + (long long)item.kvh * kD;
-          for (int idx = lane; idx < kKT * 16; idx += 32) {
-            const int rr = idx >> 4, q = idx & 15;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (b0 + rr < n_r) v = ldg_nc_v4(fresh + off + rr * rs + q * 8);
-            st_shared_v4(dst0 + (q >> 3) * kTileHalf + sw128_off(rr, q & 7), v);
+          if (lane < 2 * nb) {
+            const int bx = lane >> 1, cb = lane & 1;
+            tma_load_3d(dst0 + cb * kTileHalf + bx * kChunkRows * 128, tm_n, full, cb * 64, item.kvh,
+                        c0 + b0 + bx * kChunkRows);
+          }
+          if (rem > 0) {
+            const int row0 = nb * kChunkRows;
+            const long long off = (long long)(c0 + b0 + row0) * rs + (long long)item.kvh * kD;
+            uint4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int idx = i * 32 + lane, rr = idx >> 4, q = idx & 15;
+              v[i] = make_uint4(0, 0, 0, 0);
+              if (rr < rem) v[i] = ldg_nc_v4(fresh + off + rr * rs + q * 8);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int idx = i * 32 + lane, rr = idx >> 4, q = idx & 15;
+              st_shared_v4(dst0 + (q >> 3) * kTileHalf + sw128_off(row0 + rr, q & 7), v[i]);
+            }
           }
         }
-        if (manual) fence_proxy_async_smem();
+        if (rem > 0) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(full);
       }
@@ -366,6 +423,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int gg = first; gg < g; ++gg)
         drain_bar(is_v ? L.v_full(gg % kStages) : L.k_full(gg % kStages), (gg / kStages) & 1, prm.err);
     }
+  } else if (warp == kQWarp) {
+    // ------------------------------------------------------------- Q loader
+    // Query tile of item n: row n' = (block row n' / G, head kvh*G + n' % G), rows
+    // past the item's nq are zero.  Buffer n % Q_BUFS is refilled once QK^T of the
+    // item that used it is complete.
+    bool ok = true;
+    int n_it = 0;
+    for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
+      const AttnItem item = prm.items[it];
+      const int qb = n_it % C::Q_BUFS;
+      if (n_it >= C::Q_BUFS) {
+        ok = wait_warp(L.q_empty(qb), ((n_it / C::Q_BUFS) - 1) & 1, cx);
+        if (!ok) break;
+      }
+      const int nq = item.ni * G;
+      const long long row0 = prm.cu_seqlens[item.r] + item.i0;
+      const uint32_t qd = L.q(qb);
+      constexpr int kPer = NT * 16 / 32;   // 16-byte pieces per lane
+      constexpr int kBatch = kPer < 16 ? kPer : 16;
+#pragma unroll 1
+      for (int b0 = 0; b0 < kPer; b0 += kBatch) {
+        uint4 v[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int idx = (b0 + i) * 32 + lane, row = idx >> 4, q = idx & 15;
+          v[i] = make_uint4(0, 0, 0, 0);
+          if (row < nq)
+            v[i] = ldg_nc_v4(prm.q + ((row0 + row / G) * prm.Hq + item.kvh * G + row % G) * kD + q * 8);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int idx = (b0 + i) * 32 + lane, row = idx >> 4, q = idx & 15;
+          st_shared_v4(qd + (q >> 3) * C::Q_CB + sw128_off(row, q & 7), v[i]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(L.q_full(qb));
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -373,7 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(kD, NT, 1, 1);
       int g = 0, n_it = 0, last_pv = -1;
       bool ok = true;
-      auto issue_pv = [&](int gp, int local) -> bool {
+      // PV of tile gp (local index `local` in its item) into O^T buffer ob, over the
+      // 16-key chunks that hold visible keys only
+      auto issue_pv = [&](int gp, int local, int nch, int ob) -> bool {
         const int pb = gp % C::P_BUFS;
         if (!wait_bar(L.p_full(pb), (gp / C::P_BUFS) & 1, cx)) return false;
         tc_fence_after();
@@ -381,12 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(L.v_full(s), (gp / kStages) & 1, cx)) return false;
         tc_fence_after();
         const uint32_t vb = L.stage(s) + kKVBytes;
-#pragma unroll
-        for (int kk = 0; kk < kKT / 16; ++kk) {
+        const uint32_t d_o = tmem + C::TMEM_O + ob * NT;
+        for (int kk = 0; kk < nch; ++kk) {
           // A = V^T (M = d, MN-major), B = P^T (N = query rows, MN-major); K = 16 keys
           const uint64_t a = smem_desc(vb + kk * 2048, kTileHalf, 1024, SW_128B);
           const uint64_t b = smem_desc(L.pbuf(pb) + kk * 16 * C::P_ROW, kKT * 128, 8 * C::P_ROW, C::P_SW);
-          umma_bf16(tmem + C::TMEM_O, a, b, IDESC_PV, (local > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16(d_o, a, b, IDESC_PV, (local > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(L.p_empty(pb));
         umma_commit(L.v_empty(s));
@@ -395,8 +493,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
         const AttnItem item = prm.items[it];
-        if (!wait_bar(L.q_full(), n_it & 1, cx)) { ok = false; break; }
+        const int qb = n_it % C::Q_BUFS, ob = n_it & 1;
+        const int ctx = prm.ctx_len[item.r];
+        const int n_r = prm.cu_seqlens[item.r + 1] - prm.cu_seqlens[item.r];
+        const int ct = ceil_div(ctx, kKT);
+        if (!wait_bar(L.q_full(qb), (n_it / C::Q_BUFS) & 1, cx)) { ok = false; break; }
+        // O^T buffer ob was last read by the epilogue of item n_it - 2
+        if (n_it >= 2 && !wait_bar(L.o_free(ob), ((n_it >> 1) - 1) & 1, cx)) { ok = false; break; }
+        const uint32_t qa = L.q(qb);
         const int ntiles = item.te - item.tb;
+        int prev_nch = 0;
         for (int l = 0; l < ntiles; ++l, ++g) {
           const int s = g % kStages;
           const int sb = g & 1;
@@ -407,15 +513,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kD / 16; ++kk) {
             // A = K tile (M = 128 keys, K-major), B = Q (N = query rows, K-major); K = 16 dims
             const uint64_t a = smem_desc(L.stage(s) + (kk >> 2) * kTileHalf + (kk & 3) * 32, 16, 1024, SW_128B);
-            const uint64_t b = smem_desc(L.q() + (kk >> 2) * C::Q_CB + (kk & 3) * 32, 16, 1024, SW_128B);
+            const uint64_t b = smem_desc(qa + (kk >> 2) * C::Q_CB + (kk & 3) * 32, 16, 1024, SW_128B);
             umma_bf16(tmem + C::TMEM_S + sb * NT, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
           }
           umma_commit(L.s_full(sb));
           umma_commit(L.k_empty(s));
-          if (l >= 1 && !issue_pv(g - 1, l - 1)) { ok = false; break; }
+          if (l == ntiles - 1) umma_commit(L.q_empty(qb));
+          if (l >= 1 && !issue_pv(g - 1, l - 1, prev_nch, ob)) { ok = false; break; }
+          prev_nch = ceil_div(visible_keys(item.tb + l, ct, ctx, n_r), 16);
         }
         if (!ok) break;
-        if (!issue_pv(g - 1, ntiles - 1)) { ok = false; break; }
+        if (!issue_pv(g - 1, ntiles - 1, prev_nch, ob)) { ok = false; break; }
       }
       if (last_pv >= 0) drain_bar(L.p_empty(last_pv % C::P_BUFS), (last_pv / C::P_BUFS) & 1, prm.err);
     }
@@ -424,7 +532,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sw = warp & 3;                          // TMEM lane quadrant
     const int kl = sw * 32 + lane;                    // key of this thread within a tile (= d in O^T)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
-    const int stid = threadIdx.x - kSoftmaxWarp0 * 32;
     const float sl2 = prm.scale_log2;
     float* my_mref = s_mref + sw * NT;
     float* my_alpha = s_alpha + sw * NT;
@@ -440,20 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nq = item.ni * G;                     // valid query rows (columns)
       const int ng = (nq + 31) >> 5;                  // 32-row groups holding valid rows
       const int nc8 = (nq + 7) >> 3;                  // 8-row chunks holding valid rows
-      // ---- Q tile: row n = (block row n / G, head kvh*G + n % G); rows >= nq zero
-      for (int idx = stid; idx < NT * 16; idx += 128) {
-        const int row = idx >> 4, q = idx & 15;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < nq) {
-          const long long src =
-              ((long long)(c0 + item.i0 + row / G) * prm.Hq + item.kvh * G + row % G) * kD;
-          v = ldg_nc_v4(prm.q + src + q * 8);
-        }
-        st_shared_v4(L.q() + (q >> 3) * C::Q_CB + sw128_off(row, q & 7), v);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(L.q_full());
+      const uint32_t t_o = t_lane + C::TMEM_O + (n_it & 1) * NT;  // this item's O^T
       // per-row state, lane-distributed: row = gi*32 + lane
       float mref[C::G32], lacc[C::G32];
 #pragma unroll
@@ -538,11 +632,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < NT / 32; ++c) {
             float o[32];
-            tmem_ld32(t_lane + C::TMEM_O + c * 32, o);
+            tmem_ld32(t_o + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) o[k] *= my_alpha[c * 32 + k];
-            tmem_st32(t_lane + C::TMEM_O + c * 32, o);
+            tmem_st32(t_o + c * 32, o);
           }
           tmem_wait_st();
         }
@@ -625,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < C::G32; ++c) {
           if (c >= ng) break;
           float o[32];
-          tmem_ld32(t_lane + C::TMEM_O + c * 32, o);
+          tmem_ld32(t_o + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
@@ -634,7 +728,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c * 32 + k < nq) obase[(long long)dr * kD + kl] = o[k] * il;
           }
         }
+        // O^T of this item is read: its TMEM columns may take item n_it + 2
         tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.o_free(n_it & 1));
         // lsum is rewritten by the next item only after every warp passed its ep barrier
         // and the next tile's cross-warp barrier; the latter orders it.
       }
@@ -671,15 +768,28 @@ EncodeFn get_encode() {
 }
 
 // 4-D map over a [n_pages, P, Hkv, 128] bf16 cache; box = 64 dims x 1 head x box_rows tokens.
-bool make_cache_map(CUtensorMap* m, const void* base, int n_pages, int P, int Hkv) {
+bool make_cache_map(CUtensorMap* m, const void* base, int n_pages, int P, int Hkv, int box_rows) {
   EncodeFn enc = get_encode();
   if (!enc) return false;
-  const int box_rows = P < kKT ? P : kKT;
   cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)Hkv, (cuuint64_t)P, (cuuint64_t)n_pages};
   cuuint64_t str[3] = {(cuuint64_t)kD * 2, (cuuint64_t)Hkv * kD * 2, (cuuint64_t)P * Hkv * kD * 2};
   cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, str, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over packed block rows [max_rows, Hkv, 128] bf16; box = 64 dims x 1 head x
+// kChunkRows rows (rows past max_rows read as zero).
+bool make_rows_map(CUtensorMap* m, const void* base, int max_rows, int Hkv) {
+  EncodeFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)Hkv, (cuuint64_t)max_rows};
+  cuuint64_t str[2] = {(cuuint64_t)kD * 2, (cuuint64_t)Hkv * kD * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kChunkRows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, str, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -709,8 +819,8 @@ int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, c
                   const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
                   const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq,
                   int Hkv, int page_size, float scale, const AttnItem* items,
-                  const int* item_begin, float* out, float* lse, float* ws_o, float* ws_lse,
-                  cudaStream_t stream) {
+                  const int* item_begin, int grid, float* out, float* lse, float* ws_o,
+                  float* ws_lse, cudaStream_t stream) {
   Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
@@ -737,22 +847,24 @@ int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, c
   prm.max_rows = max_rows;
   prm.n_pages = n_pages;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  CUtensorMap tk, tv;
-  if (!make_cache_map(&tk, k_cache, n_pages, page_size, Hkv)) return DSPARK_ECUDA;
-  if (!make_cache_map(&tv, v_cache, n_pages, page_size, Hkv)) return DSPARK_ECUDA;
-  const int sms = num_sms_cached();
+  CUtensorMap tk, tv, tkn, tvn;
+  if (!make_cache_map(&tk, k_cache, n_pages, page_size, Hkv, page_size < kKT ? page_size : kKT))
+    return DSPARK_ECUDA;
+  if (!make_cache_map(&tv, v_cache, n_pages, page_size, Hkv, kChunkRows)) return DSPARK_ECUDA;
+  if (!make_rows_map(&tkn, k_new, max_rows, Hkv)) return DSPARK_ECUDA;
+  if (!make_rows_map(&tvn, v_new, max_rows, Hkv)) return DSPARK_ECUDA;
   switch (nt) {
     case 32:
       if (!configure<32>()) return DSPARK_ECUDA;
-      verify_attn_gqa_kernel<32><<<sms, kThreads, Cfg<32>::SMEM_BYTES, stream>>>(tk, tv, prm);
+      verify_attn_gqa_kernel<32><<<grid, kThreads, Cfg<32>::SMEM_BYTES, stream>>>(tk, tv, tkn, tvn, prm);
       break;
     case 64:
       if (!configure<64>()) return DSPARK_ECUDA;
-      verify_attn_gqa_kernel<64><<<sms, kThreads, Cfg<64>::SMEM_BYTES, stream>>>(tk, tv, prm);
+      verify_attn_gqa_kernel<64><<<grid, kThreads, Cfg<64>::SMEM_BYTES, stream>>>(tk, tv, tkn, tvn, prm);
       break;
     default:
       if (!configure<128>()) return DSPARK_ECUDA;
-      verify_attn_gqa_kernel<128><<<sms, kThreads, Cfg<128>::SMEM_BYTES, stream>>>(tk, tv, prm);
+      verify_attn_gqa_kernel<128><<<grid, kThreads, Cfg<128>::SMEM_BYTES, stream>>>(tk, tv, tkn, tvn, prm);
       break;
   }
   DSPARK_LAUNCH_CHECK();
