@@ -9,24 +9,30 @@ namespace dspark {
 namespace attn {
 
 // One unit of work: a tile of query rows of one request against a range of its key tiles;
-// split = which piece of its group, nsplit = the group's piece count (1: not split).
+// nsplit = the group's piece count (1: not split); a piece of a split group writes
+// partial rows into partial slot `slot`: 2c for the first piece of CTA c, 2c + 1 for
+// its last (a split piece is always one of the two).
 struct __align__(16) AttnItem {
   int r, kvh, i0, ni;        // request, KV head, first block row, block rows in the tile
   int part, split, tb, te;   // value-column part, split index, key-tile range [tb, te)
-  int nsplit, pad0, pad1, pad2;
+  int nsplit, slot, pad1, pad2;
 };
 
-// A (request, row tile, part, KV head) group whose key range was cut into pieces.
+// A (request, row tile, part, KV head) group whose key range was cut into pieces,
+// recorded at the index of the CTA that runs its last piece (nsplit = 0: none).
+// Piece s runs on CTA c_first + s; its partial slot is 2 (c_first + s), except for
+// piece 0 when it is the last but not the first piece of CTA c_first (slot0_last):
+// then 2 c_first + 1.
 struct __align__(16) SplitGroup {
   int r, kvh, part, i0;
-  int ni, c_first, nsplit, pad;
+  int ni, c_first, nsplit, slot0_last;
 };
 
 struct Plan {
   bool mla;
   int parts, rows_per_tile, nk, nt, d_part, ncta;
   long long max_items;
-  size_t off_items, off_begin, off_groups, off_ngroups, off_o, off_lse, bytes;
+  size_t off_items, off_begin, off_groups, off_o, off_lse, bytes;
 };
 
 Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_splits,

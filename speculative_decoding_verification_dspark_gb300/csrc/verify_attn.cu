@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
           float* obase;
           // a piece of a split context writes its partial rows into its own slot
           if (split)
-            obase = prm.ws_o + ((long long)it * kRows + m) * C::DV;
+            obase = prm.ws_o + ((long long)item.slot * kRows + m) * C::DV;
           else
             obase = prm.out + ((long long)row_g * prm.Hq + head) * prm.d_v_total + item.part * C::DV;
 #pragma unroll 1
@@ -598,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
           if (row_ok) {
             const float lse_v = (m_used + log2f(l_sum)) * 0.69314718055994530942f;
             if (split)
-              prm.ws_lse[(long long)it * kRows + m] = lse_v;
+              prm.ws_lse[(long long)item.slot * kRows + m] = lse_v;
             else if (item.part == 0)
               prm.lse[(long long)row_g * prm.Hq + head] = lse_v;
           }
@@ -616,98 +616,101 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
 }
 
 // ---------------------------------------------------------------- work list
-// One CTA.  Stream-K style split: the key tiles of every (request, row tile,
-// value part, KV head) group are laid end to end (U units) and CTA c of the
-// persistent grid receives units [c*U/n, (c+1)*U/n) -- the same number of tiles
-// for every CTA, whatever the context-length mix.  A group cut by CTA boundaries
-// becomes pieces; each piece writes partial (o, lse) rows into the slot of its
-// own item, and the group is listed for the combine.  Piece s of a group is the
-// last item of CTA c_first (s = 0) or the first item of CTA c_first + s.
-__device__ __forceinline__ int cta_of_unit(long long x, long long U, int ncta) {
-  return static_cast<int>(((x + 1) * ncta - 1) / U);  // largest c with c*U/ncta <= x
+// One CTA.  Stream-K style split: the key tiles of every (request, row tile, value
+// part, KV head) group are laid end to end (U units) and CTA c of the persistent
+// grid receives units [c*U/n, (c+1)*U/n) -- the same number of tiles for every
+// CTA, whatever the context-length mix.  A group cut by CTA boundaries becomes
+// pieces, one per CTA it meets; such a piece is always the first or the last piece
+// of its CTA and writes partial (o, lse) rows into slot 2c or 2c + 1.  The CTA that
+// runs the last piece of a split group records the group for the combine.
+__device__ __forceinline__ int cta_of_unit(long long x, long long U, int n) {
+  return static_cast<int>(((x + 1) * n - 1) / U);  // largest c with c*U/n <= x
+}
+
+template <class T>
+__device__ __forceinline__ T warp_incl_scan(T v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
+// Exclusive block scan (blockDim.x = 1024); *total receives the sum.
+template <class T>
+__device__ __forceinline__ T block_excl_scan(T v, T* s_w, T* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const T incl = warp_incl_scan(v, lane);
+  if (lane == 31) s_w[wid] = incl;
+  __syncthreads();
+  if (wid == 0) s_w[lane] = warp_incl_scan(s_w[lane], lane);
+  __syncthreads();
+  const T ex = (wid > 0 ? s_w[wid - 1] : T(0)) + incl - v;
+  *total = s_w[31];
+  __syncthreads();  // s_w may be reused by the caller's next scan
+  return ex;
 }
 
 __global__ void __launch_bounds__(1024)
     worklist_kernel(const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ cu_seqlens,
                     int B, int max_rows, int Hkv, int parts, int rows_per_tile, int NK, int ncta,
-                    int max_splits, int max_items, AttnItem* __restrict__ items, int* __restrict__ item_begin,
-                    SplitGroup* __restrict__ groups, int* __restrict__ n_groups,
+                    int max_splits, int max_items, AttnItem* __restrict__ items,
+                    int* __restrict__ item_begin, SplitGroup* __restrict__ groups,
                     unsigned int* __restrict__ err) {
   __shared__ long long s_off[DSPARK_MAX_B + 1];
   __shared__ int s_tt[DSPARK_MAX_B];
   __shared__ int s_n[DSPARK_MAX_B];
-  __shared__ long long s_red[32];
-  __shared__ int s_cnt[1025];
-  __shared__ int s_ngroups;
-  __shared__ int s_ok;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  __shared__ long long s_w64[32];
+  __shared__ int s_w32[32];
+  const int tid = threadIdx.x, lane = tid & 31;
   const int ng_per_tile = parts * Hkv;
+  const bool rows_ok = cu_seqlens[B] <= max_rows;  // else: report and run nothing
   long long units = 0;
   int tt = 0;
   if (tid < B) {
     const int n = cu_seqlens[tid + 1] - cu_seqlens[tid];
     tt = ceil_div(ctx_len[tid], NK) + ceil_div(n, NK);
-    const int rt = ceil_div(n, rows_per_tile);
-    units = (long long)tt * rt * ng_per_tile;
+    units = (long long)tt * ceil_div(n, rows_per_tile) * ng_per_tile;
     s_tt[tid] = tt;
     s_n[tid] = n;
   }
-  if (tid == 0) {
-    s_ngroups = 0;
-    s_ok = 1;
-    // packed rows beyond the caller's buffers: report and run nothing
-    if (cu_seqlens[B] > max_rows) {
-      raise_error(err, DSPARK_DEVERR_ROWS_OVERFLOW);
-      s_ok = 0;
-    }
-  }
-  // exclusive scan of units, and the largest group (in tiles)
-  long long v = units;
+  // largest group, in tiles
   int tmax = tt;
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long u = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += u;
-    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-  }
-  if (lane == 31) s_red[wid] = v;
-  __shared__ int s_tmax[32];
-  if (lane == 0) s_tmax[wid] = tmax;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+  if (lane == 0) s_w32[tid >> 5] = tmax;
   __syncthreads();
-  if (tid < 32) {
-    long long w = tid < (int)(blockDim.x >> 5) ? s_red[tid] : 0;
-    int tm = tid < (int)(blockDim.x >> 5) ? s_tmax[tid] : 0;
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long u = __shfl_up_sync(0xffffffffu, w, o);
-      if (tid >= o) w += u;
-      tm = max(tm, __shfl_xor_sync(0xffffffffu, tm, o));
-    }
-    s_red[tid] = w;
-    if (tid == 0) s_tmax[0] = tm;
-  }
+  tmax = s_w32[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
   __syncthreads();
-  const long long U = s_red[(blockDim.x >> 5) - 1];
-  if (tid < B) s_off[tid] = ((wid > 0) ? s_red[wid - 1] : 0) + v - units;
+  long long U;
+  const long long ex = block_excl_scan(units, s_w64, &U);
+  if (tid < B) s_off[tid] = ex;
   if (tid == 0) s_off[B] = U;
   // No group may be cut into more than max_splits pieces.  Every CTA range holds at
   // least L = floor(U/n) units, and a group of T units meets at most
   // ceil((T-1)/L) + 1 ranges, so L >= ceil((T_max-1)/(max_splits-1)) suffices:
-  // n <= U / that.  Then n <= U too, so no CTA range is empty, the pieces of a
-  // group sit in consecutive CTAs and piece s is found from c_first alone.
+  // n <= U / that.  Then n <= U too, so no CTA range is empty and the pieces of a
+  // group sit in consecutive CTAs.
   int n_eff = ncta;
   {
-    const long long t_max = s_tmax[0];
-    long long l_req = t_max > 1 ? (t_max - 1 + max_splits - 2) / (max_splits - 1) : 1;
+    long long l_req = tmax > 1 ? ((long long)tmax - 1 + max_splits - 2) / (max_splits - 1) : 1;
     if (l_req < 1) l_req = 1;
     const long long cap = U / l_req;
     if (cap < n_eff) n_eff = cap > 0 ? static_cast<int>(cap) : 1;
   }
   __syncthreads();
-  // walk one CTA's unit range: count (pass 0) or emit (pass 1) its pieces
-  auto walk = [&](int c, bool emit, int base) -> int {
-    if (c >= n_eff || U == 0) return 0;
-    const long long lo = (long long)c * U / n_eff, hi = (long long)(c + 1) * U / n_eff;
+  const int c = tid;
+  const bool active = c < ncta && c < n_eff && U > 0;
+  const long long lo = active ? (long long)c * U / n_eff : 0;
+  const long long hi = active ? (long long)(c + 1) * U / n_eff : 0;
+  // walk CTA c's unit range: count (emit = false) or write its pieces
+  auto walk = [&](bool emit, int base) -> int {
     long long u = lo;
     int k = 0;
+    bool wrote_group = false;
     while (u < hi) {
       int a = 0, b = B;  // request: s_off[a] <= u < s_off[a + 1]
       while (b - a > 1) {
@@ -733,96 +736,94 @@ __global__ void __launch_bounds__(1024)
         it.tb = static_cast<int>(lu - (long long)lg * t_r);
         it.te = it.tb + static_cast<int>(next - u);
         it.nsplit = c_last - c_first + 1;
-        it.pad0 = 0; it.pad1 = 0; it.pad2 = 0;
+        it.slot = u == lo ? 2 * c : 2 * c + 1;
+        it.pad1 = 0; it.pad2 = 0;
         items[base + k] = it;
-        if (it.split == 0 && it.nsplit > 1) {
-          const int gi = atomicAdd(&s_ngroups, 1);
+        if (it.nsplit > 1 && c == c_last) {
           SplitGroup sg;
           sg.r = r; sg.kvh = h; sg.part = p; sg.i0 = i0;
-          sg.ni = ni; sg.c_first = c_first; sg.nsplit = it.nsplit; sg.pad = 0;
-          groups[gi] = sg;
+          sg.ni = ni; sg.c_first = c_first; sg.nsplit = it.nsplit;
+          sg.slot0_last = gstart != (long long)c_first * U / n_eff;
+          groups[c] = sg;
+          wrote_group = true;
         }
       }
       ++k;
       u = next;
     }
+    if (emit && !wrote_group) {
+      SplitGroup sg{};
+      groups[c] = sg;  // nsplit = 0: no group ends here
+    }
     return k;
   };
-  for (int c = tid; c <= 1024; c += blockDim.x) s_cnt[c] = 0;
-  __syncthreads();
-  for (int c = tid; c < ncta; c += blockDim.x) s_cnt[c] = walk(c, false, 0);
-  __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int c = 0; c < ncta; ++c) {
-      const int k = s_cnt[c];
-      s_cnt[c] = acc;
-      acc += k;
-    }
-    s_cnt[ncta] = acc;
-    if (s_ok && acc > max_items) {
-      raise_error(err, DSPARK_DEVERR_WORK_OVERFLOW);
-      s_ok = 0;
+  const int cnt = walk(false, 0);
+  int total;
+  const int base = block_excl_scan(cnt, s_w32, &total);
+  const bool fits = rows_ok && total <= max_items;
+  if (tid == 0 && !fits)
+    raise_error(err, rows_ok ? DSPARK_DEVERR_WORK_OVERFLOW : DSPARK_DEVERR_ROWS_OVERFLOW);
+  if (c < ncta) item_begin[c] = fits ? base : 0;
+  if (tid == 0) item_begin[ncta] = fits ? total : 0;
+  if (c < ncta) {
+    if (fits) {
+      walk(true, base);
+    } else {
+      SplitGroup sg{};
+      groups[c] = sg;
     }
   }
-  __syncthreads();
-  const bool fits = s_ok != 0;
-  for (int c = tid; c <= ncta; c += blockDim.x) item_begin[c] = fits ? s_cnt[c] : 0;
-  if (fits)
-    for (int c = tid; c < ncta; c += blockDim.x) walk(c, true, s_cnt[c]);
-  __syncthreads();
-  if (tid == 0) *n_groups = fits ? s_ngroups : 0;
 }
 
 // ---------------------------------------------------------------- split combine
-// One warp per (split group, query row): o = sum_s e^{lse_s - lse} o_s / ...,
-// lse = log sum_s e^{lse_s}, over the group's pieces' slots.
+// Block (c, y): the split group recorded by CTA c, query rows 8y..8y+7, one warp per
+// row, lanes over 4-wide value columns:
+//   lse = log sum_s e^{lse_s},  o = sum_s e^{lse_s - lse} o_s
+// over the group's pieces' partial slots.
 __global__ void __launch_bounds__(256)
     combine_kernel(const int32_t* __restrict__ cu_seqlens, const SplitGroup* __restrict__ groups,
-                   const int* __restrict__ n_groups, const int* __restrict__ item_begin, int G,
-                   int Hq, int rows_per_slot, int d_part, int d_v_total, const float* __restrict__ ws_o,
-                   const float* __restrict__ ws_lse, float* __restrict__ out,
-                   float* __restrict__ lse, int mla) {
+                   int G, int Hq, int rows_per_slot, int d_part, int d_v_total,
+                   const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                   float* __restrict__ out, float* __restrict__ lse, int mla) {
   const int lane = threadIdx.x & 31;
-  const int ng = *n_groups;
-  const int warps_per_cta = blockDim.x >> 5;
-  for (int e = blockIdx.x; e < ng; e += gridDim.x) {
-    const SplitGroup sg = groups[e];
-    const int nq = mla ? Hq : sg.ni * G;
-    const int ns = sg.nsplit;
-    // item index of piece `lane`
-    int piece = 0;
-    if (lane < ns)
-      piece = lane == 0 ? item_begin[sg.c_first + 1] - 1 : item_begin[sg.c_first + lane];
-    const int c0 = cu_seqlens[sg.r];
-    for (int n = threadIdx.x >> 5; n < nq; n += warps_per_cta) {
-      float my = -INFINITY;
-      if (lane < ns) my = ws_lse[(long long)piece * rows_per_slot + n];
-      float mx = my;
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float wgt = lane < ns ? expf(my - mx) : 0.f;
-      float sum = wgt;
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      const float inv = 1.f / sum;
-      int row_g, head;
-      if (mla) { row_g = c0 + sg.i0; head = n; }
-      else { row_g = c0 + sg.i0 + n / G; head = sg.kvh * G + n % G; }
-      float4* dst = reinterpret_cast<float4*>(out + ((long long)row_g * Hq + head) * d_v_total +
-                                              sg.part * d_part);
-      for (int d4 = lane; d4 < (d_part >> 2); d4 += 32) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int sp = 0; sp < ns; ++sp) {
-          const float ws = __shfl_sync(0xffffffffu, wgt, sp);
-          const int pc = __shfl_sync(0xffffffffu, piece, sp);
-          const float4 v = reinterpret_cast<const float4*>(
-              ws_o + ((long long)pc * rows_per_slot + n) * d_part)[d4];
-          acc.x += ws * v.x; acc.y += ws * v.y; acc.z += ws * v.z; acc.w += ws * v.w;
-        }
-        dst[d4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      }
-      if (lane == 0 && sg.part == 0) lse[(long long)row_g * Hq + head] = mx + logf(sum);
-    }
+  const SplitGroup sg = groups[blockIdx.x];
+  const int ns = sg.nsplit;
+  if (ns <= 1) return;
+  const int nq = mla ? Hq : sg.ni * G;
+  const int n = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (n >= nq) return;
+  int slot = 0;
+  float my = -INFINITY;
+  if (lane < ns) {
+    slot = (lane == 0 && sg.slot0_last) ? 2 * sg.c_first + 1 : 2 * (sg.c_first + lane);
+    my = ws_lse[(long long)slot * rows_per_slot + n];
   }
+  float mx = my;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float wgt = lane < ns ? expf(my - mx) : 0.f;
+  float sum = wgt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = 1.f / sum;
+  int row_g, head;
+  const int c0 = cu_seqlens[sg.r];
+  if (mla) { row_g = c0 + sg.i0; head = n; }
+  else { row_g = c0 + sg.i0 + n / G; head = sg.kvh * G + n % G; }
+  float4* dst = reinterpret_cast<float4*>(out + ((long long)row_g * Hq + head) * d_v_total +
+                                          sg.part * d_part);
+  for (int d4 = lane; d4 < (d_part >> 2); d4 += 32) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < ns; ++sp) {
+      const float ws = __shfl_sync(0xffffffffu, wgt, sp);
+      const int sl = __shfl_sync(0xffffffffu, slot, sp);
+      const float4 v =
+          reinterpret_cast<const float4*>(ws_o + ((long long)sl * rows_per_slot + n) * d_part)[d4];
+      acc.x += ws * v.x; acc.y += ws * v.y; acc.z += ws * v.z; acc.w += ws * v.w;
+    }
+    dst[d4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+  if (lane == 0 && sg.part == 0) lse[(long long)row_g * Hq + head] = mx + logf(sum);
 }
 
 // ---------------------------------------------------------------- host side
@@ -863,10 +864,9 @@ Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_split
   };
   p.off_items = take(sizeof(AttnItem) * (size_t)p.max_items);
   p.off_begin = take(sizeof(int) * (size_t)(p.ncta + 1));
-  p.off_groups = take(sizeof(SplitGroup) * (size_t)groups);
-  p.off_ngroups = take(sizeof(int));
-  p.off_o = take(sizeof(float) * (size_t)p.max_items * kRows * p.d_part);
-  p.off_lse = take(sizeof(float) * (size_t)p.max_items * kRows);
+  p.off_groups = take(sizeof(SplitGroup) * (size_t)p.ncta);
+  p.off_o = take(sizeof(float) * (size_t)2 * p.ncta * kRows * p.d_part);   // slots 2c, 2c + 1
+  p.off_lse = take(sizeof(float) * (size_t)2 * p.ncta * kRows);
   p.bytes = off;
   (void)max_splits;
   return p;
@@ -881,7 +881,6 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
   AttnItem* items = reinterpret_cast<AttnItem*>(w + pl.off_items);
   int* item_begin = reinterpret_cast<int*>(w + pl.off_begin);
   SplitGroup* groups = reinterpret_cast<SplitGroup*>(w + pl.off_groups);
-  int* n_groups = reinterpret_cast<int*>(w + pl.off_ngroups);
   float* ws_o = reinterpret_cast<float*>(w + pl.off_o);
   float* ws_lse = reinterpret_cast<float*>(w + pl.off_lse);
   unsigned int* err = device_error_word();
@@ -890,9 +889,8 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
   const int splits = max_splits < 2 ? 2 : (max_splits > 32 ? 32 : max_splits);
 
   worklist_kernel<<<1, 1024, 0, stream>>>(ctx_len, cu_seqlens, B, max_rows, Hkv, pl.parts,
-                                           pl.rows_per_tile,
-                                           pl.nk, ncta, splits, max_items, items, item_begin, groups,
-                                           n_groups, err);
+                                           pl.rows_per_tile, pl.nk, ncta, splits, max_items, items,
+                                           item_begin, groups, err);
   DSPARK_LAUNCH_CHECK();
 
   if (pl.mla) {
@@ -934,9 +932,9 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
     if (rc != DSPARK_OK) return rc;
   }
   const int G = pl.mla ? Hq : Hq / Hkv;
-  combine_kernel<<<ncta * 2, 256, 0, stream>>>(cu_seqlens, groups, n_groups, item_begin, G, Hq,
-                                               kRows, pl.d_part, d_v, ws_o, ws_lse, out, lse,
-                                               pl.mla ? 1 : 0);
+  combine_kernel<<<dim3(ncta, kRows / 8), 256, 0, stream>>>(cu_seqlens, groups, G, Hq, kRows,
+                                                           pl.d_part, d_v, ws_o, ws_lse, out, lse,
+                                                           pl.mla ? 1 : 0);
   DSPARK_LAUNCH_CHECK();
   return DSPARK_OK;
 }

@@ -704,11 +704,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row_g = c0 + item.i0 + n / G;
             const int head = item.kvh * G + n % G;
             inv_l[gi] = lt > 0.f ? 1.f / lt : 0.f;
-            dst_row[gi] = split ? it * kKT + n : row_g * prm.Hq + head;
+            dst_row[gi] = split ? item.slot * kKT + n : row_g * prm.Hq + head;
             if (sw == 0) {  // warp 0 of the group writes the lse
               const float lse_v = (mref[gi] + log2f(lt)) * 0.69314718055994530942f;
               if (split)
-                prm.ws_lse[(long long)it * kKT + n] = lse_v;  // this piece's slot
+                prm.ws_lse[(long long)item.slot * kKT + n] = lse_v;  // this piece's slot
               else
                 prm.lse[(long long)row_g * prm.Hq + head] = lse_v;
             }
