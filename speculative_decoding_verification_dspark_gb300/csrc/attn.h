@@ -15,7 +15,8 @@ namespace attn {
 struct __align__(16) AttnItem {
   int r, kvh, i0, ni;        // request, KV head, first block row, block rows in the tile
   int part, split, tb, te;   // value-column part, split index, key-tile range [tb, te)
-  int nsplit, slot, pad1, pad2;
+  int nsplit, slot, pad0, pad1;
+  int ctx, c0, n_r, pad2;    // request r: ctx_len, cu_seqlens[r], segment rows
 };
 
 // A (request, row tile, part, KV head) group whose key range was cut into pieces,

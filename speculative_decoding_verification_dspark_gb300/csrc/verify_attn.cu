@@ -335,9 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
     for (int it = it_begin; it < it_end && ok; ++it) {
       const AttnItem item = prm.items[it];
       const int r = item.r;
-      const int ctx = prm.ctx_len[r];
-      const int c0 = prm.cu_seqlens[r];
-      const int n_r = prm.cu_seqlens[r + 1] - c0;
+      const int ctx = item.ctx;
+      const int c0 = item.c0;
+      const int n_r = item.n_r;
       const int ct = ceil_div(ctx, C::NK);
       const int32_t* ptab = prm.page_table + (long long)r * prm.max_pages;
       int pg[C::NK / 16];
@@ -430,10 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it) {
       const AttnItem item = prm.items[it];
-      const int r = item.r;
-      const int ctx = prm.ctx_len[r];
-      const int c0 = prm.cu_seqlens[r];
-      const int n_r = prm.cu_seqlens[r + 1] - c0;
+      const int ctx = item.ctx;
+      const int c0 = item.c0;
+      const int n_r = item.n_r;
       const int ct = ceil_div(ctx, C::NK);
       const int rows_valid = C::MLA ? kRows : item.ni * G;
       // ---- Q tile (rows beyond rows_valid are zero)
@@ -661,6 +660,8 @@ __global__ void __launch_bounds__(1024)
   __shared__ long long s_off[DSPARK_MAX_B + 1];
   __shared__ int s_tt[DSPARK_MAX_B];
   __shared__ int s_n[DSPARK_MAX_B];
+  __shared__ int s_ctx[DSPARK_MAX_B];
+  __shared__ int s_c0[DSPARK_MAX_B];
   __shared__ long long s_w64[32];
   __shared__ int s_w32[32];
   const int tid = threadIdx.x, lane = tid & 31;
@@ -669,11 +670,15 @@ __global__ void __launch_bounds__(1024)
   long long units = 0;
   int tt = 0;
   if (tid < B) {
-    const int n = cu_seqlens[tid + 1] - cu_seqlens[tid];
-    tt = ceil_div(ctx_len[tid], NK) + ceil_div(n, NK);
+    const int c0 = cu_seqlens[tid];
+    const int n = cu_seqlens[tid + 1] - c0;
+    const int ctx = ctx_len[tid];
+    tt = ceil_div(ctx, NK) + ceil_div(n, NK);
     units = (long long)tt * ceil_div(n, rows_per_tile) * ng_per_tile;
     s_tt[tid] = tt;
     s_n[tid] = n;
+    s_ctx[tid] = ctx;
+    s_c0[tid] = c0;
   }
   // largest group, in tiles
   int tmax = tt;
@@ -737,7 +742,8 @@ __global__ void __launch_bounds__(1024)
         it.te = it.tb + static_cast<int>(next - u);
         it.nsplit = c_last - c_first + 1;
         it.slot = u == lo ? 2 * c : 2 * c + 1;
-        it.pad1 = 0; it.pad2 = 0;
+        it.pad0 = 0; it.pad1 = 0;
+        it.ctx = s_ctx[r]; it.c0 = s_c0[r]; it.n_r = s_n[r]; it.pad2 = 0;
         items[base + k] = it;
         if (it.nsplit > 1 && c == c_last) {
           SplitGroup sg;

@@ -66,6 +66,7 @@ constexpr int kTileHalf = kKT * 128;  // one 64-wide column block of a [128 x 12
 constexpr int kKVBytes = 2 * kTileHalf;
 constexpr int kStageBytes = 2 * kKVBytes;  // K and V
 constexpr int kChunkRows = 16;             // V chunk = PV k-step; also the block-row box
+constexpr int kSmemItems = 32;             // work items of a CTA kept in shared memory
 
 template <int NT_>
 struct Cfg {
@@ -85,10 +86,13 @@ struct Cfg {
   static constexpr int OFF_RED = OFF_P + P_BUFS * P_BYTES;         // float wmax[2][4][NT]
   static constexpr int OFF_REF = OFF_RED + 2 * 4 * NT * 4;         // float mref[4][NT], alpha[4][NT]
   static constexpr int OFF_LS = OFF_REF + 2 * 4 * NT * 4;          // float lsum[4][NT]
-  static constexpr int OFF_BAR = OFF_LS + 4 * NT * 4;
+  static constexpr int OFF_ITEMS = OFF_LS + 4 * NT * 4;            // AttnItem[kSmemItems]
+  static constexpr int OFF_BAR = OFF_ITEMS + kSmemItems * (int)sizeof(AttnItem);
   // k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], xw[2], ep[2],
-  // o_free[2], p_full[PB], p_empty[PB], q_full[QB], q_empty[QB]
-  static constexpr int N_BARS = 18 + 2 * P_BUFS + 2 * Q_BUFS;
+  // o_free[2], stg_full, stg_free, p_full[PB], p_empty[PB], q_full[QB], q_empty[QB]
+  static constexpr int N_BARS = 20 + 2 * P_BUFS + 2 * Q_BUFS;
+  // epilogue: O / l is staged row-major (512 B per query row) in the P buffers
+  static constexpr int STG_ROWS = P_BUFS * P_BYTES / (kD * 4);
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
   static constexpr int TMEM_S = 0;          // S^T, two buffers of NT columns
@@ -202,13 +206,22 @@ struct Layout {
   __device__ uint32_t xw(int b) const { return bar(12 + b); }
   __device__ uint32_t ep(int b) const { return bar(14 + b); }
   __device__ uint32_t o_free(int b) const { return bar(16 + b); }
-  __device__ uint32_t p_full(int b) const { return bar(18 + b); }
-  __device__ uint32_t p_empty(int b) const { return bar(18 + Cfg<NT>::P_BUFS + b); }
-  __device__ uint32_t q_full(int b) const { return bar(18 + 2 * Cfg<NT>::P_BUFS + b); }
+  __device__ uint32_t stg_full() const { return bar(18); }
+  __device__ uint32_t stg_free() const { return bar(19); }
+  __device__ uint32_t p_full(int b) const { return bar(20 + b); }
+  __device__ uint32_t p_empty(int b) const { return bar(20 + Cfg<NT>::P_BUFS + b); }
+  __device__ uint32_t q_full(int b) const { return bar(20 + 2 * Cfg<NT>::P_BUFS + b); }
   __device__ uint32_t q_empty(int b) const {
-    return bar(18 + 2 * Cfg<NT>::P_BUFS + Cfg<NT>::Q_BUFS + b);
+    return bar(20 + 2 * Cfg<NT>::P_BUFS + Cfg<NT>::Q_BUFS + b);
   }
 };
+
+// Work item `it` of this CTA: from shared memory for the first kSmemItems items.
+__device__ __forceinline__ AttnItem fetch_item(const AttnItem* s_items, const AttnItem* g_items,
+                                               int it, int it_begin) {
+  const int k = it - it_begin;
+  return k < kSmemItems ? s_items[k] : g_items[it];
+}
 
 // Keys of tile t of a request that a query row can see at all: the cache tile's
 // keys below ctx, or the block tile's rows below n_r.
@@ -253,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_mref = reinterpret_cast<float*>(bp + C::OFF_REF);       // [4][NT]
   float* s_alpha = s_mref + 4 * NT;                                 // [4][NT]
   float* s_lsum = reinterpret_cast<float*>(bp + C::OFF_LS);        // [4][NT]
+  AttnItem* s_items = reinterpret_cast<AttnItem*>(bp + C::OFF_ITEMS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + C::OFF_MISC);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bp + C::OFF_MISC + 16);
   const Ctx cx{abort_flag, prm.err};
@@ -271,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(L.ep(b), 4);
       mbar_init(L.o_free(b), 4);
     }
+    mbar_init(L.stg_full(), 4);
+    mbar_init(L.stg_free(), 1);
     for (int b = 0; b < C::P_BUFS; ++b) {
       mbar_init(L.p_full(b), 4);
       mbar_init(L.p_empty(b), 1);
@@ -293,12 +309,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
+  const int it_begin = prm.item_begin[blockIdx.x];
+  const int it_end = prm.item_begin[blockIdx.x + 1];
+  {
+    const int n_s = min(kSmemItems, it_end - it_begin);
+    constexpr int kWords = (int)(sizeof(AttnItem) / sizeof(uint4));
+    for (int i = threadIdx.x; i < n_s * kWords; i += kThreads)
+      reinterpret_cast<uint4*>(s_items)[i] = reinterpret_cast<const uint4*>(prm.items + it_begin)[i];
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int it_begin = prm.item_begin[blockIdx.x];
-  const int it_end = prm.item_begin[blockIdx.x + 1];
   const int G = prm.Hq / prm.Hkv;
   const int P = prm.page_size;
   const int lp = prm.log2_page;
@@ -319,11 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it) {
-      const AttnItem item = prm.items[it];
+      const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
       const int r = item.r;
-      const int ctx = prm.ctx_len[r];
-      const int c0 = prm.cu_seqlens[r];
-      const int n_r = prm.cu_seqlens[r + 1] - c0;
+      const int ctx = item.ctx;
+      const int c0 = item.c0;
+      const int n_r = item.n_r;
       const int ct = ceil_div(ctx, kKT);
       const int32_t* ptab = prm.page_table + (long long)r * prm.max_pages;
       const long long rs = (long long)prm.Hkv * kD;
@@ -431,14 +453,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int n_it = 0;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
-      const AttnItem item = prm.items[it];
+      const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
       const int qb = n_it % C::Q_BUFS;
       if (n_it >= C::Q_BUFS) {
         ok = wait_warp(L.q_empty(qb), ((n_it / C::Q_BUFS) - 1) & 1, cx);
         if (!ok) break;
       }
       const int nq = item.ni * G;
-      const long long row0 = prm.cu_seqlens[item.r] + item.i0;
+      const long long row0 = item.c0 + item.i0;
       const uint32_t qd = L.q(qb);
       constexpr int kPer = NT * 16 / 32;   // 16-byte pieces per lane
       constexpr int kBatch = kPer < 16 ? kPer : 16;
@@ -492,10 +514,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
-        const AttnItem item = prm.items[it];
+        const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
         const int qb = n_it % C::Q_BUFS, ob = n_it & 1;
-        const int ctx = prm.ctx_len[item.r];
-        const int n_r = prm.cu_seqlens[item.r + 1] - prm.cu_seqlens[item.r];
+        const int ctx = item.ctx;
+        const int n_r = item.n_r;
         const int ct = ceil_div(ctx, kKT);
         if (!wait_bar(L.q_full(qb), (n_it / C::Q_BUFS) & 1, cx)) { ok = false; break; }
         // O^T buffer ob was last read by the epilogue of item n_it - 2
@@ -535,14 +557,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = prm.scale_log2;
     float* my_mref = s_mref + sw * NT;
     float* my_alpha = s_alpha + sw * NT;
-    int g = 0, n_it = 0;
+    int g = 0, n_it = 0, n_stg = 0, n_sf = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
-      const AttnItem item = prm.items[it];
-      const int r = item.r;
-      const int ctx = prm.ctx_len[r];
-      const int c0 = prm.cu_seqlens[r];
-      const int n_r = prm.cu_seqlens[r + 1] - c0;
+      const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
+      const int ctx = item.ctx;
+      const int c0 = item.c0;
+      const int n_r = item.n_r;
       const int ct = ceil_div(ctx, kKT);
       const int nq = item.ni * G;                     // valid query rows (columns)
       const int ng = (nq + 31) >> 5;                  // 32-row groups holding valid rows
@@ -594,6 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           wmax[sw * NT + gi * 32 + lane] = transpose_reduce<true>(v, lane) * sl2;
         }
         __syncwarp();
+        // P buffers double as the epilogue's staging area: its bulk reads must be done
+        // before any warp passes this exchange and writes P
+        if (warp == kSoftmaxWarp0 && lane == 0) bulk_wait_read_all();
         if (lane == 0) mbar_arrive(L.xw(g & 1));
         if (!wait_warp(L.xw(g & 1), (g >> 1) & 1, cx)) { ok = false; break; }
         bool need_any = false;
@@ -690,44 +714,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(L.p_empty(gl % C::P_BUFS), (gl / C::P_BUFS) & 1, cx)) { ok = false; break; }
         tc_fence_after();
         const bool split = item.nsplit > 1;
-        // Row n = gi*32 + lane: 1/l and the destination row (in units of kD floats) are
-        // computed once per row, lane-distributed, and broadcast in the store loop.
+        // Row n = gi*32 + lane: 1/l, computed once per row and broadcast below.
         float inv_l[C::G32];
-        int dst_row[C::G32];
 #pragma unroll
         for (int gi = 0; gi < C::G32; ++gi) {
           const int n = gi * 32 + lane;
           inv_l[gi] = 0.f;
-          dst_row[gi] = 0;
           if (gi < ng && n < nq) {
             const float lt = lsum[n] + lsum[NT + n] + lsum[2 * NT + n] + lsum[3 * NT + n];
-            const int row_g = c0 + item.i0 + n / G;
-            const int head = item.kvh * G + n % G;
             inv_l[gi] = lt > 0.f ? 1.f / lt : 0.f;
-            dst_row[gi] = split ? item.slot * kKT + n : row_g * prm.Hq + head;
             if (sw == 0) {  // warp 0 of the group writes the lse
               const float lse_v = (mref[gi] + log2f(lt)) * 0.69314718055994530942f;
               if (split)
                 prm.ws_lse[(long long)item.slot * kKT + n] = lse_v;  // this piece's slot
               else
-                prm.lse[(long long)row_g * prm.Hq + head] = lse_v;
+                prm.lse[((long long)c0 + item.i0 + n / G) * prm.Hq + item.kvh * G + n % G] = lse_v;
             }
           }
         }
-        float* const obase = split ? prm.ws_o : prm.out;
-#pragma unroll
-        for (int c = 0; c < C::G32; ++c) {
-          if (c >= ng) break;
-          float o[32];
-          tmem_ld32(t_o + c * 32, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float il = __shfl_sync(0xffffffffu, inv_l[c], k);
-            const int dr = __shfl_sync(0xffffffffu, dst_row[c], k);
-            if (c * 32 + k < nq) obase[(long long)dr * kD + kl] = o[k] * il;
+        // O^T / l -> row-major rows in the (now idle) P buffers, STG_ROWS rows per pass;
+        // one thread then writes each pass out with bulk copies: a slot of ws_o is one
+        // contiguous run, an output block row is G consecutive heads.
+        float* stg = reinterpret_cast<float*>(bp + C::OFF_P);
+        for (int p0 = 0; p0 < nq; p0 += C::STG_ROWS) {
+          const int p1 = min(nq, p0 + C::STG_ROWS);
+          if (p0 > 0) {  // the previous pass must have been read out of the buffers
+            if (!wait_warp(L.stg_free(), n_sf & 1, cx)) { ok = false; break; }
+            ++n_sf;
           }
+#pragma unroll
+          for (int c = 0; c < C::G32; ++c) {
+            if (c * 32 >= p1 || c * 32 < p0) continue;   // chunk outside this pass (uniform)
+            float o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const float il = __shfl_sync(0xffffffffu, inv_l[c], k);
+              if (c * 32 + k < p1) stg[(c * 32 + k - p0) * kD + kl] = o[k] * il;
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(L.stg_full());
+          if (warp == kSoftmaxWarp0 && lane == 0) {
+            if (!wait_bar(L.stg_full(), n_stg & 1, cx)) {
+              ok = false;
+            } else {
+              const uint32_t src = L.pbuf(0);
+              if (split) {
+                bulk_store_s2g(prm.ws_o + ((long long)item.slot * kKT + p0) * kD, src,
+                               (uint32_t)(p1 - p0) * kD * 4);
+              } else {
+                for (int n = p0; n < p1;) {
+                  const int b = n / G, h0 = n % G;
+                  const int run = min(p1 - n, G - h0);
+                  bulk_store_s2g(prm.out + (((long long)c0 + item.i0 + b) * prm.Hq + item.kvh * G + h0) * kD,
+                                 src + (uint32_t)(n - p0) * kD * 4, (uint32_t)run * kD * 4);
+                  n += run;
+                }
+              }
+              bulk_commit();
+              if (p1 < nq) {
+                bulk_wait_read_all();
+                mbar_arrive(L.stg_free());
+              }
+            }
+          }
+          ++n_stg;
+          if (!__all_sync(0xffffffffu, ok)) break;
         }
+        if (!ok) break;
         // O^T of this item is read: its TMEM columns may take item n_it + 2
         tc_fence_before();
         __syncwarp();
@@ -736,6 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // and the next tile's cross-warp barrier; the latter orders it.
       }
     }
+    if (warp == kSoftmaxWarp0 && lane == 0) bulk_wait_all();  // output writes complete
   }
 
   tc_fence_before();
