@@ -39,12 +39,13 @@ import workloads as W  # noqa: E402
 
 METRIC = "verify steps/s & packed tokens/s at B=1..256, % of HBM roofline per kernel"
 UNIT = "verify steps/s"
-KERNELS_PER_STEP = 10   # schedule 1, pack 1, attention 3, accept 3, compact 2
+KERNELS_PER_STEP = 11   # schedule 2, pack 1, attention 3, accept 3, compact 2
 PROFILES = os.path.join(ROOT, "profiles")
-ATTN_SRC = os.path.join(ROOT, "speculative_decoding_verification_dspark_gb300", "csrc",
-                        "verify_attn.cu")
-ACCEPT_SRC = os.path.join(ROOT, "speculative_decoding_verification_dspark_gb300", "csrc",
-                          "accept.cu")
+_CSRC = os.path.join(ROOT, "speculative_decoding_verification_dspark_gb300", "csrc")
+# sources whose change invalidates a committed DRAM-traffic figure
+ATTN_SRC = [os.path.join(_CSRC, f) for f in
+            ("verify_attn.cu", "verify_attn_gqa.cu", "attn.h", "ptx.cuh", "common.cuh")]
+ACCEPT_SRC = [os.path.join(_CSRC, f) for f in ("accept.cu", "common.cuh")]
 
 
 def workload_desc(wl: W.Workload, mode: str) -> str:
@@ -296,7 +297,8 @@ def gpu_arm(args, wl, mode, dist, world, rank, device):
             "verify_attn": {"us": attn_us, "GB/s": attn_gbs, "frac_hbm": attn_gbs / hbm,
                             "TFLOP/s": a_flops / (attn_us * 1e-6) / 1e12, "bytes": a_bytes},
             "accept": {"us": accept_us, "GB/s": acc_gbs, "frac_hbm": acc_gbs / hbm,
-                       "bytes": c_bytes},
+                       "bytes": c_bytes,
+                       "traffic": load_traffic("accept", wl.name, ACCEPT_SRC)},
         },
         "e2e": e2e,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
@@ -354,9 +356,12 @@ def load_peaks():
         return {}
 
 
-def src_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def src_hash(paths):
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_traffic(kernel, workload, src):
