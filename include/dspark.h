@@ -20,9 +20,9 @@
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless the
  *     argument's comment says "host".  Tensors are dense row-major, no strides.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is enqueued
- *     on it; no call synchronises, allocates or frees memory.  Each call launches
- *     a fixed sequence of kernels whose grid does not depend on device data, so
- *     the sequence can be captured in a CUDA graph.
+ *     on it; no call synchronises, allocates or frees memory.  Each of the five
+ *     step calls launches a fixed sequence of kernels whose grid does not depend
+ *     on device data, so the step can be captured in a CUDA graph.
  *   - Return value: a dspark_status.  Arguments are checked on the host before
  *     anything is launched; a non-OK return means nothing was enqueued (except
  *     DSPARK_ECUDA, which reports a failed launch).  Nothing throws or aborts.
