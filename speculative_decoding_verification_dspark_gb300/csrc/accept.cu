@@ -11,13 +11,15 @@
 //                        u*p_d(d_j) <= p_t(d_j) over the verified positions ->
 //                        committed length, cap, and which packed row is sampled
 //                        (residual or target).
-//   accept_vocab_kernel  persistent grid over (packed row, vocab chunk): one pass of
-//                        128-bit coalesced loads of p_t and p_d computes the partial
-//                        L1 distance for c*, and on the sampled row the partial
+//   accept_vocab_kernel  persistent, one CTA per SM over (packed row, vocab chunk)
+//                        items: bulk copies stream p_t, p_d and the noise row through
+//                        a shared-memory ring; one pass computes the partial L1
+//                        distance for c*, and on the sampled row the partial
 //                        exponential-race argmax (w_v / e_v, lowest index on ties)
 //                        for both the residual max(0, p_t - p_d) and p_t itself.
 //   accept_final_kernel  one warp per request: fixed-order fp64 sums of the chunk
-//                        partials (c*) and the chunk-ordered argmax (token).
+//                        partials (c*) and the argmax over the chunk partials
+//                        (token), with the p_t race behind an all-zero residual.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -28,17 +30,22 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace dspark {
 
 namespace {
 
-constexpr int kVocabThreads = 256;
 constexpr int kChunk = 8192;  // vocabulary entries per work item (32 per thread)
 
 struct RowInfo {        // per request
   int commit, cap, sample_row, residual;
 };
+
+// row_desc flags: low 16 bits = position j of the row in its request's segment
+constexpr int kRowL1 = 1 << 16;        // c* needs this row's L1 distance
+constexpr int kRowSample = 1 << 17;    // the token is drawn on this row
+constexpr int kRowResidual = 1 << 18;  // ... from max(0, p_t - p_d) (a correction)
 
 struct __align__(16) Partial {  // per (packed row, chunk)
   double l1;
@@ -52,30 +59,6 @@ __device__ __forceinline__ float ld_p(const float* p, long long i) { return __ld
 __device__ __forceinline__ float ld_p(const __nv_bfloat16* p, long long i) {
   return __bfloat162float(p[i]);
 }
-
-template <class T>
-struct Vec8;  // eight consecutive probabilities as fp32
-template <>
-struct Vec8<float> {
-  __device__ static void load(const float* p, float (&x)[8]) {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  }
-};
-template <>
-struct Vec8<__nv_bfloat16> {
-  __device__ static void load(const __nv_bfloat16* p, float (&x)[8]) {
-    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  }
-};
 
 __device__ __forceinline__ void better(float& k, int& i, float k2, int i2) {
   if (k2 > k || (k2 == k && i2 < i)) {
@@ -95,7 +78,7 @@ __global__ void __launch_bounds__(128)
                        const int32_t* __restrict__ windows, const int32_t* __restrict__ cu,
                        int mode, int B, int gamma, int max_rows, int32_t* __restrict__ accept_len,
                        int32_t* __restrict__ cap_len, RowInfo* __restrict__ info,
-                       unsigned int* __restrict__ err) {
+                       int2* __restrict__ row_desc, unsigned int* __restrict__ err) {
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (cu[B] > max_rows) {  // packed rows beyond the caller's buffers: report, touch nothing
@@ -134,106 +117,363 @@ __global__ void __launch_bounds__(128)
     accept_len[r] = commit;
     cap_len[r] = L;
   }
-}
-
-template <class T>
-__global__ void __launch_bounds__(kVocabThreads)
-    accept_vocab_kernel(const T* __restrict__ p_t, const T* __restrict__ p_d,
-                        const float* __restrict__ exp_noise, int V, int n_chunks,
-                        const int32_t* __restrict__ cu, int B, int gamma, int max_rows,
-                        const RowInfo* __restrict__ info, Partial* __restrict__ part) {
-  __shared__ double s_l1[kVocabThreads / 32];
-  __shared__ float s_kr[kVocabThreads / 32], s_kt[kVocabThreads / 32];
-  __shared__ int s_ir[kVocabThreads / 32], s_it[kVocabThreads / 32];
-  const int M = cu[B];
-  if (M > max_rows) return;  // reported by the test kernel
-  const long long n_items = (long long)M * n_chunks;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int row = static_cast<int>(item / n_chunks);
-    const int ch = static_cast<int>(item % n_chunks);
-    const int r = upper_segment(cu, B, row);
-    const int j = row - cu[r];
-    const RowInfo ri = info[r];
-    const bool do_l1 = j < gamma;
-    const bool do_samp = j == ri.sample_row;
-    if (!do_l1 && !do_samp) continue;  // block-uniform
-    const bool need_d = do_l1 || (do_samp && ri.residual);
-    const T* pt_row = p_t + (long long)row * V;
-    const T* pd_row = p_d + ((long long)r * gamma + (j < gamma ? j : 0)) * V;
-    const float* e_row = exp_noise + (long long)r * V;
-    const int v0 = ch * kChunk;
-    const int v1 = (v0 + kChunk < V) ? v0 + kChunk : V;
-    float l1 = 0.f;
-    float kr = -1.f, kt = -1.f;
-    int ir = 0x7fffffff, it_ = 0x7fffffff;
-    for (int v = v0 + threadIdx.x * 8; v < v1; v += kVocabThreads * 8) {
-      float a[8], d[8];
-      Vec8<T>::load(pt_row + v, a);
-      if (need_d) {
-        Vec8<T>::load(pd_row + v, d);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) d[q] = 0.f;
-      }
-      if (do_l1) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) l1 += fabsf(d[q] - a[q]);
-      }
-      if (do_samp) {
-        const float4 e0 = __ldcs(reinterpret_cast<const float4*>(e_row + v));
-        const float4 e1 = __ldcs(reinterpret_cast<const float4*>(e_row + v) + 1);
-        const float e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float kq = __fdiv_rn(a[q], e[q]);
-          if (kq > kt) { kt = kq; it_ = v + q; }
-          if (ri.residual) {
-            const float res = fmaxf(__fsub_rn(a[q], d[q]), 0.f);
-            const float rq = __fdiv_rn(res, e[q]);
-            if (rq > kr) { kr = rq; ir = v + q; }
-          }
-        }
-      }
-    }
-    // block reduction (fixed tree: deterministic)
-    double l1d = static_cast<double>(l1);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      l1d += __shfl_xor_sync(0xffffffffu, l1d, o);
-      better(kr, ir, __shfl_xor_sync(0xffffffffu, kr, o), __shfl_xor_sync(0xffffffffu, ir, o));
-      better(kt, it_, __shfl_xor_sync(0xffffffffu, kt, o), __shfl_xor_sync(0xffffffffu, it_, o));
-    }
-    if (lane == 0) {
-      s_l1[wid] = l1d;
-      s_kr[wid] = kr; s_ir[wid] = ir;
-      s_kt[wid] = kt; s_it[wid] = it_;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      Partial pp;
-      pp.l1 = 0.0;
-      pp.key_res = -1.f; pp.idx_res = 0x7fffffff;
-      pp.key_t = -1.f; pp.idx_t = 0x7fffffff;
-      for (int q = 0; q < kVocabThreads / 32; ++q) {
-        pp.l1 += s_l1[q];
-        better(pp.key_res, pp.idx_res, s_kr[q], s_ir[q]);
-        better(pp.key_t, pp.idx_t, s_kt[q], s_it[q]);
-      }
-      part[(long long)row * n_chunks + ch] = pp;
-    }
-    __syncthreads();
+  // what the vocabulary pass does on each of this request's packed rows
+  const int commit = __shfl_sync(0xffffffffu, L < w ? L : w, 0);
+  for (int j = lane; j < n_rows; j += 32) {
+    int flags = j;
+    if (j < gamma) flags |= kRowL1;
+    if (j == commit) flags |= kRowSample | (commit < w ? kRowResidual : 0);
+    row_desc[base + j] = make_int2(r, flags);
   }
 }
 
+// ---------------------------------------------------------------- vocabulary pass
+// Persistent, one CTA per SM over a contiguous range of (packed row, 8192-entry
+// chunk) items.  One thread streams the rows the method needs (p_t always, p_d for
+// c* rows and corrections, the noise row on the sampled row) with bulk copies, in
+// 4096-entry sub-chunks, into a five-slot shared-memory ring (noise into a ring of
+// its own), running ahead across items; sixteen consumer warps reduce each sub-chunk from shared memory; a
+// reducer warp combines the sixteen warps' results of an item into its partial.
+constexpr int kSub = 4096;                    // entries per stage
+constexpr int kVStages = 5;                   // main ring: p_t | p_d
+constexpr int kVStageBytes = 2 * kSub * 4;    // (fp32 sizes)
+constexpr int kNStages = 3;                   // noise ring, sampled rows only
+constexpr int kConsumerWarps = 16;
+constexpr int kProducerWarp = 16, kReducerWarp = 17;
+constexpr int kVocabCtaThreads = 18 * 32;
+constexpr uint64_t kVocabWaitNs = 2000000000ull;
+
+struct WarpPart {
+  double l1;
+  float kr, kt;
+  int ir, it;
+  int pad[2];
+};
+
+struct VocabSmem {
+  uint8_t stage[kVStages][kVStageBytes];
+  uint8_t noise[kNStages][kSub * 4];
+  WarpPart red[2][kConsumerWarps];
+  uint64_t full[kVStages], empty[kVStages], nempty[kNStages], red_full[2], red_free[2];
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool vwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      unsigned int* err) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  uint32_t n = 0;
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if ((++n & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > kVocabWaitNs) {
+        *abort_flag = 1;
+        raise_error(err, DSPARK_DEVERR_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Work of row `row` of the packed batch, decoded from the test kernel's descriptor.
+struct RowWork {
+  int r, j;
+  bool l1, samp, residual, need_d;
+};
+__device__ __forceinline__ RowWork row_work(const int2* row_desc, int row) {
+  const int2 d = row_desc[row];
+  RowWork w;
+  w.r = d.x;
+  w.j = d.y & 0xffff;
+  w.l1 = (d.y & kRowL1) != 0;
+  w.samp = (d.y & kRowSample) != 0;
+  w.residual = (d.y & kRowResidual) != 0;
+  w.need_d = w.l1 || w.residual;
+  return w;
+}
+
+// x[q] for a run-time q without dynamic indexing (keeps x in registers).
+__device__ __forceinline__ float pick8(const float (&x)[8], int q) {
+  float v = x[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) v = q == i ? x[i] : v;
+  return v;
+}
+
+// Approximate reciprocal (hardware, relative error well below 2^-20 for normal e).
+__device__ __forceinline__ float approx_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Keys are >= 0.  The approximate quotient a * rcp.approx(e) is within 2^-21 of
+// the exact one (relative).  Once some entry's approximate key is K, the final
+// maximum is at least K (1 - 2^-21); an entry whose approximate key is at or
+// below K (1 - 2^-15) has an exact key below K (1 - 2^-16), whose rounding is
+// strictly below the final maximum: it can neither win nor tie.
+constexpr float kFilter = 1.0f - 1.0f / 32768.0f;
+constexpr float kHuge = 3.0e38f;  // marks an entry that must take the exact path
+
+template <class T>
+__device__ __forceinline__ void smem_vec8(const uint8_t* p, float (&x)[8]);
+template <>
+__device__ __forceinline__ void smem_vec8<float>(const uint8_t* p, float (&x)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 16);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void smem_vec8<__nv_bfloat16>(const uint8_t* p, float (&x)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <class T>
+__global__ void __launch_bounds__(kVocabCtaThreads, 1)
+    accept_vocab_kernel(const T* __restrict__ p_t, const T* __restrict__ p_d,
+                        const float* __restrict__ exp_noise, int V, int n_chunks,
+                        const int32_t* __restrict__ cu, int B, int gamma, int max_rows,
+                        const int2* __restrict__ row_desc, Partial* __restrict__ part,
+                        unsigned int* __restrict__ err) {
+  extern __shared__ __align__(128) uint8_t vsmem_raw[];
+  VocabSmem& S = *reinterpret_cast<VocabSmem*>(vsmem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = cu[B];
+  if (M > max_rows) return;  // reported by the test kernel (block-uniform)
+  // items round-robin over the CTAs: the chunks of one row (and so the costlier
+  // sampled rows) spread over many SMs
+  const long long n_items = (long long)M * n_chunks;
+  volatile int* abort_flag = &S.abort_flag;
+  if (threadIdx.x == 0) {
+    S.abort_flag = 0;
+    for (int s = 0; s < kVStages; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&S.full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&S.empty[s]), kConsumerWarps);
+    }
+    for (int s = 0; s < kNStages; ++s) ptx::mbar_init(ptx::smem_addr(&S.nempty[s]), kConsumerWarps);
+    for (int p = 0; p < 2; ++p) {
+      ptx::mbar_init(ptx::smem_addr(&S.red_full[p]), kConsumerWarps);
+      ptx::mbar_init(ptx::smem_addr(&S.red_free[p]), 1);
+    }
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  constexpr int ES = static_cast<int>(sizeof(T));
+  auto n_sub_of = [&](int ch) {
+    const int len = min(kChunk, V - ch * kChunk);
+    return (len + kSub - 1) / kSub;
+  };
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      int g = 0, gn = 0;  // main-ring and noise-ring sub-chunks issued
+      bool ok = true;
+      long long item = blockIdx.x;
+      RowWork w_next;
+      if (item < n_items) w_next = row_work(row_desc, static_cast<int>(item / n_chunks));
+      for (; item < n_items && ok; item += gridDim.x) {
+        const int row = static_cast<int>(item / n_chunks), ch = static_cast<int>(item % n_chunks);
+        const RowWork w = w_next;
+        // the next item's descriptor is loaded while this one's copies are issued
+        if (item + gridDim.x < n_items)
+          w_next = row_work(row_desc, static_cast<int>((item + gridDim.x) / n_chunks));
+        if (!w.l1 && !w.samp) continue;
+        const T* pt_row = p_t + (long long)row * V;
+        const T* pd_row = p_d + ((long long)w.r * gamma + (w.j < gamma ? w.j : 0)) * V;
+        const float* e_row = exp_noise + (long long)w.r * V;
+        const int ns = n_sub_of(ch);
+        for (int sb = 0; sb < ns; ++sb, ++g) {
+          const int s = g % kVStages;
+          if (g >= kVStages &&
+              !vwait(ptx::smem_addr(&S.empty[s]), ((g / kVStages) - 1) & 1, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          const int sn = gn % kNStages;
+          if (w.samp && gn >= kNStages &&
+              !vwait(ptx::smem_addr(&S.nempty[sn]), ((gn / kNStages) - 1) & 1, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          const int v0 = ch * kChunk + sb * kSub;
+          const uint32_t len = static_cast<uint32_t>(min(kSub, V - v0));
+          const uint32_t full = ptx::smem_addr(&S.full[s]);
+          const uint32_t base = ptx::smem_addr(S.stage[s]);
+          const uint32_t bytes = len * ES * (w.need_d ? 2u : 1u) + (w.samp ? len * 4u : 0u);
+          ptx::mbar_expect_tx(full, bytes);
+          ptx::bulk_load_g2s(base, pt_row + v0, len * ES, full);
+          if (w.need_d) ptx::bulk_load_g2s(base + kSub * 4, pd_row + v0, len * ES, full);
+          if (w.samp) {
+            ptx::bulk_load_g2s(ptx::smem_addr(S.noise[sn]), e_row + v0, len * 4, full);
+            ++gn;
+          }
+          ptx::mbar_arrive(full);
+        }
+      }
+    }
+  } else if (warp == kReducerWarp) {
+    // the consumer warps' results of an item -> its partial (fixed order: deterministic)
+    int n_it = 0;
+    bool ok = true;
+    for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int row = static_cast<int>(item / n_chunks), ch = static_cast<int>(item % n_chunks);
+      const RowWork w = row_work(row_desc, row);
+      if (!w.l1 && !w.samp) continue;
+      const int p = n_it & 1;
+      ok = vwait(ptx::smem_addr(&S.red_full[p]), (n_it >> 1) & 1, abort_flag, err);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      if (lane == 0) {
+        Partial pp;
+        pp.l1 = 0.0;
+        pp.key_res = -1.f; pp.idx_res = 0x7fffffff;
+        pp.key_t = -1.f; pp.idx_t = 0x7fffffff;
+        for (int q = 0; q < kConsumerWarps; ++q) {
+          const WarpPart& wp = S.red[p][q];
+          pp.l1 += wp.l1;
+          better(pp.key_res, pp.idx_res, wp.kr, wp.ir);
+          better(pp.key_t, pp.idx_t, wp.kt, wp.it);
+        }
+        part[(long long)row * n_chunks + ch] = pp;
+        ptx::mbar_arrive(ptx::smem_addr(&S.red_free[p]));
+      }
+      __syncwarp();
+      ++n_it;
+    }
+  } else {
+    // consumers: thread t owns entries 8t..8t+7 of each sub-chunk
+    int g = 0, gn = 0, n_it = 0;
+    bool ok = true;
+    for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int row = static_cast<int>(item / n_chunks), ch = static_cast<int>(item % n_chunks);
+      const RowWork w = row_work(row_desc, row);
+      if (!w.l1 && !w.samp) continue;
+      const int ns = n_sub_of(ch);
+      float l1 = 0.f;
+      float kbest = -1.f;                // this lane's race maximum and its index
+      int ibest = 0x7fffffff;
+      float thr = -1.f;                  // warp-wide filter (below every key at first)
+      for (int sb = 0; sb < ns; ++sb, ++g) {
+        const int s = g % kVStages;
+        ok = vwait(ptx::smem_addr(&S.full[s]), (g / kVStages) & 1, abort_flag, err);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const int v0 = ch * kChunk + sb * kSub;
+        const int len = min(kSub, V - v0);
+        const uint8_t* st = S.stage[s];
+        const int sn = gn % kNStages;
+        const uint8_t* nz = S.noise[sn];
+#pragma unroll
+        for (int k = 0; k < kSub / (kConsumerWarps * 32 * 8); ++k) {
+          const int e = (k * kConsumerWarps * 32 + threadIdx.x) * 8;
+          const bool valid = e < len;
+          float a[8], d[8], en[8], ka[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) { a[q] = 0.f; d[q] = 0.f; en[q] = 1.f; ka[q] = -1.f; }
+          if (valid) {
+            smem_vec8<T>(st + e * ES, a);
+            if (w.need_d) smem_vec8<T>(st + kSub * 4 + e * ES, d);
+            if (w.l1) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) l1 += fabsf(d[q] - a[q]);
+            }
+            if (w.samp) {
+              // race weights: the residual max(0, p_t - p_d) for a correction, p_t
+              // for a bonus token (the p_t race behind an all-zero residual is
+              // left to the final kernel)
+              smem_vec8<float>(nz + e * 4, en);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                if (w.residual) a[q] = fmaxf(__fsub_rn(a[q], d[q]), 0.f);
+                const float inv = approx_rcp(en[q]);
+                // e beyond the reciprocal's range: force the exact path
+                ka[q] = inv == 0.f ? kHuge : a[q] * inv;
+              }
+            }
+          }
+          if (w.samp) {  // warp-uniform
+            // Raise the filter to just below the warp's largest approximate key:
+            // the final maximum is at least that key's exact value.
+            float mt = ka[0];
+#pragma unroll
+            for (int q = 1; q < 8; ++q) mt = fmaxf(mt, ka[q]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+            // (a zero maximum leaves the filter: zero keys still reach the exact
+            // path, so an all-zero range still yields its lowest index)
+            if (mt < kHuge && mt > 0.f) thr = fmaxf(thr, mt * kFilter);
+            // A lane visits its entries in increasing index order and keeps the first
+            // strict maximum of its rounded keys fl(w / e); an entry at or below the
+            // filter has fl(w / e) strictly below the final maximum, so only the few
+            // others take the exact division.
+            unsigned cand = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (valid && ka[q] > thr) cand |= 1u << q;
+#pragma unroll 1
+            for (; cand; cand &= cand - 1) {
+              const int q = __ffs(cand) - 1;
+              const float kq = __fdiv_rn(pick8(a, q), pick8(en, q));
+              if (kq > kbest) { kbest = kq; ibest = v0 + e + q; }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(ptx::smem_addr(&S.empty[s]));
+          if (w.samp) ptx::mbar_arrive(ptx::smem_addr(&S.nempty[sn]));
+        }
+        if (w.samp) ++gn;
+      }
+      if (!ok) break;
+      float kr = -1.f, kt = -1.f;
+      int ir = 0x7fffffff, it_ = 0x7fffffff;
+      if (w.residual) { kr = kbest; ir = ibest; } else { kt = kbest; it_ = ibest; }
+      double l1d = static_cast<double>(l1);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        l1d += __shfl_xor_sync(0xffffffffu, l1d, o);
+        better(kr, ir, __shfl_xor_sync(0xffffffffu, kr, o), __shfl_xor_sync(0xffffffffu, ir, o));
+        better(kt, it_, __shfl_xor_sync(0xffffffffu, kt, o), __shfl_xor_sync(0xffffffffu, it_, o));
+      }
+      const int p = n_it & 1;
+      // slot p was last read by the reducer for item n_it - 2
+      if (n_it >= 2) {
+        ok = vwait(ptx::smem_addr(&S.red_free[p]), ((n_it >> 1) - 1) & 1, abort_flag, err);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        WarpPart& wp = S.red[p][warp];
+        wp.l1 = l1d;
+        wp.kr = kr; wp.ir = ir;
+        wp.kt = kt; wp.it = it_;
+        ptx::mbar_arrive(ptx::smem_addr(&S.red_full[p]));
+      }
+      __syncwarp();
+      ++n_it;
+    }
+  }
+  __syncthreads();
+}
+
+template <class T>
 __global__ void __launch_bounds__(128)
-    accept_final_kernel(const int32_t* __restrict__ cu, int B, int gamma, int max_rows,
+    accept_final_kernel(const T* __restrict__ p_t, const float* __restrict__ exp_noise, int V,
+                        const int32_t* __restrict__ cu, int B, int gamma, int max_rows,
                         int n_chunks, const RowInfo* __restrict__ info,
                         const Partial* __restrict__ part, int32_t* __restrict__ out_tok,
                         float* __restrict__ cstar, int32_t* __restrict__ fallback) {
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (r >= B || cu[B] > max_rows) return;
+  if (r >= B || cu[B] > max_rows) return;  // warp-uniform
   const int base = cu[r];
   const int n_rows = cu[r + 1] - base;
   const RowInfo ri = info[r];
@@ -246,29 +486,62 @@ __global__ void __launch_bounds__(128)
     }
     cstar[r * gamma + j] = c;
   }
+  // token: the sampled row's race maximum over the chunk partials (max, then lowest
+  // index: order-independent)
+  const long long prow = (long long)(base + ri.sample_row) * n_chunks;
+  float k = -1.f;
+  int idx = 0x7fffffff;
+  for (int ch = lane; ch < n_chunks; ch += 32) {
+    const Partial p = part[prow + ch];
+    if (ri.residual) better(k, idx, p.key_res, p.idx_res);
+    else better(k, idx, p.key_t, p.idx_t);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    better(k, idx, __shfl_xor_sync(0xffffffffu, k, o), __shfl_xor_sync(0xffffffffu, idx, o));
+  int fb = 0;
+  if (ri.residual && !(k > 0.f)) {
+    // An all-zero residual (reachable only through rounding): the token is drawn
+    // from p_t on the same row with the same noise; the vocabulary pass raced only
+    // the residual there, so this warp races p_t.
+    fb = 1;
+    k = -1.f;
+    idx = 0x7fffffff;
+    const long long trow = (long long)(base + ri.sample_row) * V;
+    for (int v = lane; v < V; v += 32) {
+      const float kq = __fdiv_rn(ld_p(p_t, trow + v), exp_noise[(long long)r * V + v]);
+      if (kq > k) { k = kq; idx = v; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      better(k, idx, __shfl_xor_sync(0xffffffffu, k, o), __shfl_xor_sync(0xffffffffu, idx, o));
+  }
   if (lane == 0) {
-    const long long prow = (long long)(base + ri.sample_row) * n_chunks;
-    float kr = -1.f, kt = -1.f;
-    int ir = 0x7fffffff, it_ = 0x7fffffff;
-    for (int ch = 0; ch < n_chunks; ++ch) {
-      const Partial p = part[prow + ch];
-      better(kr, ir, p.key_res, p.idx_res);
-      better(kt, it_, p.key_t, p.idx_t);
-    }
-    int tok = it_, fb = 0;
-    if (ri.residual) {
-      if (kr > 0.f) tok = ir;
-      else fb = 1;
-    }
-    out_tok[r] = tok;
+    out_tok[r] = idx;
     if (fallback) fallback[r] = fb;
   }
 }
 
+bool vocab_configure() {
+  static int state = 0;  // 0: not yet, 1: ok, -1: failed
+  if (state == 0) {
+    const int bytes = static_cast<int>(sizeof(VocabSmem));
+    const bool ok =
+        cudaFuncSetAttribute(accept_vocab_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) == cudaSuccess &&
+        cudaFuncSetAttribute(accept_vocab_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+    state = ok ? 1 : -1;
+  }
+  return state == 1;
+}
+
+// workspace: RowInfo[B] | int2 row_desc[max_rows] | Partial[max_rows][n_chunks]
 size_t accept_workspace(int B, int max_rows, int V) {
   const int n_chunks = ceil_div(V, kChunk);
-  size_t a = ((size_t)B * sizeof(RowInfo) + 255) & ~size_t(255);
-  return a + (size_t)max_rows * n_chunks * sizeof(Partial);
+  const size_t a = ((size_t)B * sizeof(RowInfo) + 255) & ~size_t(255);
+  const size_t b = ((size_t)max_rows * sizeof(int2) + 255) & ~size_t(255);
+  return a + b + (size_t)max_rows * n_chunks * sizeof(Partial);
 }
 
 // Scratch of dspark_accept_noalloc: a fixed array in the library image, one per
@@ -295,37 +568,45 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
                   cudaStream_t stream) {
   const int n_chunks = ceil_div(V, kChunk);
   RowInfo* info = static_cast<RowInfo*>(ws);
-  Partial* part = reinterpret_cast<Partial*>(static_cast<uint8_t*>(ws) +
-                                             (((size_t)B * sizeof(RowInfo) + 255) & ~size_t(255)));
+  const size_t off_desc = ((size_t)B * sizeof(RowInfo) + 255) & ~size_t(255);
+  int2* row_desc = reinterpret_cast<int2*>(static_cast<uint8_t*>(ws) + off_desc);
+  Partial* part = reinterpret_cast<Partial*>(
+      static_cast<uint8_t*>(ws) + off_desc + (((size_t)max_rows * sizeof(int2) + 255) & ~size_t(255)));
   unsigned int* err = device_error_word();
   const int sms = num_sms_cached();
   const long long max_items = (long long)max_rows * n_chunks;
-  long long grid = (long long)sms * 8;
+  long long grid = sms;  // persistent, one CTA per SM
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
+  if (!vocab_configure()) return DSPARK_ECUDA;
   if (pdt == DSPARK_F32) {
     const float* t = static_cast<const float*>(p_t);
     const float* d = static_cast<const float*>(p_d);
     accept_test_kernel<float><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
         t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, max_rows, accept_len, cap_len, info,
-        err);
+        row_desc, err);
     DSPARK_LAUNCH_CHECK();
-    accept_vocab_kernel<float><<<(int)grid, kVocabThreads, 0, stream>>>(t, d, exp_noise, V, n_chunks,
-                                                                        cu, B, gamma, max_rows, info,
-                                                                        part);
+    accept_vocab_kernel<float><<<(int)grid, kVocabCtaThreads, sizeof(VocabSmem), stream>>>(
+        t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows, row_desc, part, err);
   } else {
     const __nv_bfloat16* t = static_cast<const __nv_bfloat16*>(p_t);
     const __nv_bfloat16* d = static_cast<const __nv_bfloat16*>(p_d);
     accept_test_kernel<__nv_bfloat16><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
         t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, max_rows, accept_len, cap_len, info,
-        err);
+        row_desc, err);
     DSPARK_LAUNCH_CHECK();
-    accept_vocab_kernel<__nv_bfloat16><<<(int)grid, kVocabThreads, 0, stream>>>(
-        t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows, info, part);
+    accept_vocab_kernel<__nv_bfloat16><<<(int)grid, kVocabCtaThreads, sizeof(VocabSmem), stream>>>(
+        t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows, row_desc, part, err);
   }
   DSPARK_LAUNCH_CHECK();
-  accept_final_kernel<<<ceil_div(B * 32, 128), 128, 0, stream>>>(cu, B, gamma, max_rows, n_chunks,
-                                                                 info, part, out_tok, cstar, fallback);
+  if (pdt == DSPARK_F32)
+    accept_final_kernel<float><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
+        static_cast<const float*>(p_t), exp_noise, V, cu, B, gamma, max_rows, n_chunks, info, part,
+        out_tok, cstar, fallback);
+  else
+    accept_final_kernel<__nv_bfloat16><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(p_t), exp_noise, V, cu, B, gamma, max_rows, n_chunks,
+        info, part, out_tok, cstar, fallback);
   DSPARK_LAUNCH_CHECK();
   return DSPARK_OK;
 }

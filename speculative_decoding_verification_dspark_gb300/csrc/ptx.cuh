@@ -69,6 +69,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Bulk (non-tensor) copy global -> shared, completing `bytes` on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t sdst, const void* gsrc, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          sdst),
+      "l"(gsrc), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Bulk (non-tensor) copy shared -> global, tracked by the issuing thread's bulk groups.
 __device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),

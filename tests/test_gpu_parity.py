@@ -237,6 +237,28 @@ def test_ragged_edges(mode):
         assert sch.windows[0] == wl.gamma and sch.windows[1] == 0
 
 
+@pytest.mark.parametrize("mode", ["compact", "cap_accept"])
+def test_all_zero_residual_falls_back_to_target(mode):
+    """Draft = target everywhere except one inflated draft probability at request 0's
+    first draft token, with u close to 1: that draft is rejected and the residual
+    max(0, p_t - p_d) is zero on the whole row, so the correction is drawn from p_t
+    (reading A12); every other request accepts its whole window."""
+    wl = W.WORKLOADS["tiny"]
+    inp = W.make_inputs(wl, 4)
+    conf = inp["conf"].clone()
+    conf[0] = 20.0                                   # request 0 verifies its whole block
+    inp["conf"] = conf
+    pd = inp["p_target_dense"][:, :wl.gamma].clone()
+    x = int(inp["draft_tok"][0, 0])
+    pd[0, 0, x] = pd[0, 0, x] * 1.5
+    inp["p_draft"] = pd
+    u = inp["uniforms"].clone()
+    u[0, 0] = 0.99
+    inp["uniforms"] = u
+    g, sch, pk, acc = run_and_check(inp, MODES[mode])
+    assert acc.residual_fallback[0] and int(acc.accept_len[0]) == 0
+
+
 @pytest.mark.parametrize("B,G", [(3, 1), (5, 7), (2, 16)])
 def test_group_sizes_and_row_tiles(B, G):
     """Query heads per KV head from 1 to 16 (16 x (gamma+1) > 128 rows: two row tiles)."""
