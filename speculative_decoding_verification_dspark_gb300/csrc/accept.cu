@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(128)
                        int mode, int B, int gamma, int max_rows, int32_t* __restrict__ accept_len,
                        int32_t* __restrict__ cap_len, RowInfo* __restrict__ info,
                        int2* __restrict__ row_desc, unsigned int* __restrict__ err) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (cu[B] > max_rows) {  // packed rows beyond the caller's buffers: report, touch nothing
@@ -245,6 +247,8 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
   extern __shared__ __align__(128) uint8_t vsmem_raw[];
   VocabSmem& S = *reinterpret_cast<VocabSmem*>(vsmem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_release();
+  pdl_wait();  // row descriptors come from the test kernel
   const int M = cu[B];
   if (M > max_rows) return;  // reported by the test kernel (block-uniform)
   // items round-robin over the CTAs: the chunks of one row (and so the costlier
@@ -471,6 +475,8 @@ __global__ void __launch_bounds__(128)
                         int n_chunks, const RowInfo* __restrict__ info,
                         const Partial* __restrict__ part, int32_t* __restrict__ out_tok,
                         float* __restrict__ cstar, int32_t* __restrict__ fallback) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= B || cu[B] > max_rows) return;  // warp-uniform
@@ -582,32 +588,36 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
   if (pdt == DSPARK_F32) {
     const float* t = static_cast<const float*>(p_t);
     const float* d = static_cast<const float*>(p_d);
-    accept_test_kernel<float><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
-        t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, max_rows, accept_len, cap_len, info,
-        row_desc, err);
-    DSPARK_LAUNCH_CHECK();
-    accept_vocab_kernel<float><<<(int)grid, kVocabCtaThreads, sizeof(VocabSmem), stream>>>(
-        t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows, row_desc, part, err);
+    if (launch_pdl(accept_test_kernel<float>, dim3(ceil_div(B * 32, 128)), dim3(128), 0, stream, t,
+                   d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, max_rows, accept_len,
+                   cap_len, info, row_desc, err) != cudaSuccess)
+      return DSPARK_ECUDA;
+    if (launch_pdl(accept_vocab_kernel<float>, dim3((int)grid), dim3(kVocabCtaThreads),
+                   sizeof(VocabSmem), stream, t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows,
+                   row_desc, part, err) != cudaSuccess)
+      return DSPARK_ECUDA;
   } else {
     const __nv_bfloat16* t = static_cast<const __nv_bfloat16*>(p_t);
     const __nv_bfloat16* d = static_cast<const __nv_bfloat16*>(p_d);
-    accept_test_kernel<__nv_bfloat16><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
-        t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, max_rows, accept_len, cap_len, info,
-        row_desc, err);
-    DSPARK_LAUNCH_CHECK();
-    accept_vocab_kernel<__nv_bfloat16><<<(int)grid, kVocabCtaThreads, sizeof(VocabSmem), stream>>>(
-        t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows, row_desc, part, err);
+    if (launch_pdl(accept_test_kernel<__nv_bfloat16>, dim3(ceil_div(B * 32, 128)), dim3(128), 0,
+                   stream, t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, max_rows,
+                   accept_len, cap_len, info, row_desc, err) != cudaSuccess)
+      return DSPARK_ECUDA;
+    if (launch_pdl(accept_vocab_kernel<__nv_bfloat16>, dim3((int)grid), dim3(kVocabCtaThreads),
+                   sizeof(VocabSmem), stream, t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows,
+                   row_desc, part, err) != cudaSuccess)
+      return DSPARK_ECUDA;
   }
-  DSPARK_LAUNCH_CHECK();
+  cudaError_t e;
   if (pdt == DSPARK_F32)
-    accept_final_kernel<float><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
-        static_cast<const float*>(p_t), exp_noise, V, cu, B, gamma, max_rows, n_chunks, info, part,
-        out_tok, cstar, fallback);
+    e = launch_pdl(accept_final_kernel<float>, dim3(ceil_div(B * 32, 128)), dim3(128), 0, stream,
+                   static_cast<const float*>(p_t), exp_noise, V, cu, B, gamma, max_rows, n_chunks,
+                   info, part, out_tok, cstar, fallback);
   else
-    accept_final_kernel<__nv_bfloat16><<<ceil_div(B * 32, 128), 128, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(p_t), exp_noise, V, cu, B, gamma, max_rows, n_chunks,
-        info, part, out_tok, cstar, fallback);
-  DSPARK_LAUNCH_CHECK();
+    e = launch_pdl(accept_final_kernel<__nv_bfloat16>, dim3(ceil_div(B * 32, 128)), dim3(128), 0,
+                   stream, static_cast<const __nv_bfloat16*>(p_t), exp_noise, V, cu, B, gamma,
+                   max_rows, n_chunks, info, part, out_tok, cstar, fallback);
+  if (e != cudaSuccess) return DSPARK_ECUDA;
   return DSPARK_OK;
 }
 

@@ -30,10 +30,30 @@ __device__ __forceinline__ int upper_segment(const int32_t* cu, int n, int x) {
 
 int num_sms_cached();
 
-}  // namespace dspark
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// launch_pdl, may therefore start while the kernel before it in the stream is
+// still running, and calls pdl_wait() before it touches global memory that
+// earlier work writes or reads.  pdl_release() lets the next kernel start
+// launching (its own pdl_wait() still waits for this grid to complete).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
-#define DSPARK_LAUNCH_CHECK()                                  \
-  do {                                                         \
-    cudaError_t e__ = cudaGetLastError();                      \
-    if (e__ != cudaSuccess) return DSPARK_ECUDA;                \
-  } while (0)
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+}  // namespace dspark

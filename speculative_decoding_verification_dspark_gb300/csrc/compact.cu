@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(1024)
                          int32_t* __restrict__ committed, int32_t* __restrict__ n_committed,
                          CompactWs* __restrict__ cws, int* __restrict__ old_ctx,
                          unsigned int* __restrict__ err) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
   __shared__ int s_warp[32];
   __shared__ int s_flags;
   __shared__ int s_top;
@@ -122,6 +124,8 @@ __global__ void __launch_bounds__(128)
                         const int* __restrict__ old_ctx, const CompactWs* __restrict__ cws,
                         uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
                         unsigned int* __restrict__ err) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
   const int r = blockIdx.x;
   const int i = blockIdx.y;
   if (!cws->ok) return;
@@ -156,18 +160,17 @@ int launch_compact(const void* k_new, const void* v_new, int row_bytes, int max_
                    cudaStream_t stream) {
   CompactWs* cws = static_cast<CompactWs*>(ws);
   int* old_ctx = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + sizeof(CompactWs));
-  compact_alloc_kernel<<<1, 1024, 0, stream>>>(cu, max_rows, accept_len, out_tok, draft_tok, B, gamma,
-                                               page_size,
-                                               max_pages, n_pages, page_table, ctx_len, anchor,
-                                               free_pages, free_top, committed, n_committed, cws,
-                                               old_ctx, device_error_word());
-  DSPARK_LAUNCH_CHECK();
+  if (launch_pdl(compact_alloc_kernel, dim3(1), dim3(1024), 0, stream, cu, max_rows, accept_len,
+                 out_tok, draft_tok, B, gamma, page_size, max_pages, n_pages, page_table, ctx_len,
+                 anchor, free_pages, free_top, committed, n_committed, cws, old_ctx,
+                 device_error_word()) != cudaSuccess)
+    return DSPARK_ECUDA;
   dim3 grid(B, gamma + 1);
-  compact_copy_kernel<<<grid, 128, 0, stream>>>(
-      static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), row_bytes, cu,
-      accept_len, gamma, page_size, max_pages, n_pages, page_table, old_ctx, cws,
-      static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), device_error_word());
-  DSPARK_LAUNCH_CHECK();
+  if (launch_pdl(compact_copy_kernel, grid, dim3(128), 0, stream, static_cast<const uint8_t*>(k_new),
+                 static_cast<const uint8_t*>(v_new), row_bytes, cu, accept_len, gamma, page_size,
+                 max_pages, n_pages, page_table, old_ctx, cws, static_cast<uint8_t*>(k_cache),
+                 static_cast<uint8_t*>(v_cache), device_error_word()) != cudaSuccess)
+    return DSPARK_ECUDA;
   return DSPARK_OK;
 }
 

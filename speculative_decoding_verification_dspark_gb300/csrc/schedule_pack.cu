@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(64)
     calibrate_kernel(const float* __restrict__ conf, int conf_is_logit,
                      const float* __restrict__ sts_temp, int B, int gamma,
                      float* __restrict__ a_hat) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
   const int r = blockIdx.x * 2 + (threadIdx.x >> 5);
   const int j = threadIdx.x & 31;
   if (r >= B) return;  // warp-uniform
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(kSchedThreads)
     greedy_kernel(const float* __restrict__ a_hat, const float* __restrict__ cost, int B,
                   int gamma, int max_tokens, int mode, int32_t* __restrict__ windows,
                   int32_t* __restrict__ M_out, double* __restrict__ E_out) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
   __shared__ unsigned long long keys[DSPARK_MAX_CANDS];
   __shared__ double s_warp[32];
   __shared__ int s_first;
@@ -218,6 +222,8 @@ __global__ void __launch_bounds__(1024)
                 int32_t* __restrict__ tier_out, int32_t* __restrict__ row_req,
                 int32_t* __restrict__ row_pos, int32_t* __restrict__ row_tok,
                 unsigned int* __restrict__ err) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
   __shared__ int s_cu[DSPARK_MAX_B + 1];
   __shared__ int s_warp[32];
   __shared__ int s_tier;
@@ -280,17 +286,18 @@ int launch_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
                     const float* cost_table, int B, int gamma, int max_tokens, int mode,
                     int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
                     cudaStream_t stream) {
-  calibrate_kernel<<<ceil_div(B, 2), 64, 0, stream>>>(conf, conf_is_logit, sts_temp, B, gamma, a_hat);
-  DSPARK_LAUNCH_CHECK();
+  if (launch_pdl(calibrate_kernel, dim3(ceil_div(B, 2)), dim3(64), 0, stream, conf, conf_is_logit,
+                 sts_temp, B, gamma, a_hat) != cudaSuccess)
+    return DSPARK_ECUDA;
   // kPerThread candidates per thread, no more warps than the candidates need:
   // the fp64 scan and tests run at the part's (low) fp64 rate.
   int npow = 1;
   while (npow < B * gamma) npow <<= 1;
   int threads = ceil_div(ceil_div(npow, kPerThread), 32) * 32;
   threads = threads < 32 ? 32 : (threads > kSchedThreads ? kSchedThreads : threads);
-  greedy_kernel<<<1, threads, 0, stream>>>(a_hat, cost_table, B, gamma, max_tokens, mode, windows,
-                                           M_out, E_out);
-  DSPARK_LAUNCH_CHECK();
+  if (launch_pdl(greedy_kernel, dim3(1), dim3(threads), 0, stream, a_hat, cost_table, B, gamma,
+                 max_tokens, mode, windows, M_out, E_out) != cudaSuccess)
+    return DSPARK_ECUDA;
   return DSPARK_OK;
 }
 
@@ -298,10 +305,10 @@ int launch_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* a
                 const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
                 int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out, int32_t* tier_out,
                 int32_t* row_req, int32_t* row_pos, int32_t* row_tok, cudaStream_t stream) {
-  pack_kernel<<<1, 1024, 0, stream>>>(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma,
-                                      mode, max_rows, cu_seqlens, M_out, tier_out, row_req, row_pos,
-                                      row_tok, device_error_word());
-  DSPARK_LAUNCH_CHECK();
+  if (launch_pdl(pack_kernel, dim3(1), dim3(1024), 0, stream, windows, ctx_len, anchor, draft_tok,
+                 tiers, n_tiers, B, gamma, mode, max_rows, cu_seqlens, M_out, tier_out, row_req,
+                 row_pos, row_tok, device_error_word()) != cudaSuccess)
+    return DSPARK_ECUDA;
   return DSPARK_OK;
 }
 

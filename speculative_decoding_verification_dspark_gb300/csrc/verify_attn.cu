@@ -323,6 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const Params p
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  pdl_release();
+  pdl_wait();  // the work list and the step's inputs come from earlier kernels
   const int it_begin = prm.item_begin[blockIdx.x];
   const int it_end = prm.item_begin[blockIdx.x + 1];
   const int G = C::MLA ? kRows : prm.Hq / prm.Hkv;  // query rows per block row
@@ -657,6 +659,8 @@ __global__ void __launch_bounds__(1024)
                     int max_splits, int max_items, AttnItem* __restrict__ items,
                     int* __restrict__ item_begin, SplitGroup* __restrict__ groups,
                     unsigned int* __restrict__ err) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
   __shared__ long long s_off[DSPARK_MAX_B + 1];
   __shared__ int s_tt[DSPARK_MAX_B];
   __shared__ int s_n[DSPARK_MAX_B];
@@ -791,6 +795,8 @@ __global__ void __launch_bounds__(256)
                    int G, int Hq, int rows_per_slot, int d_part, int d_v_total,
                    const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                    float* __restrict__ out, float* __restrict__ lse, int mla) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
   const int lane = threadIdx.x & 31;
   const SplitGroup sg = groups[blockIdx.x];
   const int ns = sg.nsplit;
@@ -894,10 +900,10 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
   const int max_items = pl.max_items > 0x7fffffff ? 0x7fffffff : (int)pl.max_items;
   const int splits = max_splits < 2 ? 2 : (max_splits > 32 ? 32 : max_splits);
 
-  worklist_kernel<<<1, 1024, 0, stream>>>(ctx_len, cu_seqlens, B, max_rows, Hkv, pl.parts,
-                                           pl.rows_per_tile, pl.nk, ncta, splits, max_items, items,
-                                           item_begin, groups, err);
-  DSPARK_LAUNCH_CHECK();
+  if (launch_pdl(worklist_kernel, dim3(1), dim3(1024), 0, stream, ctx_len, cu_seqlens, B, max_rows,
+                 Hkv, pl.parts, pl.rows_per_tile, pl.nk, ncta, splits, max_items, items, item_begin,
+                 groups, err) != cudaSuccess)
+    return DSPARK_ECUDA;
 
   if (pl.mla) {
     Params prm;
@@ -928,8 +934,9 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
     prm.n_pages = n_pages;
     prm.scale_log2 = scale * 1.4426950408889634f;
     if (!configure_smem<CfgMLA>()) return DSPARK_ECUDA;
-    verify_attn_kernel<CfgMLA><<<ncta, kThreads, CfgMLA::SMEM_BYTES, stream>>>(prm);
-    DSPARK_LAUNCH_CHECK();
+    if (launch_pdl(verify_attn_kernel<CfgMLA>, dim3(ncta), dim3(kThreads), CfgMLA::SMEM_BYTES, stream,
+                   prm) != cudaSuccess)
+      return DSPARK_ECUDA;
   } else {
     const int rc = gqa::launch_kernel(pl.nt, q, k_new, v_new, k_cache, v_cache, n_pages, page_table,
                                       max_pages, ctx_len, cu_seqlens, B, max_rows, Hq, Hkv,
@@ -938,10 +945,9 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
     if (rc != DSPARK_OK) return rc;
   }
   const int G = pl.mla ? Hq : Hq / Hkv;
-  combine_kernel<<<dim3(ncta, kRows / 8), 256, 0, stream>>>(cu_seqlens, groups, G, Hq, kRows,
-                                                           pl.d_part, d_v, ws_o, ws_lse, out, lse,
-                                                           pl.mla ? 1 : 0);
-  DSPARK_LAUNCH_CHECK();
+  if (launch_pdl(combine_kernel, dim3(ncta, kRows / 8), dim3(256), 0, stream, cu_seqlens, groups, G,
+                 Hq, kRows, pl.d_part, d_v, ws_o, ws_lse, out, lse, pl.mla ? 1 : 0) != cudaSuccess)
+    return DSPARK_ECUDA;
   return DSPARK_OK;
 }
 

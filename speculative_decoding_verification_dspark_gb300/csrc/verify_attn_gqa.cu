@@ -309,6 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
+  pdl_release();
+  pdl_wait();  // the work list and the step's inputs come from earlier kernels
   const int it_begin = prm.item_begin[blockIdx.x];
   const int it_end = prm.item_begin[blockIdx.x + 1];
   {
@@ -914,18 +916,23 @@ int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, c
   switch (nt) {
     case 32:
       if (!configure<32>()) return DSPARK_ECUDA;
-      verify_attn_gqa_kernel<32><<<grid, kThreads, Cfg<32>::SMEM_BYTES, stream>>>(tk, tv, tkn, tvn, prm);
+      if (launch_pdl(verify_attn_gqa_kernel<32>, dim3(grid), dim3(kThreads), Cfg<32>::SMEM_BYTES,
+                     stream, tk, tv, tkn, tvn, prm) != cudaSuccess)
+        return DSPARK_ECUDA;
       break;
     case 64:
       if (!configure<64>()) return DSPARK_ECUDA;
-      verify_attn_gqa_kernel<64><<<grid, kThreads, Cfg<64>::SMEM_BYTES, stream>>>(tk, tv, tkn, tvn, prm);
+      if (launch_pdl(verify_attn_gqa_kernel<64>, dim3(grid), dim3(kThreads), Cfg<64>::SMEM_BYTES,
+                     stream, tk, tv, tkn, tvn, prm) != cudaSuccess)
+        return DSPARK_ECUDA;
       break;
     default:
       if (!configure<128>()) return DSPARK_ECUDA;
-      verify_attn_gqa_kernel<128><<<grid, kThreads, Cfg<128>::SMEM_BYTES, stream>>>(tk, tv, tkn, tvn, prm);
+      if (launch_pdl(verify_attn_gqa_kernel<128>, dim3(grid), dim3(kThreads), Cfg<128>::SMEM_BYTES,
+                     stream, tk, tv, tkn, tvn, prm) != cudaSuccess)
+        return DSPARK_ECUDA;
       break;
   }
-  DSPARK_LAUNCH_CHECK();
   return DSPARK_OK;
 }
 
