@@ -102,10 +102,23 @@ __global__ void __launch_bounds__(64)
   if (j < gamma) a_hat[r * gamma + j] = v;
 }
 
-// Greedy window choice over the calibrated survival (one CTA of 1024 threads):
-// bitonic sort of the <= 4096 (a_hat, request, position) keys, fp64 block-wide
-// prefix sums of a_hat in sorted order (E before each candidate), every
-// candidate's throughput test in parallel, first failure by a block minimum.
+// Compare-exchange of register slots A < B (indices tid + A*T < tid + B*T) in
+// bitonic stage k.
+template <int A, int Bq>
+__device__ __forceinline__ void bitonic_slots(unsigned long long (&kv)[4], int tid, int T, int k) {
+  const bool asc = ((tid + A * T) & k) == 0;
+  const unsigned long long a = kv[A], b = kv[Bq];
+  if ((a > b) == asc) {
+    kv[A] = b;
+    kv[Bq] = a;
+  }
+}
+
+// Greedy window choice over the calibrated survival (one CTA, one thread per
+// candidate up to 1024): bitonic sort of the <= 4096 (a_hat, request, position)
+// keys, fp64 block-wide prefix sums of a_hat in sorted order (E before each
+// candidate), every candidate's throughput test in parallel, first failure by a
+// block minimum.
 __global__ void __launch_bounds__(kSchedThreads)
     greedy_kernel(const float* __restrict__ a_hat, const float* __restrict__ cost, int B,
                   int gamma, int max_tokens, int mode, int32_t* __restrict__ windows,
@@ -122,35 +135,68 @@ __global__ void __launch_bounds__(kSchedThreads)
   while (npow < n) npow <<= 1;
 
   if (tid == 0) s_first = n;
-  for (int k = tid; k < npow; k += blockDim.x) {
+  for (int r = tid; r < B; r += blockDim.x) s_win[r] = 0;
+  // Bitonic sort, ascending keys = survival descending.  Thread t holds the keys
+  // at t + q*T (T = blockDim.x, q < npow/T) in registers: pairs at distance < 32
+  // are exchanged by shuffles, at distance >= T inside the thread, and only the
+  // distances 32..T/2 go through shared memory.
+  const int T = blockDim.x;
+  if (npow < T) npow = T;  // at least one key per thread (padding keys sort last)
+  const int m = npow / T;  // 1, 2 or 4 (npow <= T * kPerThread, T >= 32)
+  unsigned long long kv[kPerThread];
+#pragma unroll
+  for (int q = 0; q < kPerThread; ++q) {
+    const int k = tid + q * T;
     unsigned long long key = ~0ull;
-    if (k < n) {
+    if (q < m && k < n) {
       const int r = k / gamma, j = k - r * gamma;
       key = (static_cast<unsigned long long>(~__float_as_uint(a_hat[k])) << 32) |
             (static_cast<unsigned>(r) << 16) | static_cast<unsigned>(j);
     }
-    keys[k] = key;
+    kv[q] = key;
   }
-  for (int r = tid; r < B; r += blockDim.x) s_win[r] = 0;
-  __syncthreads();
-
-  // bitonic sort, ascending keys = survival descending
   for (int k = 2; k <= npow; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < npow; i += blockDim.x) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long a = keys[i], b = keys[ixj];
-          const bool up = (i & k) == 0;
-          if ((a > b) == up) {
-            keys[i] = b;
-            keys[ixj] = a;
+      if (j >= T) {  // partner in this thread: slot q ^ (j / T), j / T = 1 or 2
+        if (j == T) {
+          bitonic_slots<0, 1>(kv, tid, T, k);
+          if (m > 2) bitonic_slots<2, 3>(kv, tid, T, k);
+        } else {
+          bitonic_slots<0, 2>(kv, tid, T, k);
+          bitonic_slots<1, 3>(kv, tid, T, k);
+        }
+      } else if (j >= 32) {  // partner in another warp: through shared memory
+#pragma unroll
+        for (int q = 0; q < kPerThread; ++q)
+          if (q < m) keys[tid + q * T] = kv[q];
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < kPerThread; ++q) {
+          if (q < m) {
+            const int i = tid + q * T;
+            const unsigned long long p = keys[i ^ j];
+            const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+            kv[q] = keep_min ? (kv[q] < p ? kv[q] : p) : (kv[q] > p ? kv[q] : p);
+          }
+        }
+        __syncthreads();
+      } else {  // partner lane ^ j of this warp
+#pragma unroll
+        for (int q = 0; q < kPerThread; ++q) {
+          if (q < m) {  // uniform over the block
+            const int i = tid + q * T;
+            const unsigned long long p = __shfl_xor_sync(0xffffffffu, kv[q], j);
+            const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+            kv[q] = keep_min ? (kv[q] < p ? kv[q] : p) : (kv[q] > p ? kv[q] : p);
           }
         }
       }
-      __syncthreads();
     }
   }
+#pragma unroll
+  for (int q = 0; q < kPerThread; ++q)
+    if (q < m) keys[tid + q * T] = kv[q];
+  __syncthreads();
 
   // E_k = B + sum_{i<k} a_hat(i), fp64, thread owns 4 consecutive candidates
   double v[kPerThread];
@@ -200,7 +246,7 @@ __global__ void __launch_bounds__(kSchedThreads)
 
   for (int k = tid; k < kstar; k += blockDim.x) {
     const int r = static_cast<int>((keys[k] >> 16) & 0xFFFFu);
-    atomicAdd(&s_win[r], 1);
+    if (r < B) atomicAdd(&s_win[r], 1);
   }
   // E before candidate k*: the owning thread recomputes it
   if (kstar < n && kstar / kPerThread == tid) {
@@ -289,12 +335,10 @@ int launch_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
   if (launch_pdl(calibrate_kernel, dim3(ceil_div(B, 2)), dim3(64), 0, stream, conf, conf_is_logit,
                  sts_temp, B, gamma, a_hat) != cudaSuccess)
     return DSPARK_ECUDA;
-  // kPerThread candidates per thread, no more warps than the candidates need:
-  // the fp64 scan and tests run at the part's (low) fp64 rate.
   int npow = 1;
   while (npow < B * gamma) npow <<= 1;
-  int threads = ceil_div(ceil_div(npow, kPerThread), 32) * 32;
-  threads = threads < 32 ? 32 : (threads > kSchedThreads ? kSchedThreads : threads);
+  // one sorting key per thread up to 1024 keys (two or four beyond), at least a warp
+  const int threads = npow < 32 ? 32 : (npow > kSchedThreads ? kSchedThreads : npow);
   if (launch_pdl(greedy_kernel, dim3(1), dim3(threads), 0, stream, a_hat, cost_table, B, gamma,
                  max_tokens, mode, windows, M_out, E_out) != cudaSuccess)
     return DSPARK_ECUDA;
