@@ -336,8 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_v = warp == kVWarp;
     const CUtensorMap* tm_c = is_v ? &tm_v : &tm_k;
     const CUtensorMap* tm_n = is_v ? &tm_vn : &tm_kn;
-    const __nv_bfloat16* cache = prm.v_cache;
-    const __nv_bfloat16* fresh = prm.v_new;
     // K boxes follow the page (up to a tile); V boxes are 16-key chunks
     const int box_rows = is_v ? kChunkRows : (P < kKT ? P : kKT);
     int g = 0;
@@ -350,7 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_r = item.n_r;
       const int ct = ceil_div(ctx, kKT);
       const int32_t* ptab = prm.page_table + (long long)r * prm.max_pages;
-      const long long rs = (long long)prm.Hkv * kD;
       int win_base = -1, win_page = 0;
       for (int t = item.tb; t < item.te; ++t, ++g) {
         const int s = g % kStages;
@@ -361,12 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t dst0 = L.stage(s) + (is_v ? kKVBytes : 0);
         const int vis = visible_keys(t, ct, ctx, n_r);  // >= 1
-        // boxes copied whole by TMA: K every box with a visible key, V the full chunks;
-        // cache boxes are box_rows keys, block-row boxes kChunkRows rows
+        // boxes copied by TMA: K every box with a visible key, V every 16-key chunk
+        // with one (the MMA warp zeroes the V rows past them); cache boxes are
+        // box_rows keys, block-row boxes kChunkRows rows
         const int rows_box = t < ct ? box_rows : kChunkRows;
-        const int nb = is_v ? (vis >> 4) : ceil_div(vis, rows_box);
-        const int rem = is_v ? (vis & 15) : 0;            // V rows of the partial chunk
-        if (lane == 0 && nb > 0) mbar_expect_tx(full, nb * 2 * rows_box * 128);
+        const int nb = ceil_div(vis, rows_box);
+        if (lane == 0) mbar_expect_tx(full, nb * 2 * rows_box * 128);
         __syncwarp();
         if (t < ct) {
           const int slot0 = (t * kKT) >> lp;
@@ -393,25 +390,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_4d(dst0 + cb * kTileHalf + bx * box_rows * 128, tm_c, full, cb * 64,
                           item.kvh, kg & (P - 1), page);
           }
-          if (rem > 0) {
-            // V: the partial chunk, all loads in flight at once, zeros past ctx
-            const int kg = t * kKT + nb * kChunkRows;
-            const int page = __shfl_sync(0xffffffffu, win_page, ((kg >> lp) - win_base) & 31);
-            const long long off =
-                ((long long)(page >= 0 ? page : 0) * P + (kg & (P - 1))) * rs + (long long)item.kvh * kD;
-            uint4 v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int idx = i * 32 + lane, rr = idx >> 4, q = idx & 15;
-              v[i] = make_uint4(0, 0, 0, 0);
-              if (rr < rem && page >= 0) v[i] = ldg_nc_v4(cache + off + rr * rs + q * 8);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int idx = i * 32 + lane, rr = idx >> 4, q = idx & 15;
-              st_shared_v4(dst0 + (q >> 3) * kTileHalf + sw128_off(nb * kChunkRows + rr, q & 7), v[i]);
-            }
-          }
         } else {
           // block tile: the request's own rows b0.., 16-row boxes of the packed buffer
           const int b0 = (t - ct) * kKT;
@@ -420,24 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(dst0 + cb * kTileHalf + bx * kChunkRows * 128, tm_n, full, cb * 64, item.kvh,
                         c0 + b0 + bx * kChunkRows);
           }
-          if (rem > 0) {
-            const int row0 = nb * kChunkRows;
-            const long long off = (long long)(c0 + b0 + row0) * rs + (long long)item.kvh * kD;
-            uint4 v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int idx = i * 32 + lane, rr = idx >> 4, q = idx & 15;
-              v[i] = make_uint4(0, 0, 0, 0);
-              if (rr < rem) v[i] = ldg_nc_v4(fresh + off + rr * rs + q * 8);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int idx = i * 32 + lane, rr = idx >> 4, q = idx & 15;
-              st_shared_v4(dst0 + (q >> 3) * kTileHalf + sw128_off(row0 + rr, q & 7), v[i]);
-            }
-          }
         }
-        if (rem > 0) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(full);
       }
@@ -488,21 +449,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = idesc_bf16_f32(kKT, NT, 0, 0);
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(kD, NT, 1, 1);
-      int g = 0, n_it = 0, last_pv = -1;
-      bool ok = true;
-      // PV of tile gp (local index `local` in its item) into O^T buffer ob, over the
-      // 16-key chunks that hold visible keys only
-      auto issue_pv = [&](int gp, int local, int nch, int ob) -> bool {
-        const int pb = gp % C::P_BUFS;
-        if (!wait_bar(L.p_full(pb), (gp / C::P_BUFS) & 1, cx)) return false;
+    // The whole warp runs the loop (lane 0 issues); before the PV product of a
+    // tile whose visible keys end inside a 16-key chunk, the warp zeroes that
+    // chunk's V rows past them (TMA copied the whole chunk), so that no stale or
+    // foreign value meets a zero probability.
+    constexpr uint32_t IDESC_QK = idesc_bf16_f32(kKT, NT, 0, 0);
+    constexpr uint32_t IDESC_PV = idesc_bf16_f32(kD, NT, 1, 1);
+    int g = 0, n_it = 0, last_pv = -1;
+    bool ok = true;
+    // PV of tile gp (local index `local` in its item) into O^T buffer ob, over the
+    // 16-key chunks that hold visible keys only
+    auto issue_pv = [&](int gp, int local, int vis, int ob) -> bool {
+      const int pb = gp % C::P_BUFS;
+      if (!wait_warp(L.p_full(pb), (gp / C::P_BUFS) & 1, cx)) return false;
+      const int s = gp % kStages;
+      if (!wait_warp(L.v_full(s), (gp / kStages) & 1, cx)) return false;
+      const uint32_t vb = L.stage(s) + kKVBytes;
+      const int nch = ceil_div(vis, 16);
+      if (vis & 15) {
+        // rows vis .. 16*nch - 1: (rows) x 2 column blocks x 8 16-byte pieces
+        const int r0 = vis, nz = (16 * nch - vis) * 16;
+        for (int idx = lane; idx < nz; idx += 32) {
+          const int row = r0 + (idx >> 4), cb = (idx >> 3) & 1, c = idx & 7;
+          st_shared_v4(vb + cb * kTileHalf + sw128_off(row, c), make_uint4(0, 0, 0, 0));
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) {
         tc_fence_after();
-        const int s = gp % kStages;
-        if (!wait_bar(L.v_full(s), (gp / kStages) & 1, cx)) return false;
-        tc_fence_after();
-        const uint32_t vb = L.stage(s) + kKVBytes;
         const uint32_t d_o = tmem + C::TMEM_O + ob * NT;
         for (int kk = 0; kk < nch; ++kk) {
           // A = V^T (M = d, MN-major), B = P^T (N = query rows, MN-major); K = 16 keys
@@ -512,26 +487,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(L.p_empty(pb));
         umma_commit(L.v_empty(s));
-        last_pv = gp;
-        return true;
-      };
-      for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
-        const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
-        const int qb = n_it % C::Q_BUFS, ob = n_it & 1;
-        const int ctx = item.ctx;
-        const int n_r = item.n_r;
-        const int ct = ceil_div(ctx, kKT);
-        if (!wait_bar(L.q_full(qb), (n_it / C::Q_BUFS) & 1, cx)) { ok = false; break; }
-        // O^T buffer ob was last read by the epilogue of item n_it - 2
-        if (n_it >= 2 && !wait_bar(L.o_free(ob), ((n_it >> 1) - 1) & 1, cx)) { ok = false; break; }
-        const uint32_t qa = L.q(qb);
-        const int ntiles = item.te - item.tb;
-        int prev_nch = 0;
-        for (int l = 0; l < ntiles; ++l, ++g) {
-          const int s = g % kStages;
-          const int sb = g & 1;
-          if (!wait_bar(L.k_full(s), (g / kStages) & 1, cx)) { ok = false; break; }
-          if (g >= 2 && !wait_bar(L.s_free(sb), ((g >> 1) - 1) & 1, cx)) { ok = false; break; }
+      }
+      __syncwarp();
+      last_pv = gp;
+      return true;
+    };
+    for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
+      const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
+      const int qb = n_it % C::Q_BUFS, ob = n_it & 1;
+      const int ctx = item.ctx;
+      const int n_r = item.n_r;
+      const int ct = ceil_div(ctx, kKT);
+      if (!wait_warp(L.q_full(qb), (n_it / C::Q_BUFS) & 1, cx)) { ok = false; break; }
+      // O^T buffer ob was last read by the epilogue of item n_it - 2
+      if (n_it >= 2 && !wait_warp(L.o_free(ob), ((n_it >> 1) - 1) & 1, cx)) { ok = false; break; }
+      const uint32_t qa = L.q(qb);
+      const int ntiles = item.te - item.tb;
+      int prev_vis = 0;
+      for (int l = 0; l < ntiles; ++l, ++g) {
+        const int s = g % kStages;
+        const int sb = g & 1;
+        if (!wait_warp(L.k_full(s), (g / kStages) & 1, cx)) { ok = false; break; }
+        if (g >= 2 && !wait_warp(L.s_free(sb), ((g >> 1) - 1) & 1, cx)) { ok = false; break; }
+        if (lane == 0) {
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
@@ -543,14 +521,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(L.s_full(sb));
           umma_commit(L.k_empty(s));
           if (l == ntiles - 1) umma_commit(L.q_empty(qb));
-          if (l >= 1 && !issue_pv(g - 1, l - 1, prev_nch, ob)) { ok = false; break; }
-          prev_nch = ceil_div(visible_keys(item.tb + l, ct, ctx, n_r), 16);
         }
-        if (!ok) break;
-        if (!issue_pv(g - 1, ntiles - 1, prev_nch, ob)) { ok = false; break; }
+        __syncwarp();
+        if (l >= 1 && !issue_pv(g - 1, l - 1, prev_vis, ob)) { ok = false; break; }
+        prev_vis = visible_keys(item.tb + l, ct, ctx, n_r);
       }
-      if (last_pv >= 0) drain_bar(L.p_empty(last_pv % C::P_BUFS), (last_pv / C::P_BUFS) & 1, prm.err);
+      if (!ok) break;
+      if (!issue_pv(g - 1, ntiles - 1, prev_vis, ob)) { ok = false; break; }
     }
+    if (lane == 0 && last_pv >= 0)
+      drain_bar(L.p_empty(last_pv % C::P_BUFS), (last_pv / C::P_BUFS) & 1, prm.err);
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------- softmax / epilogue
     const int sw = warp & 3;                          // TMEM lane quadrant
