@@ -78,11 +78,13 @@ __global__ void __launch_bounds__(128)
                        const int32_t* __restrict__ windows, const int32_t* __restrict__ cu,
                        int mode, int B, int gamma, int max_rows, int32_t* __restrict__ accept_len,
                        int32_t* __restrict__ cap_len, RowInfo* __restrict__ info,
-                       int2* __restrict__ row_desc, unsigned int* __restrict__ err) {
+                       int2* __restrict__ row_desc, int* __restrict__ claim,
+                       unsigned int* __restrict__ err) {
   pdl_release();
   pdl_wait();  // inputs come from the kernels before this one
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *claim = 0;  // the vocabulary pass's item counter
   if (cu[B] > max_rows) {  // packed rows beyond the caller's buffers: report, touch nothing
     if (r == 0 && lane == 0) raise_error(err, DSPARK_DEVERR_ROWS_OVERFLOW);
     return;
@@ -156,6 +158,7 @@ struct VocabSmem {
   uint8_t stage[kVStages][kVStageBytes];
   uint8_t noise[kNStages][kSub * 4];
   WarpPart red[2][kConsumerWarps];
+  int4 meta[kVStages];  // item, sub-chunk | sub-chunks << 8, request, row flags
   uint64_t full[kVStages], empty[kVStages], nempty[kNStages], red_full[2], red_free[2];
   int abort_flag;
 };
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
                         const float* __restrict__ exp_noise, int V, int n_chunks,
                         const int32_t* __restrict__ cu, int B, int gamma, int max_rows,
                         const int2* __restrict__ row_desc, Partial* __restrict__ part,
-                        unsigned int* __restrict__ err) {
+                        int* __restrict__ claim, unsigned int* __restrict__ err) {
   extern __shared__ __align__(128) uint8_t vsmem_raw[];
   VocabSmem& S = *reinterpret_cast<VocabSmem*>(vsmem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -276,28 +279,40 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
   };
 
   if (warp == kProducerWarp) {
+    // Items are claimed one at a time from a counter shared by all CTAs (the costlier
+    // sampled rows then balance out); each stage carries its item in meta[].
     if (lane == 0) {
       int g = 0, gn = 0;  // main-ring and noise-ring sub-chunks issued
       bool ok = true;
-      long long item = blockIdx.x;
-      RowWork w_next;
-      if (item < n_items) w_next = row_work(row_desc, static_cast<int>(item / n_chunks));
-      for (; item < n_items && ok; item += gridDim.x) {
+      long long item = atomicAdd(claim, 1);
+      while (ok) {
+        long long next = n_items;
+        RowWork w{};
+        bool work = false;
+        if (item < n_items) {
+          next = atomicAdd(claim, 1);  // taken ahead: its latency hides behind this item
+          w = row_work(row_desc, static_cast<int>(item / n_chunks));
+          work = w.l1 || w.samp;
+        }
+        const int s = g % kVStages;
+        if (item < n_items && !work) {  // nothing to do on this row: next claim
+          item = next;
+          continue;
+        }
         const int row = static_cast<int>(item / n_chunks), ch = static_cast<int>(item % n_chunks);
-        const RowWork w = w_next;
-        // the next item's descriptor is loaded while this one's copies are issued
-        if (item + gridDim.x < n_items)
-          w_next = row_work(row_desc, static_cast<int>((item + gridDim.x) / n_chunks));
-        if (!w.l1 && !w.samp) continue;
-        const T* pt_row = p_t + (long long)row * V;
-        const T* pd_row = p_d + ((long long)w.r * gamma + (w.j < gamma ? w.j : 0)) * V;
-        const float* e_row = exp_noise + (long long)w.r * V;
-        const int ns = n_sub_of(ch);
+        const int ns = item < n_items ? n_sub_of(ch) : 1;
         for (int sb = 0; sb < ns; ++sb, ++g) {
-          const int s = g % kVStages;
+          const int st = g % kVStages;
           if (g >= kVStages &&
-              !vwait(ptx::smem_addr(&S.empty[s]), ((g / kVStages) - 1) & 1, abort_flag, err)) {
+              !vwait(ptx::smem_addr(&S.empty[st]), ((g / kVStages) - 1) & 1, abort_flag, err)) {
             ok = false;
+            break;
+          }
+          const uint32_t full = ptx::smem_addr(&S.full[st]);
+          if (item >= n_items) {  // end marker: a stage without data
+            S.meta[st] = make_int4(-1, 0, 0, 0);
+            ptx::mbar_arrive(full);
+            ok = false;  // done
             break;
           }
           const int sn = gn % kNStages;
@@ -306,11 +321,14 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
             ok = false;
             break;
           }
+          const T* pt_row = p_t + (long long)row * V;
+          const T* pd_row = p_d + ((long long)w.r * gamma + (w.j < gamma ? w.j : 0)) * V;
+          const float* e_row = exp_noise + (long long)w.r * V;
           const int v0 = ch * kChunk + sb * kSub;
           const uint32_t len = static_cast<uint32_t>(min(kSub, V - v0));
-          const uint32_t full = ptx::smem_addr(&S.full[s]);
-          const uint32_t base = ptx::smem_addr(S.stage[s]);
+          const uint32_t base = ptx::smem_addr(S.stage[st]);
           const uint32_t bytes = len * ES * (w.need_d ? 2u : 1u) + (w.samp ? len * 4u : 0u);
+          S.meta[st] = make_int4(static_cast<int>(item), sb | (ns << 8), w.r, row_desc[row].y);
           ptx::mbar_expect_tx(full, bytes);
           ptx::bulk_load_g2s(base, pt_row + v0, len * ES, full);
           if (w.need_d) ptx::bulk_load_g2s(base + kSub * 4, pd_row + v0, len * ES, full);
@@ -320,20 +338,21 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
           }
           ptx::mbar_arrive(full);
         }
+        (void)s;
+        item = next;
       }
     }
   } else if (warp == kReducerWarp) {
     // the consumer warps' results of an item -> its partial (fixed order: deterministic)
     int n_it = 0;
     bool ok = true;
-    for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int row = static_cast<int>(item / n_chunks), ch = static_cast<int>(item % n_chunks);
-      const RowWork w = row_work(row_desc, row);
-      if (!w.l1 && !w.samp) continue;
+    while (ok) {
       const int p = n_it & 1;
       ok = vwait(ptx::smem_addr(&S.red_full[p]), (n_it >> 1) & 1, abort_flag, err);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
+      const int item = S.red[p][0].pad[0];
+      if (item < 0) break;  // the consumers are done
       if (lane == 0) {
         Partial pp;
         pp.l1 = 0.0;
@@ -345,30 +364,54 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
           better(pp.key_res, pp.idx_res, wp.kr, wp.ir);
           better(pp.key_t, pp.idx_t, wp.kt, wp.it);
         }
-        part[(long long)row * n_chunks + ch] = pp;
+        part[item] = pp;  // item = row * n_chunks + chunk
         ptx::mbar_arrive(ptx::smem_addr(&S.red_free[p]));
       }
       __syncwarp();
       ++n_it;
     }
   } else {
-    // consumers: thread t owns entries 8t..8t+7 of each sub-chunk
+    // consumers: thread t owns entries 8t..8t+7 of each sub-chunk; the stages' meta[]
+    // gives their items
     int g = 0, gn = 0, n_it = 0;
     bool ok = true;
-    for (long long item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int row = static_cast<int>(item / n_chunks), ch = static_cast<int>(item % n_chunks);
-      const RowWork w = row_work(row_desc, row);
-      if (!w.l1 && !w.samp) continue;
-      const int ns = n_sub_of(ch);
-      float l1 = 0.f;
-      float kbest = -1.f;                // this lane's race maximum and its index
-      int ibest = 0x7fffffff;
-      float thr = -1.f;                  // warp-wide filter (below every key at first)
-      for (int sb = 0; sb < ns; ++sb, ++g) {
-        const int s = g % kVStages;
-        ok = vwait(ptx::smem_addr(&S.full[s]), (g / kVStages) & 1, abort_flag, err);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
+    float l1 = 0.f, kbest = -1.f, thr = -1.f;
+    int ibest = 0x7fffffff;
+    while (ok) {
+      const int s = g % kVStages;
+      ok = vwait(ptx::smem_addr(&S.full[s]), (g / kVStages) & 1, abort_flag, err);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const int4 m = S.meta[s];
+      if (m.x < 0) {  // end: tell the reducer
+        const int p = n_it & 1;
+        if (n_it >= 2) {
+          ok = vwait(ptx::smem_addr(&S.red_free[p]), ((n_it >> 1) - 1) & 1, abort_flag, err);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          S.red[p][warp].pad[0] = -1;
+          ptx::mbar_arrive(ptx::smem_addr(&S.red_full[p]));
+        }
+        break;
+      }
+      const int sb = m.y & 0xff, ns = m.y >> 8;
+      RowWork w;
+      w.r = m.z;
+      w.j = m.w & 0xffff;
+      w.l1 = (m.w & kRowL1) != 0;
+      w.samp = (m.w & kRowSample) != 0;
+      w.residual = (m.w & kRowResidual) != 0;
+      w.need_d = w.l1 || w.residual;
+      const int ch = m.x % n_chunks;
+      if (sb == 0) {
+        l1 = 0.f;
+        kbest = -1.f;
+        ibest = 0x7fffffff;
+        thr = -1.f;
+      }
+      {
         const int v0 = ch * kChunk + sb * kSub;
         const int len = min(kSub, V - v0);
         const uint8_t* st = S.stage[s];
@@ -436,7 +479,9 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
         }
         if (w.samp) ++gn;
       }
-      if (!ok) break;
+      ++g;
+      if (sb != ns - 1) continue;
+      // item done: warp results to the reducer
       float kr = -1.f, kt = -1.f;
       int ir = 0x7fffffff, it_ = 0x7fffffff;
       if (w.residual) { kr = kbest; ir = ibest; } else { kt = kbest; it_ = ibest; }
@@ -459,6 +504,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
         wp.l1 = l1d;
         wp.kr = kr; wp.ir = ir;
         wp.kt = kt; wp.it = it_;
+        wp.pad[0] = m.x;
         ptx::mbar_arrive(ptx::smem_addr(&S.red_full[p]));
       }
       __syncwarp();
@@ -542,12 +588,12 @@ bool vocab_configure() {
   return state == 1;
 }
 
-// workspace: RowInfo[B] | int2 row_desc[max_rows] | Partial[max_rows][n_chunks]
+// workspace: RowInfo[B] | claim counter | int2 row_desc[max_rows] | Partial[max_rows][n_chunks]
 size_t accept_workspace(int B, int max_rows, int V) {
   const int n_chunks = ceil_div(V, kChunk);
   const size_t a = ((size_t)B * sizeof(RowInfo) + 255) & ~size_t(255);
   const size_t b = ((size_t)max_rows * sizeof(int2) + 255) & ~size_t(255);
-  return a + b + (size_t)max_rows * n_chunks * sizeof(Partial);
+  return a + 256 + b + (size_t)max_rows * n_chunks * sizeof(Partial);
 }
 
 // Scratch of dspark_accept_noalloc: a fixed array in the library image, one per
@@ -574,7 +620,9 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
                   cudaStream_t stream) {
   const int n_chunks = ceil_div(V, kChunk);
   RowInfo* info = static_cast<RowInfo*>(ws);
-  const size_t off_desc = ((size_t)B * sizeof(RowInfo) + 255) & ~size_t(255);
+  const size_t off_claim = ((size_t)B * sizeof(RowInfo) + 255) & ~size_t(255);
+  int* claim = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + off_claim);
+  const size_t off_desc = off_claim + 256;
   int2* row_desc = reinterpret_cast<int2*>(static_cast<uint8_t*>(ws) + off_desc);
   Partial* part = reinterpret_cast<Partial*>(
       static_cast<uint8_t*>(ws) + off_desc + (((size_t)max_rows * sizeof(int2) + 255) & ~size_t(255)));
@@ -590,22 +638,22 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
     const float* d = static_cast<const float*>(p_d);
     if (launch_pdl(accept_test_kernel<float>, dim3(ceil_div(B * 32, 128)), dim3(128), 0, stream, t,
                    d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, max_rows, accept_len,
-                   cap_len, info, row_desc, err) != cudaSuccess)
+                   cap_len, info, row_desc, claim, err) != cudaSuccess)
       return DSPARK_ECUDA;
     if (launch_pdl(accept_vocab_kernel<float>, dim3((int)grid), dim3(kVocabCtaThreads),
                    sizeof(VocabSmem), stream, t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows,
-                   row_desc, part, err) != cudaSuccess)
+                   row_desc, part, claim, err) != cudaSuccess)
       return DSPARK_ECUDA;
   } else {
     const __nv_bfloat16* t = static_cast<const __nv_bfloat16*>(p_t);
     const __nv_bfloat16* d = static_cast<const __nv_bfloat16*>(p_d);
     if (launch_pdl(accept_test_kernel<__nv_bfloat16>, dim3(ceil_div(B * 32, 128)), dim3(128), 0,
                    stream, t, d, V, draft_tok, uniforms, windows, cu, mode, B, gamma, max_rows,
-                   accept_len, cap_len, info, row_desc, err) != cudaSuccess)
+                   accept_len, cap_len, info, row_desc, claim, err) != cudaSuccess)
       return DSPARK_ECUDA;
     if (launch_pdl(accept_vocab_kernel<__nv_bfloat16>, dim3((int)grid), dim3(kVocabCtaThreads),
                    sizeof(VocabSmem), stream, t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows,
-                   row_desc, part, err) != cudaSuccess)
+                   row_desc, part, claim, err) != cudaSuccess)
       return DSPARK_ECUDA;
   }
   cudaError_t e;
