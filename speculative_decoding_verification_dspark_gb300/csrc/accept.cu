@@ -17,9 +17,10 @@
 //                        distance for c*, and on the sampled row the partial
 //                        exponential-race argmax (w_v / e_v, lowest index on ties)
 //                        for both the residual max(0, p_t - p_d) and p_t itself.
-//   accept_final_kernel  one warp per request: fixed-order fp64 sums of the chunk
-//                        partials (c*) and the argmax over the chunk partials
-//                        (token), with the p_t race behind an all-zero residual.
+//   accept_final_kernel  one block per request: fixed-order fp64 sums of the chunk
+//                        partials (c*, a warp per row) and the argmax over the
+//                        chunk partials (token), with the p_t race behind an
+//                        all-zero residual.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -514,8 +515,11 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
   __syncthreads();
 }
 
+// One block per request: warp w sums the chunk partials of c* rows w, w + 8, ...
+// (lanes over chunks, a fixed shuffle tree: deterministic), warp 0 also takes the
+// token from the sampled row's partials.
 template <class T>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(256)
     accept_final_kernel(const T* __restrict__ p_t, const float* __restrict__ exp_noise, int V,
                         const int32_t* __restrict__ cu, int B, int gamma, int max_rows,
                         int n_chunks, const RowInfo* __restrict__ info,
@@ -523,21 +527,24 @@ __global__ void __launch_bounds__(128)
                         float* __restrict__ cstar, int32_t* __restrict__ fallback) {
   pdl_release();
   pdl_wait();  // inputs come from the kernels before this one
-  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= B || cu[B] > max_rows) return;  // warp-uniform
+  const int r = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (r >= B || cu[B] > max_rows) return;  // block-uniform
   const int base = cu[r];
   const int n_rows = cu[r + 1] - base;
-  const RowInfo ri = info[r];
-  for (int j = lane; j < gamma; j += 32) {
+  for (int j = warp; j < gamma; j += 8) {
     float c = __int_as_float(0x7fc00000);  // NaN: no target row for this position
     if (j < n_rows) {
       double s = 0.0;
-      for (int ch = 0; ch < n_chunks; ++ch) s += part[(long long)(base + j) * n_chunks + ch].l1;
+      for (int ch = lane; ch < n_chunks; ch += 32) s += part[(long long)(base + j) * n_chunks + ch].l1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       c = __double2float_rn(1.0 - 0.5 * s);
     }
-    cstar[r * gamma + j] = c;
+    if (lane == 0) cstar[r * gamma + j] = c;
   }
+  if (warp != 0) return;
+  const RowInfo ri = info[r];
   // token: the sampled row's race maximum over the chunk partials (max, then lowest
   // index: order-independent)
   const long long prow = (long long)(base + ri.sample_row) * n_chunks;
@@ -658,13 +665,13 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
   }
   cudaError_t e;
   if (pdt == DSPARK_F32)
-    e = launch_pdl(accept_final_kernel<float>, dim3(ceil_div(B * 32, 128)), dim3(128), 0, stream,
+    e = launch_pdl(accept_final_kernel<float>, dim3(B), dim3(256), 0, stream,
                    static_cast<const float*>(p_t), exp_noise, V, cu, B, gamma, max_rows, n_chunks,
                    info, part, out_tok, cstar, fallback);
   else
-    e = launch_pdl(accept_final_kernel<__nv_bfloat16>, dim3(ceil_div(B * 32, 128)), dim3(128), 0,
-                   stream, static_cast<const __nv_bfloat16*>(p_t), exp_noise, V, cu, B, gamma,
-                   max_rows, n_chunks, info, part, out_tok, cstar, fallback);
+    e = launch_pdl(accept_final_kernel<__nv_bfloat16>, dim3(B), dim3(256), 0, stream,
+                   static_cast<const __nv_bfloat16*>(p_t), exp_noise, V, cu, B, gamma, max_rows,
+                   n_chunks, info, part, out_tok, cstar, fallback);
   if (e != cudaSuccess) return DSPARK_ECUDA;
   return DSPARK_OK;
 }
