@@ -1,6 +1,7 @@
 // Internal interface of the verify-attention launchers (host side).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -56,7 +57,20 @@ int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, c
                   const int* item_begin, int grid, float* out, float* lse, float* ws_o,
                   float* ws_lse, cudaStream_t stream);
 constexpr int kKeyTile = 128;
+// bf16 tiled tensor map, 128-byte swizzle (rank <= 5; strides in bytes of dims 1..).
+bool encode_bf16_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box);
 }  // namespace gqa
+
+namespace mla {
+constexpr int kKeyTile = 64;
+// Two-CTA clusters that can be resident at once (the kernel's grid, in clusters).
+int clusters();
+int launch_kernel(const void* q, const void* k_new, const void* k_cache, int n_pages,
+                  const int32_t* page_table, int max_pages, int max_rows, int page_size,
+                  float scale, const AttnItem* items, const int* item_begin, int n_clusters,
+                  float* out, float* lse, float* ws_o, float* ws_lse, cudaStream_t stream);
+}  // namespace mla
 
 }  // namespace attn
 }  // namespace dspark

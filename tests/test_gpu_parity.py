@@ -280,6 +280,17 @@ def test_mla_small():
     run_and_check(inp, O.STATIC)
 
 
+def test_mla_page16_split():
+    """Latent KV with 16-token pages (four TMA boxes per key tile) and contexts long
+    enough that groups are cut into pieces across clusters."""
+    wl = W.Workload(
+        name="mla_p16", B=5, gamma=6, attn="mla", Hq=128, Hkv=1, d_qk=576, d_v=512, page_size=16,
+        ctx=("uniform", 100, 2000), conf=("logit", 1.2, 1.0), vocab=1024, p_dtype="f32",
+        target_logit_std=3.0, draft_noise_std=0.7, tiers=(8, 16, 32, 64))
+    inp = W.make_inputs(wl, seed=5)
+    run_and_check(inp, O.COMPACT)
+
+
 def _full(name, seed=0):
     wl = W.WORKLOADS[name]
     return W.make_inputs(wl, seed, device=W.gen_device(wl))
