@@ -14,9 +14,9 @@
 //   * the QK^T reduction is split the same way: CTA rho multiplies dims
 //     256 rho .. +255 (its own value columns) and rope dims 512 + 32 rho .. +31.
 //     It loads only those 5 of the 9 64-wide column blocks of a key tile;
-//   * the two partial score tiles are swapped through distributed shared memory
-//     and added; fp32 addition commutes, so both CTAs hold bit-identical scores and
-//     run the identical softmax (same P, max and sum);
+//   * the two partial score tiles (fp32) are swapped through distributed shared
+//     memory and added; fp32 addition commutes, so both CTAs hold bit-identical
+//     scores and run the identical softmax (same P, max and sum);
 //   * Q (this CTA's 288 dims) and P sit in TMEM and are the A operand of the MMAs,
 //     so each product reads only the key tile (B) from shared memory.
 //
@@ -24,13 +24,20 @@
 //   S = S_0 + S_1 (exchanged); P = exp2(scale' S - m)             (fp32, SFU)
 //   O_rho [128 x 256] += P . K[:, 256 rho .. 256 rho + 255]       (tcgen05, TMEM)
 //
+// The swap is the narrow point: the SM-to-SM network moves about 15 bytes per clock
+// per SM (st.async; bulk copies reach about half that), so a 32 KB tile of partials
+// takes about as long as the tile's products.  Dedicated exchange warps send it
+// with st.async, whose bytes complete on the receiver's mbarrier, so no thread
+// waits on a cluster-scope fence, and the send overlaps the softmax of the tile
+// before.
+//
 // TMEM columns: O [0, 256), S [256, 320), P [320, 352), Q [352, 496).
-// Warp roles: 0 TMA producer (a 4-stage ring of key tiles), 1 MMA issuer (one lane)
+// Warp roles: 0 TMA producer (a 3-stage ring of key tiles), 1 MMA issuer (one lane)
 // that first zeroes the key rows past the visible range of a partial tile (value
-// rows met by a zero probability must be finite), 2-5 softmax and epilogue, thread
-// = query head = TMEM lane.  Every wait is bounded in time; on expiry the CTA raises
-// DSPARK_DEVERR_WAIT_TIMEOUT and leaves its loops, and the peer's waits then expire
-// as well.
+// rows met by a zero probability must be finite), 2-5 softmax and epilogue, 6-9
+// score exchange; in both groups thread = query head = TMEM lane.  Every wait is
+// bounded in time; on expiry the CTA raises DSPARK_DEVERR_WAIT_TIMEOUT and leaves
+// its loops, and the peer's waits then expire as well.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -56,26 +63,30 @@ constexpr int kHalf = 256;       // value dims of one CTA
 constexpr int kCBs = 5;          // 64-wide column blocks one CTA loads per key tile
 constexpr int kCBBytes = kNK * 128;
 constexpr int kStageBytes = kCBs * kCBBytes;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kQKSteps = 18;     // 288 dims / 16
-constexpr int kXBytes = kRows * kNK * 4;  // one fp32 score tile
+// Partial score exchange: a row is 64 fp32 partials (256 B); 16-byte piece c of row m
+// sits at piece c ^ (m mod 16), which keeps 8 consecutive rows on distinct banks.
+constexpr int kXRow = 256;
+constexpr int kXBytes = kRows * kXRow;
 constexpr int kChunkRows = 16;   // block-row box
 constexpr int kProdWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kSoftmaxWarp0 = 2;
-constexpr int kThreads = 6 * 32;
+constexpr int kExchWarp0 = 6;
+constexpr int kThreads = 10 * 32;
 constexpr int OFF_STAGE = 0;
 constexpr int OFF_X = OFF_STAGE + kStages * kStageBytes;
 constexpr int OFF_BAR = OFF_X + 2 * kXBytes;
-// kv_full[S], kv_empty[S], s_full, s_free, p_full, p_empty, q_full, x_full[2], x_empty[2]
-constexpr int N_BARS = 2 * kStages + 9;
+// kv_full[S], kv_empty[S], s_full, s_free, p_full, p_empty, q_full, x_full[2], xc
+constexpr int N_BARS = 2 * kStages + 8;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_O = 0, TMEM_S = 256, TMEM_P = 320, TMEM_Q = 352;
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(TMEM_Q + kQKSteps * 8 <= TMEM_COLS, "tensor memory budget");
-static_assert(kStageBytes % 1024 == 0 && kXBytes % 1024 == 0, "alignment");
+static_assert(kStageBytes % 1024 == 0 && kXBytes % 16 == 0, "alignment");
 
 struct Ctx {
   volatile int* abort_flag;
@@ -170,7 +181,7 @@ struct Layout {
   __device__ uint32_t p_empty() const { return bar(2 * kStages + 3); }
   __device__ uint32_t q_full() const { return bar(2 * kStages + 4); }
   __device__ uint32_t x_full(int b) const { return bar(2 * kStages + 5 + b); }
-  __device__ uint32_t x_empty(int b) const { return bar(2 * kStages + 7 + b); }
+  __device__ uint32_t xc() const { return bar(2 * kStages + 7); }
 };
 
 // Keys of tile t of a request that a query row can see at all: the cache tile's
@@ -222,14 +233,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(L.kv_empty(s), 1);
     }
     mbar_init(L.s_full(), 1);
-    mbar_init(L.s_free(), 4);
+    mbar_init(L.s_free(), 8);   // softmax and exchange warps both read S
     mbar_init(L.p_full(), 4);
     mbar_init(L.p_empty(), 1);
     mbar_init(L.q_full(), 4);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(L.x_full(b), kRows);   // one arrival per peer softmax thread
-      mbar_init(L.x_empty(b), kRows);
-    }
+    // armed (expect_tx) by this CTA, completed by the peer's asynchronous stores
+    for (int b = 0; b < 2; ++b) mbar_init(L.x_full(b), 1);
+    mbar_init(L.xc(), 4);
     fence_mbar_init();
   }
   if (warp == kProdWarp && lane == 0) {
@@ -388,18 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // product issued may be a QK^T)
     if (lane == 0 && last_pv >= 0) drain_bar(L.p_empty(), last_pv & 1, prm.err);
     if (lane == 0 && last_qk > last_pv) drain_bar(L.s_full(), last_qk & 1, prm.err);
-  } else if (warp >= kSoftmaxWarp0) {
+  } else if (warp >= kSoftmaxWarp0 && warp < kExchWarp0) {
     // ------------------------------------------------------------- softmax / epilogue
     const int sw = warp & 3;                 // TMEM lane quadrant of this warp
     const int m = sw * 32 + lane;            // query head of this thread
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
     const float sl2 = prm.scale_log2;
-    // the peer's copy of this CTA's shared-memory layout
-    const uint32_t x_peer = mapa_shared(L.x(0), peer) + m * 256;
-    const uint32_t xf_peer = mapa_shared(L.x_full(0), peer);
-    const uint32_t xe_peer = mapa_shared(L.x_empty(0), peer);
-    const uint32_t x_mine = L.x(0) + m * 256;
-    const int sx = m & 15;                   // 16-byte piece swizzle of row m
+    const uint32_t x_row = static_cast<uint32_t>(m * kXRow);
+    const int sx = m & 15;
     int g = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it) {
@@ -458,7 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int l = 0; l < ntiles; ++l, ++g) {
         const int t = item.tb + l;
         const int xb = g & 1;
-        // ---- this CTA's partial scores
+        // ---- S = S_0 + S_1: this CTA's partial from TMEM, the peer's from the exchange
+        // slot (stored here by the peer's exchange warps); fp32 addition commutes, so
+        // both CTAs get identical bits
         if (!wait_warp(L.s_full(), g & 1, cx)) { ok = false; break; }
         tc_fence_after();
         float s[kNK];
@@ -473,31 +481,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(L.s_free());
-        // ---- to the peer (its buffer xb is free once it has read tile g - 2)
-        if (g >= 2 && !wait_warp<true>(L.x_empty(xb), ((g >> 1) - 1) & 1, cx)) { ok = false; break; }
-        {
-          const uint32_t dst = x_peer + xb * kXBytes;
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            st_cluster_v4(dst + ((c ^ sx) << 4),
-                          make_uint4(__float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
-                                     __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3])));
-          mbar_arrive_remote(xf_peer + 8 * xb);
-        }
-        // ---- the peer's partial: S = S_0 + S_1
+        if (m == 0) mbar_arrive_expect_tx(L.x_full(xb), kXBytes);  // what the peer sends here
         if (!wait_warp<true>(L.x_full(xb), (g >> 1) & 1, cx)) { ok = false; break; }
         {
-          const uint32_t src = x_mine + xb * kXBytes;
+          const uint32_t rp = L.x(xb) + x_row;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const float4 v = ld_shared_f4(src + ((c ^ sx) << 4));
+            const float4 v = ld_shared_f4(rp + ((c ^ sx) << 4));
             s[4 * c] += v.x;
             s[4 * c + 1] += v.y;
             s[4 * c + 2] += v.z;
             s[4 * c + 3] += v.w;
           }
-          mbar_arrive_remote(xe_peer + 8 * xb);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.xc());  // tile g's exchange buffers are read
         // ---- mask: keys [0, lim) of this tile are visible to the block row (the
         // same for every head, so the branch is uniform)
         const int lim = t >= ct ? min(bi + 1, n_r) - (t - ct) * kNK : ctx - t * kNK;
@@ -587,6 +585,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
+      }
+    }
+  }
+
+  if (warp >= kExchWarp0) {
+    // ------------------------------------------------------------- score exchange
+    // Per tile: S_rho from TMEM (released once the softmax warps have read it too),
+    // sent to the peer's exchange slot.  The send of tile g waits until this
+    // CTA's softmax has read tile g - 1: the peer's slot of tile g (used for g - 2
+    // before) is then free, because the peer sent tile g - 1 only after its own
+    // softmax had read tile g - 2.
+    const int sw = warp & 3;
+    const int m = sw * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
+    const uint32_t x_row = static_cast<uint32_t>(m * kXRow);
+    const int sx = m & 15;
+    const uint32_t x_peer = mapa_shared(L.x(0), peer) + x_row;
+    const uint32_t xf_peer = mapa_shared(L.x_full(0), peer);
+    int g = 0;
+    bool ok = true;
+    for (int it = it_begin; it < it_end && ok; ++it) {
+      const AttnItem item = prm.items[it];
+      const int ntiles = item.te - item.tb;
+      for (int l = 0; l < ntiles; ++l, ++g) {
+        const int xb = g & 1;
+        if (!wait_warp(L.s_full(), g & 1, cx)) { ok = false; break; }
+        tc_fence_after();
+        float s[kNK];
+        {
+          float a[32], b[32];
+          tmem_ld32(t_lane + TMEM_S, a);
+          tmem_ld32(t_lane + TMEM_S + 32, b);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) { s[k] = a[k]; s[32 + k] = b[k]; }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.s_free());
+        if (g >= 1 && !wait_warp(L.xc(), (g - 1) & 1, cx)) { ok = false; break; }
+        const uint32_t dst = x_peer + xb * kXBytes;
+        const uint32_t bar = xf_peer + 8 * xb;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          st_async_v4(dst + ((c ^ sx) << 4),
+                      make_uint4(__float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
+                                 __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3])),
+                      bar);
       }
     }
   }
