@@ -38,6 +38,11 @@ constexpr int kRows = 128;  // query rows of one work item (UMMA M / N side)
 // pieces, one per CTA it meets; such a piece is always the first or the last piece
 // of its CTA and writes partial (o, lse) rows into slot 2c or 2c + 1.  The CTA that
 // runs the last piece of a split group records the group for the combine.
+//
+// Built in parallel: a thread per CTA counts the groups its range meets (they are
+// consecutive, so the count is the difference of two group indices) and a block scan
+// gives each CTA's first item; then a thread per group writes the group's pieces
+// straight to their places (piece of group g in CTA c: item base_c + g - first_c).
 __device__ __forceinline__ int cta_of_unit(long long x, long long U, int n) {
   return static_cast<int>(((x + 1) * n - 1) / U);  // largest c with c*U/n <= x
 }
@@ -67,6 +72,17 @@ __device__ __forceinline__ T block_excl_scan(T v, T* s_w, T* total) {
   return ex;
 }
 
+// Largest r in [0, n) with off[r] <= x (off non-decreasing, off[0] = 0 <= x).
+template <class T>
+__device__ __forceinline__ int last_at_or_below(const T* off, int n, T x) {
+  int a = 0, b = n;
+  while (b - a > 1) {
+    const int mid = (a + b) >> 1;
+    if (off[mid] <= x) a = mid; else b = mid;
+  }
+  return a;
+}
+
 __global__ void __launch_bounds__(1024)
     worklist_kernel(const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ cu_seqlens,
                     int B, int max_rows, int Hkv, int parts, int rows_per_tile, int NK, int ncta,
@@ -75,24 +91,28 @@ __global__ void __launch_bounds__(1024)
                     unsigned int* __restrict__ err) {
   pdl_release();
   pdl_wait();  // inputs come from the kernels before this one
-  __shared__ long long s_off[DSPARK_MAX_B + 1];
-  __shared__ int s_tt[DSPARK_MAX_B];
+  __shared__ long long s_off[DSPARK_MAX_B + 1];  // first unit of request r
+  __shared__ int s_goff[DSPARK_MAX_B + 1];       // first group of request r
+  __shared__ int s_tt[DSPARK_MAX_B];             // tiles per group of request r
   __shared__ int s_n[DSPARK_MAX_B];
   __shared__ int s_ctx[DSPARK_MAX_B];
   __shared__ int s_c0[DSPARK_MAX_B];
+  __shared__ int s_base[1024];                   // first item of CTA c
+  __shared__ int s_gfirst[1024];                 // first group CTA c meets
   __shared__ long long s_w64[32];
   __shared__ int s_w32[32];
   const int tid = threadIdx.x, lane = tid & 31;
   const int ng_per_tile = parts * Hkv;
   const bool rows_ok = cu_seqlens[B] <= max_rows;  // else: report and run nothing
   long long units = 0;
-  int tt = 0;
+  int tt = 0, ngr = 0;
   if (tid < B) {
     const int c0 = cu_seqlens[tid];
     const int n = cu_seqlens[tid + 1] - c0;
     const int ctx = ctx_len[tid];
     tt = ceil_div(ctx, NK) + ceil_div(n, NK);
-    units = (long long)tt * ceil_div(n, rows_per_tile) * ng_per_tile;
+    ngr = ceil_div(n, rows_per_tile) * ng_per_tile;
+    units = (long long)tt * ngr;
     s_tt[tid] = tt;
     s_n[tid] = n;
     s_ctx[tid] = ctx;
@@ -110,8 +130,16 @@ __global__ void __launch_bounds__(1024)
   __syncthreads();
   long long U;
   const long long ex = block_excl_scan(units, s_w64, &U);
-  if (tid < B) s_off[tid] = ex;
-  if (tid == 0) s_off[B] = U;
+  int NG;
+  const int gex = block_excl_scan(ngr, s_w32, &NG);
+  if (tid < B) {
+    s_off[tid] = ex;
+    s_goff[tid] = gex;
+  }
+  if (tid == 0) {
+    s_off[B] = U;
+    s_goff[B] = NG;
+  }
   // No group may be cut into more than max_splits pieces.  Every CTA range holds at
   // least L = floor(U/n) units, and a group of T units meets at most
   // ceil((T-1)/L) + 1 ranges, so L >= ceil((T_max-1)/(max_splits-1)) suffices:
@@ -125,76 +153,69 @@ __global__ void __launch_bounds__(1024)
     if (cap < n_eff) n_eff = cap > 0 ? static_cast<int>(cap) : 1;
   }
   __syncthreads();
+  // ---- per CTA: the groups its range meets
   const int c = tid;
   const bool active = c < ncta && c < n_eff && U > 0;
-  const long long lo = active ? (long long)c * U / n_eff : 0;
-  const long long hi = active ? (long long)(c + 1) * U / n_eff : 0;
-  // walk CTA c's unit range: count (emit = false) or write its pieces
-  auto walk = [&](bool emit, int base) -> int {
-    long long u = lo;
-    int k = 0;
-    bool wrote_group = false;
-    while (u < hi) {
-      int a = 0, b = B;  // request: s_off[a] <= u < s_off[a + 1]
-      while (b - a > 1) {
-        const int mid = (a + b) >> 1;
-        if (s_off[mid] <= u) a = mid; else b = mid;
-      }
-      const int r = a;
-      const int t_r = s_tt[r];
-      const long long lu = u - s_off[r];
-      const int lg = static_cast<int>(lu / t_r);          // group within the request
-      const long long gstart = s_off[r] + (long long)lg * t_r;
-      const long long gend = gstart + t_r;
-      const long long next = gend < hi ? gend : hi;
-      if (emit) {
-        const int c_first = cta_of_unit(gstart, U, n_eff);
-        const int c_last = cta_of_unit(gend - 1, U, n_eff);
-        const int t = lg / ng_per_tile, p = (lg / Hkv) % parts, h = lg % Hkv;
-        const int i0 = t * rows_per_tile;
-        const int ni = min(rows_per_tile, s_n[r] - i0);
-        AttnItem it;
-        it.r = r; it.kvh = h; it.i0 = i0; it.ni = ni;
-        it.part = p; it.split = c - c_first;
-        it.tb = static_cast<int>(lu - (long long)lg * t_r);
-        it.te = it.tb + static_cast<int>(next - u);
-        it.nsplit = c_last - c_first + 1;
-        it.slot = u == lo ? 2 * c : 2 * c + 1;
-        it.pad0 = 0; it.pad1 = 0;
-        it.ctx = s_ctx[r]; it.c0 = s_c0[r]; it.n_r = s_n[r]; it.pad2 = 0;
-        items[base + k] = it;
-        if (it.nsplit > 1 && c == c_last) {
-          SplitGroup sg;
-          sg.r = r; sg.kvh = h; sg.part = p; sg.i0 = i0;
-          sg.ni = ni; sg.c_first = c_first; sg.nsplit = it.nsplit;
-          sg.slot0_last = gstart != (long long)c_first * U / n_eff;
-          groups[c] = sg;
-          wrote_group = true;
-        }
-      }
-      ++k;
-      u = next;
-    }
-    if (emit && !wrote_group) {
-      SplitGroup sg{};
-      groups[c] = sg;  // nsplit = 0: no group ends here
-    }
-    return k;
-  };
-  const int cnt = walk(false, 0);
+  int gfirst = 0, cnt = 0;
+  if (active) {
+    const long long lo = (long long)c * U / n_eff;
+    const long long hi = (long long)(c + 1) * U / n_eff;
+    const int r0 = last_at_or_below(s_off, B, lo);
+    const int r1 = last_at_or_below(s_off, B, hi - 1);
+    gfirst = s_goff[r0] + static_cast<int>((lo - s_off[r0]) / s_tt[r0]);
+    const int glast = s_goff[r1] + static_cast<int>((hi - 1 - s_off[r1]) / s_tt[r1]);
+    cnt = glast - gfirst + 1;
+  }
   int total;
   const int base = block_excl_scan(cnt, s_w32, &total);
   const bool fits = rows_ok && total <= max_items;
   if (tid == 0 && !fits)
     raise_error(err, rows_ok ? DSPARK_DEVERR_WORK_OVERFLOW : DSPARK_DEVERR_ROWS_OVERFLOW);
-  if (c < ncta) item_begin[c] = fits ? base : 0;
-  if (tid == 0) item_begin[ncta] = fits ? total : 0;
   if (c < ncta) {
-    if (fits) {
-      walk(true, base);
-    } else {
-      SplitGroup sg{};
-      groups[c] = sg;
+    item_begin[c] = fits ? base : 0;
+    s_base[c] = base;
+    s_gfirst[c] = gfirst;
+    SplitGroup sg{};
+    groups[c] = sg;  // nsplit = 0 unless a split group ends in CTA c (written below)
+  }
+  if (tid == 0) item_begin[ncta] = fits ? total : 0;
+  __syncthreads();
+  if (!fits || U == 0) return;
+  // ---- per group: its pieces
+  for (int g = tid; g < NG; g += blockDim.x) {
+    const int r = last_at_or_below(s_goff, B, g);
+    const int lg = g - s_goff[r];                  // group within the request
+    const int t_r = s_tt[r];
+    const long long gstart = s_off[r] + (long long)lg * t_r;
+    const long long gend = gstart + t_r;
+    const int c_first = cta_of_unit(gstart, U, n_eff);
+    const int c_last = cta_of_unit(gend - 1, U, n_eff);
+    const int t = lg / ng_per_tile, p = (lg / Hkv) % parts, h = lg % Hkv;
+    const int i0 = t * rows_per_tile;
+    const int ni = min(rows_per_tile, s_n[r] - i0);
+    const int nsplit = c_last - c_first + 1;
+    for (int cc = c_first; cc <= c_last; ++cc) {
+      const long long lo = (long long)cc * U / n_eff;
+      const long long hi = (long long)(cc + 1) * U / n_eff;
+      const long long u0 = gstart > lo ? gstart : lo;
+      const long long u1 = gend < hi ? gend : hi;
+      AttnItem it;
+      it.r = r; it.kvh = h; it.i0 = i0; it.ni = ni;
+      it.part = p; it.split = cc - c_first;
+      it.tb = static_cast<int>(u0 - gstart);
+      it.te = static_cast<int>(u1 - gstart);
+      it.nsplit = nsplit;
+      it.slot = u0 == lo ? 2 * cc : 2 * cc + 1;
+      it.pad0 = 0; it.pad1 = 0;
+      it.ctx = s_ctx[r]; it.c0 = s_c0[r]; it.n_r = s_n[r]; it.pad2 = 0;
+      items[s_base[cc] + (g - s_gfirst[cc])] = it;
+    }
+    if (nsplit > 1) {
+      SplitGroup sg;
+      sg.r = r; sg.kvh = h; sg.part = p; sg.i0 = i0;
+      sg.ni = ni; sg.c_first = c_first; sg.nsplit = nsplit;
+      sg.slot0_last = gstart != (long long)c_first * U / n_eff;
+      groups[c_last] = sg;
     }
   }
 }
