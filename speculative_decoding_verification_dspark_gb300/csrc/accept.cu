@@ -135,14 +135,16 @@ __global__ void __launch_bounds__(128)
 // ---------------------------------------------------------------- vocabulary pass
 // Persistent, one CTA per SM over a contiguous range of (packed row, 8192-entry
 // chunk) items.  One thread streams the rows the method needs (p_t always, p_d for
-// c* rows and corrections, the noise row on the sampled row) with bulk copies, in
-// 4096-entry sub-chunks, into a five-slot shared-memory ring (noise into a ring of
-// its own), running ahead across items; sixteen consumer warps reduce each sub-chunk from shared memory; a
-// reducer warp combines the sixteen warps' results of an item into its partial.
+// c* rows and corrections, the noise row on the sampled row) with bulk copies into a
+// five-slot shared-memory ring (noise into a ring of its own), running ahead across
+// items; sixteen consumer warps reduce each slot from shared memory; a reducer warp
+// combines the sixteen warps' results of an item into its partial.  A slot holds
+// 16 KB of each probability row: 4096 fp32 or 8192 bf16 entries (so a bf16 item is
+// one slot, and the per-slot bookkeeping is spread over twice the entries).
 constexpr int kSub = 4096;                    // entries per stage
 constexpr int kVStages = 5;                   // main ring: p_t | p_d
 constexpr int kVStageBytes = 2 * kSub * 4;    // (fp32 sizes)
-constexpr int kNStages = 3;                   // noise ring, sampled rows only
+constexpr int kNoiseBytes = 64 * 1024;        // noise ring, sampled rows only
 constexpr int kConsumerWarps = 16;
 constexpr int kProducerWarp = 16, kReducerWarp = 17;
 constexpr int kVocabCtaThreads = 18 * 32;
@@ -157,10 +159,10 @@ struct WarpPart {
 
 struct VocabSmem {
   uint8_t stage[kVStages][kVStageBytes];
-  uint8_t noise[kNStages][kSub * 4];
+  uint8_t noise[kNoiseBytes];  // 4 slots of 4096 fp32 noise entries, or 2 of 8192
   WarpPart red[2][kConsumerWarps];
   int4 meta[kVStages];  // item, sub-chunk | sub-chunks << 8, request, row flags
-  uint64_t full[kVStages], empty[kVStages], nempty[kNStages], red_full[2], red_free[2];
+  uint64_t full[kVStages], empty[kVStages], nempty[4], red_full[2], red_free[2];
   int abort_flag;
 };
 
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
       ptx::mbar_init(ptx::smem_addr(&S.full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&S.empty[s]), kConsumerWarps);
     }
-    for (int s = 0; s < kNStages; ++s) ptx::mbar_init(ptx::smem_addr(&S.nempty[s]), kConsumerWarps);
+    for (int s = 0; s < 4; ++s) ptx::mbar_init(ptx::smem_addr(&S.nempty[s]), kConsumerWarps);
     for (int p = 0; p < 2; ++p) {
       ptx::mbar_init(ptx::smem_addr(&S.red_full[p]), kConsumerWarps);
       ptx::mbar_init(ptx::smem_addr(&S.red_free[p]), 1);
@@ -274,9 +276,12 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
   }
   __syncthreads();
   constexpr int ES = static_cast<int>(sizeof(T));
+  constexpr int kSubT = kSub * 4 / ES;                  // entries per slot
+  constexpr int kNStages = kNoiseBytes / (kSubT * 4);   // noise slots
+  static_assert(kNStages >= 2 && kNStages <= 4, "noise ring");
   auto n_sub_of = [&](int ch) {
     const int len = min(kChunk, V - ch * kChunk);
-    return (len + kSub - 1) / kSub;
+    return (len + kSubT - 1) / kSubT;
   };
 
   if (warp == kProducerWarp) {
@@ -325,8 +330,8 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
           const T* pt_row = p_t + (long long)row * V;
           const T* pd_row = p_d + ((long long)w.r * gamma + (w.j < gamma ? w.j : 0)) * V;
           const float* e_row = exp_noise + (long long)w.r * V;
-          const int v0 = ch * kChunk + sb * kSub;
-          const uint32_t len = static_cast<uint32_t>(min(kSub, V - v0));
+          const int v0 = ch * kChunk + sb * kSubT;
+          const uint32_t len = static_cast<uint32_t>(min(kSubT, V - v0));
           const uint32_t base = ptx::smem_addr(S.stage[st]);
           const uint32_t bytes = len * ES * (w.need_d ? 2u : 1u) + (w.samp ? len * 4u : 0u);
           S.meta[st] = make_int4(static_cast<int>(item), sb | (ns << 8), w.r, row_desc[row].y);
@@ -334,7 +339,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
           ptx::bulk_load_g2s(base, pt_row + v0, len * ES, full);
           if (w.need_d) ptx::bulk_load_g2s(base + kSub * 4, pd_row + v0, len * ES, full);
           if (w.samp) {
-            ptx::bulk_load_g2s(ptx::smem_addr(S.noise[sn]), e_row + v0, len * 4, full);
+            ptx::bulk_load_g2s(ptx::smem_addr(S.noise + sn * kSubT * 4), e_row + v0, len * 4, full);
             ++gn;
           }
           ptx::mbar_arrive(full);
@@ -413,13 +418,13 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
         thr = -1.f;
       }
       {
-        const int v0 = ch * kChunk + sb * kSub;
-        const int len = min(kSub, V - v0);
+        const int v0 = ch * kChunk + sb * kSubT;
+        const int len = min(kSubT, V - v0);
         const uint8_t* st = S.stage[s];
         const int sn = gn % kNStages;
-        const uint8_t* nz = S.noise[sn];
+        const uint8_t* nz = S.noise + sn * kSubT * 4;
 #pragma unroll
-        for (int k = 0; k < kSub / (kConsumerWarps * 32 * 8); ++k) {
+        for (int k = 0; k < kSubT / (kConsumerWarps * 32 * 8); ++k) {
           const int e = (k * kConsumerWarps * 32 + threadIdx.x) * 8;
           const bool valid = e < len;
           float a[8], d[8], en[8], ka[8];
