@@ -39,7 +39,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "verify steps/s & packed tokens/s at B=1..256, % of HBM roofline per kernel"
 UNIT = "verify steps/s"
-KERNELS_PER_STEP = 10   # schedule 2, pack 1, attention 2, accept 3, compact 2
+KERNELS_PER_STEP = 11   # schedule 2, pack 1, attention 3, accept 3, compact 2
 PROFILES = os.path.join(ROOT, "profiles")
 _CSRC = os.path.join(ROOT, "speculative_decoding_verification_dspark_gb300", "csrc")
 # sources whose change invalidates a committed DRAM-traffic figure

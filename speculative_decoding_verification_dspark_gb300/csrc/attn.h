@@ -30,21 +30,11 @@ struct __align__(16) SplitGroup {
   int ni, c_first, nsplit, slot0_last;
 };
 
-// What an attention CTA needs to build its part of the work list (see attn_work.cuh).
-struct WorkArgs {
-  const int32_t* ctx_len;
-  const int32_t* cu_seqlens;
-  AttnItem* items;      // global list: slot c's items at [base_c, base_c + count_c)
-  SplitGroup* groups;   // [n_slots]: the split group whose last piece runs in slot c
-  unsigned int* err;
-  int B, max_rows, Hkv, parts, rows_per_tile, NK, n_slots, max_splits, max_items;
-};
-
 struct Plan {
   bool mla;
   int parts, rows_per_tile, nk, nt, d_part, ncta;
   long long max_items;
-  size_t off_items, off_groups, off_o, off_lse, bytes;
+  size_t off_items, off_begin, off_groups, off_o, off_lse, bytes;
 };
 
 Plan plan(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v, int max_splits,
@@ -63,8 +53,9 @@ int query_tile(int Hq, int Hkv, int max_block_rows);
 int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, const void* k_cache,
                   const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
                   const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq,
-                  int Hkv, int page_size, float scale, const WorkArgs& wa, int grid, float* out,
-                  float* lse, float* ws_o, float* ws_lse, cudaStream_t stream);
+                  int Hkv, int page_size, float scale, const AttnItem* items,
+                  const int* item_begin, int grid, float* out, float* lse, float* ws_o,
+                  float* ws_lse, cudaStream_t stream);
 constexpr int kKeyTile = 128;
 // bf16 tiled tensor map, 128-byte swizzle (rank <= 5; strides in bytes of dims 1..).
 bool encode_bf16_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
@@ -77,7 +68,7 @@ constexpr int kKeyTile = 64;
 int clusters();
 int launch_kernel(const void* q, const void* k_new, const void* k_cache, int n_pages,
                   const int32_t* page_table, int max_pages, int max_rows, int page_size,
-                  float scale, const WorkArgs& wa, int n_clusters,
+                  float scale, const AttnItem* items, const int* item_begin, int n_clusters,
                   float* out, float* lse, float* ws_o, float* ws_lse, cudaStream_t stream);
 }  // namespace mla
 

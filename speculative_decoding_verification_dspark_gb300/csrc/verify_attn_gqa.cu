@@ -43,7 +43,6 @@
 #include <stdint.h>
 
 #include "attn.h"
-#include "attn_work.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -101,7 +100,6 @@ struct Cfg {
   static constexpr int TMEM_COLS = 4 * NT <= 128 ? 128 : (4 * NT <= 256 ? 256 : 512);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(NT == 32 || NT == 64 || NT == 128, "query tile");
-  static_assert(sizeof(WorkScratch) <= kStages * kStageBytes, "work-list scratch in the stages");
 };
 
 struct Ctx {
@@ -241,8 +239,8 @@ struct Params {
   const int32_t* page_table;
   const int32_t* ctx_len;
   const int32_t* cu_seqlens;
-  const AttnItem* items;  // work list (this CTA's part written by itself in the prologue)
-  WorkArgs wa;
+  const AttnItem* items;
+  const int* item_begin;  // [gridDim.x + 1]: CTA c runs items [item_begin[c], item_begin[c+1])
   float* out;
   float* lse;
   float* ws_o;
@@ -312,11 +310,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   pdl_release();
-  pdl_wait();  // the step's inputs come from earlier kernels
-  int it_begin = 0;
-  const int n_items = build_items(prm.wa, blockIdx.x, reinterpret_cast<WorkScratch*>(bp + C::OFF_STAGE),
-                                  s_items, kSmemItems, true, &it_begin);
-  const int it_end = it_begin + n_items;
+  pdl_wait();  // the work list and the step's inputs come from earlier kernels
+  const int it_begin = prm.item_begin[blockIdx.x];
+  const int it_end = prm.item_begin[blockIdx.x + 1];
+  {
+    const int n_s = min(kSmemItems, it_end - it_begin);
+    constexpr int kWords = (int)(sizeof(AttnItem) / sizeof(uint4));
+    for (int i = threadIdx.x; i < n_s * kWords; i += kThreads)
+      reinterpret_cast<uint4*>(s_items)[i] = reinterpret_cast<const uint4*>(prm.items + it_begin)[i];
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -879,8 +881,9 @@ int query_tile(int Hq, int Hkv, int max_block_rows) {
 int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, const void* k_cache,
                   const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
                   const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq,
-                  int Hkv, int page_size, float scale, const WorkArgs& wa, int grid, float* out,
-                  float* lse, float* ws_o, float* ws_lse, cudaStream_t stream) {
+                  int Hkv, int page_size, float scale, const AttnItem* items,
+                  const int* item_begin, int grid, float* out, float* lse, float* ws_o,
+                  float* ws_lse, cudaStream_t stream) {
   Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
@@ -890,8 +893,8 @@ int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, c
   prm.page_table = page_table;
   prm.ctx_len = ctx_len;
   prm.cu_seqlens = cu_seqlens;
-  prm.items = wa.items;
-  prm.wa = wa;
+  prm.items = items;
+  prm.item_begin = item_begin;
   prm.out = out;
   prm.lse = lse;
   prm.ws_o = ws_o;

@@ -45,7 +45,6 @@
 #include <stdint.h>
 
 #include "attn.h"
-#include "attn_work.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -78,9 +77,7 @@ constexpr int kExchWarp0 = 6;
 constexpr int kThreads = 10 * 32;
 constexpr int OFF_STAGE = 0;
 constexpr int OFF_X = OFF_STAGE + kStages * kStageBytes;
-constexpr int kSmemItems = 32;  // work items kept in shared memory (the rest from global)
-constexpr int OFF_ITEMS = OFF_X + 2 * kXBytes;
-constexpr int OFF_BAR = OFF_ITEMS + kSmemItems * (int)sizeof(AttnItem);
+constexpr int OFF_BAR = OFF_X + 2 * kXBytes;
 // kv_full[S], kv_empty[S], s_full, s_free, p_full, p_empty, q_full, x_full[2], xc
 constexpr int N_BARS = 2 * kStages + 8;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
@@ -90,7 +87,6 @@ constexpr uint32_t TMEM_COLS = 512;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(TMEM_Q + kQKSteps * 8 <= TMEM_COLS, "tensor memory budget");
 static_assert(kStageBytes % 1024 == 0 && kXBytes % 16 == 0, "alignment");
-static_assert(sizeof(WorkScratch) <= kStages * kStageBytes, "work-list scratch in the stages");
 
 struct Ctx {
   volatile int* abort_flag;
@@ -188,13 +184,6 @@ struct Layout {
   __device__ uint32_t xc() const { return bar(2 * kStages + 7); }
 };
 
-// Work item `it` of this cluster: from shared memory for the first kSmemItems items.
-__device__ __forceinline__ AttnItem fetch_item(const AttnItem* s_items, const AttnItem* g_items,
-                                               int it, int it_begin) {
-  const int k = it - it_begin;
-  return k < kSmemItems ? s_items[k] : g_items[it];
-}
-
 // Keys of tile t of a request that a query row can see at all: the cache tile's
 // keys below ctx, or the block tile's rows below n_r.
 __device__ __forceinline__ int visible_keys(int t, int ct, int ctx, int n_r) {
@@ -210,8 +199,8 @@ __device__ __forceinline__ int global_cb(int j, uint32_t rho) {
 struct Params {
   const __nv_bfloat16* q;
   const int32_t* page_table;
-  const AttnItem* items;  // work list (slot c = cluster c; built by its CTAs in the prologue)
-  WorkArgs wa;
+  const AttnItem* items;
+  const int* item_begin;  // [clusters + 1]: cluster c runs items [item_begin[c], item_begin[c+1])
   float* out;
   float* lse;
   float* ws_o;
@@ -267,15 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   pdl_release();
-  pdl_wait();  // the step's inputs come from earlier kernels
-  // both CTAs of the cluster build the same list; rank 0 also writes it to global
-  AttnItem* s_items = reinterpret_cast<AttnItem*>(bp + OFF_ITEMS);
-  int it_begin = 0;
-  const int n_items = build_items(prm.wa, pair, reinterpret_cast<WorkScratch*>(bp + OFF_STAGE),
-                                  s_items, kSmemItems, rho == 0, &it_begin);
-  const int it_end = it_begin + n_items;
-  // items past the shared-memory copy come from the global list, written by rank 0
-  cluster_sync();
+  pdl_wait();  // the work list and the step's inputs come from earlier kernels
+  const int it_begin = prm.item_begin[pair];
+  const int it_end = prm.item_begin[pair + 1];
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------- TMA producer
@@ -288,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it) {
-      const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
+      const AttnItem item = prm.items[it];
       const int ctx = item.ctx;
       const int ct = ceil_div(ctx, kNK);
       const int32_t* ptab = prm.page_table + (long long)item.r * prm.max_pages;
@@ -371,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
-      const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
+      const AttnItem item = prm.items[it];
       const int ct = ceil_div(item.ctx, kNK);
       if (!wait_warp(L.q_full(), n_it & 1, cx)) { ok = false; break; }
       const int ntiles = item.te - item.tb;
@@ -426,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it) {
-      const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
+      const AttnItem item = prm.items[it];
       const int ctx = item.ctx;
       const int n_r = item.n_r;
       const int ct = ceil_div(ctx, kNK);
@@ -468,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(L.q_full());
         // warm L2 with the next item's query row
         if (it + 1 < it_end) {
-          const AttnItem nx = fetch_item(s_items, prm.items, it + 1, it_begin);
+          const AttnItem nx = prm.items[it + 1];
           const char* nq = reinterpret_cast<const char*>(
               prm.q + ((long long)(nx.c0 + nx.i0) * kRows + m) * kDqk);
 #pragma unroll
@@ -623,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it) {
-      const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
+      const AttnItem item = prm.items[it];
       const int ntiles = item.te - item.tb;
       for (int l = 0; l < ntiles; ++l, ++g) {
         const int xb = g & 1;
@@ -708,13 +691,13 @@ int clusters() {
 
 int launch_kernel(const void* q, const void* k_new, const void* k_cache, int n_pages,
                   const int32_t* page_table, int max_pages, int max_rows, int page_size,
-                  float scale, const WorkArgs& wa, int n_clusters,
+                  float scale, const AttnItem* items, const int* item_begin, int n_clusters,
                   float* out, float* lse, float* ws_o, float* ws_lse, cudaStream_t stream) {
   Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.page_table = page_table;
-  prm.items = wa.items;
-  prm.wa = wa;
+  prm.items = items;
+  prm.item_begin = item_begin;
   prm.out = out;
   prm.lse = lse;
   prm.ws_o = ws_o;
