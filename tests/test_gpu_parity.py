@@ -291,6 +291,23 @@ def test_mla_page16_split():
     run_and_check(inp, O.COMPACT)
 
 
+@pytest.mark.parametrize("page_size", [32, 128])
+def test_mla_ragged_edges(page_size):
+    """Latent KV: ctx = 0, exactly one page, exactly one 64-key tile, ragged tails and a
+    page boundary at the block, with windows forced to gamma and to 0."""
+    wl = W.Workload(
+        name=f"mla_edges_p{page_size}", B=8, gamma=5, attn="mla", Hq=128, Hkv=1, d_qk=576,
+        d_v=512, page_size=page_size, ctx=("const", 0), conf=("logit", 1.0, 1.0), vocab=1024,
+        p_dtype="f32", target_logit_std=2.0, draft_noise_std=0.5, tiers=(8, 16, 32, 64),
+        cost_theta_ms=0.05)
+    inp = W.make_inputs(wl, seed=6, ctx_override=[0, page_size, 64, 100, 257, 700, 1023, 47])
+    conf = inp["conf"].clone()
+    conf[0] = 20.0
+    conf[1] = -20.0
+    inp["conf"] = conf
+    run_and_check(inp, O.COMPACT)
+
+
 def _full(name, seed=0):
     wl = W.WORKLOADS[name]
     return W.make_inputs(wl, seed, device=W.gen_device(wl))
