@@ -182,7 +182,7 @@ def accept_bytes(wl, windows, n_rows, accept_len, mode):
 
 # ------------------------------------------------------------------ GPU arm
 
-def gpu_arm(args, wl, mode, dist, world, rank, device):
+def gpu_arm(args, wl, mode, dist, world, rank, device, with_e2e=True):
     import harness
     import speculative_decoding_verification_dspark_gb300 as dspark
 
@@ -191,6 +191,9 @@ def gpu_arm(args, wl, mode, dist, world, rank, device):
     snap = harness.snapshot_state(d)
     small = {k: snap[k] for k in ("page_table", "ctx_len", "anchor", "free_top")}
     stream = torch.cuda.Stream()
+    # inputs, packed rows and the state snapshot were made on the default stream
+    stream.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
 
     def one_step():
         for k, v in small.items():
@@ -288,8 +291,14 @@ def gpu_arm(args, wl, mode, dist, world, rank, device):
                 "traffic": traffic, "algorithmic_bytes": a_bytes, "us_per_launch": attn_us,
                 "peak_source": f"{peak_src} hbm_gbs (burst copy)"}
 
+    err = dspark.read_device_error()
+    if err:
+        raise RuntimeError(f"device error word {err:#x} while timing the calls")
     # ---- end to end through the public API with host buffers
-    e2e = e2e_arm(args, wl, mode, d, step, small, stream)
+    e2e = e2e_arm(args, wl, mode, d, step, small, stream) if with_e2e else None
+    err = dspark.read_device_error()
+    if err:
+        raise RuntimeError(f"device error word {err:#x} in the end-to-end arm")
 
     steps_per_s = args.steps / (ms_max / 1e3)
     value = world * args.steps / (ms_max / 1e3)
@@ -320,7 +329,49 @@ def gpu_arm(args, wl, mode, dist, world, rank, device):
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk.summary(),
     }
+    if mode == W.MODE_CAP_ACCEPT:
+        cap = step.cap_len.cpu().numpy()
+        result["commit_over_cap"] = float(acc_len.sum() / max(1, cap.sum()))
     return result, inp
+
+
+def sweep_arm(args, dist, world, rank, device):
+    """Step rate over the batch sizes of the budget/tier sweep (Qwen3-8B shape, gamma 16,
+    ctx 2048, confidence mean 0.85, cost slope 0.19 ms/token) in the three modes.
+    Points whose inputs fit in L2 are marked: their per-kernel fractions are not HBM
+    figures."""
+    import copy
+    sargs = copy.copy(args)
+    sargs.steps = min(args.steps, 300)
+    sargs.warmup = max(3, min(args.warmup, 20))
+    sargs.kernel_iters = min(args.kernel_iters, 5)
+    pts = []
+    for B in W.SWEEP_B:
+        for mname in ("compact", "static", "cap_accept"):
+            wl = W.sweep_point(B, 0.85, 0.19)
+            sargs.mode = mname
+            try:
+                res, inp = gpu_arm(sargs, wl, W.MODE_NAMES[mname], dist, world, rank, device,
+                                   with_e2e=False)
+            except RuntimeError as e:  # reported in the line, the other points still run
+                pts.append({"B": B, "mode": mname, "error": str(e)})
+                torch.cuda.empty_cache()
+                continue
+            k = res["kernels"]
+            pt = {"B": B, "mode": mname, "steps_per_s": res["value"],
+                  "ms_per_step": res["ms_per_step"],
+                  "packed_tokens_per_s": res["packed_tokens_per_s"],
+                  "accepted_tokens_per_step": res["accepted_tokens_per_step"],
+                  "M": res["config"]["packed_rows_M"], "tier": res["config"]["tier"],
+                  "attn_us": k["verify_attn"]["us"], "attn_frac_hbm": k["verify_attn"]["frac_hbm"],
+                  "accept_us": k["accept"]["us"], "accept_frac_hbm": k["accept"]["frac_hbm"],
+                  "l2_resident": k["verify_attn"]["bytes"] + k["accept"]["bytes"] < 129e6}
+            if "commit_over_cap" in res:
+                pt["commit_over_cap"] = res["commit_over_cap"]
+            pts.append(pt)
+            del inp
+            torch.cuda.empty_cache()
+    return pts
 
 
 def e2e_arm(args, wl, mode, d, step, small, stream):
@@ -503,6 +554,8 @@ def main():
     ap.add_argument("--kernel-iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="also report the step rate at B = 1..256 in the three modes")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -561,6 +614,8 @@ def main():
     import __graft_entry__ as g
     g.build()
     result, inp = gpu_arm(args, wl, mode, dist, world, rank, device)
+    if args.sweep:
+        result["sweep"] = sweep_arm(args, dist, world, rank, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t_step, reps, reqs = oracle_timing(inp, wl, mode, args.cpu_budget_s, 2)
         result["cpu_baseline"] = cpu_baseline_block(t_step, reps, reqs, wl)
