@@ -561,6 +561,127 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sb = g & 1;
         if (!wait_warp(L.s_full(sb), (g >> 1) & 1, cx)) { ok = false; break; }
         tc_fence_after();
+        if constexpr (NT == 128) {
+        // NT = 128: two passes over the 32-column groups of S^T in rolled loops (the
+        // fully unrolled 128-column code outgrows the instruction cache next to the
+        // other roles' loops); the second pass reads S^T from TMEM again.
+        // Keys of this tile visible to column (query row) n: cache tile -> key < ctx;
+        // block tile -> block row b visible to n iff b < n_r and n >= (b - i0) * G.
+        const bool cache_tile = t < ct;
+        const bool key_dead = cache_tile && (t * kKT + kl >= ctx);
+        int nmin = 0;
+        if (!cache_tile) {
+          const int b = (t - ct) * kKT + kl;          // block row of this key
+          nmin = b < n_r ? (b - item.i0) * G : 0x7fffffff;
+        }
+        const uint32_t s_col = t_lane + C::TMEM_S + sb * NT;
+        // ---- pass 1: tile max per row (warp transpose-reduce), then across the 4 warps
+        float* wmax = s_wmax + (g & 1) * 4 * NT;
+#pragma unroll 1
+        for (int gi = 0; gi < ng; ++gi) {
+          float v[32];
+          tmem_ld32(s_col + gi * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            v[k] = (key_dead || gi * 32 + k < nmin) ? -INFINITY : v[k];
+          wmax[sw * NT + gi * 32 + lane] = transpose_reduce<true>(v, lane) * sl2;
+        }
+        __syncwarp();
+        // P buffers double as the epilogue's staging area: its bulk reads must be done
+        // before any warp passes this exchange and writes P
+        if (warp == kSoftmaxWarp0 && lane == 0) bulk_wait_read_all();
+        if (lane == 0) mbar_arrive(L.xw(g & 1));
+        if (!wait_warp(L.xw(g & 1), (g >> 1) & 1, cx)) { ok = false; break; }
+        bool need_any = false;
+#pragma unroll
+        for (int gi = 0; gi < C::G32; ++gi) {
+          if (gi >= ng) break;
+          const int n = gi * 32 + lane;
+          const float tm = fmaxf(fmaxf(wmax[n], wmax[NT + n]), fmaxf(wmax[2 * NT + n], wmax[3 * NT + n]));
+          float alpha = 1.f;
+          if (tm > mref[gi] + 8.0f) {        // lazy: move the reference only on a 2^8 jump
+            alpha = (mref[gi] == -INFINITY) ? 0.f : fast_exp2(mref[gi] - tm);
+            mref[gi] = tm;
+            lacc[gi] *= alpha;
+            need_any = true;
+          }
+          my_mref[n] = mref[gi] == -INFINITY ? 0.f : mref[gi];
+          my_alpha[n] = alpha;
+        }
+        const bool rescale = __any_sync(0xffffffffu, need_any) && l > 0;
+        __syncwarp();
+        // P buffer of this tile must be free: PV(g - P_BUFS) done
+        const int pb = g % C::P_BUFS;
+        if (g >= C::P_BUFS &&
+            !wait_warp(L.p_empty((g - C::P_BUFS) % C::P_BUFS), ((g - C::P_BUFS) / C::P_BUFS) & 1, cx)) {
+          ok = false;
+          break;
+        }
+        if (rescale) {
+          // O^T must hold PV(g-1) before its columns are rescaled
+          if (C::P_BUFS > 1 &&
+              !wait_warp(L.p_empty((g - 1) % C::P_BUFS), ((g - 1) / C::P_BUFS) & 1, cx)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < NT / 32; ++c) {
+            float o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= my_alpha[c * 32 + k];
+            tmem_st32(t_o + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        // ---- pass 2: P^T row of this key, exp2(s * scale - mref[n]) in bf16, and the
+        // per-row partial sums over this warp's 32 keys.  Only the 8-column chunks
+        // holding valid rows are written: padding columns of P^T are left as they are
+        // -- they only reach their own columns of O^T, which are never stored.
+        const uint32_t prow = L.pbuf(pb);
+#pragma unroll 1
+        for (int gi = 0; gi < ng; ++gi) {
+          float v[32];
+          tmem_ld32(s_col + gi * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            v[k] = (key_dead || gi * 32 + k < nmin) ? -INFINITY : v[k];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int n8 = gi * 4 + q;
+            if (n8 >= nc8) break;
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int k = q * 8 + 2 * h;
+              const int n = gi * 32 + k;
+              const float p0 = fast_exp2(fmaf(v[k], sl2, -my_mref[n]));
+              const float p1 = fast_exp2(fmaf(v[k + 1], sl2, -my_mref[n + 1]));
+              v[k] = p0;
+              v[k + 1] = p1;
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              w[h] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            const uint32_t off = (n8 >> 3) * (kKT * 128) + sw128_off(kl, n8 & 7);
+            st_shared_v4(prow + off, make_uint4(w[0], w[1], w[2], w[3]));
+          }
+          const float rs = transpose_reduce<false>(v, lane);
+#pragma unroll
+          for (int i = 0; i < C::G32; ++i)
+            if (i == gi) lacc[i] += rs;
+        }
+        // S^T of this tile is read: its TMEM columns may take tile g + 2
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.s_free(sb));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.p_full(pb));
+        } else {
         float s[NT];
 #pragma unroll
         for (int c = 0; c < NT / 32; ++c) {
@@ -681,6 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = s[gi * 32 + k];
           lacc[gi] += transpose_reduce<false>(v, lane);
+        }
         }
       }
       if (!ok) break;
