@@ -14,25 +14,28 @@
 //   * the QK^T reduction is split the same way: CTA rho multiplies dims
 //     256 rho .. +255 (its own value columns) and rope dims 512 + 32 rho .. +31.
 //     It loads only those 5 of the 9 64-wide column blocks of a key tile;
-//   * the two partial score tiles (fp32) are swapped through distributed shared
-//     memory and added; fp32 addition commutes, so both CTAs hold bit-identical
-//     scores and run the identical softmax (same P, max and sum);
+//   * the two partial score tiles, scaled to the log2 domain and rounded to fp16,
+//     are swapped through distributed shared memory and added in fp32; each CTA
+//     adds the same two rounded values, so both hold bit-identical scores and run
+//     the identical softmax (same P, max and sum).  The rounding moves a logit by at
+//     most 2^-11 of the partial's magnitude, the size of the bf16 rounding of P;
 //   * Q (this CTA's 288 dims) and P sit in TMEM and are the A operand of the MMAs,
 //     so each product reads only the key tile (B) from shared memory.
 //
 //   S_rho [128 heads x 64 keys] = Q_rho . K_rho^T                 (tcgen05, TMEM)
-//   S = S_0 + S_1 (exchanged); P = exp2(scale' S - m)             (fp32, SFU)
+//   x = fp16(scale' S_0) + fp16(scale' S_1) (exchanged); P = exp2(x - m)  (SFU)
 //   O_rho [128 x 256] += P . K[:, 256 rho .. 256 rho + 255]       (tcgen05, TMEM)
 //
 // The swap is the narrow point: the SM-to-SM network moves about 15 bytes per clock
-// per SM (st.async; bulk copies reach about half that), so a 32 KB tile of partials
-// takes about as long as the tile's products.  Dedicated exchange warps send it
+// per SM (st.async; bulk copies reach about half that), so even the 16 KB of fp16
+// partials of a tile take about as long as the tile's products (fp32 partials took
+// twice that).  Dedicated exchange warps send them
 // with st.async, whose bytes complete on the receiver's mbarrier, so no thread
 // waits on a cluster-scope fence, and the send overlaps the softmax of the tile
 // before.
 //
 // TMEM columns: O [0, 256), S [256, 320), P [320, 352), Q [352, 496).
-// Warp roles: 0 TMA producer (a 3-stage ring of key tiles), 1 MMA issuer (one lane)
+// Warp roles: 0 TMA producer (a 4-stage ring of key tiles), 1 MMA issuer (one lane)
 // that first zeroes the key rows past the visible range of a partial tile (value
 // rows met by a zero probability must be finite), 2-5 softmax and epilogue, 6-9
 // score exchange; in both groups thread = query head = TMEM lane.  Every wait is
@@ -41,6 +44,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -63,11 +67,11 @@ constexpr int kHalf = 256;       // value dims of one CTA
 constexpr int kCBs = 5;          // 64-wide column blocks one CTA loads per key tile
 constexpr int kCBBytes = kNK * 128;
 constexpr int kStageBytes = kCBs * kCBBytes;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kQKSteps = 18;     // 288 dims / 16
-// Partial score exchange: a row is 64 fp32 partials (256 B); 16-byte piece c of row m
-// sits at piece c ^ (m mod 16), which keeps 8 consecutive rows on distinct banks.
-constexpr int kXRow = 256;
+// Partial score exchange: a row is 64 fp16 partials (128 B); 16-byte piece c of row m
+// sits at piece c ^ (m mod 8), which keeps 8 consecutive rows on distinct banks.
+constexpr int kXRow = 128;
 constexpr int kXBytes = kRows * kXRow;
 constexpr int kChunkRows = 16;   // block-row box
 constexpr int kProdWarp = 0;
@@ -142,6 +146,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Scaled partial scores as exchanged: a pair of fp32 values rounded to fp16 (the
+// 32-bit word sent) and the same pair widened back.
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_h2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
@@ -405,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
     const float sl2 = prm.scale_log2;
     const uint32_t x_row = static_cast<uint32_t>(m * kXRow);
-    const int sx = m & 15;
+    const int sx = m & 7;
     int g = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it) {
@@ -458,15 +472,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 9; ++i) prefetch_l2(nq + i * 128);
         }
       }
-      // m_used: reference max (log2 domain, scaled); l_sum: sum of exp2(s*sl2 - m_used)
+      // m_used: reference max of x; l_sum: sum of exp2(x - m_used)
       float m_used = -INFINITY, l_sum = 0.f;
       const int ntiles = item.te - item.tb;
       for (int l = 0; l < ntiles; ++l, ++g) {
         const int t = item.tb + l;
         const int xb = g & 1;
-        // ---- S = S_0 + S_1: this CTA's partial from TMEM, the peer's from the exchange
-        // slot (stored here by the peer's exchange warps); fp32 addition commutes, so
-        // both CTAs get identical bits
+        // ---- x = S * scale * log2(e) = x_0 + x_1: both partials are rounded to fp16
+        // (this CTA's from TMEM, the peer's as received in the exchange slot) and added
+        // in fp32; the sum commutes, so both CTAs get identical bits
         if (!wait_warp(L.s_full(), g & 1, cx)) { ok = false; break; }
         tc_fence_after();
         float s[kNK];
@@ -476,7 +490,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_lane + TMEM_S + 32, b);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) { s[k] = a[k]; s[32 + k] = b[k]; }
+          for (int k = 0; k < 16; ++k) {
+            const float2 ra = unpack_h2(pack_h2(a[2 * k] * sl2, a[2 * k + 1] * sl2));
+            const float2 rb = unpack_h2(pack_h2(b[2 * k] * sl2, b[2 * k + 1] * sl2));
+            s[2 * k] = ra.x;
+            s[2 * k + 1] = ra.y;
+            s[32 + 2 * k] = rb.x;
+            s[32 + 2 * k + 1] = rb.y;
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -486,12 +507,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const uint32_t rp = L.x(xb) + x_row;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
+          for (int c = 0; c < 8; ++c) {
             const float4 v = ld_shared_f4(rp + ((c ^ sx) << 4));
-            s[4 * c] += v.x;
-            s[4 * c + 1] += v.y;
-            s[4 * c + 2] += v.z;
-            s[4 * c + 3] += v.w;
+            const float2 h0 = unpack_h2(__float_as_uint(v.x)), h1 = unpack_h2(__float_as_uint(v.y));
+            const float2 h2 = unpack_h2(__float_as_uint(v.z)), h3 = unpack_h2(__float_as_uint(v.w));
+            s[8 * c] += h0.x;
+            s[8 * c + 1] += h0.y;
+            s[8 * c + 2] += h1.x;
+            s[8 * c + 3] += h1.y;
+            s[8 * c + 4] += h2.x;
+            s[8 * c + 5] += h2.y;
+            s[8 * c + 6] += h3.x;
+            s[8 * c + 7] += h3.y;
           }
         }
         __syncwarp();
@@ -509,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 8; k < kNK; ++k) mx[k & 7] = fmaxf(mx[k & 7], s[k]);
         const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         // lazy rescale: move the reference only when the max grows by more than 2^8
         const bool need = mt > m_used + 8.0f;
         const float m_new = need ? mt : m_used;
@@ -518,8 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float psum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float p0 = fast_exp2(fmaf(s[2 * k], sl2, -mref));
-          const float p1 = fast_exp2(fmaf(s[2 * k + 1], sl2, -mref));
+          const float p0 = fast_exp2(s[2 * k] - mref);
+          const float p1 = fast_exp2(s[2 * k + 1] - mref);
           psum[k & 3] += p0 + p1;
           __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
           pw[k] = *reinterpret_cast<uint32_t*>(&b2);
@@ -600,7 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m = sw * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
     const uint32_t x_row = static_cast<uint32_t>(m * kXRow);
-    const int sx = m & 15;
+    const int sx = m & 7;
+    const float sl2 = prm.scale_log2;
     const uint32_t x_peer = mapa_shared(L.x(0), peer) + x_row;
     const uint32_t xf_peer = mapa_shared(L.x_full(0), peer);
     int g = 0;
@@ -628,10 +656,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = x_peer + xb * kXBytes;
         const uint32_t bar = xf_peer + 8 * xb;
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
+        for (int c = 0; c < 8; ++c)
           st_async_v4(dst + ((c ^ sx) << 4),
-                      make_uint4(__float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
-                                 __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3])),
+                      make_uint4(pack_h2(s[8 * c] * sl2, s[8 * c + 1] * sl2),
+                                 pack_h2(s[8 * c + 2] * sl2, s[8 * c + 3] * sl2),
+                                 pack_h2(s[8 * c + 4] * sl2, s[8 * c + 5] * sl2),
+                                 pack_h2(s[8 * c + 6] * sl2, s[8 * c + 7] * sl2)),
                       bar);
       }
     }

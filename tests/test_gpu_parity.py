@@ -291,16 +291,21 @@ def test_mla_page16_split():
     run_and_check(inp, O.COMPACT)
 
 
-@pytest.mark.parametrize("page_size", [32, 128])
-def test_mla_ragged_edges(page_size):
-    """Latent KV: ctx = 0, exactly one page, exactly one 64-key tile, ragged tails and a
-    page boundary at the block, with windows forced to gamma and to 0."""
+@pytest.mark.parametrize("page_size,ctxs", [
+    (32, [0, 32, 64, 100, 257, 700, 1023, 47]),
+    (128, [0, 128, 64, 100, 257, 700, 1023, 47]),
+    (64, [0, 64, 32, 33, 31, 97, 511, 1]),
+])
+def test_mla_ragged_edges(page_size, ctxs):
+    """Latent KV: ctx = 0, exactly one page, one whole 64-key tile, a single key, keys
+    just below, at and past half a tile, ragged tails and a page boundary at the block,
+    with windows forced to gamma and to 0."""
     wl = W.Workload(
         name=f"mla_edges_p{page_size}", B=8, gamma=5, attn="mla", Hq=128, Hkv=1, d_qk=576,
         d_v=512, page_size=page_size, ctx=("const", 0), conf=("logit", 1.0, 1.0), vocab=1024,
         p_dtype="f32", target_logit_std=2.0, draft_noise_std=0.5, tiers=(8, 16, 32, 64),
         cost_theta_ms=0.05)
-    inp = W.make_inputs(wl, seed=6, ctx_override=[0, page_size, 64, 100, 257, 700, 1023, 47])
+    inp = W.make_inputs(wl, seed=6, ctx_override=ctxs)
     conf = inp["conf"].clone()
     conf[0] = 20.0
     conf[1] = -20.0
