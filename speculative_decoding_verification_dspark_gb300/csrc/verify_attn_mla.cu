@@ -26,15 +26,18 @@
 //   x = fp16(scale' S_0) + fp16(scale' S_1) (exchanged); P = exp2(x - m)  (SFU)
 //   O_rho [128 x 256] += P . K[:, 256 rho .. 256 rho + 255]       (tcgen05, TMEM)
 //
-// The swap is the narrow point: the SM-to-SM network moves about 15 bytes per clock
-// per SM (st.async; bulk copies reach about half that), so even the 16 KB of fp16
-// partials of a tile take about as long as the tile's products (fp32 partials took
-// twice that).  Dedicated exchange warps send them
-// with st.async, whose bytes complete on the receiver's mbarrier, so no thread
-// waits on a cluster-scope fence, and the send overlaps the softmax of the tile
-// before.
+// The swap is the narrow point: with both CTAs sending at once and the key tiles
+// streaming in, the SM-to-SM network moves only about 7 bytes per clock each way, so
+// even the 16 KB of fp16 partials of a tile take longer than the tile's products
+// (fp32 partials took twice as long).  Dedicated exchange warps read S from TMEM
+// (releasing it for the next tile's QK^T at once), round it, send it with st.async,
+// whose bytes complete on the receiver's mbarrier (no thread waits on a
+// cluster-scope fence), and keep the CTA's own rounded copy beside the peer's in the
+// exchange slot; the softmax reads both from shared memory.
 //
 // TMEM columns: O [0, 256), S [256, 320), P [320, 352), Q [352, 496).
+// Shared memory: a 4-stage ring of key tiles (5 blocks x 64 keys, 40 KB) and two
+// exchange slots (peer's and own partials, 2 x 16 KB each).
 // Warp roles: 0 TMA producer (a 4-stage ring of key tiles), 1 MMA issuer (one lane)
 // that first zeroes the key rows past the visible range of a partial tile (value
 // rows met by a zero probability must be finite), 2-5 softmax and epilogue, 6-9
@@ -81,7 +84,8 @@ constexpr int kExchWarp0 = 6;
 constexpr int kThreads = 10 * 32;
 constexpr int OFF_STAGE = 0;
 constexpr int OFF_X = OFF_STAGE + kStages * kStageBytes;
-constexpr int OFF_BAR = OFF_X + 2 * kXBytes;
+// two exchange slots, each the peer's partials then this CTA's own rounded partials
+constexpr int OFF_BAR = OFF_X + 4 * kXBytes;
 // kv_full[S], kv_empty[S], s_full, s_free, p_full, p_empty, q_full, x_full[2], xc
 constexpr int N_BARS = 2 * kStages + 8;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
@@ -185,7 +189,8 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 struct Layout {
   uint32_t base;
   __device__ uint32_t stage(int s) const { return base + OFF_STAGE + s * kStageBytes; }
-  __device__ uint32_t x(int b) const { return base + OFF_X + b * kXBytes; }
+  __device__ uint32_t x(int b) const { return base + OFF_X + b * 2 * kXBytes; }
+  __device__ uint32_t xo(int b) const { return x(b) + kXBytes; }
   __device__ uint32_t bar(int i) const { return base + OFF_BAR + 8 * i; }
   __device__ uint32_t kv_full(int s) const { return bar(s); }
   __device__ uint32_t kv_empty(int s) const { return bar(kStages + s); }
@@ -247,12 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(L.kv_empty(s), 1);
     }
     mbar_init(L.s_full(), 1);
-    mbar_init(L.s_free(), 8);   // softmax and exchange warps both read S
+    mbar_init(L.s_free(), 4);   // the exchange warps read S
     mbar_init(L.p_full(), 4);
     mbar_init(L.p_empty(), 1);
     mbar_init(L.q_full(), 4);
-    // armed (expect_tx) by this CTA, completed by the peer's asynchronous stores
-    for (int b = 0; b < 2; ++b) mbar_init(L.x_full(b), 1);
+    // armed (expect_tx) by this CTA's softmax, completed by the peer's asynchronous
+    // stores and by this CTA's exchange warps (own partials in place)
+    for (int b = 0; b < 2; ++b) mbar_init(L.x_full(b), 5);
     mbar_init(L.xc(), 4);
     fence_mbar_init();
   }
@@ -417,7 +423,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sw = warp & 3;                 // TMEM lane quadrant of this warp
     const int m = sw * 32 + lane;            // query head of this thread
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
-    const float sl2 = prm.scale_log2;
     const uint32_t x_row = static_cast<uint32_t>(m * kXRow);
     const int sx = m & 7;
     int g = 0;
@@ -478,47 +483,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int l = 0; l < ntiles; ++l, ++g) {
         const int t = item.tb + l;
         const int xb = g & 1;
-        // ---- x = S * scale * log2(e) = x_0 + x_1: both partials are rounded to fp16
-        // (this CTA's from TMEM, the peer's as received in the exchange slot) and added
-        // in fp32; the sum commutes, so both CTAs get identical bits
-        if (!wait_warp(L.s_full(), g & 1, cx)) { ok = false; break; }
-        tc_fence_after();
-        float s[kNK];
-        {
-          float a[32], b[32];
-          tmem_ld32(t_lane + TMEM_S, a);
-          tmem_ld32(t_lane + TMEM_S + 32, b);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 ra = unpack_h2(pack_h2(a[2 * k] * sl2, a[2 * k + 1] * sl2));
-            const float2 rb = unpack_h2(pack_h2(b[2 * k] * sl2, b[2 * k + 1] * sl2));
-            s[2 * k] = ra.x;
-            s[2 * k + 1] = ra.y;
-            s[32 + 2 * k] = rb.x;
-            s[32 + 2 * k + 1] = rb.y;
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(L.s_free());
+        // ---- x = S * scale * log2(e) = x_0 + x_1: both partials sit in the exchange
+        // slot as fp16 (this CTA's stored by its exchange warps, the peer's sent by the
+        // peer's) and are added in fp32; the sum commutes, so both CTAs get identical bits
         if (m == 0) mbar_arrive_expect_tx(L.x_full(xb), kXBytes);  // what the peer sends here
         if (!wait_warp<true>(L.x_full(xb), (g >> 1) & 1, cx)) { ok = false; break; }
+        float s[kNK];
         {
-          const uint32_t rp = L.x(xb) + x_row;
+          const uint32_t rp = L.x(xb) + x_row, ro = L.xo(xb) + x_row;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const float4 v = ld_shared_f4(rp + ((c ^ sx) << 4));
-            const float2 h0 = unpack_h2(__float_as_uint(v.x)), h1 = unpack_h2(__float_as_uint(v.y));
-            const float2 h2 = unpack_h2(__float_as_uint(v.z)), h3 = unpack_h2(__float_as_uint(v.w));
-            s[8 * c] += h0.x;
-            s[8 * c + 1] += h0.y;
-            s[8 * c + 2] += h1.x;
-            s[8 * c + 3] += h1.y;
-            s[8 * c + 4] += h2.x;
-            s[8 * c + 5] += h2.y;
-            s[8 * c + 6] += h3.x;
-            s[8 * c + 7] += h3.y;
+            const uint32_t off = static_cast<uint32_t>((c ^ sx) << 4);
+            const float4 vo = ld_shared_f4(ro + off), vp = ld_shared_f4(rp + off);
+            const float wo[4] = {vo.x, vo.y, vo.z, vo.w}, wp[4] = {vp.x, vp.y, vp.z, vp.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 a = unpack_h2(__float_as_uint(wo[i]));
+              const float2 b = unpack_h2(__float_as_uint(wp[i]));
+              s[8 * c + 2 * i] = a.x + b.x;
+              s[8 * c + 2 * i + 1] = a.y + b.y;
+            }
           }
         }
         __syncwarp();
@@ -618,11 +602,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kExchWarp0) {
     // ------------------------------------------------------------- score exchange
-    // Per tile: S_rho from TMEM (released once the softmax warps have read it too),
-    // sent to the peer's exchange slot.  The send of tile g waits until this
-    // CTA's softmax has read tile g - 1: the peer's slot of tile g (used for g - 2
-    // before) is then free, because the peer sent tile g - 1 only after its own
-    // softmax had read tile g - 2.
+    // Per tile: S_rho from TMEM (released as soon as it is in registers), rounded,
+    // sent to the peer's exchange slot and stored in this CTA's own half of the
+    // slot.  The send of tile g waits until this CTA's softmax has read tile g - 1:
+    // the peer's slot of tile g (used for g - 2 before) is then free, because the
+    // peer sent tile g - 1 only after its own softmax had read tile g - 2; this
+    // CTA's own half of the slot was read with tile g - 2 as well.
     const int sw = warp & 3;
     const int m = sw * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
@@ -652,17 +637,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(L.s_free());
-        if (g >= 1 && !wait_warp(L.xc(), (g - 1) & 1, cx)) { ok = false; break; }
-        const uint32_t dst = x_peer + xb * kXBytes;
-        const uint32_t bar = xf_peer + 8 * xb;
+        uint4 w[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          st_async_v4(dst + ((c ^ sx) << 4),
-                      make_uint4(pack_h2(s[8 * c] * sl2, s[8 * c + 1] * sl2),
-                                 pack_h2(s[8 * c + 2] * sl2, s[8 * c + 3] * sl2),
-                                 pack_h2(s[8 * c + 4] * sl2, s[8 * c + 5] * sl2),
-                                 pack_h2(s[8 * c + 6] * sl2, s[8 * c + 7] * sl2)),
-                      bar);
+          w[c] = make_uint4(pack_h2(s[8 * c] * sl2, s[8 * c + 1] * sl2),
+                            pack_h2(s[8 * c + 2] * sl2, s[8 * c + 3] * sl2),
+                            pack_h2(s[8 * c + 4] * sl2, s[8 * c + 5] * sl2),
+                            pack_h2(s[8 * c + 6] * sl2, s[8 * c + 7] * sl2));
+        if (g >= 1 && !wait_warp(L.xc(), (g - 1) & 1, cx)) { ok = false; break; }
+        const uint32_t dst = x_peer + xb * 2 * kXBytes;
+        const uint32_t bar = xf_peer + 8 * xb;
+        const uint32_t own = L.xo(xb) + x_row;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_async_v4(dst + ((c ^ sx) << 4), w[c], bar);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_shared_v4(own + ((c ^ sx) << 4), w[c]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(L.x_full(xb));  // own partials in place
       }
     }
   }
