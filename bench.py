@@ -43,9 +43,15 @@ KERNELS_PER_STEP = 11   # schedule 2, pack 1, attention 3, accept 3, compact 2
 PROFILES = os.path.join(ROOT, "profiles")
 _CSRC = os.path.join(ROOT, "speculative_decoding_verification_dspark_gb300", "csrc")
 # sources whose change invalidates a committed DRAM-traffic figure
-ATTN_SRC = [os.path.join(_CSRC, f) for f in
-            ("verify_attn.cu", "verify_attn_gqa.cu", "verify_attn_mla.cu", "attn.h", "ptx.cuh",
-             "common.cuh")]
+_ATTN_COMMON = ("verify_attn.cu", "attn.h", "ptx.cuh", "common.cuh")
+
+
+def attn_src(wl):
+    """The attention call's sources for this workload's head shape."""
+    main = "verify_attn_mla.cu" if wl.attn == "mla" else "verify_attn_gqa.cu"
+    return [os.path.join(_CSRC, f) for f in _ATTN_COMMON + (main,)]
+
+
 ACCEPT_SRC = [os.path.join(_CSRC, f) for f in ("accept.cu", "common.cuh")]
 
 
@@ -182,6 +188,26 @@ def accept_bytes(wl, windows, n_rows, accept_len, mode):
 
 # ------------------------------------------------------------------ GPU arm
 
+def restore_pairs(d, keys):
+    """(destination, saved copy) pairs that put the step's small mutable state back.
+    When the tensors share a dtype they are moved into one buffer first (each a view
+    at a 256-byte boundary), so the restore is a single copy."""
+    ts = [d[k] for k in keys]
+    if len({t.dtype for t in ts}) != 1 or len({t.device for t in ts}) != 1:
+        return [(d[k], d[k].clone()) for k in keys]
+    per = 256 // ts[0].element_size()
+    offs, total = [], 0
+    for t in ts:
+        offs.append(total)
+        total += (t.numel() + per - 1) // per * per
+    flat = torch.zeros(total, dtype=ts[0].dtype, device=ts[0].device)
+    for k, t, o in zip(keys, ts, offs):
+        view = flat[o:o + t.numel()].view(t.shape)
+        view.copy_(t)
+        d[k] = view
+    return [(flat, flat.clone())]
+
+
 def gpu_arm(args, wl, mode, dist, world, rank, device, with_e2e=True):
     import harness
     import speculative_decoding_verification_dspark_gb300 as dspark
@@ -189,15 +215,15 @@ def gpu_arm(args, wl, mode, dist, world, rank, device, with_e2e=True):
     inp = W.make_inputs(wl, seed=args.seed + rank, device=W.gen_device(wl))
     d, step = harness.prepare(inp, mode)
     snap = harness.snapshot_state(d)
-    small = {k: snap[k] for k in ("page_table", "ctx_len", "anchor", "free_top")}
+    small = restore_pairs(d, ("page_table", "ctx_len", "anchor", "free_top"))
     stream = torch.cuda.Stream()
     # inputs, packed rows and the state snapshot were made on the default stream
     stream.wait_stream(torch.cuda.current_stream())
     torch.cuda.synchronize()
 
     def one_step():
-        for k, v in small.items():
-            d[k].copy_(v, non_blocking=True)
+        for dst, src in small:
+            dst.copy_(src, non_blocking=True)
         step.run(d, mode)
 
     # eager warm-up (also compiles nothing: all kernels are precompiled)
@@ -272,7 +298,7 @@ def gpu_arm(args, wl, mode, dist, world, rank, device, with_e2e=True):
     attn_gbs = a_bytes / (attn_us * 1e-6) / 1e9
     acc_gbs = c_bytes / (accept_us * 1e-6) / 1e9
     attn_tfs = a_flops / (attn_us * 1e-6) / 1e12
-    traffic = load_traffic("verify_attn", wl.name, ATTN_SRC)
+    traffic = load_traffic("verify_attn", wl.name, attn_src(wl))
     # the attention call is tensor-bound when its flops per algorithmic byte exceed the
     # ridge point of the measured peaks (the latent-KV shape), else HBM-bound
     tf_peak = peaks.get("bf16_tflops")
@@ -392,8 +418,8 @@ def e2e_arm(args, wl, mode, d, step, small, stream):
     def one():
         for k, v in host.items():
             dev_view[k].copy_(v, non_blocking=True)
-        for k, v in small.items():
-            d[k].copy_(v, non_blocking=True)
+        for dst, src in small:
+            dst.copy_(src, non_blocking=True)
         step.run(d, mode)
         for k in out_keys:
             host_out[k].copy_(getattr(step, k), non_blocking=True)
