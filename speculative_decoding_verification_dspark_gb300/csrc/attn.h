@@ -9,8 +9,11 @@
 namespace dspark {
 namespace attn {
 
-// One unit of work: a tile of query rows of one request against a range of its key tiles;
-// nsplit = the group's piece count (1: not split); a piece of a split group writes
+// One unit of work: a tile of query rows of one request against a range of its key tiles
+// (tiles tb .. te-1 of the request's ceil(ctx/nk) cache tiles followed by its block
+// tiles; in the latent-KV work list the range may pass the tile count T and then
+// wraps: tile t >= T means t - T); nsplit = the group's piece count (1: not split); a
+// piece of a split group writes
 // partial rows into partial slot `slot`: 2c for the first piece of CTA c, 2c + 1 for
 // its last (a split piece is always one of the two).
 struct __align__(16) AttnItem {

@@ -39,6 +39,11 @@ constexpr int kRows = 128;  // query rows of one work item (UMMA M / N side)
 // of its CTA and writes partial (o, lse) rows into slot 2c or 2c + 1.  The CTA that
 // runs the last piece of a split group records the group for the combine.
 //
+// Latent-KV items take their group's tiles in a rotated order (see the group loop):
+// a request's block rows run as separate groups, and rotating each by the time it
+// starts makes the rows that run at the same time on different clusters read the
+// same key tile, which the L2 then serves once.
+//
 // Built in parallel: a thread per CTA counts the groups its range meets (they are
 // consecutive, so the count is the difference of two group indices) and a block scan
 // gives each CTA's first item; then a thread per group writes the group's pieces
@@ -86,7 +91,7 @@ __device__ __forceinline__ int last_at_or_below(const T* off, int n, T x) {
 __global__ void __launch_bounds__(1024)
     worklist_kernel(const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ cu_seqlens,
                     int B, int max_rows, int Hkv, int parts, int rows_per_tile, int NK, int ncta,
-                    int max_splits, int max_items, AttnItem* __restrict__ items,
+                    int max_splits, int rotate, int max_items, AttnItem* __restrict__ items,
                     int* __restrict__ item_begin, SplitGroup* __restrict__ groups,
                     unsigned int* __restrict__ err) {
   pdl_release();
@@ -194,6 +199,11 @@ __global__ void __launch_bounds__(1024)
     const int i0 = t * rows_per_tile;
     const int ni = min(rows_per_tile, s_n[r] - i0);
     const int nsplit = c_last - c_first + 1;
+    // rotate: the group's tiles are taken in the order rot, rot + 1, ... (mod t_r),
+    // rot = the time (in units) at which the group starts on its first CTA; every
+    // group started this way reads tile (time mod t_r) at a given time, so the rows
+    // of one request that run at the same time on different CTAs read the same tile
+    const int rot = rotate ? static_cast<int>((gstart - (long long)c_first * U / n_eff) % t_r) : 0;
     for (int cc = c_first; cc <= c_last; ++cc) {
       const long long lo = (long long)cc * U / n_eff;
       const long long hi = (long long)(cc + 1) * U / n_eff;
@@ -202,8 +212,9 @@ __global__ void __launch_bounds__(1024)
       AttnItem it;
       it.r = r; it.kvh = h; it.i0 = i0; it.ni = ni;
       it.part = p; it.split = cc - c_first;
-      it.tb = static_cast<int>(u0 - gstart);
-      it.te = static_cast<int>(u1 - gstart);
+      it.tb = static_cast<int>(u0 - gstart) + rot;
+      if (it.tb >= t_r) it.tb -= t_r;
+      it.te = it.tb + static_cast<int>(u1 - u0);  // may pass t_r: the tile index wraps
       it.nsplit = nsplit;
       it.slot = u0 == lo ? 2 * cc : 2 * cc + 1;
       it.pad0 = 0; it.pad1 = 0;
@@ -323,7 +334,8 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
   const int splits = max_splits < 2 ? 2 : (max_splits > 32 ? 32 : max_splits);
 
   if (launch_pdl(worklist_kernel, dim3(1), dim3(1024), 0, stream, ctx_len, cu_seqlens, B, max_rows,
-                 Hkv, pl.parts, pl.rows_per_tile, pl.nk, ncta, splits, max_items, items, item_begin,
+                 Hkv, pl.parts, pl.rows_per_tile, pl.nk, ncta, splits, pl.mla ? 1 : 0, max_items,
+                 items, item_begin,
                  groups, err) != cudaSuccess)
     return DSPARK_ECUDA;
 

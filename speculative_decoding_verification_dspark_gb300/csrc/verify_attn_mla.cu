@@ -295,8 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ctx = item.ctx;
       const int ct = ceil_div(ctx, kNK);
       const int32_t* ptab = prm.page_table + (long long)item.r * prm.max_pages;
+      const int nt = ct + ceil_div(item.n_r, kNK);  // the item's tile range wraps at nt
       int win_base = -1, win_page = 0;
-      for (int t = item.tb; t < item.te; ++t, ++g) {
+      for (int tt = item.tb; tt < item.te; ++tt, ++g) {
+        const int t = tt < nt ? tt : tt - nt;
         const int s = g % kStages;
         if (g >= kStages) {
           ok = wait_warp(L.kv_empty(s), ((g / kStages) - 1) & 1, cx);
@@ -312,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < ct) {
           const int slot0 = (t * kNK) >> lp;
           const int nslot = ceil_div(kNK, P);
-          if (win_base < 0 || slot0 + nslot > win_base + 32) {
+          if (win_base < 0 || slot0 < win_base || slot0 + nslot > win_base + 32) {
             win_base = slot0;
             const int sl = win_base + lane;
             const bool used = (sl << lp) < ctx;
@@ -376,13 +378,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
       const AttnItem item = prm.items[it];
       const int ct = ceil_div(item.ctx, kNK);
+      const int nt = ct + ceil_div(item.n_r, kNK);  // the item's tile range wraps at nt
       if (!wait_warp(L.q_full(), n_it & 1, cx)) { ok = false; break; }
       const int ntiles = item.te - item.tb;
       for (int l = 0; l < ntiles; ++l, ++g) {
         const int s = g % kStages;
         const uint32_t st = L.stage(s);
         if (!wait_warp(L.kv_full(s), (g / kStages) & 1, cx)) { ok = false; break; }
-        const int vis = visible_keys(item.tb + l, ct, item.ctx, item.n_r);
+        const int tt = item.tb + l;
+        const int vis = visible_keys(tt < nt ? tt : tt - nt, ct, item.ctx, item.n_r);
         if (vis < kNK) {
           // rows vis..63 of the 5 column blocks, 8 16-byte pieces per row
           const int nz = (kNK - vis) * kCBs * 8;
@@ -480,8 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // m_used: reference max of x; l_sum: sum of exp2(x - m_used)
       float m_used = -INFINITY, l_sum = 0.f;
       const int ntiles = item.te - item.tb;
+      const int nt = ct + ceil_div(n_r, kNK);  // the item's tile range wraps at nt
       for (int l = 0; l < ntiles; ++l, ++g) {
-        const int t = item.tb + l;
+        const int t = item.tb + l < nt ? item.tb + l : item.tb + l - nt;
         const int xb = g & 1;
         // ---- x = S * scale * log2(e) = x_0 + x_1: both partials sit in the exchange
         // slot as fp16 (this CTA's stored by its exchange warps, the peer's sent by the
