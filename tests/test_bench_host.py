@@ -1,0 +1,71 @@
+"""Host-side helpers of bench.py on CPU: the one-copy restore of the step's small
+mutable state, and which sources a committed DRAM-traffic figure is keyed to."""
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads as W  # noqa: E402
+
+KEYS = ("page_table", "ctx_len", "anchor", "free_top")
+
+
+def _state():
+    g = torch.Generator().manual_seed(3)
+    return {
+        "page_table": torch.randint(-1, 500, (5, 7), generator=g, dtype=torch.int32),
+        "ctx_len": torch.randint(0, 900, (5,), generator=g, dtype=torch.int32),
+        "anchor": torch.randint(0, 1000, (5,), generator=g, dtype=torch.int32),
+        "free_top": torch.tensor([123], dtype=torch.int32),
+    }
+
+
+def test_restore_pairs_is_one_copy_of_views():
+    d = _state()
+    before = {k: v.clone() for k, v in d.items()}
+    pairs = bench.restore_pairs(d, KEYS)
+    assert len(pairs) == 1
+    flat, saved = pairs[0]
+    for k in KEYS:
+        assert torch.equal(d[k], before[k]) and d[k].shape == before[k].shape
+        assert d[k].is_contiguous()
+        assert d[k].untyped_storage().data_ptr() == flat.untyped_storage().data_ptr()
+        assert (d[k].data_ptr() - flat.data_ptr()) % 256 == 0  # each view on a 256-byte boundary
+    # the step mutates the state in place; one copy puts all of it back
+    d["page_table"].fill_(-7)
+    d["ctx_len"] += 5
+    d["anchor"].zero_()
+    d["free_top"][0] = 0
+    for dst, src in pairs:
+        dst.copy_(src)
+    for k in KEYS:
+        assert torch.equal(d[k], before[k])
+    assert not torch.equal(saved, torch.zeros_like(saved))
+
+
+def test_restore_pairs_falls_back_on_mixed_dtypes():
+    d = _state()
+    d["anchor"] = d["anchor"].to(torch.int64)
+    before = {k: v.clone() for k, v in d.items()}
+    pairs = bench.restore_pairs(d, KEYS)
+    assert len(pairs) == len(KEYS)
+    for k in KEYS:
+        d[k].zero_()
+    for dst, src in pairs:
+        dst.copy_(src)
+    for k in KEYS:
+        assert torch.equal(d[k], before[k])
+
+
+def test_traffic_sources_follow_the_head_shape():
+    gqa = {os.path.basename(p) for p in bench.attn_src(W.WORKLOADS["qwen3_8b"])}
+    mla = {os.path.basename(p) for p in bench.attn_src(W.WORKLOADS["mla"])}
+    assert "verify_attn_gqa.cu" in gqa and "verify_attn_mla.cu" not in gqa
+    assert "verify_attn_mla.cu" in mla and "verify_attn_gqa.cu" not in mla
+    assert {"verify_attn.cu", "attn.h", "ptx.cuh", "common.cuh"} <= gqa & mla
+    for p in bench.attn_src(W.WORKLOADS["mla"]) + bench.ACCEPT_SRC:
+        assert os.path.isfile(p), p
