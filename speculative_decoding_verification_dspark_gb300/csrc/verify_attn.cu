@@ -48,10 +48,6 @@ constexpr int kRows = 128;  // query rows of one work item (UMMA M / N side)
 // consecutive, so the count is the difference of two group indices) and a block scan
 // gives each CTA's first item; then a thread per group writes the group's pieces
 // straight to their places (piece of group g in CTA c: item base_c + g - first_c).
-__device__ __forceinline__ int cta_of_unit(long long x, long long U, int n) {
-  return static_cast<int>(((x + 1) * n - 1) / U);  // largest c with c*U/n <= x
-}
-
 template <class T>
 __device__ __forceinline__ T warp_incl_scan(T v, int lane) {
 #pragma unroll
@@ -104,6 +100,7 @@ __global__ void __launch_bounds__(1024)
   __shared__ int s_c0[DSPARK_MAX_B];
   __shared__ int s_base[1024];                   // first item of CTA c
   __shared__ int s_gfirst[1024];                 // first group CTA c meets
+  __shared__ long long s_lo[1025];               // first unit of CTA c: c*U/n
   __shared__ long long s_w64[32];
   __shared__ int s_w32[32];
   const int tid = threadIdx.x, lane = tid & 31;
@@ -157,18 +154,25 @@ __global__ void __launch_bounds__(1024)
     const long long cap = U / l_req;
     if (cap < n_eff) n_eff = cap > 0 ? static_cast<int>(cap) : 1;
   }
+  // The CTA boundaries, once: the CTA of a unit is then a search over them (the
+  // 64-bit divisions were the kernel's longest dependency chains).  U >= n_eff, so
+  // the boundaries strictly increase.
+  for (int cc = tid; cc <= n_eff; cc += blockDim.x) s_lo[cc] = (long long)cc * U / n_eff;
+  const bool small = U < (1ll << 31);  // unit offsets fit 32-bit division
   __syncthreads();
   // ---- per CTA: the groups its range meets
   const int c = tid;
   const bool active = c < ncta && c < n_eff && U > 0;
   int gfirst = 0, cnt = 0;
   if (active) {
-    const long long lo = (long long)c * U / n_eff;
-    const long long hi = (long long)(c + 1) * U / n_eff;
+    const long long lo = s_lo[c];
+    const long long hi = s_lo[c + 1];
     const int r0 = last_at_or_below(s_off, B, lo);
     const int r1 = last_at_or_below(s_off, B, hi - 1);
-    gfirst = s_goff[r0] + static_cast<int>((lo - s_off[r0]) / s_tt[r0]);
-    const int glast = s_goff[r1] + static_cast<int>((hi - 1 - s_off[r1]) / s_tt[r1]);
+    const long long d0 = lo - s_off[r0], d1 = hi - 1 - s_off[r1];
+    gfirst = s_goff[r0] + (small ? static_cast<int>(d0) / s_tt[r0] : static_cast<int>(d0 / s_tt[r0]));
+    const int glast =
+        s_goff[r1] + (small ? static_cast<int>(d1) / s_tt[r1] : static_cast<int>(d1 / s_tt[r1]));
     cnt = glast - gfirst + 1;
   }
   int total;
@@ -193,8 +197,8 @@ __global__ void __launch_bounds__(1024)
     const int t_r = s_tt[r];
     const long long gstart = s_off[r] + (long long)lg * t_r;
     const long long gend = gstart + t_r;
-    const int c_first = cta_of_unit(gstart, U, n_eff);
-    const int c_last = cta_of_unit(gend - 1, U, n_eff);
+    const int c_first = last_at_or_below(s_lo, n_eff, gstart);  // largest c: c*U/n <= x
+    const int c_last = last_at_or_below(s_lo, n_eff, gend - 1);
     const int t = lg / ng_per_tile, p = (lg / Hkv) % parts, h = lg % Hkv;
     const int i0 = t * rows_per_tile;
     const int ni = min(rows_per_tile, s_n[r] - i0);
@@ -203,10 +207,13 @@ __global__ void __launch_bounds__(1024)
     // rot = the time (in units) at which the group starts on its first CTA; every
     // group started this way reads tile (time mod t_r) at a given time, so the rows
     // of one request that run at the same time on different CTAs read the same tile
-    const int rot = rotate ? static_cast<int>((gstart - (long long)c_first * U / n_eff) % t_r) : 0;
+    const long long since = gstart - s_lo[c_first];
+    const int rot = !rotate ? 0
+                    : small ? static_cast<int>(since) % t_r
+                            : static_cast<int>(since % t_r);
     for (int cc = c_first; cc <= c_last; ++cc) {
-      const long long lo = (long long)cc * U / n_eff;
-      const long long hi = (long long)(cc + 1) * U / n_eff;
+      const long long lo = s_lo[cc];
+      const long long hi = s_lo[cc + 1];
       const long long u0 = gstart > lo ? gstart : lo;
       const long long u1 = gend < hi ? gend : hi;
       AttnItem it;
@@ -225,7 +232,7 @@ __global__ void __launch_bounds__(1024)
       SplitGroup sg;
       sg.r = r; sg.kvh = h; sg.part = p; sg.i0 = i0;
       sg.ni = ni; sg.c_first = c_first; sg.nsplit = nsplit;
-      sg.slot0_last = gstart != (long long)c_first * U / n_eff;
+      sg.slot0_last = gstart != s_lo[c_first];
       groups[c_last] = sg;
     }
   }
