@@ -177,6 +177,39 @@ int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, cons
                        void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * dspark_pack_plan + dspark_verify_attn_planned -- the same two steps with the
+ * attention's work list built inside the pack kernel (one kernel fewer between
+ * the schedule and the attention of a step).
+ *
+ * dspark_pack_plan takes dspark_pack's arguments (same meaning, same outputs)
+ * followed by the shape of the dspark_verify_attn_planned call that will use
+ * the plan: Hq, Hkv, d_qk, d_v, its max_rows (attn_max_rows), max_splits and
+ * max_block_rows, and that call's workspace (attn_workspace, at least
+ * dspark_verify_attn_workspace_size(B, attn_max_rows, ...) bytes, 256-B
+ * aligned).  It writes the work list for the cu_seqlens it computes and the
+ * given ctx_len into attn_workspace.
+ * dspark_verify_attn_planned has dspark_verify_attn's arguments and result, and
+ * uses that work list: the caller passes the same workspace, shape, B, ctx_len
+ * and cu_seqlens, on the same stream after the pack, with nothing writing the
+ * workspace in between.  Errors: as dspark_pack and dspark_verify_attn; an
+ * unsupported head shape gives DSPARK_EUNSUPPORTED from either call.
+ * ------------------------------------------------------------------------- */
+int dspark_pack_plan(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
+                     const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
+                     int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out,
+                     int32_t* tier_out, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
+                     int Hq, int Hkv, int d_qk, int d_v, int attn_max_rows, int max_splits,
+                     int max_block_rows, void* attn_workspace, size_t attn_ws_bytes,
+                     void* stream);
+int dspark_verify_attn_planned(const void* q, const void* k_new, const void* v_new,
+                               const void* k_cache, const void* v_cache, int n_pages,
+                               const int32_t* page_table, int max_pages, const int32_t* ctx_len,
+                               const int32_t* cu_seqlens, int B, int max_rows, int Hq, int Hkv,
+                               int d_qk, int d_v, int page_size, float scale, int max_splits,
+                               int max_block_rows, float* out, float* lse, void* workspace,
+                               size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * dspark_accept -- prefix speculative sampling ([notes] 02; [lesson]
  * "Background" and "Confidence scheduler 与 verify 模式"; c* label [notes] 07).
  *

@@ -44,6 +44,10 @@ _SIGNATURES = {
     "dspark_verify_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "dspark_verify_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                 _F, _I, _I, _P, _P, _P, _Z, _P]),
+    "dspark_verify_attn_planned": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                                        _I, _I, _F, _I, _I, _P, _P, _P, _Z, _P]),
+    "dspark_pack_plan": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                              _I, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "dspark_accept_workspace_size": (_Z, [_I, _I, _I, _I]),
     "dspark_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                            _P, _Z, _P]),
@@ -133,6 +137,20 @@ def pack(windows, ctx_len, anchor, draft_tok, tiers, mode, cu_seqlens, M_out, ti
         _ptr(row_req), _ptr(row_pos), _ptr(row_tok), _stream(stream)))
 
 
+def pack_plan(windows, ctx_len, anchor, draft_tok, tiers, mode, cu_seqlens, M_out, tier_out,
+              row_req, row_pos, row_tok, Hq, Hkv, d_qk, d_v, attn_max_rows, max_splits,
+              attn_workspace, stream=None, max_block_rows=0):
+    """pack, plus the work list of the verify_attn_planned call that follows (same shape
+    and workspace)."""
+    B, gamma = draft_tok.shape
+    _check("dspark_pack_plan", lib().dspark_pack_plan(
+        _ptr(windows), _ptr(ctx_len), _ptr(anchor), _ptr(draft_tok), _ptr(tiers), tiers.numel(), B,
+        gamma, int(mode), row_req.numel(), _ptr(cu_seqlens), _ptr(M_out), _ptr(tier_out),
+        _ptr(row_req), _ptr(row_pos), _ptr(row_tok), int(Hq), int(Hkv), int(d_qk), int(d_v),
+        int(attn_max_rows), int(max_splits), int(max_block_rows), _ptr(attn_workspace),
+        attn_workspace.numel() * attn_workspace.element_size(), _stream(stream)))
+
+
 def verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits,
                                max_block_rows=0) -> int:
     return lib().dspark_verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits,
@@ -143,12 +161,26 @@ def verify_attn(q, k_new, v_new, k_cache, v_cache, page_table, ctx_len, cu_seqle
                 max_splits, out, lse, workspace, stream=None, max_block_rows=0):
     """GQA: q [rows, Hq, 128], k/v_new [rows, Hkv, 128], caches [pages, P, Hkv, 128].
     MLA: q [rows, 128, 576], k_new [rows, 576], k_cache [pages, P, 576], v_* None."""
+    _verify_attn("dspark_verify_attn", q, k_new, v_new, k_cache, v_cache, page_table, ctx_len,
+                 cu_seqlens, scale, max_splits, out, lse, workspace, stream, max_block_rows)
+
+
+def verify_attn_planned(q, k_new, v_new, k_cache, v_cache, page_table, ctx_len, cu_seqlens,
+                        scale, max_splits, out, lse, workspace, stream=None, max_block_rows=0):
+    """verify_attn over the work list that pack_plan wrote into ``workspace``."""
+    _verify_attn("dspark_verify_attn_planned", q, k_new, v_new, k_cache, v_cache, page_table,
+                 ctx_len, cu_seqlens, scale, max_splits, out, lse, workspace, stream,
+                 max_block_rows)
+
+
+def _verify_attn(name, q, k_new, v_new, k_cache, v_cache, page_table, ctx_len, cu_seqlens, scale,
+                 max_splits, out, lse, workspace, stream, max_block_rows):
     max_rows, Hq, d_qk = q.shape
     mla = v_cache is None
     Hkv = 1 if mla else k_cache.shape[2]
     d_v = out.shape[2]
     B = ctx_len.numel()
-    _check("dspark_verify_attn", lib().dspark_verify_attn(
+    _check(name, getattr(lib(), name)(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
         _ptr(page_table), page_table.shape[1], _ptr(ctx_len), _ptr(cu_seqlens), B, max_rows, Hq,
         Hkv, d_qk, d_v, k_cache.shape[1], float(scale), int(max_splits), int(max_block_rows),
@@ -202,7 +234,8 @@ class VerifyStep:
     """Device buffers and workspaces for repeated verification steps of one shape.
 
     ``run`` enqueues the five calls of one step on the current stream:
-    schedule -> pack -> verify_attn -> accept -> compact.  The per-row inputs
+    schedule -> pack (with the attention work list: pack_plan) -> verify_attn (over that
+    work list: verify_attn_planned) -> accept -> compact.  The per-row inputs
     (q, k_new, v_new, p_target) are read from the packed buffers the caller
     fills; state (caches, page table, ctx_len, anchor, free stack) is updated in
     place by compact.
@@ -256,6 +289,19 @@ class VerifyStep:
                     self.max_splits, self.out, self.lse, self.ws_attn, stream,
                     max_block_rows=self.gamma + 1)
 
+    def pack_plan(self, inp, mode, stream=None):
+        """pack, with the attention work list built in the same kernel (for attention_planned)."""
+        pack_plan(self.windows, inp["ctx_len"], inp["anchor"], inp["draft_tok"], inp["tiers"], mode,
+                  self.cu_seqlens, self.M_pack, self.tier, self.row_req, self.row_pos,
+                  self.row_tok, self.Hq, self.Hkv, self.d_qk, self.d_v, self.max_rows,
+                  self.max_splits, self.ws_attn, stream, max_block_rows=self.gamma + 1)
+
+    def attention_planned(self, inp, stream=None):
+        verify_attn_planned(inp["q"], inp["k_new"], inp.get("v_new"), inp["k_cache"],
+                            inp.get("v_cache"), inp["page_table"], inp["ctx_len"],
+                            self.cu_seqlens, inp["scale"], self.max_splits, self.out, self.lse,
+                            self.ws_attn, stream, max_block_rows=self.gamma + 1)
+
     def accept(self, inp, mode, stream=None):
         accept(inp["p_target"], inp["p_draft"], inp["draft_tok"], inp["uniforms"],
                inp["exp_noise"], self.windows, self.cu_seqlens, mode, self.accept_len,
@@ -269,7 +315,7 @@ class VerifyStep:
 
     def run(self, inp, mode, stream=None):
         self.schedule(inp, mode, stream)
-        self.pack(inp, mode, stream)
-        self.attention(inp, stream)
+        self.pack_plan(inp, mode, stream)
+        self.attention_planned(inp, stream)
         self.accept(inp, mode, stream)
         self.compact(inp, stream)

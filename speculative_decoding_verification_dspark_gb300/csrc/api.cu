@@ -158,12 +158,13 @@ size_t dspark_verify_attn_workspace_size(int B, int max_rows, int Hq, int Hkv, i
   return attn::plan(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits, max_block_rows).bytes;
 }
 
-int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                       const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
-                       const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows,
-                       int Hq, int Hkv, int d_qk, int d_v, int page_size, float scale,
-                       int max_splits, int max_block_rows, float* out, float* lse, void* workspace,
-                       size_t ws_bytes, void* stream) {
+static int verify_attn_impl(const void* q, const void* k_new, const void* v_new,
+                            const void* k_cache, const void* v_cache, int n_pages,
+                            const int32_t* page_table, int max_pages, const int32_t* ctx_len,
+                            const int32_t* cu_seqlens, int B, int max_rows, int Hq, int Hkv,
+                            int d_qk, int d_v, int page_size, float scale, int max_splits,
+                            int max_block_rows, float* out, float* lse, void* workspace,
+                            size_t ws_bytes, void* stream, bool planned) {
   CHECK(attn_shape_ok(Hq, Hkv, d_qk, d_v, page_size), DSPARK_EUNSUPPORTED);
   const bool mla = d_qk == 576;
   CHECK(q && k_new && k_cache && page_table && ctx_len && cu_seqlens && out && lse && workspace,
@@ -183,7 +184,58 @@ int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, cons
   CHECK(ws_bytes >= pl.bytes, DSPARK_ENOSPACE);
   return attn::launch(q, k_new, v_new, k_cache, v_cache, n_pages, page_table, max_pages, ctx_len,
                       cu_seqlens, B, max_rows, Hq, Hkv, d_qk, d_v, page_size, scale, max_splits,
-                      out, lse, workspace, pl, static_cast<cudaStream_t>(stream));
+                      out, lse, workspace, pl, static_cast<cudaStream_t>(stream), planned);
+}
+
+int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                       const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
+                       const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows,
+                       int Hq, int Hkv, int d_qk, int d_v, int page_size, float scale,
+                       int max_splits, int max_block_rows, float* out, float* lse, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  return verify_attn_impl(q, k_new, v_new, k_cache, v_cache, n_pages, page_table, max_pages,
+                          ctx_len, cu_seqlens, B, max_rows, Hq, Hkv, d_qk, d_v, page_size, scale,
+                          max_splits, max_block_rows, out, lse, workspace, ws_bytes, stream, false);
+}
+
+int dspark_verify_attn_planned(const void* q, const void* k_new, const void* v_new,
+                               const void* k_cache, const void* v_cache, int n_pages,
+                               const int32_t* page_table, int max_pages, const int32_t* ctx_len,
+                               const int32_t* cu_seqlens, int B, int max_rows, int Hq, int Hkv,
+                               int d_qk, int d_v, int page_size, float scale, int max_splits,
+                               int max_block_rows, float* out, float* lse, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  return verify_attn_impl(q, k_new, v_new, k_cache, v_cache, n_pages, page_table, max_pages,
+                          ctx_len, cu_seqlens, B, max_rows, Hq, Hkv, d_qk, d_v, page_size, scale,
+                          max_splits, max_block_rows, out, lse, workspace, ws_bytes, stream, true);
+}
+
+int dspark_pack_plan(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
+                     const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
+                     int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out,
+                     int32_t* tier_out, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
+                     int Hq, int Hkv, int d_qk, int d_v, int attn_max_rows, int max_splits,
+                     int max_block_rows, void* attn_workspace, size_t attn_ws_bytes,
+                     void* stream) {
+  CHECK(windows && ctx_len && anchor && draft_tok && cu_seqlens && M_out && tier_out && row_req &&
+            row_pos && row_tok && attn_workspace,
+        DSPARK_EINVAL);
+  CHECK(n_tiers >= 0 && n_tiers <= DSPARK_MAX_TIERS && (n_tiers == 0 || tiers), DSPARK_EINVAL);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
+  CHECK(mode >= DSPARK_COMPACT && mode <= DSPARK_CAP_ACCEPT, DSPARK_EINVAL);
+  CHECK(max_rows >= 1 && attn_max_rows >= 1, DSPARK_EINVAL);
+  CHECK(attn_shape_ok(Hq, Hkv, d_qk, d_v, 16), DSPARK_EUNSUPPORTED);  // the plan has no page size
+  CHECK(max_splits >= 1 && max_splits <= 32, DSPARK_EINVAL);
+  CHECK((reinterpret_cast<uintptr_t>(attn_workspace) & 255u) == 0, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  const attn::Plan pl =
+      attn::plan(B, attn_max_rows, Hq, Hkv, d_qk, d_v, max_splits, max_block_rows);
+  CHECK(attn_ws_bytes >= pl.bytes, DSPARK_ENOSPACE);
+  return launch_pack_plan(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode,
+                          max_rows, cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok,
+                          attn_max_rows, Hkv, max_splits, pl, attn_workspace,
+                          static_cast<cudaStream_t>(stream));
 }
 
 size_t dspark_accept_workspace_size(int B, int gamma, int max_rows, int V) {

@@ -47,7 +47,7 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
            const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,
            const int32_t* ctx_len, const int32_t* cu_seqlens, int B, int max_rows, int Hq, int Hkv,
            int d_qk, int d_v, int page_size, float scale, int max_splits, float* out, float* lse,
-           void* ws, const Plan& pl, cudaStream_t stream);
+           void* ws, const Plan& pl, cudaStream_t stream, bool planned = false);
 
 namespace gqa {
 // Query-row tile (32, 64 or 128) for G = Hq/Hkv heads per KV head and at most

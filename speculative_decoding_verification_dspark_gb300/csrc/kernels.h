@@ -17,6 +17,18 @@ int launch_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* a
                 int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out, int32_t* tier_out,
                 int32_t* row_req, int32_t* row_pos, int32_t* row_tok, cudaStream_t stream);
 
+namespace attn {
+struct Plan;
+}
+// launch_pack and, in the same kernel, the attention work list of plan `pl` into the
+// attention workspace `attn_ws` (the rest of the attention call then skips it).
+int launch_pack_plan(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
+                     const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
+                     int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out,
+                     int32_t* tier_out, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
+                     int attn_max_rows, int Hkv, int max_splits, const attn::Plan& pl,
+                     void* attn_ws, cudaStream_t stream);
+
 size_t accept_workspace(int B, int max_rows, int V);
 int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_t* draft_tok,
                   const float* uniforms, const float* exp_noise, const int32_t* windows,

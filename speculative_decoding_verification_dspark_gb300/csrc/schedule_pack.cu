@@ -22,8 +22,10 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "attn.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "worklist.cuh"
 
 namespace dspark {
 
@@ -260,16 +262,16 @@ __global__ void __launch_bounds__(kSchedThreads)
   if (tid == 0) *M_out = B + kstar;
 }
 
-__global__ void __launch_bounds__(1024)
-    pack_kernel(const int32_t* __restrict__ windows, const int32_t* __restrict__ ctx_len,
-                const int32_t* __restrict__ anchor, const int32_t* __restrict__ draft_tok,
-                const int32_t* __restrict__ tiers, int n_tiers, int B, int gamma, int mode,
-                int max_rows, int32_t* __restrict__ cu_seqlens, int32_t* __restrict__ M_out,
-                int32_t* __restrict__ tier_out, int32_t* __restrict__ row_req,
-                int32_t* __restrict__ row_pos, int32_t* __restrict__ row_tok,
-                unsigned int* __restrict__ err) {
-  pdl_release();
-  pdl_wait();  // inputs come from the kernels before this one
+// The pack of one step, by every thread of a 1024-thread CTA.
+__device__ inline void pack_body(const int32_t* __restrict__ windows,
+                                 const int32_t* __restrict__ ctx_len,
+                                 const int32_t* __restrict__ anchor,
+                                 const int32_t* __restrict__ draft_tok,
+                                 const int32_t* __restrict__ tiers, int n_tiers, int B, int gamma,
+                                 int mode, int max_rows, int32_t* __restrict__ cu_seqlens,
+                                 int32_t* __restrict__ M_out, int32_t* __restrict__ tier_out,
+                                 int32_t* __restrict__ row_req, int32_t* __restrict__ row_pos,
+                                 int32_t* __restrict__ row_tok, unsigned int* __restrict__ err) {
   __shared__ int s_cu[DSPARK_MAX_B + 1];
   __shared__ int s_warp[32];
   __shared__ int s_tier;
@@ -328,6 +330,50 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+__global__ void __launch_bounds__(1024)
+    pack_kernel(const int32_t* __restrict__ windows, const int32_t* __restrict__ ctx_len,
+                const int32_t* __restrict__ anchor, const int32_t* __restrict__ draft_tok,
+                const int32_t* __restrict__ tiers, int n_tiers, int B, int gamma, int mode,
+                int max_rows, int32_t* __restrict__ cu_seqlens, int32_t* __restrict__ M_out,
+                int32_t* __restrict__ tier_out, int32_t* __restrict__ row_req,
+                int32_t* __restrict__ row_pos, int32_t* __restrict__ row_tok,
+                unsigned int* __restrict__ err) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
+  pack_body(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode, max_rows,
+            cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok, err);
+}
+
+// Pack, then the attention work list of the same step from the cu_seqlens just
+// written (this CTA's own global writes, visible to it after the barrier): one kernel
+// fewer between the step's schedule and its attention.
+struct PackPlanArgs {
+  int attn_max_rows, Hkv, parts, rows_per_tile, nk, ncta, max_splits, rotate, max_items;
+  attn::AttnItem* items;
+  int* item_begin;
+  attn::SplitGroup* groups;
+};
+
+__global__ void __launch_bounds__(1024)
+    pack_plan_kernel(const int32_t* __restrict__ windows, const int32_t* __restrict__ ctx_len,
+                     const int32_t* __restrict__ anchor, const int32_t* __restrict__ draft_tok,
+                     const int32_t* __restrict__ tiers, int n_tiers, int B, int gamma, int mode,
+                     int max_rows, int32_t* __restrict__ cu_seqlens, int32_t* __restrict__ M_out,
+                     int32_t* __restrict__ tier_out, int32_t* __restrict__ row_req,
+                     int32_t* __restrict__ row_pos, int32_t* __restrict__ row_tok,
+                     const PackPlanArgs a, unsigned int* __restrict__ err) {
+  pdl_release();
+  pdl_wait();  // inputs come from the kernels before this one
+  pack_body(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode, max_rows,
+            cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok, err);
+  __syncthreads();  // cu_seqlens (global, written above by this CTA) is complete
+  extern __shared__ __align__(16) uint8_t pack_plan_smem[];
+  attn::WorkListSmem& S = *reinterpret_cast<attn::WorkListSmem*>(pack_plan_smem);
+  attn::build_work_list(S, ctx_len, cu_seqlens, B, a.attn_max_rows, a.Hkv, a.parts,
+                        a.rows_per_tile, a.nk, a.ncta, a.max_splits, a.rotate, a.max_items, a.items,
+                        a.item_begin, a.groups, err);
+}
+
 int launch_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
                     const float* cost_table, int B, int gamma, int max_tokens, int mode,
                     int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
@@ -341,6 +387,41 @@ int launch_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
   const int threads = npow < 32 ? 32 : (npow > kSchedThreads ? kSchedThreads : npow);
   if (launch_pdl(greedy_kernel, dim3(1), dim3(threads), 0, stream, a_hat, cost_table, B, gamma,
                  max_tokens, mode, windows, M_out, E_out) != cudaSuccess)
+    return DSPARK_ECUDA;
+  return DSPARK_OK;
+}
+
+int launch_pack_plan(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
+                     const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
+                     int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out,
+                     int32_t* tier_out, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
+                     int attn_max_rows, int Hkv, int max_splits, const attn::Plan& pl,
+                     void* attn_ws, cudaStream_t stream) {
+  static bool configured = false;
+  const int smem = static_cast<int>(sizeof(attn::WorkListSmem));
+  if (!configured) {
+    if (cudaFuncSetAttribute(pack_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return DSPARK_ECUDA;
+    configured = true;
+  }
+  uint8_t* w = static_cast<uint8_t*>(attn_ws);
+  PackPlanArgs a;
+  a.attn_max_rows = attn_max_rows;
+  a.Hkv = Hkv;
+  a.parts = pl.parts;
+  a.rows_per_tile = pl.rows_per_tile;
+  a.nk = pl.nk;
+  a.ncta = pl.ncta;
+  a.max_splits = max_splits < 2 ? 2 : (max_splits > 32 ? 32 : max_splits);
+  a.rotate = pl.mla ? 1 : 0;  // as the attention call's own work list
+  a.max_items = pl.max_items > 0x7fffffff ? 0x7fffffff : static_cast<int>(pl.max_items);
+  a.items = reinterpret_cast<attn::AttnItem*>(w + pl.off_items);
+  a.item_begin = reinterpret_cast<int*>(w + pl.off_begin);
+  a.groups = reinterpret_cast<attn::SplitGroup*>(w + pl.off_groups);
+  if (launch_pdl(pack_plan_kernel, dim3(1), dim3(1024), smem, stream, windows, ctx_len, anchor,
+                 draft_tok, tiers, n_tiers, B, gamma, mode, max_rows, cu_seqlens, M_out, tier_out,
+                 row_req, row_pos, row_tok, a, device_error_word()) != cudaSuccess)
     return DSPARK_ECUDA;
   return DSPARK_OK;
 }

@@ -411,3 +411,38 @@ def test_rows_overflow_is_reported():
     for k, v in before.items():
         if isinstance(v, torch.Tensor):
             assert torch.equal(d[k], v), k
+    # the same through the fused pack + work list and the planned attention
+    step.pack_plan(d, O.STATIC)
+    assert dspark.read_device_error() & 0x1
+    step.attention_planned(d)
+    assert dspark.read_device_error() & 0x1
+    for k, v in before.items():
+        if isinstance(v, torch.Tensor):
+            assert torch.equal(d[k], v), k
+
+
+@pytest.mark.parametrize("shape", ["gqa", "mla"])
+def test_planned_attention_equals_standalone(shape):
+    """The work list built inside the pack kernel is the attention call's own: the planned
+    attention gives the standalone call's outputs bit for bit."""
+    if shape == "gqa":
+        wl = W.WORKLOADS["tiny"]
+        inp = W.make_inputs(wl, 4)
+    else:
+        wl = W.Workload(
+            name="mla_plan", B=5, gamma=6, attn="mla", Hq=128, Hkv=1, d_qk=576, d_v=512,
+            page_size=16, ctx=("uniform", 100, 2000), conf=("logit", 1.2, 1.0), vocab=1024,
+            p_dtype="f32", target_logit_std=3.0, draft_noise_std=0.7, tiers=(8, 16, 32, 64))
+        inp = W.make_inputs(wl, 7)
+    d, step = harness.prepare(inp, O.COMPACT)
+    M = int(step.cu_seqlens[-1])
+    step.attention(d)
+    torch.cuda.synchronize()
+    out0, lse0 = step.out[:M].clone(), step.lse[:M].clone()
+    step.out.zero_()
+    step.lse.zero_()
+    step.pack_plan(d, O.COMPACT)
+    step.attention_planned(d)
+    torch.cuda.synchronize()
+    assert torch.equal(step.out[:M], out0)
+    assert torch.equal(step.lse[:M], lse0)
