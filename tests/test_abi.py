@@ -52,6 +52,17 @@ def test_host_validation_without_device(lib):
                                   16, ctypes.c_float(0.1), 4, 9, nul, nul, nul, 0, nul) == -2
     # vocabulary not a multiple of 8
     fake = ctypes.c_void_p(4096)
+    # pack + work list: NULL pointers; then valid pointers with an unsupported attention
+    # shape (head dim 96); the planned attention validates as the standalone call
+    assert lib.dspark_pack_plan(nul, nul, nul, nul, nul, 0, 4, 6, 0, 8, nul, nul, nul, nul, nul,
+                                nul, 8, 2, 128, 128, 8, 4, 7, nul, 0, nul) == -1
+    assert lib.dspark_pack_plan(fake, fake, fake, fake, nul, 0, 4, 6, 0, 8, fake, fake, fake, fake,
+                                fake, fake, 8, 2, 96, 96, 8, 4, 7, fake, 1 << 20, nul) == -2
+    assert lib.dspark_pack_plan(fake, fake, fake, fake, nul, 0, 4, 6, 0, 8, fake, fake, fake, fake,
+                                fake, fake, 8, 2, 128, 128, 8, 33, 7, fake, 1 << 20, nul) == -1
+    assert lib.dspark_verify_attn_planned(nul, nul, nul, nul, nul, 1, nul, 1, nul, nul, 1, 8, 8, 2,
+                                          96, 96, 16, ctypes.c_float(0.1), 4, 9, nul, nul, nul, 0,
+                                          nul) == -2
     assert lib.dspark_accept(fake, fake, 0, 1001, fake, fake, fake, fake, fake, 0, 4, 6, 8, fake,
                              fake, fake, fake, nul, fake, 1 << 20, nul) == -2
     # the fixed-scratch variant: a problem larger than its scratch is refused (ENOSPACE)
