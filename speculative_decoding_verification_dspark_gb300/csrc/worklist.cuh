@@ -80,8 +80,10 @@ struct WorkListSmem {
 };
 
 // Called by every thread of a 1024-thread CTA, after the inputs are visible to it.
+// cu_seqlens is not __restrict__: in the pack kernel this CTA has just written it, so
+// its loads must not take the read-only (non-coherent) path.
 __device__ inline void build_work_list(WorkListSmem& S, const int32_t* __restrict__ ctx_len,
-                                       const int32_t* __restrict__ cu_seqlens, int B, int max_rows,
+                                       const int32_t* cu_seqlens, int B, int max_rows,
                                        int Hkv, int parts, int rows_per_tile, int NK, int ncta,
                                        int max_splits, int rotate, int max_items,
                                        AttnItem* __restrict__ items, int* __restrict__ item_begin,
