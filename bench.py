@@ -43,7 +43,7 @@ KERNELS_PER_STEP = 10   # schedule 2, pack + work list 1, attention 2, accept 3,
 PROFILES = os.path.join(ROOT, "profiles")
 _CSRC = os.path.join(ROOT, "speculative_decoding_verification_dspark_gb300", "csrc")
 # sources whose change invalidates a committed DRAM-traffic figure
-_ATTN_COMMON = ("verify_attn.cu", "attn.h", "ptx.cuh", "common.cuh")
+_ATTN_COMMON = ("verify_attn.cu", "worklist.cuh", "attn.h", "ptx.cuh", "common.cuh")
 
 
 def attn_src(wl):

@@ -66,6 +66,6 @@ def test_traffic_sources_follow_the_head_shape():
     mla = {os.path.basename(p) for p in bench.attn_src(W.WORKLOADS["mla"])}
     assert "verify_attn_gqa.cu" in gqa and "verify_attn_mla.cu" not in gqa
     assert "verify_attn_mla.cu" in mla and "verify_attn_gqa.cu" not in mla
-    assert {"verify_attn.cu", "attn.h", "ptx.cuh", "common.cuh"} <= gqa & mla
+    assert {"verify_attn.cu", "worklist.cuh", "attn.h", "ptx.cuh", "common.cuh"} <= gqa & mla
     for p in bench.attn_src(W.WORKLOADS["mla"]) + bench.ACCEPT_SRC:
         assert os.path.isfile(p), p
