@@ -446,3 +446,41 @@ def test_planned_attention_equals_standalone(shape):
     torch.cuda.synchronize()
     assert torch.equal(step.out[:M], out0)
     assert torch.equal(step.lse[:M], lse0)
+
+
+@pytest.mark.parametrize("windows", [[3, 2, 1], [3, 2, 2], [6, 6, 6], [0]])
+def test_pack_tier_edges_on_gpu(windows):
+    """M equal to a tier, one row past it, above every tier, and a single anchor-only
+    request: the pack call and the pack + work list call both give the oracle's rows."""
+    import speculative_decoding_verification_dspark_gb300 as dspark
+    gamma, B, max_rows = 6, len(windows), 32
+    tiers = [4, 9, 16]
+    dev = torch.device("cuda")
+    i32 = dict(dtype=torch.int32, device=dev)
+    w = torch.tensor(windows, **i32)
+    ctx = torch.tensor([0, 16, 100][:B], **i32)
+    anchor = torch.tensor([5, 6, 7][:B], **i32)
+    drafts = torch.arange(B * gamma, **i32).reshape(B, gamma)
+    tiers_d = torch.tensor(tiers, **i32)
+    pk = O.pack(np.array(windows, np.int32), ctx.cpu().numpy(), anchor.cpu().numpy(),
+                drafts.cpu().numpy(), tiers, O.COMPACT, gamma)
+    ws = torch.empty(dspark.verify_attn_workspace_size(B, max_rows, 8, 2, 128, 128, 8, gamma + 1),
+                     dtype=torch.uint8, device=dev)
+    dspark.read_device_error()
+    for fused in (False, True):
+        cu, M, tier = torch.zeros(B + 1, **i32), torch.zeros(1, **i32), torch.zeros(1, **i32)
+        rr, rp, rt = (torch.full((max_rows,), 99, **i32) for _ in range(3))
+        if fused:
+            dspark.pack_plan(w, ctx, anchor, drafts, tiers_d, O.COMPACT, cu, M, tier, rr, rp, rt,
+                             8, 2, 128, 128, max_rows, 8, ws, max_block_rows=gamma + 1)
+        else:
+            dspark.pack(w, ctx, anchor, drafts, tiers_d, O.COMPACT, cu, M, tier, rr, rp, rt)
+        torch.cuda.synchronize()
+        assert cu.cpu().numpy().tolist() == pk.cu_seqlens.tolist()
+        assert int(M) == pk.M and int(tier) == pk.tier
+        T = pk.tier
+        assert rr.cpu().numpy()[:T].tolist() == pk.row_req.tolist()
+        assert rp.cpu().numpy()[:T].tolist() == pk.row_pos.tolist()
+        assert rt.cpu().numpy()[:T].tolist() == pk.row_tok.tolist()
+        assert rr.cpu().numpy()[T:].tolist() == [99] * (max_rows - T)  # rows past the tier untouched
+        assert dspark.read_device_error() == 0

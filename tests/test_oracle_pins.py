@@ -192,6 +192,25 @@ def test_pack_invariants(mode):
     assert np.all(pk.row_req[pk.M:] == -1)
 
 
+def test_pack_tier_edges():
+    """M equal to a tier takes that tier (no padding); one more row takes the next; M
+    above every tier runs unpadded; a single request with w = 0 packs its anchor alone."""
+    gamma = 6
+    anchor, ctx = np.array([5, 6, 7]), np.array([0, 16, 100])
+    drafts = np.arange(3 * gamma).reshape(3, gamma)
+    tiers = [4, 9, 16]
+    exact = O.pack(np.array([3, 2, 1], np.int32), ctx, anchor, drafts, tiers, O.COMPACT, gamma)
+    assert exact.M == 9 and exact.tier == 9 and np.all(exact.row_req >= 0)
+    plus1 = O.pack(np.array([3, 2, 2], np.int32), ctx, anchor, drafts, tiers, O.COMPACT, gamma)
+    assert plus1.M == 10 and plus1.tier == 16 and plus1.row_req[10:].tolist() == [-1] * 6
+    over = O.pack(np.array([6, 6, 6], np.int32), ctx, anchor, drafts, tiers, O.COMPACT, gamma)
+    assert over.M == 21 and over.tier == 21
+    one = O.pack(np.array([0], np.int32), ctx[:1], anchor[:1], drafts[:1], tiers, O.COMPACT,
+                 gamma)
+    assert one.cu_seqlens.tolist() == [0, 1] and one.M == 1 and one.tier == 4
+    assert one.row_tok.tolist() == [5, -1, -1, -1] and one.row_pos[0] == 0
+
+
 # ---------------------------------------------------------------- attention
 
 def _toy_gqa(rng, B=2, Hq=4, Hkv=2, D=8, P=4, ctx=(5, 0), n=(3, 2)):
