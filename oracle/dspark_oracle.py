@@ -24,8 +24,8 @@ Sources, cited by short name below:
             "09 · End-to-End Cycle".
 
 Parity status per function (what pins it is listed in tests/test_oracle_pins.py):
-pinned: survival/STS, greedy schedule, pack, verify attention (GQA and MLA),
-acceptance, compaction.  The composed ``step`` adds no arithmetic of its own and
+pinned: confidence sigmoid, survival/STS, greedy schedule, pack, verify
+attention (GQA and MLA), acceptance (test, race, fallback, c*), compaction.  The composed ``step`` adds no arithmetic of its own and
 is pinned only through its parts (no page prints end-to-end values).
 """
 from __future__ import annotations
@@ -48,7 +48,10 @@ def confidence(conf: np.ndarray, is_logit: bool) -> np.ndarray:
     """c_k from the confidence head: a linear layer followed by a sigmoid
     ([notes] §07; [lesson] "DSpark：sequential head 加验证预算").
 
-    The sigmoid is evaluated in fp64 and rounded once to fp32.
+    The sigmoid is evaluated in fp64 and rounded once to fp32, so c is the
+    fp32 number nearest to sigma(z) up to one fp64 rounding (reading A21: the
+    pages fix no arithmetic for the scheduler; this one lets two independent
+    implementations agree to within one fp32 ulp).
     """
     x = np.asarray(conf, dtype=np.float32)
     if not is_logit:
@@ -140,11 +143,16 @@ def schedule(conf, conf_is_logit, sts_temp, cost_table, max_tokens, mode) -> Sch
     candidate that does not raise it, or when M + 1 would exceed the largest
     captured tier.  T is the profiled step-cost table indexed by M.
 
-    E and the comparison are fp64 (E summed in sorted order; the two ratios
-    compared cross-multiplied, T > 0).  Every decision whose relative margin
-    |lhs - rhs| / rhs is below 1e-5, and a near-tie
-    between the stopping candidate and the last accepted one of another
-    request, is recorded in ``listed``.
+    Arithmetic (reading A21): E is kept in fp64 and the two ratios are compared
+    cross-multiplied in fp64 (T > 0).  Here E is summed in sorted order; any other
+    order gives the same decisions outside the listing margin, because an fp64
+    sum of n <= 4096 terms in [0, 1] is within n * 2^-53 * E of exact (below
+    1e-12 relative), whereas an fp32 running sum could be off by n * 2^-24
+    (2.4e-4 at n = 4096), more than the margin.  Every decision whose relative
+    margin |lhs - rhs| / rhs is below 1e-5 is recorded in ``listed``; so are the
+    requests of all candidates within 1e-5 (relative) of the stopping
+    candidate's survival when they belong to two or more requests, since a
+    rounding of a_hat could reorder them across the stop.
 
     static mode verifies the whole block: w_r = gamma.
     """
@@ -188,11 +196,15 @@ def schedule(conf, conf_is_logit, sts_temp, cost_table, max_tokens, mode) -> Sch
     else:
         k = len(cands)
     n_acc = int(windows.sum())
-    if stop in ("decline", "budget") and n_acc > 0:
-        v_stop, r_s, j_s = cands[n_acc]
-        v_last, r_l, j_l = cands[n_acc - 1]
-        if r_s != r_l and v_last > 0 and (v_last - v_stop) <= MARGIN_LIST_REL * v_last:
-            listed.append(("tie", r_s, j_s, (v_last - v_stop) / v_last))
+    if stop in ("decline", "budget") and n_acc < len(cands):
+        # candidates whose survival is within the margin of the stopping one: a
+        # one-ulp difference in a_hat could put any of them on either side
+        v_stop = cands[n_acc][0]
+        band = [(k2, v2, r2, j2) for k2, (v2, r2, j2) in enumerate(cands)
+                if abs(v2 - v_stop) <= MARGIN_LIST_REL * v_stop]
+        if len({r2 for (_, _, r2, _) in band}) > 1 and v_stop > 0:
+            for (k2, v2, r2, j2) in band:
+                listed.append(("tie", r2, j2, abs(v2 - v_stop) / v_stop))
     return Schedule(windows, ah, M, E, cands, n_acc, stop, listed)
 
 
@@ -355,12 +367,24 @@ class Accept:
 def _race_argmax(weights_f32: np.ndarray, exp_noise_f32: np.ndarray) -> tuple:
     """Gumbel-max in its exponential-race form: argmax_v w_v / e_v, e_v ~ Exp(1).
 
-    argmax log w_v + G_v with G_v = -log e_v is the same index.  Keys are fp32
-    quotients; the lowest index wins ties.  Returns (index, best key).
+    argmax log w_v + G_v with G_v = -log e_v is the same index (reading A11 of
+    the Gumbel-max draw in [lesson] "Background" and [notes] §02).  Keys are fp32
+    quotients; the lowest index wins ties.  An entry whose weight is not positive
+    (zero, or NaN) has log w = -inf and never wins, whatever its noise; a key that
+    is NaN never wins either.  If no weight is positive the draw is undefined and
+    the lowest index (0) is returned.  Returns (index, best key, any positive
+    weight).
     """
-    keys = (weights_f32 / exp_noise_f32).astype(np.float32)
+    w = np.asarray(weights_f32, dtype=np.float32)
+    e = np.asarray(exp_noise_f32, dtype=np.float32)
+    live = w > 0
+    if not np.any(live):
+        return 0, float("-inf"), False
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        q = (w / e).astype(np.float32)
+    keys = np.where(live & ~np.isnan(q), q, np.float32(-np.inf))
     idx = int(np.argmax(keys))
-    return idx, float(keys[idx])
+    return idx, float(keys[idx]), True
 
 
 def accept(p_target, p_draft, draft_tok, uniforms, exp_noise, windows, cu_seqlens, mode, gamma) -> Accept:
@@ -380,8 +404,9 @@ def accept(p_target, p_draft, draft_tok, uniforms, exp_noise, windows, cu_seqlen
       the residual max(0, p_t - p_d) at that position; when the whole window is
       accepted, a bonus drawn from p_t at position w_r + 1 (the bonus is the
       same token in every mode).  Draws are the exponential race against the
-      per-request Exp(1) noise row.  An all-zero residual (reachable only
-      through rounding) falls back to p_t at that position.
+      per-request Exp(1) noise row; entries of zero weight never win.  A
+      residual with no positive entry (reachable only through rounding) falls
+      back to p_t at that position.
     * c*_j = 1 - 1/2 ||p_d,j - p_t,j||_1 ([notes] §07 training label) for every
       position j <= gamma that has a target row: j <= w_r + 1 in compact mode,
       j <= gamma otherwise.  fp64 sum, rounded to fp32.
@@ -413,13 +438,13 @@ def accept(p_target, p_draft, draft_tok, uniforms, exp_noise, windows, cu_seqlen
             row_t = np.asarray(p_target[base + commit], dtype=np.float32)
             row_d = np.asarray(p_draft[r, commit], dtype=np.float32)
             resid = np.maximum(F32(0), (row_t - row_d).astype(np.float32))
-            tok, best = _race_argmax(resid, noise)
-            if not best > 0.0:
+            tok, _, any_pos = _race_argmax(resid, noise)
+            if not any_pos:  # no positive residual entry (reading A12)
                 fb[r] = True
-                tok, _ = _race_argmax(row_t, noise)
+                tok, _, _ = _race_argmax(row_t, noise)
         else:
             row_t = np.asarray(p_target[base + w], dtype=np.float32)
-            tok, _ = _race_argmax(row_t, noise)
+            tok, _, _ = _race_argmax(row_t, noise)
         n_rows = int(cu_seqlens[r + 1]) - base
         for j in range(1, min(n_rows, gamma) + 1):
             d = np.asarray(p_draft[r, j - 1], dtype=np.float64)

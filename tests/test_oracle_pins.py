@@ -505,3 +505,104 @@ def test_compact_no_space_raises():
         O.compact(kn, kn, np.array([0, 2]), np.array([1]), np.array([0]), np.zeros((1, 3), np.int32),
                   2, np.array([[0, -1]]), np.array([2]), np.array([0]), np.array([], np.int32), 0,
                   np.zeros((2, 2, 1, 1)), np.zeros((2, 2, 1, 1)))
+
+
+# ---------------------------------------------------------------- confidence sigmoid
+
+def _ulps(a, b):
+    a = np.asarray(a, np.float32).view(np.int32).astype(np.int64)
+    b = np.asarray(b, np.float32).view(np.int32).astype(np.int64)
+    return np.abs(a - b)
+
+
+def test_confidence_sigmoid_hand_values():
+    """sigma(0) = 1/2, sigma(ln 3) = 3/4, sigma(-ln 3) = 1/4: the fp32 rounding of
+    ln 3 moves sigma by about 4e-9, under half an ulp of 3/4 and of 1/4, so all
+    three are exact; a sign flip or a dropped term gives 1/4 for 3/4."""
+    z = np.array([[0.0, math.log(3.0), -math.log(3.0)]], np.float32)
+    c = O.confidence(z, True)
+    assert c[0].tolist() == [0.5, 0.75, 0.25]
+    # is_logit = 0 passes the confidence through unchanged
+    x = np.array([[0.3, 0.9]], np.float32)
+    assert np.array_equal(O.confidence(x, False), x)
+
+
+def test_confidence_sigmoid_matches_scipy_expit():
+    from scipy.special import expit
+    z = np.linspace(-30, 30, 2001, dtype=np.float32)[None, :]
+    c = O.confidence(z, True)
+    ref = expit(z.astype(np.float64)).astype(np.float32)
+    assert np.all(_ulps(c, ref) <= 1)
+    assert np.all(np.diff(c[0]) >= 0) and c[0, 0] < 1e-12 and c[0, -1] == 1.0
+
+
+# ---------------------------------------------------------------- race rule (reading A11)
+
+def test_race_zero_weight_never_wins_even_with_zero_noise():
+    """w / e with w = 0 and e = 0 is NaN; the entry must still lose to any positive
+    weight (log 0 = -inf in the Gumbel form)."""
+    w = np.array([0.0, 0.25, 0.0, 0.1], np.float32)
+    e = np.array([0.0, 1.0, 0.0, 5.0], np.float32)
+    idx, key, live = O._race_argmax(w, e)
+    assert (idx, live) == (1, True) and key == 0.25
+    # a NaN noise entry on a positive weight is not a winner either
+    e2 = np.array([1.0, np.nan, 1.0, 5.0], np.float32)
+    assert O._race_argmax(w, e2)[0] == 3
+
+
+def test_race_all_zero_weights_give_index_zero_and_no_live_entry():
+    idx, key, live = O._race_argmax(np.zeros(5, np.float32), np.ones(5, np.float32))
+    assert (idx, live) == (0, False) and key == float("-inf")
+
+
+def test_race_infinite_keys_tie_to_lowest_index():
+    """e = 0 on positive weights gives +inf keys: the lowest such index wins."""
+    w = np.array([0.5, 0.0, 0.2, 0.3], np.float32)
+    e = np.array([1.0, 0.0, 0.0, 0.0], np.float32)
+    assert O._race_argmax(w, e)[0] == 2
+
+
+def test_race_positive_weight_with_underflowing_key_beats_zero_weights():
+    """A positive weight whose quotient rounds to 0 is still a live entry: it wins
+    against zero weights (which are -inf), lowest index among equal keys."""
+    w = np.array([0.0, 1e-44, 0.0], np.float32)
+    e = np.array([1.0, 1e30, 1.0], np.float32)
+    idx, key, live = O._race_argmax(w, e)
+    assert (idx, key, live) == (1, 0.0, True)
+
+
+def test_correction_fallback_only_without_any_positive_residual():
+    """Reading A12: the p_t fallback is taken iff max(0, p_t - p_d) has no positive
+    entry; a residual whose only positive entry gives a zero key is still raced."""
+    V, gamma = 4, 1
+    pt = np.array([[0.25, 0.25, 0.25, 0.25], [0.25, 0.25, 0.25, 0.25]], np.float32)
+    d = np.array([[0]], np.int32)
+    u = np.array([[0.99]], np.float32)
+    e = np.array([[1.0, 1.0, 1e30, 1.0]], np.float32)
+    cu = np.array([0, 2])
+    # rejected draft, residual zero everywhere -> fallback to p_t
+    pd0 = np.array([[[0.5, 0.25, 0.25, 0.25]]], np.float32)
+    a = O.accept(pt, pd0, d, u, e, np.array([1], np.int32), cu, O.COMPACT, gamma)
+    assert a.accept_len[0] == 0 and a.residual_fallback[0] and a.out_tok[0] == 0
+    # one tiny positive residual entry at index 2 whose key underflows to 0 -> no fallback
+    pd1 = pd0.copy()
+    pd1[0, 0, 2] = np.nextafter(np.float32(0.25), np.float32(0))
+    a1 = O.accept(pt, pd1, d, u, e, np.array([1], np.int32), cu, O.COMPACT, gamma)
+    assert not a1.residual_fallback[0] and a1.out_tok[0] == 2
+
+
+# ---------------------------------------------------------------- input generator
+
+def test_generator_uniforms_are_exact_and_open():
+    """The seeded uniforms are odd multiples of 2^-24 (exact fp32, never 0 or 1) and
+    the exponential noise -log u is finite and strictly positive."""
+    import torch
+    import workloads as W
+    wl = W.WORKLOADS["tiny"].replace(B=64, vocab=4096)
+    inp = W.make_inputs(wl, 9)
+    for u in (inp["uniforms"],):
+        k = u.to(torch.float64) * 2.0 ** 24
+        assert torch.all(k == torch.round(k)) and torch.all(torch.remainder(k, 2) == 1)
+        assert float(u.min()) > 0.0 and float(u.max()) < 1.0
+    e = inp["exp_noise"]
+    assert torch.all(torch.isfinite(e)) and float(e.min()) > 0.0

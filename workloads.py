@@ -121,9 +121,14 @@ def _gen(seed: int, name: str, device) -> torch.Generator:
 
 
 def _uniform_open01_f32(shape, g, device) -> torch.Tensor:
-    """U = (k + 1/2) 2^-24 with k uniform on [0, 2^24): exact fp32, strictly inside (0, 1)."""
-    k = torch.randint(0, 1 << 24, shape, generator=g, device=device, dtype=torch.int64)
-    return ((k.to(torch.float64) + 0.5) * 2.0 ** -24).to(torch.float32)
+    """U = (2k + 1) 2^-24 with k uniform on [0, 2^23): the 2^23 odd multiples of 2^-24.
+
+    An odd integer below 2^24 has at most 24 significant bits, so every value is an
+    exact fp32 number, the smallest 2^-24 and the largest 1 - 2^-24: never 0, never 1
+    (so -log U is finite and strictly positive).
+    """
+    k = torch.randint(0, 1 << 23, shape, generator=g, device=device, dtype=torch.int64)
+    return ((2 * k + 1).to(torch.float64) * 2.0 ** -24).to(torch.float32)
 
 
 def _ctx_lengths(wl: Workload, g, device) -> torch.Tensor:
@@ -268,13 +273,6 @@ def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
     u2 = _uniform_open01_f32((B, V), _gen(seed, "exp_noise", dev), dev)
     out["exp_noise"] = (-torch.log(u2.to(torch.float64))).to(torch.float32)
     return out
-
-
-def rows_per_request(windows: torch.Tensor, mode: int, gamma: int) -> torch.Tensor:
-    """Verify rows each request occupies: anchor + verified drafts."""
-    if mode == MODE_CAP_ACCEPT:
-        return torch.full_like(windows, gamma + 1)
-    return windows + 1
 
 
 def to_packed(dense: torch.Tensor, cu_seqlens: torch.Tensor, total_rows: int) -> torch.Tensor:
