@@ -32,6 +32,11 @@
  *     the offending writes.  dspark_read_device_error() returns and clears it.
  *   - The library must have been built for sm_103a; on any other device the
  *     first call returns DSPARK_EUNSUPPORTED.
+ *   - Per-device set-up (kernel attributes, the address of the error word and of
+ *     fixed scratch) is done once per device on the first call made with that
+ *     device current, and is safe when several host threads make that first call
+ *     at once.  It is kept for the life of the process: the library is not usable
+ *     after a cudaDeviceReset in the same process.
  */
 #ifndef DSPARK_H
 #define DSPARK_H
@@ -122,6 +127,13 @@ int dspark_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
  *   cu_seqlens  int32 [B+1] out: exclusive prefix sum of n_r
  *   M_out       int32 [1]   out: cu_seqlens[B]
  *   tier_out    int32 [1]   out: smallest entry of `tiers` >= M, or M if none is
+ *   tier_host   int32 [1]   out, nullable, HOST: pinned memory mapped into the
+ *               device (cudaHostAlloc with cudaHostAllocMapped, or registered
+ *               with cudaHostRegisterMapped); the kernel also stores the tier
+ *               there, so a host-side engine can read it once the pack kernel
+ *               has finished (an event after this call) without synchronising
+ *               the stream, and pick the target forward captured for that tier
+ *               ([lesson] "Ragged verify under full CUDA graphs").
  *   row_req     int32 [max_rows] out: request of each packed row, -1 on padding
  *   row_pos     int32 [max_rows] out: absolute position ctx_len[r] + i, -1 on padding
  *                                     (its page is page_table[r][pos / page_size])
@@ -133,7 +145,8 @@ int dspark_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
 int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
                 const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
                 int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out, int32_t* tier_out,
-                int32_t* row_req, int32_t* row_pos, int32_t* row_tok, void* stream);
+                int32_t* tier_host, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
+                void* stream);
 
 /* ---------------------------------------------------------------------------
  * dspark_verify_attn -- variable-length verify attention over the paged cache
@@ -197,8 +210,9 @@ int dspark_verify_attn(const void* q, const void* k_new, const void* v_new, cons
 int dspark_pack_plan(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
                      const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
                      int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out,
-                     int32_t* tier_out, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
-                     int Hq, int Hkv, int d_qk, int d_v, int attn_max_rows, int max_splits,
+                     int32_t* tier_out, int32_t* tier_host, int32_t* row_req, int32_t* row_pos,
+                     int32_t* row_tok, int Hq, int Hkv, int d_qk, int d_v, int attn_max_rows,
+                     int max_splits,
                      int max_block_rows, void* attn_workspace, size_t attn_ws_bytes,
                      void* stream);
 int dspark_verify_attn_planned(const void* q, const void* k_new, const void* v_new,
@@ -261,7 +275,10 @@ int dspark_accept(const void* p_target, const void* p_draft, int pdt, int V,
  * is written earlier in the same call.
  * The first call on a device looks up the scratch address with that device
  * current (DSPARK_ECUDA if the lookup fails); make that first call before any
- * stream capture begins.  All calls on one device share the one array, so two
+ * stream capture begins.  The address is kept for the life of the process: after
+ * a cudaDeviceReset it would be stale, so this call (like the rest of the
+ * library, whose per-device set-up is cached the same way) must not be used
+ * after a device reset in the same process.  All calls on one device share the one array, so two
  * calls that may run at the same time (on different streams, or from host threads
  * without ordering between them) race on it and give undefined results: order
  * them on one stream.
@@ -306,6 +323,113 @@ int dspark_compact(const void* k_new, const void* v_new, int row_bytes, int max_
                    const int32_t* free_pages, int32_t* free_top, void* k_cache, void* v_cache,
                    int32_t* committed, int32_t* n_committed, void* workspace, size_t ws_bytes,
                    void* stream);
+
+/* ---------------------------------------------------------------------------
+ * dspark_step_graph -- the whole verification step as one CUDA graph, with the
+ * captured tier chosen on the device ([lesson] "Ragged verify under full CUDA
+ * graphs": the packed batch is rounded up to a captured tier and that tier's
+ * graph runs; [lesson] "Zero-overhead scheduling 与 kernel": the step runs from
+ * device-resident state with no host synchronisation).
+ *
+ * The graph runs dspark_schedule, dspark_pack_plan and then a switch node with
+ * one body per captured tier: body i holds dspark_verify_attn_planned,
+ * dspark_accept and dspark_compact with their row counts (max_rows) set to
+ * tiers[i], and body n_tiers the same with max_rows for a batch above every tier.
+ * The pack kernel selects the body from the M it computes, so consecutive
+ * launches may run different tiers without the host reading anything; a batch
+ * larger than max_rows sets DSPARK_DEVERR_ROWS_OVERFLOW and runs no body.
+ *
+ * Every pointer in the descriptor is a device pointer that stays valid (and keeps
+ * its meaning) for the life of the graph: a launch reads the buffers' current
+ * contents, so the caller refills the input buffers between launches (on the
+ * launch stream) and the state (page_table, ctx_len, anchor, free_top, caches)
+ * carries over from one step to the next.  Field meanings, layouts and sizes are
+ * those of the five calls; workspaces as their *_workspace_size functions give for
+ * (B, gamma, max_rows, ...).  Optional:
+ *   tier_host  nullable HOST pinned, mapped int32 word: receives each step's tier
+ *   body_log   nullable device int32 [1 + log_len]: body_log[0] counts launches
+ *              (the caller zeroes it) and body_log[1 + k] receives the body index
+ *              run by launch k < log_len (observability of the device's choice)
+ * dspark_step_graph_create captures and instantiates the graph on the current
+ * device (it launches nothing, and allocates only the graph); it returns
+ * DSPARK_EINVAL / DSPARK_EUNSUPPORTED for descriptors the five calls would refuse
+ * and DSPARK_ECUDA if graph construction fails.  dspark_step_graph_launch enqueues
+ * one step on `stream`; a graph must not run on two streams at once.  The graph
+ * cannot be captured into another graph (it holds a conditional node).
+ * ------------------------------------------------------------------------- */
+typedef struct dspark_step_desc {
+  /* shapes */
+  int B, gamma, mode;
+  int Hq, Hkv, d_qk, d_v, page_size, max_pages, n_pages;
+  int V, pdt;
+  int max_rows;               /* rows of q, k_new, v_new, p_target, out, lse, row_* */
+  int n_tiers;                /* <= DSPARK_MAX_TIERS, ascending, each <= max_rows */
+  const int32_t* tiers_host;  /* HOST [n_tiers] */
+  const int32_t* tiers;       /* device copy of the same tiers */
+  int conf_is_logit, cost_len, max_tokens, max_splits, max_block_rows;
+  float scale;
+  /* inputs */
+  const float* conf;
+  const float* sts_temp;
+  const float* cost_table;
+  const int32_t* draft_tok;
+  const void* q;
+  const void* k_new;
+  const void* v_new;          /* NULL for the latent-KV shape */
+  const void* p_target;
+  const void* p_draft;
+  const float* uniforms;
+  const float* exp_noise;
+  const int32_t* free_pages;
+  /* state, updated in place by every step */
+  int32_t* page_table;
+  int32_t* ctx_len;
+  int32_t* anchor;
+  int32_t* free_top;
+  void* k_cache;
+  void* v_cache;              /* NULL for the latent-KV shape */
+  /* outputs */
+  int32_t* windows;
+  float* a_hat;
+  int32_t* M;
+  double* E;
+  int32_t* cu_seqlens;
+  int32_t* M_pack;
+  int32_t* tier;
+  int32_t* row_req;
+  int32_t* row_pos;
+  int32_t* row_tok;
+  float* out;
+  float* lse;
+  int32_t* accept_len;
+  int32_t* cap_len;
+  int32_t* out_tok;
+  float* cstar;
+  int32_t* fallback;
+  int32_t* committed;
+  int32_t* n_committed;
+  int32_t* tier_host;
+  int32_t* body_log;
+  int log_len;
+  /* workspaces */
+  void* ws_attn;
+  size_t ws_attn_bytes;
+  void* ws_accept;
+  size_t ws_accept_bytes;
+  void* ws_compact;
+  size_t ws_compact_bytes;
+} dspark_step_desc;
+
+typedef struct dspark_step_graph dspark_step_graph;
+int dspark_step_graph_create(const dspark_step_desc* desc, dspark_step_graph** graph_out);
+int dspark_step_graph_launch(dspark_step_graph* graph, void* stream);
+/* How the graph was captured: DSPARK_STEP_GRAPH_PDL if its kernels keep their
+ * programmatic dependencies (each may start while the one before it finishes);
+ * otherwise they are plainly stream-ordered. */
+#define DSPARK_STEP_GRAPH_PDL 1
+int dspark_step_graph_flags(const dspark_step_graph* graph);
+/* Frees the graph (NULL is ignored); the caller makes sure no launch is running. */
+int dspark_step_graph_destroy(dspark_step_graph* graph);
 
 #ifdef __cplusplus
 }

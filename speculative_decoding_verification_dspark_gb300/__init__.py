@@ -17,7 +17,7 @@ __all__ = [
     "COMPACT", "STATIC", "CAP_ACCEPT", "F32", "BF16", "DSparkError", "lib", "load",
     "schedule", "pack", "verify_attn", "accept", "accept_noalloc", "compact", "read_device_error",
     "verify_attn_workspace_size", "accept_workspace_size", "compact_workspace_size",
-    "VerifyStep", "DEVERR",
+    "VerifyStep", "StepGraph", "DEVERR",
 ]
 
 COMPACT, STATIC, CAP_ACCEPT = 0, 1, 2
@@ -40,13 +40,13 @@ _SIGNATURES = {
     "dspark_read_device_error": (_I, [_P]),
     "dspark_num_sms": (_I, []),
     "dspark_schedule": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
-    "dspark_pack": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "dspark_pack": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dspark_verify_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "dspark_verify_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                 _F, _I, _I, _P, _P, _P, _Z, _P]),
     "dspark_verify_attn_planned": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                                         _I, _I, _F, _I, _I, _P, _P, _P, _Z, _P]),
-    "dspark_pack_plan": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+    "dspark_pack_plan": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                               _I, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "dspark_accept_workspace_size": (_Z, [_I, _I, _I, _I]),
     "dspark_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
@@ -54,6 +54,10 @@ _SIGNATURES = {
     "dspark_accept_noalloc": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P,
                                    _P, _P, _P]),
     "dspark_compact_workspace_size": (_Z, [_I]),
+    "dspark_step_graph_create": (_I, [_P, _P]),
+    "dspark_step_graph_launch": (_I, [_P, _P]),
+    "dspark_step_graph_destroy": (_I, [_P]),
+    "dspark_step_graph_flags": (_I, [_P]),
     "dspark_compact": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                             _P, _P, _P, _P, _Z, _P]),
 }
@@ -128,25 +132,36 @@ def schedule(conf, conf_is_logit, sts_temp, cost_table, max_tokens, mode, window
         _stream(stream)))
 
 
+def _host_ptr(t):
+    """A pinned host tensor's address (for the mapped tier word), or None."""
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("expected a pinned host tensor")
+    return t.data_ptr()
+
+
 def pack(windows, ctx_len, anchor, draft_tok, tiers, mode, cu_seqlens, M_out, tier_out, row_req,
-         row_pos, row_tok, stream=None):
+         row_pos, row_tok, stream=None, tier_host=None):
+    """``tier_host``: optional pinned host int32 tensor that also receives the tier."""
     B, gamma = draft_tok.shape
     _check("dspark_pack", lib().dspark_pack(
         _ptr(windows), _ptr(ctx_len), _ptr(anchor), _ptr(draft_tok), _ptr(tiers), tiers.numel(), B,
         gamma, int(mode), row_req.numel(), _ptr(cu_seqlens), _ptr(M_out), _ptr(tier_out),
-        _ptr(row_req), _ptr(row_pos), _ptr(row_tok), _stream(stream)))
+        _host_ptr(tier_host), _ptr(row_req), _ptr(row_pos), _ptr(row_tok), _stream(stream)))
 
 
 def pack_plan(windows, ctx_len, anchor, draft_tok, tiers, mode, cu_seqlens, M_out, tier_out,
               row_req, row_pos, row_tok, Hq, Hkv, d_qk, d_v, attn_max_rows, max_splits,
-              attn_workspace, stream=None, max_block_rows=0):
+              attn_workspace, stream=None, max_block_rows=0, tier_host=None):
     """pack, plus the work list of the verify_attn_planned call that follows (same shape
     and workspace)."""
     B, gamma = draft_tok.shape
     _check("dspark_pack_plan", lib().dspark_pack_plan(
         _ptr(windows), _ptr(ctx_len), _ptr(anchor), _ptr(draft_tok), _ptr(tiers), tiers.numel(), B,
         gamma, int(mode), row_req.numel(), _ptr(cu_seqlens), _ptr(M_out), _ptr(tier_out),
-        _ptr(row_req), _ptr(row_pos), _ptr(row_tok), int(Hq), int(Hkv), int(d_qk), int(d_v),
+        _host_ptr(tier_host), _ptr(row_req), _ptr(row_pos), _ptr(row_tok), int(Hq), int(Hkv),
+        int(d_qk), int(d_v),
         int(attn_max_rows), int(max_splits), int(max_block_rows), _ptr(attn_workspace),
         attn_workspace.numel() * attn_workspace.element_size(), _stream(stream)))
 
@@ -228,6 +243,60 @@ def compact(k_new, v_new, cu_seqlens, accept_len, out_tok, draft_tok, page_table
         _ptr(page_table), _ptr(ctx_len), _ptr(anchor), _ptr(free_pages), _ptr(free_top),
         _ptr(k_cache), _ptr(v_cache), _ptr(committed), _ptr(n_committed), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+class StepDesc(ctypes.Structure):
+    """dspark_step_desc (field for field)."""
+    _fields_ = (
+        [(n, _I) for n in ("B", "gamma", "mode", "Hq", "Hkv", "d_qk", "d_v", "page_size",
+                           "max_pages", "n_pages", "V", "pdt", "max_rows", "n_tiers")]
+        + [("tiers_host", _P), ("tiers", _P)]
+        + [(n, _I) for n in ("conf_is_logit", "cost_len", "max_tokens", "max_splits",
+                             "max_block_rows")]
+        + [("scale", _F)]
+        + [(n, _P) for n in ("conf", "sts_temp", "cost_table", "draft_tok", "q", "k_new", "v_new",
+                             "p_target", "p_draft", "uniforms", "exp_noise", "free_pages",
+                             "page_table", "ctx_len", "anchor", "free_top", "k_cache", "v_cache",
+                             "windows", "a_hat", "M", "E", "cu_seqlens", "M_pack", "tier",
+                             "row_req", "row_pos", "row_tok", "out", "lse", "accept_len",
+                             "cap_len", "out_tok", "cstar", "fallback", "committed",
+                             "n_committed", "tier_host", "body_log")]
+        + [("log_len", _I), ("ws_attn", _P), ("ws_attn_bytes", _Z), ("ws_accept", _P),
+           ("ws_accept_bytes", _Z), ("ws_compact", _P), ("ws_compact_bytes", _Z)]
+    )
+
+
+class StepGraph:
+    """The whole verification step as one library-built CUDA graph whose captured tier
+    is chosen on the device (dspark_step_graph_*): each ``launch`` runs one step from
+    the current contents of the buffers it was built on."""
+
+    def __init__(self, desc: StepDesc, keep):
+        self._keep = keep            # tensors the descriptor points into
+        self._desc = desc
+        h = ctypes.c_void_p()
+        _check("dspark_step_graph_create",
+               lib().dspark_step_graph_create(ctypes.byref(desc), ctypes.byref(h)))
+        self._h = h
+
+    def launch(self, stream=None):
+        _check("dspark_step_graph_launch", lib().dspark_step_graph_launch(self._h, _stream(stream)))
+
+    @property
+    def pdl(self) -> bool:
+        """True if the graph's kernels keep their programmatic dependencies."""
+        return bool(lib().dspark_step_graph_flags(self._h) & 1)
+
+    def close(self):
+        if self._h:
+            lib().dspark_step_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class VerifyStep:
@@ -312,6 +381,43 @@ class VerifyStep:
                 inp["draft_tok"], inp["page_table"], inp["ctx_len"], inp["anchor"],
                 inp["free_pages"], inp["free_top"], inp["k_cache"], inp.get("v_cache"),
                 self.committed, self.n_committed, self.ws_compact, stream)
+
+    def graph(self, inp, mode, tier_host=None, body_log=None) -> StepGraph:
+        """The step on these buffers and ``inp``'s tensors as a StepGraph (tier chosen
+        on the device).  ``tier_host``: optional pinned host int32 word receiving each
+        step's tier; ``body_log``: optional device int32 [1 + n] recording the body
+        index each launch ran (element 0 counts launches; the caller zeroes it)."""
+        pdt = inp["p_target"].dtype
+        tiers = inp["tiers"]
+        tiers_dev = tiers.to(self.windows.device, torch.int32)
+        tiers_host = tiers.cpu().to(torch.int32).contiguous()
+        d = StepDesc()
+        d.B, d.gamma, d.mode = self.B, self.gamma, int(mode)
+        d.Hq, d.Hkv, d.d_qk, d.d_v = self.Hq, self.Hkv, self.d_qk, self.d_v
+        d.page_size, d.max_pages = inp["k_cache"].shape[1], inp["page_table"].shape[1]
+        d.n_pages, d.V = inp["k_cache"].shape[0], self.vocab
+        d.pdt = BF16 if pdt == torch.bfloat16 else F32
+        d.max_rows, d.n_tiers = self.max_rows, tiers_host.numel()
+        d.tiers_host, d.tiers = tiers_host.data_ptr(), _ptr(tiers_dev)
+        d.conf_is_logit, d.cost_len = int(inp["conf_is_logit"]), inp["cost_table"].numel()
+        d.max_tokens, d.max_splits, d.max_block_rows = int(inp["max_tokens"]), self.max_splits, self.gamma + 1
+        d.scale = float(inp["scale"])
+        for k in ("conf", "sts_temp", "cost_table", "draft_tok", "q", "k_new", "p_target", "p_draft",
+                  "uniforms", "exp_noise", "free_pages", "page_table", "ctx_len", "anchor",
+                  "free_top", "k_cache"):
+            setattr(d, k, _ptr(inp[k]))
+        d.v_new, d.v_cache = _ptr(inp.get("v_new")), _ptr(inp.get("v_cache"))
+        for k in ("windows", "a_hat", "M", "E", "cu_seqlens", "M_pack", "tier", "row_req",
+                  "row_pos", "row_tok", "out", "lse", "accept_len", "cap_len", "out_tok", "cstar",
+                  "fallback", "committed", "n_committed"):
+            setattr(d, k, _ptr(getattr(self, k)))
+        d.tier_host = _host_ptr(tier_host)
+        d.body_log = _ptr(body_log)
+        d.log_len = 0 if body_log is None else body_log.numel() - 1
+        d.ws_attn, d.ws_attn_bytes = _ptr(self.ws_attn), self.ws_attn.numel()
+        d.ws_accept, d.ws_accept_bytes = _ptr(self.ws_accept), self.ws_accept.numel()
+        d.ws_compact, d.ws_compact_bytes = _ptr(self.ws_compact), self.ws_compact.numel()
+        return StepGraph(d, (tiers_dev, tiers_host, inp, tier_host, body_log))
 
     def run(self, inp, mode, stream=None):
         self.schedule(inp, mode, stream)

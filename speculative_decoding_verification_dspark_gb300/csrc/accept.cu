@@ -19,15 +19,16 @@
 //                        for both the residual max(0, p_t - p_d) and p_t itself.
 //   accept_final_kernel  one block per request: fixed-order fp64 sums of the chunk
 //                        partials (c*, a warp per row) and the argmax over the
-//                        chunk partials (token), with the p_t race behind an
-//                        all-zero residual.
+//                        chunk partials (token), with the p_t race behind a
+//                        residual that has no positive entry.
+//
+// Race rule (the Gumbel-max draw as an exponential race): key w_v / e_v in fp32,
+// lowest index on ties; an entry with w_v = 0 has log w_v = -inf and never wins.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
-
-#include <atomic>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -60,6 +61,13 @@ __device__ __forceinline__ float ld_p(const float* p, long long i) { return __ld
 __device__ __forceinline__ float ld_p(const __nv_bfloat16* p, long long i) {
   return __bfloat162float(p[i]);
 }
+
+// Race key of an entry whose weight is not positive: -inf, below every live key.
+// Bests start at kDead with index kNoIndex, and entries are taken on a strict
+// comparison, so a dead entry is never taken and a row with no positive weight
+// ends with index kNoIndex (reading A11: such an entry never wins).
+constexpr float kDead = -__builtin_huge_valf();
+constexpr int kNoIndex = 0x7fffffff;
 
 __device__ __forceinline__ void better(float& k, int& i, float k2, int i2) {
   if (k2 > k || (k2 == k && i2 < i)) {
@@ -362,8 +370,8 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
       if (lane == 0) {
         Partial pp;
         pp.l1 = 0.0;
-        pp.key_res = -1.f; pp.idx_res = 0x7fffffff;
-        pp.key_t = -1.f; pp.idx_t = 0x7fffffff;
+        pp.key_res = kDead; pp.idx_res = kNoIndex;
+        pp.key_t = kDead; pp.idx_t = kNoIndex;
         for (int q = 0; q < kConsumerWarps; ++q) {
           const WarpPart& wp = S.red[p][q];
           pp.l1 += wp.l1;
@@ -381,8 +389,8 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
     // gives their items
     int g = 0, gn = 0, n_it = 0;
     bool ok = true;
-    float l1 = 0.f, kbest = -1.f, thr = -1.f;
-    int ibest = 0x7fffffff;
+    float l1 = 0.f, kbest = kDead, thr = -1.f;
+    int ibest = kNoIndex;
     while (ok) {
       const int s = g % kVStages;
       ok = vwait(ptx::smem_addr(&S.full[s]), (g / kVStages) & 1, abort_flag, err);
@@ -413,8 +421,8 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
       const int ch = m.x % n_chunks;
       if (sb == 0) {
         l1 = 0.f;
-        kbest = -1.f;
-        ibest = 0x7fffffff;
+        kbest = kDead;
+        ibest = kNoIndex;
         thr = -1.f;
       }
       {
@@ -429,7 +437,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
           const bool valid = e < len;
           float a[8], d[8], en[8], ka[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) { a[q] = 0.f; d[q] = 0.f; en[q] = 1.f; ka[q] = -1.f; }
+          for (int q = 0; q < 8; ++q) { a[q] = 0.f; d[q] = 0.f; en[q] = 1.f; ka[q] = kDead; }
           if (valid) {
             smem_vec8<T>(st + e * ES, a);
             if (w.need_d) smem_vec8<T>(st + kSub * 4 + e * ES, d);
@@ -446,8 +454,9 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
               for (int q = 0; q < 8; ++q) {
                 if (w.residual) a[q] = fmaxf(__fsub_rn(a[q], d[q]), 0.f);
                 const float inv = approx_rcp(en[q]);
-                // e beyond the reciprocal's range: force the exact path
-                ka[q] = inv == 0.f ? kHuge : a[q] * inv;
+                // a weight that is not positive never wins (log 0 = -inf in the
+                // Gumbel form); e beyond the reciprocal's range forces the exact path
+                ka[q] = !(a[q] > 0.f) ? kDead : (inv == 0.f ? kHuge : a[q] * inv);
               }
             }
           }
@@ -459,8 +468,8 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
             for (int q = 1; q < 8; ++q) mt = fmaxf(mt, ka[q]);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-            // (a zero maximum leaves the filter: zero keys still reach the exact
-            // path, so an all-zero range still yields its lowest index)
+            // (a zero maximum leaves the filter: live entries whose key rounds to 0
+            // still reach the exact path; dead entries never pass it)
             if (mt < kHuge && mt > 0.f) thr = fmaxf(thr, mt * kFilter);
             // A lane visits its entries in increasing index order and keeps the first
             // strict maximum of its rounded keys fl(w / e); an entry at or below the
@@ -488,8 +497,8 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
       ++g;
       if (sb != ns - 1) continue;
       // item done: warp results to the reducer
-      float kr = -1.f, kt = -1.f;
-      int ir = 0x7fffffff, it_ = 0x7fffffff;
+      float kr = kDead, kt = kDead;
+      int ir = kNoIndex, it_ = kNoIndex;
       if (w.residual) { kr = kbest; ir = ibest; } else { kt = kbest; it_ = ibest; }
       double l1d = static_cast<double>(l1);
 #pragma unroll
@@ -553,8 +562,8 @@ __global__ void __launch_bounds__(256)
   // token: the sampled row's race maximum over the chunk partials (max, then lowest
   // index: order-independent)
   const long long prow = (long long)(base + ri.sample_row) * n_chunks;
-  float k = -1.f;
-  int idx = 0x7fffffff;
+  float k = kDead;
+  int idx = kNoIndex;
   for (int ch = lane; ch < n_chunks; ch += 32) {
     const Partial p = part[prow + ch];
     if (ri.residual) better(k, idx, p.key_res, p.idx_res);
@@ -564,16 +573,16 @@ __global__ void __launch_bounds__(256)
   for (int o = 16; o > 0; o >>= 1)
     better(k, idx, __shfl_xor_sync(0xffffffffu, k, o), __shfl_xor_sync(0xffffffffu, idx, o));
   int fb = 0;
-  if (ri.residual && !(k > 0.f)) {
-    // An all-zero residual (reachable only through rounding): the token is drawn
-    // from p_t on the same row with the same noise; the vocabulary pass raced only
-    // the residual there, so this warp races p_t.
+  if (ri.residual && idx == kNoIndex) {
+    // A residual with no positive entry (reachable only through rounding): the
+    // token is drawn from p_t on the same row with the same noise; the vocabulary
+    // pass raced only the residual there, so this warp races p_t.
     fb = 1;
-    k = -1.f;
-    idx = 0x7fffffff;
+    k = kDead;
     const long long trow = (long long)(base + ri.sample_row) * V;
     for (int v = lane; v < V; v += 32) {
-      const float kq = __fdiv_rn(ld_p(p_t, trow + v), exp_noise[(long long)r * V + v]);
+      const float p = ld_p(p_t, trow + v);
+      const float kq = p > 0.f ? __fdiv_rn(p, exp_noise[(long long)r * V + v]) : kDead;
       if (kq > k) { k = kq; idx = v; }
     }
 #pragma unroll
@@ -581,23 +590,21 @@ __global__ void __launch_bounds__(256)
       better(k, idx, __shfl_xor_sync(0xffffffffu, k, o), __shfl_xor_sync(0xffffffffu, idx, o));
   }
   if (lane == 0) {
-    out_tok[r] = idx;
+    // no positive weight on the raced row at all: the lowest index (undefined draw)
+    out_tok[r] = idx == kNoIndex ? 0 : idx;
     if (fallback) fallback[r] = fb;
   }
 }
 
 bool vocab_configure() {
-  static int state = 0;  // 0: not yet, 1: ok, -1: failed
-  if (state == 0) {
+  static PerDevice<bool> done;
+  return once_per_device(done, false, [] {
     const int bytes = static_cast<int>(sizeof(VocabSmem));
-    const bool ok =
-        cudaFuncSetAttribute(accept_vocab_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes) == cudaSuccess &&
-        cudaFuncSetAttribute(accept_vocab_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
-    state = ok ? 1 : -1;
-  }
-  return state == 1;
+    return cudaFuncSetAttribute(accept_vocab_kernel<float>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+           cudaFuncSetAttribute(accept_vocab_kernel<__nv_bfloat16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+  });
 }
 
 // workspace: RowInfo[B] | claim counter | int2 row_desc[max_rows] | Partial[max_rows][n_chunks]
@@ -613,16 +620,11 @@ size_t accept_workspace(int B, int max_rows, int V) {
 static __device__ __align__(256) unsigned char g_accept_scratch[DSPARK_ACCEPT_NOALLOC_SCRATCH_BYTES];
 
 void* accept_fixed_scratch() {
-  constexpr int kMaxDevices = 64;
-  static std::atomic<void*> addr[kMaxDevices];
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  void* p = addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess) return nullptr;
-    addr[dev].store(p, std::memory_order_release);
-  }
-  return p;
+  static PerDevice<void*> addr;
+  return once_per_device(addr, static_cast<void*>(nullptr), [] {
+    void* p = nullptr;
+    return cudaGetSymbolAddress(&p, g_accept_scratch) == cudaSuccess ? p : nullptr;
+  });
 }
 
 int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_t* draft_tok,

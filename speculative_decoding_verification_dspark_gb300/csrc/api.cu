@@ -15,32 +15,36 @@ __device__ unsigned int g_device_error;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 struct DeviceState {
-  bool init = false;
+  bool ok = false;  // the state below was read
   bool supported = false;
   int sms = 0;
   unsigned int* err = nullptr;
 };
-DeviceState g_dev[kMaxDevices];
 
+// The current device's state, read once per device (thread-safe); nullptr when
+// the current device cannot be read.
 DeviceState* state() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  DeviceState& s = g_dev[dev];
-  if (!s.init) {
-    int major = 0, minor = 0;
+  static PerDevice<DeviceState> st;
+  static DeviceState none;
+  DeviceState s = once_per_device(st, none, [] {
+    DeviceState d;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return d;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     void* p = nullptr;
     const bool sym = cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess;
-    s.err = static_cast<unsigned int*>(p);
-    s.supported = sym && major == 10 && minor == 3 && s.sms > 0;
-    s.init = true;
-  }
-  return &s;
+    d.err = static_cast<unsigned int*>(p);
+    d.supported = sym && major == 10 && minor == 3 && d.sms > 0;
+    d.ok = true;
+    return d;
+  });
+  if (!s.ok) return nullptr;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return &st.value[dev];
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -71,6 +75,52 @@ static int device_ok() {
   if (!s) return DSPARK_ECUDA;
   return s->supported ? DSPARK_OK : DSPARK_EUNSUPPORTED;
 }
+
+static bool attn_shape_ok(int Hq, int Hkv, int d_qk, int d_v, int page_size) {
+  if (page_size < 16 || (page_size & (page_size - 1)) != 0) return false;  // power of two
+  if (d_qk == 128 && d_v == 128) {
+    if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || Hq / Hkv > 128) return false;
+    if (page_size < 16 || page_size % 16 != 0) return false;
+    return page_size <= 64 ? (64 % page_size == 0) : (page_size % 64 == 0);
+  }
+  if (d_qk == 576 && d_v == 512) {
+    if (Hkv != 1 || Hq != 128) return false;
+    if (page_size < 16 || page_size % 16 != 0) return false;
+    return page_size <= 32 ? (32 % page_size == 0) : (page_size % 32 == 0);
+  }
+  return false;
+}
+
+namespace dspark {
+
+int pack_plan_checked(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
+                      const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
+                      int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out,
+                      int32_t* tier_out, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
+                      int Hq, int Hkv, int d_qk, int d_v, int attn_max_rows, int max_splits,
+                      int max_block_rows, void* attn_workspace, size_t attn_ws_bytes,
+                      const TierSel& ts, cudaStream_t stream) {
+  CHECK(windows && ctx_len && anchor && draft_tok && cu_seqlens && M_out && tier_out && row_req &&
+            row_pos && row_tok && attn_workspace,
+        DSPARK_EINVAL);
+  CHECK(n_tiers >= 0 && n_tiers <= DSPARK_MAX_TIERS && (n_tiers == 0 || tiers), DSPARK_EINVAL);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
+  CHECK(mode >= DSPARK_COMPACT && mode <= DSPARK_CAP_ACCEPT, DSPARK_EINVAL);
+  CHECK(max_rows >= 1 && attn_max_rows >= 1, DSPARK_EINVAL);
+  CHECK(attn_shape_ok(Hq, Hkv, d_qk, d_v, 16), DSPARK_EUNSUPPORTED);  // the plan has no page size
+  CHECK(max_splits >= 1 && max_splits <= 32, DSPARK_EINVAL);
+  CHECK((reinterpret_cast<uintptr_t>(attn_workspace) & 255u) == 0, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  const attn::Plan pl =
+      attn::plan(B, attn_max_rows, Hq, Hkv, d_qk, d_v, max_splits, max_block_rows);
+  CHECK(attn_ws_bytes >= pl.bytes, DSPARK_ENOSPACE);
+  return launch_pack_plan(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode,
+                          max_rows, cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok,
+                          attn_max_rows, Hkv, max_splits, pl, attn_workspace, ts, stream);
+}
+
+}  // namespace dspark
 
 extern "C" {
 
@@ -121,7 +171,8 @@ int dspark_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
 int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
                 const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
                 int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out, int32_t* tier_out,
-                int32_t* row_req, int32_t* row_pos, int32_t* row_tok, void* stream) {
+                int32_t* tier_host, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
+                void* stream) {
   CHECK(windows && ctx_len && anchor && draft_tok && cu_seqlens && M_out && tier_out && row_req &&
             row_pos && row_tok,
         DSPARK_EINVAL);
@@ -131,25 +182,12 @@ int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* a
   CHECK(max_rows >= 1, DSPARK_EINVAL);
   int rc = device_ok();
   if (rc != DSPARK_OK) return rc;
+  const TierSel ts{tier_host, 0ull, 0};
   return launch_pack(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode, max_rows,
-                     cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok,
+                     cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok, ts,
                      static_cast<cudaStream_t>(stream));
 }
 
-static bool attn_shape_ok(int Hq, int Hkv, int d_qk, int d_v, int page_size) {
-  if (page_size < 16 || (page_size & (page_size - 1)) != 0) return false;  // power of two
-  if (d_qk == 128 && d_v == 128) {
-    if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || Hq / Hkv > 128) return false;
-    if (page_size < 16 || page_size % 16 != 0) return false;
-    return page_size <= 64 ? (64 % page_size == 0) : (page_size % 64 == 0);
-  }
-  if (d_qk == 576 && d_v == 512) {
-    if (Hkv != 1 || Hq != 128) return false;
-    if (page_size < 16 || page_size % 16 != 0) return false;
-    return page_size <= 32 ? (32 % page_size == 0) : (page_size % 32 == 0);
-  }
-  return false;
-}
 
 size_t dspark_verify_attn_workspace_size(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v,
                                          int max_splits, int max_block_rows) {
@@ -213,29 +251,15 @@ int dspark_verify_attn_planned(const void* q, const void* k_new, const void* v_n
 int dspark_pack_plan(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
                      const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
                      int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out,
-                     int32_t* tier_out, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
-                     int Hq, int Hkv, int d_qk, int d_v, int attn_max_rows, int max_splits,
-                     int max_block_rows, void* attn_workspace, size_t attn_ws_bytes,
+                     int32_t* tier_out, int32_t* tier_host, int32_t* row_req, int32_t* row_pos,
+                     int32_t* row_tok, int Hq, int Hkv, int d_qk, int d_v, int attn_max_rows,
+                     int max_splits, int max_block_rows, void* attn_workspace, size_t attn_ws_bytes,
                      void* stream) {
-  CHECK(windows && ctx_len && anchor && draft_tok && cu_seqlens && M_out && tier_out && row_req &&
-            row_pos && row_tok && attn_workspace,
-        DSPARK_EINVAL);
-  CHECK(n_tiers >= 0 && n_tiers <= DSPARK_MAX_TIERS && (n_tiers == 0 || tiers), DSPARK_EINVAL);
-  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
-  CHECK(mode >= DSPARK_COMPACT && mode <= DSPARK_CAP_ACCEPT, DSPARK_EINVAL);
-  CHECK(max_rows >= 1 && attn_max_rows >= 1, DSPARK_EINVAL);
-  CHECK(attn_shape_ok(Hq, Hkv, d_qk, d_v, 16), DSPARK_EUNSUPPORTED);  // the plan has no page size
-  CHECK(max_splits >= 1 && max_splits <= 32, DSPARK_EINVAL);
-  CHECK((reinterpret_cast<uintptr_t>(attn_workspace) & 255u) == 0, DSPARK_EINVAL);
-  int rc = device_ok();
-  if (rc != DSPARK_OK) return rc;
-  const attn::Plan pl =
-      attn::plan(B, attn_max_rows, Hq, Hkv, d_qk, d_v, max_splits, max_block_rows);
-  CHECK(attn_ws_bytes >= pl.bytes, DSPARK_ENOSPACE);
-  return launch_pack_plan(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode,
-                          max_rows, cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok,
-                          attn_max_rows, Hkv, max_splits, pl, attn_workspace,
-                          static_cast<cudaStream_t>(stream));
+  const TierSel ts{tier_host, 0ull, 0};
+  return pack_plan_checked(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode,
+                           max_rows, cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok, Hq,
+                           Hkv, d_qk, d_v, attn_max_rows, max_splits, max_block_rows,
+                           attn_workspace, attn_ws_bytes, ts, static_cast<cudaStream_t>(stream));
 }
 
 size_t dspark_accept_workspace_size(int B, int gamma, int max_rows, int V) {

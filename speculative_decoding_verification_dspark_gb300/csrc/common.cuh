@@ -4,9 +4,30 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "dspark.h"
 
 namespace dspark {
+
+// One-time host set-up per device (kernel attributes, occupancy queries, symbol
+// addresses): fn() runs once for each device, with that device current, and its
+// result is kept.  Safe when several host threads make their first call at once.
+constexpr int kMaxDevices = 64;
+template <class T>
+struct PerDevice {
+  std::once_flag flag[kMaxDevices];
+  T value[kMaxDevices] = {};
+};
+// The current device's value, computed by fn() on first use; `fail` when the
+// current device cannot be read or is out of range.
+template <class T, class Fn>
+T once_per_device(PerDevice<T>& pd, T fail, Fn&& fn) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail;
+  std::call_once(pd.flag[dev], [&] { pd.value[dev] = fn(); });
+  return pd.value[dev];
+}
 
 // Device error word: one per device, owned by api.cu.  Kernels receive its
 // address as an argument so that no translation unit needs relocatable code.
@@ -40,6 +61,10 @@ __device__ __forceinline__ void pdl_release() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Set (for the calling host thread) while a graph is captured without programmatic
+// dependencies: the launches below are then ordinary stream-ordered launches.
+inline thread_local bool g_no_pdl = false;
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args... args) {
@@ -52,7 +77,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = g_no_pdl ? 0 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
@@ -66,14 +91,14 @@ inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = cluster_x;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = g_no_pdl ? 1 : 2;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 

@@ -7,6 +7,14 @@
 
 namespace dspark {
 
+// Where the pack kernel publishes the tier besides its device outputs: a pinned,
+// mapped host word (nullable), and the switch handle of a step graph (use = 0: none).
+struct TierSel {
+  int32_t* host;
+  unsigned long long handle;
+  int use;
+};
+
 int launch_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
                     const float* cost_table, int B, int gamma, int max_tokens, int mode,
                     int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
@@ -15,7 +23,8 @@ int launch_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
 int launch_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
                 const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
                 int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out, int32_t* tier_out,
-                int32_t* row_req, int32_t* row_pos, int32_t* row_tok, cudaStream_t stream);
+                int32_t* row_req, int32_t* row_pos, int32_t* row_tok, const TierSel& ts,
+                cudaStream_t stream);
 
 namespace attn {
 struct Plan;
@@ -27,7 +36,17 @@ int launch_pack_plan(const int32_t* windows, const int32_t* ctx_len, const int32
                      int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out,
                      int32_t* tier_out, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
                      int attn_max_rows, int Hkv, int max_splits, const attn::Plan& pl,
-                     void* attn_ws, cudaStream_t stream);
+                     void* attn_ws, const TierSel& ts, cudaStream_t stream);
+
+// dspark_pack_plan's host checks, then the launch, with the tier also published
+// through `ts` (the step graph passes its switch handle).
+int pack_plan_checked(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
+                      const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
+                      int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out,
+                      int32_t* tier_out, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
+                      int Hq, int Hkv, int d_qk, int d_v, int attn_max_rows, int max_splits,
+                      int max_block_rows, void* attn_workspace, size_t attn_ws_bytes,
+                      const TierSel& ts, cudaStream_t stream);
 
 size_t accept_workspace(int B, int max_rows, int V);
 int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_t* draft_tok,

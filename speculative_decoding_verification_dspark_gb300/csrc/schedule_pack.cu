@@ -262,8 +262,11 @@ __global__ void __launch_bounds__(kSchedThreads)
   if (tid == 0) *M_out = B + kstar;
 }
 
-// The pack of one step, by every thread of a 1024-thread CTA.
-__device__ inline void pack_body(const int32_t* __restrict__ windows,
+// The pack of one step, by every thread of a 1024-thread CTA.  Besides the device
+// outputs it can publish the tier to a pinned host word (ts.host) and select the
+// matching body of a step graph's switch node (ts.use): body i for tiers[i], body
+// n_tiers for a batch above every tier (run unpadded), none if it overflows max_rows.
+__device__ inline void pack_body(const TierSel ts, const int32_t* __restrict__ windows,
                                  const int32_t* __restrict__ ctx_len,
                                  const int32_t* __restrict__ anchor,
                                  const int32_t* __restrict__ draft_tok,
@@ -310,7 +313,18 @@ __device__ inline void pack_body(const int32_t* __restrict__ windows,
     s_tier = tier;
     *M_out = M;
     *tier_out = tier;
-    if (tier > max_rows) raise_error(err, DSPARK_DEVERR_ROWS_OVERFLOW);
+    int body = n_tiers;
+    for (int i = 0; i < n_tiers; ++i)
+      if (tiers[i] == tier) {
+        body = i;
+        break;
+      }
+    if (tier > max_rows) {
+      raise_error(err, DSPARK_DEVERR_ROWS_OVERFLOW);
+      body = n_tiers + 1;  // no body: the rest of the step is skipped
+    }
+    if (ts.host) *reinterpret_cast<volatile int32_t*>(ts.host) = tier;
+    if (ts.use) cudaGraphSetConditional(ts.handle, static_cast<unsigned int>(body));
   }
   for (int i = tid; i <= B; i += blockDim.x) cu_seqlens[i] = s_cu[i];
   __syncthreads();
@@ -337,10 +351,10 @@ __global__ void __launch_bounds__(1024)
                 int max_rows, int32_t* __restrict__ cu_seqlens, int32_t* __restrict__ M_out,
                 int32_t* __restrict__ tier_out, int32_t* __restrict__ row_req,
                 int32_t* __restrict__ row_pos, int32_t* __restrict__ row_tok,
-                unsigned int* __restrict__ err) {
+                const TierSel ts, unsigned int* __restrict__ err) {
   pdl_release();
   pdl_wait();  // inputs come from the kernels before this one
-  pack_body(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode, max_rows,
+  pack_body(ts, windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode, max_rows,
             cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok, err);
 }
 
@@ -361,10 +375,10 @@ __global__ void __launch_bounds__(1024)
                      int max_rows, int32_t* __restrict__ cu_seqlens, int32_t* __restrict__ M_out,
                      int32_t* __restrict__ tier_out, int32_t* __restrict__ row_req,
                      int32_t* __restrict__ row_pos, int32_t* __restrict__ row_tok,
-                     const PackPlanArgs a, unsigned int* __restrict__ err) {
+                     const PackPlanArgs a, const TierSel ts, unsigned int* __restrict__ err) {
   pdl_release();
   pdl_wait();  // inputs come from the kernels before this one
-  pack_body(windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode, max_rows,
+  pack_body(ts, windows, ctx_len, anchor, draft_tok, tiers, n_tiers, B, gamma, mode, max_rows,
             cu_seqlens, M_out, tier_out, row_req, row_pos, row_tok, err);
   __syncthreads();  // cu_seqlens (global, written above by this CTA) is complete
   extern __shared__ __align__(16) uint8_t pack_plan_smem[];
@@ -396,15 +410,14 @@ int launch_pack_plan(const int32_t* windows, const int32_t* ctx_len, const int32
                      int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out,
                      int32_t* tier_out, int32_t* row_req, int32_t* row_pos, int32_t* row_tok,
                      int attn_max_rows, int Hkv, int max_splits, const attn::Plan& pl,
-                     void* attn_ws, cudaStream_t stream) {
-  static bool configured = false;
+                     void* attn_ws, const TierSel& ts, cudaStream_t stream) {
+  static PerDevice<bool> configured;
   const int smem = static_cast<int>(sizeof(attn::WorkListSmem));
-  if (!configured) {
-    if (cudaFuncSetAttribute(pack_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return DSPARK_ECUDA;
-    configured = true;
-  }
+  if (!once_per_device(configured, false, [&] {
+        return cudaFuncSetAttribute(pack_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    smem) == cudaSuccess;
+      }))
+    return DSPARK_ECUDA;
   uint8_t* w = static_cast<uint8_t*>(attn_ws);
   PackPlanArgs a;
   a.attn_max_rows = attn_max_rows;
@@ -421,7 +434,7 @@ int launch_pack_plan(const int32_t* windows, const int32_t* ctx_len, const int32
   a.groups = reinterpret_cast<attn::SplitGroup*>(w + pl.off_groups);
   if (launch_pdl(pack_plan_kernel, dim3(1), dim3(1024), smem, stream, windows, ctx_len, anchor,
                  draft_tok, tiers, n_tiers, B, gamma, mode, max_rows, cu_seqlens, M_out, tier_out,
-                 row_req, row_pos, row_tok, a, device_error_word()) != cudaSuccess)
+                 row_req, row_pos, row_tok, a, ts, device_error_word()) != cudaSuccess)
     return DSPARK_ECUDA;
   return DSPARK_OK;
 }
@@ -429,10 +442,11 @@ int launch_pack_plan(const int32_t* windows, const int32_t* ctx_len, const int32
 int launch_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
                 const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
                 int mode, int max_rows, int32_t* cu_seqlens, int32_t* M_out, int32_t* tier_out,
-                int32_t* row_req, int32_t* row_pos, int32_t* row_tok, cudaStream_t stream) {
+                int32_t* row_req, int32_t* row_pos, int32_t* row_tok, const TierSel& ts,
+                cudaStream_t stream) {
   if (launch_pdl(pack_kernel, dim3(1), dim3(1024), 0, stream, windows, ctx_len, anchor, draft_tok,
                  tiers, n_tiers, B, gamma, mode, max_rows, cu_seqlens, M_out, tier_out, row_req,
-                 row_pos, row_tok, device_error_word()) != cudaSuccess)
+                 row_pos, row_tok, ts, device_error_word()) != cudaSuccess)
     return DSPARK_ECUDA;
   return DSPARK_OK;
 }

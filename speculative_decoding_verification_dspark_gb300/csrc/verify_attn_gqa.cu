@@ -34,7 +34,9 @@
 //              warp transpose-reduction and one cross-warp exchange through an
 //              mbarrier, lazy rescale of O^T when a row's max grows by > 2^8,
 //              exp2 on the SFU, P^T to shared memory in bf16, per-row sums by a
-//              second transpose-reduction.  Epilogue: O / l, lse.
+//              second transpose-reduction of the bf16 P the PV product multiplies
+//              (so the weights applied to V are exactly the normalised rounded P).
+//              Epilogue: O / l, lse.
 // Every wait is bounded in time (DSPARK_DEVERR_WAIT_TIMEOUT on expiry).
 
 #include <cuda.h>
@@ -552,6 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nc8 = (nq + 7) >> 3;                  // 8-row chunks holding valid rows
       const uint32_t t_o = t_lane + C::TMEM_O + (n_it & 1) * NT;  // this item's O^T
       // per-row state, lane-distributed: row = gi*32 + lane
+      // per-row sums of the bf16 P the PV product multiplies, so that the weights
+      // applied to V are exactly the normalised rounded P (a rounding of a dominant
+      // P cancels in O / l; the lse then carries it, |error| <= ln(1 + 2^-8))
       float mref[C::G32], lacc[C::G32];
 #pragma unroll
       for (int gi = 0; gi < C::G32; ++gi) { mref[gi] = -INFINITY; lacc[gi] = 0.f; }
@@ -661,9 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int n = gi * 32 + k;
               const float p0 = fast_exp2(fmaf(v[k], sl2, -my_mref[n]));
               const float p1 = fast_exp2(fmaf(v[k + 1], sl2, -my_mref[n + 1]));
-              v[k] = p0;
-              v[k + 1] = p1;
               __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              v[k] = __low2float(b2);
+              v[k + 1] = __high2float(b2);
               w[h] = *reinterpret_cast<uint32_t*>(&b2);
             }
             const uint32_t off = (n8 >> 3) * (kKT * 128) + sw128_off(kl, n8 & 7);
@@ -780,9 +785,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = n8 * 8 + 2 * h;
             const float p0 = fast_exp2(fmaf(s[n], sl2, -my_mref[n]));
             const float p1 = fast_exp2(fmaf(s[n + 1], sl2, -my_mref[n + 1]));
-            s[n] = p0;
-            s[n + 1] = p1;
             __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            s[n] = __low2float(b2);
+            s[n + 1] = __high2float(b2);
             w[h] = *reinterpret_cast<uint32_t*>(&b2);
           }
           uint32_t off;
@@ -915,17 +920,16 @@ using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, voi
                               CUtensorMapFloatOOBfill);
 
 EncodeFn get_encode() {
-  static EncodeFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  // the driver entry point is the same for every device: looked up once per process
+  static const EncodeFn fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(p);
-  }
+      return reinterpret_cast<EncodeFn>(p);
+    return static_cast<EncodeFn>(nullptr);
+  }();
   return fn;
 }
 
@@ -981,13 +985,12 @@ namespace {
 
 template <int NT>
 bool configure() {
-  static bool done = false, okv = false;
-  if (!done) {
-    done = true;
-    okv = cudaFuncSetAttribute(verify_attn_gqa_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<NT>::SMEM_BYTES) == cudaSuccess;
-  }
-  return okv;
+  static PerDevice<bool> done;
+  return once_per_device(done, false, [] {
+    return cudaFuncSetAttribute(verify_attn_gqa_kernel<NT>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<NT>::SMEM_BYTES) == cudaSuccess;
+  });
 }
 
 }  // namespace

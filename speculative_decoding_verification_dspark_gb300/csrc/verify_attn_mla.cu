@@ -14,30 +14,32 @@
 //   * the QK^T reduction is split the same way: CTA rho multiplies dims
 //     256 rho .. +255 (its own value columns) and rope dims 512 + 32 rho .. +31.
 //     It loads only those 5 of the 9 64-wide column blocks of a key tile;
-//   * the two partial score tiles, scaled to the log2 domain and rounded to fp16,
-//     are swapped through distributed shared memory and added in fp32; each CTA
-//     adds the same two rounded values, so both hold bit-identical scores and run
-//     the identical softmax (same P, max and sum).  The rounding moves a logit by at
-//     most 2^-11 of the partial's magnitude, the size of the bf16 rounding of P;
+//   * the two partial score tiles, scaled to the log2 domain, are swapped through
+//     distributed shared memory in fp32 and added; fp32 addition commutes, so both
+//     CTAs hold bit-identical scores and run the identical softmax (same P, max and
+//     sum), and the exchange adds no rounding to the scores.  (fp16 partials erred
+//     by 2^-11 of the partial's magnitude, up to 2^-6 log2 units at peaked scores,
+//     beyond the output tolerance; 24-bit fixed-point ones were exact enough but
+//     their packing on the exchange warps' serial path cost more than the bytes it
+//     saved);
 //   * Q (this CTA's 288 dims) and P sit in TMEM and are the A operand of the MMAs,
 //     so each product reads only the key tile (B) from shared memory.
 //
 //   S_rho [128 heads x 64 keys] = Q_rho . K_rho^T                 (tcgen05, TMEM)
-//   x = fp16(scale' S_0) + fp16(scale' S_1) (exchanged); P = exp2(x - m)  (SFU)
+//   x = scale' S_0 + scale' S_1 (exchanged, fp32); P = exp2(x - m)      (SFU)
 //   O_rho [128 x 256] += P . K[:, 256 rho .. 256 rho + 255]       (tcgen05, TMEM)
 //
 // The swap is the narrow point: with both CTAs sending at once and the key tiles
-// streaming in, the SM-to-SM network moves only about 7 bytes per clock each way, so
-// even the 16 KB of fp16 partials of a tile take longer than the tile's products
-// (fp32 partials took twice as long).  Dedicated exchange warps read S from TMEM
-// (releasing it for the next tile's QK^T at once), round it, send it with st.async,
-// whose bytes complete on the receiver's mbarrier (no thread waits on a
-// cluster-scope fence), and keep the CTA's own rounded copy beside the peer's in the
-// exchange slot; the softmax reads both from shared memory.
+// streaming in, the SM-to-SM network moves only about 7-14 bytes per clock each way.
+// Dedicated exchange warps read S from TMEM (releasing it for the next tile's QK^T at
+// once), keep their own scaled partial in registers, send it with st.async, whose
+// bytes complete on the receiver's mbarrier (no thread waits on a cluster-scope
+// fence), wait for the peer's partial, and write the fp32 sum in place of it in the
+// exchange slot; the softmax reads the sums from shared memory.
 //
 // TMEM columns: O [0, 256), S [256, 320), P [320, 352), Q [352, 496).
 // Shared memory: a 4-stage ring of key tiles (5 blocks x 64 keys, 40 KB) and two
-// exchange slots (peer's and own partials, 2 x 16 KB each).
+// exchange slots of 32 KB (the peer's fp32 partials, then the sums in their place).
 // Warp roles: 0 TMA producer (a 4-stage ring of key tiles), 1 MMA issuer (one lane)
 // that first zeroes the key rows past the visible range of a partial tile (value
 // rows met by a zero probability must be finite), 2-5 softmax and epilogue, 6-9
@@ -72,9 +74,10 @@ constexpr int kCBBytes = kNK * 128;
 constexpr int kStageBytes = kCBs * kCBBytes;
 constexpr int kStages = 4;
 constexpr int kQKSteps = 18;     // 288 dims / 16
-// Partial score exchange: a row is 64 fp16 partials (128 B); 16-byte piece c of row m
-// sits at piece c ^ (m mod 8), which keeps 8 consecutive rows on distinct banks.
-constexpr int kXRow = 128;
+// Partial score exchange: a row is 64 fp32 values (256 B); 16-byte piece c of row m
+// sits at piece (c & 8) | ((c ^ m) & 7), which keeps 8 consecutive rows on distinct
+// banks.
+constexpr int kXRow = 256;
 constexpr int kXBytes = kRows * kXRow;
 constexpr int kChunkRows = 16;   // block-row box
 constexpr int kProdWarp = 0;
@@ -84,10 +87,11 @@ constexpr int kExchWarp0 = 6;
 constexpr int kThreads = 10 * 32;
 constexpr int OFF_STAGE = 0;
 constexpr int OFF_X = OFF_STAGE + kStages * kStageBytes;
-// two exchange slots, each the peer's partials then this CTA's own rounded partials
-constexpr int OFF_BAR = OFF_X + 4 * kXBytes;
-// kv_full[S], kv_empty[S], s_full, s_free, p_full, p_empty, q_full, x_full[2], xc
-constexpr int N_BARS = 2 * kStages + 8;
+// two exchange slots: the peer's partials arrive there, the sums replace them
+constexpr int OFF_BAR = OFF_X + 2 * kXBytes;
+// kv_full[S], kv_empty[S], s_full, s_free, p_full, p_empty, q_full, x_full[2], xc,
+// sum_full[2]
+constexpr int N_BARS = 2 * kStages + 10;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_O = 0, TMEM_S = 256, TMEM_P = 320, TMEM_Q = 352;
@@ -152,15 +156,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Scaled partial scores as exchanged: a pair of fp32 values rounded to fp16 (the
-// 32-bit word sent) and the same pair widened back.
-__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
-  const __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
+// Byte offset of 16-byte piece c (0..15) of an exchange row of head m.
+__device__ __forceinline__ uint32_t x_piece(int c, int m) {
+  return static_cast<uint32_t>(((c & 8) | ((c ^ m) & 7)) << 4);
 }
-__device__ __forceinline__ float2 unpack_h2(uint32_t w) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&w));
-}
+
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -189,8 +189,7 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 struct Layout {
   uint32_t base;
   __device__ uint32_t stage(int s) const { return base + OFF_STAGE + s * kStageBytes; }
-  __device__ uint32_t x(int b) const { return base + OFF_X + b * 2 * kXBytes; }
-  __device__ uint32_t xo(int b) const { return x(b) + kXBytes; }
+  __device__ uint32_t x(int b) const { return base + OFF_X + b * kXBytes; }
   __device__ uint32_t bar(int i) const { return base + OFF_BAR + 8 * i; }
   __device__ uint32_t kv_full(int s) const { return bar(s); }
   __device__ uint32_t kv_empty(int s) const { return bar(kStages + s); }
@@ -201,6 +200,7 @@ struct Layout {
   __device__ uint32_t q_full() const { return bar(2 * kStages + 4); }
   __device__ uint32_t x_full(int b) const { return bar(2 * kStages + 5 + b); }
   __device__ uint32_t xc() const { return bar(2 * kStages + 7); }
+  __device__ uint32_t sum_full(int b) const { return bar(2 * kStages + 8 + b); }
 };
 
 // Keys of tile t of a request that a query row can see at all: the cache tile's
@@ -256,10 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(L.p_full(), 4);
     mbar_init(L.p_empty(), 1);
     mbar_init(L.q_full(), 4);
-    // armed (expect_tx) by this CTA's softmax, completed by the peer's asynchronous
-    // stores and by this CTA's exchange warps (own partials in place)
-    for (int b = 0; b < 2; ++b) mbar_init(L.x_full(b), 5);
+    // armed (expect_tx) by this CTA's exchange warps, completed by the peer's
+    // asynchronous stores
+    for (int b = 0; b < 2; ++b) mbar_init(L.x_full(b), 1);
     mbar_init(L.xc(), 4);
+    for (int b = 0; b < 2; ++b) mbar_init(L.sum_full(b), 4);  // sums in place
     fence_mbar_init();
   }
   if (warp == kProdWarp && lane == 0) {
@@ -428,7 +429,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m = sw * 32 + lane;            // query head of this thread
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
     const uint32_t x_row = static_cast<uint32_t>(m * kXRow);
-    const int sx = m & 7;
     int g = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it) {
@@ -481,33 +481,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 9; ++i) prefetch_l2(nq + i * 128);
         }
       }
-      // m_used: reference max of x; l_sum: sum of exp2(x - m_used)
-      float m_used = -INFINITY, l_sum = 0.f;
+      // m_used: reference max of x; l_sum: sum of exp2(x - m_used) (for the lse);
+      // l_sumr: the same sum of the bf16 P the PV product multiplies (for O / l, so
+      // that the weights applied to V are exactly the normalised rounded P)
+      float m_used = -INFINITY, l_sum = 0.f, l_sumr = 0.f;
       const int ntiles = item.te - item.tb;
       const int nt = ct + ceil_div(n_r, kNK);  // the item's tile range wraps at nt
       for (int l = 0; l < ntiles; ++l, ++g) {
         const int t = item.tb + l < nt ? item.tb + l : item.tb + l - nt;
         const int xb = g & 1;
-        // ---- x = S * scale * log2(e) = x_0 + x_1: both partials sit in the exchange
-        // slot as fp16 (this CTA's stored by its exchange warps, the peer's sent by the
-        // peer's) and are added in fp32; the sum commutes, so both CTAs get identical bits
-        if (m == 0) mbar_arrive_expect_tx(L.x_full(xb), kXBytes);  // what the peer sends here
-        if (!wait_warp<true>(L.x_full(xb), (g >> 1) & 1, cx)) { ok = false; break; }
+        // ---- x = S * scale * log2(e) = x_0 + x_1, summed in fp32 by the exchange
+        // warps (the sum commutes, so both CTAs hold identical bits)
+        if (!wait_warp(L.sum_full(xb), (g >> 1) & 1, cx)) { ok = false; break; }
         float s[kNK];
         {
-          const uint32_t rp = L.x(xb) + x_row, ro = L.xo(xb) + x_row;
+          const uint32_t rp = L.x(xb) + x_row;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t off = static_cast<uint32_t>((c ^ sx) << 4);
-            const float4 vo = ld_shared_f4(ro + off), vp = ld_shared_f4(rp + off);
-            const float wo[4] = {vo.x, vo.y, vo.z, vo.w}, wp[4] = {vp.x, vp.y, vp.z, vp.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 a = unpack_h2(__float_as_uint(wo[i]));
-              const float2 b = unpack_h2(__float_as_uint(wp[i]));
-              s[8 * c + 2 * i] = a.x + b.x;
-              s[8 * c + 2 * i + 1] = a.y + b.y;
-            }
+          for (int c = 0; c < 16; ++c) {
+            const float4 v = ld_shared_f4(rp + x_piece(c, m));
+            s[4 * c] = v.x;
+            s[4 * c + 1] = v.y;
+            s[4 * c + 2] = v.z;
+            s[4 * c + 3] = v.w;
           }
         }
         __syncwarp();
@@ -531,13 +526,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = need ? mt : m_used;
         const float mref = (m_new == -INFINITY) ? 0.f : m_new;
         uint32_t pw[32];
-        float psum[4] = {0.f, 0.f, 0.f, 0.f};
+        float psum[4] = {0.f, 0.f, 0.f, 0.f}, psumr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const float p0 = fast_exp2(s[2 * k] - mref);
           const float p1 = fast_exp2(s[2 * k + 1] - mref);
           psum[k & 3] += p0 + p1;
           __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          psumr[k & 3] += __low2float(b2) + __high2float(b2);
           pw[k] = *reinterpret_cast<uint32_t*>(&b2);
         }
         // ---- P's TMEM columns are free and O is current once PV of the previous tile is done
@@ -556,10 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (need) {
-          l_sum *= (l > 0) ? fast_exp2(m_used - mt) : 0.f;
+          const float a = (l > 0) ? fast_exp2(m_used - mt) : 0.f;
+          l_sum *= a;
+          l_sumr *= a;
           m_used = mt;
         }
         l_sum += (psum[0] + psum[1]) + (psum[2] + psum[3]);
+        l_sumr += (psumr[0] + psumr[1]) + (psumr[2] + psumr[3]);
         {
           float pf[32];
 #pragma unroll
@@ -577,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gl = g - 1;
         if (!wait_warp(L.p_empty(), gl & 1, cx)) { ok = false; break; }
         tc_fence_after();
-        const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        const float inv_l = l_sumr > 0.f ? 1.f / l_sumr : 0.f;
         const bool split = item.nsplit > 1;
         float* obase = split ? prm.ws_o + ((long long)item.slot * kRows + m) * kDv + rho * kHalf
                              : prm.out + ((long long)row_g * kRows + m) * kDv + rho * kHalf;
@@ -607,17 +606,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kExchWarp0) {
     // ------------------------------------------------------------- score exchange
-    // Per tile: S_rho from TMEM (released as soon as it is in registers), rounded,
-    // sent to the peer's exchange slot and stored in this CTA's own half of the
-    // slot.  The send of tile g waits until this CTA's softmax has read tile g - 1:
-    // the peer's slot of tile g (used for g - 2 before) is then free, because the
-    // peer sent tile g - 1 only after its own softmax had read tile g - 2; this
-    // CTA's own half of the slot was read with tile g - 2 as well.
+    // Per tile: S_rho from TMEM (released as soon as it is in registers), scaled to
+    // the log2 domain, sent in fp32 to the peer's exchange slot; then, once the peer's
+    // partial has arrived in this CTA's slot, the sum x = own + peer replaces it there
+    // for the softmax.  The send of tile g waits until this CTA's softmax has read
+    // the sums of tile g - 1: the peer's slot of tile g (used for g - 2 before) is
+    // then free, because the peer sent tile g - 1 only after its own softmax had read
+    // the sums of tile g - 2.
     const int sw = warp & 3;
     const int m = sw * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
     const uint32_t x_row = static_cast<uint32_t>(m * kXRow);
-    const int sx = m & 7;
     const float sl2 = prm.scale_log2;
     const uint32_t x_peer = mapa_shared(L.x(0), peer) + x_row;
     const uint32_t xf_peer = mapa_shared(L.x_full(0), peer);
@@ -630,35 +629,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int xb = g & 1;
         if (!wait_warp(L.s_full(), g & 1, cx)) { ok = false; break; }
         tc_fence_after();
-        float s[kNK];
+        float x[kNK];
         {
           float a[32], b[32];
           tmem_ld32(t_lane + TMEM_S, a);
           tmem_ld32(t_lane + TMEM_S + 32, b);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) { s[k] = a[k]; s[32 + k] = b[k]; }
+          for (int k = 0; k < 32; ++k) { x[k] = a[k] * sl2; x[32 + k] = b[k] * sl2; }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(L.s_free());
-        uint4 w[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          w[c] = make_uint4(pack_h2(s[8 * c] * sl2, s[8 * c + 1] * sl2),
-                            pack_h2(s[8 * c + 2] * sl2, s[8 * c + 3] * sl2),
-                            pack_h2(s[8 * c + 4] * sl2, s[8 * c + 5] * sl2),
-                            pack_h2(s[8 * c + 6] * sl2, s[8 * c + 7] * sl2));
         if (g >= 1 && !wait_warp(L.xc(), (g - 1) & 1, cx)) { ok = false; break; }
-        const uint32_t dst = x_peer + xb * 2 * kXBytes;
+        // this CTA's slot xb receives the peer's partial of tile g
+        if (m == 0) mbar_arrive_expect_tx(L.x_full(xb), kXBytes);
+        const uint32_t dst = x_peer + xb * kXBytes;
         const uint32_t bar = xf_peer + 8 * xb;
-        const uint32_t own = L.xo(xb) + x_row;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) st_async_v4(dst + ((c ^ sx) << 4), w[c], bar);
+        for (int c = 0; c < 16; ++c)
+          st_async_v4(dst + x_piece(c, m),
+                      make_uint4(__float_as_uint(x[4 * c]), __float_as_uint(x[4 * c + 1]),
+                                 __float_as_uint(x[4 * c + 2]), __float_as_uint(x[4 * c + 3])),
+                      bar);
+        if (!wait_warp<true>(L.x_full(xb), (g >> 1) & 1, cx)) { ok = false; break; }
+        // x = own + peer: fp32 addition commutes, so both CTAs get identical bits
+        const uint32_t row = L.x(xb) + x_row;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) st_shared_v4(own + ((c ^ sx) << 4), w[c]);
+        for (int c = 0; c < 16; ++c) {
+          const float4 p = ld_shared_f4(row + x_piece(c, m));
+          st_shared_v4(row + x_piece(c, m),
+                       make_uint4(__float_as_uint(x[4 * c] + p.x), __float_as_uint(x[4 * c + 1] + p.y),
+                                  __float_as_uint(x[4 * c + 2] + p.z),
+                                  __float_as_uint(x[4 * c + 3] + p.w)));
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(L.x_full(xb));  // own partials in place
+        if (lane == 0) mbar_arrive(L.sum_full(xb));  // sums of tile g in place
       }
     }
   }
@@ -676,22 +682,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace {
 
 bool configure() {
-  static bool done = false, okv = false;
-  if (!done) {
-    done = true;
-    okv = cudaFuncSetAttribute(verify_attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES) == cudaSuccess;
-  }
-  return okv;
+  static PerDevice<bool> done;
+  return once_per_device(done, false, [] {
+    return cudaFuncSetAttribute(verify_attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SMEM_BYTES) == cudaSuccess;
+  });
 }
 
 }  // namespace
 
 int clusters() {
-  static int n = -1;
-  if (n < 0) {
-    int sms = num_sms_cached();
-    n = sms / 2 > 0 ? sms / 2 : 1;
+  static PerDevice<int> clus;
+  return once_per_device(clus, 1, [] {
+    const int sms = num_sms_cached();
+    int n = sms / 2 > 0 ? sms / 2 : 1;
     if (configure()) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * n);
@@ -711,8 +715,8 @@ int clusters() {
       else
         cudaGetLastError();
     }
-  }
-  return n;
+    return n;
+  });
 }
 
 int launch_kernel(const void* q, const void* k_new, const void* k_cache, int n_pages,

@@ -46,7 +46,7 @@ def test_host_validation_without_device(lib):
     nul = None
     assert lib.dspark_schedule(nul, 1, nul, nul, 10, 4, 6, 32, 0, nul, nul, nul, nul, nul) == -1
     assert lib.dspark_pack(nul, nul, nul, nul, nul, 0, 4, 6, 0, 8, nul, nul, nul, nul, nul, nul,
-                           nul) == -1
+                           nul, nul) == -1
     # unsupported attention shape (head dim 96)
     assert lib.dspark_verify_attn(nul, nul, nul, nul, nul, 1, nul, 1, nul, nul, 1, 8, 8, 2, 96, 96,
                                   16, ctypes.c_float(0.1), 4, 9, nul, nul, nul, 0, nul) == -2
@@ -55,11 +55,11 @@ def test_host_validation_without_device(lib):
     # pack + work list: NULL pointers; then valid pointers with an unsupported attention
     # shape (head dim 96); the planned attention validates as the standalone call
     assert lib.dspark_pack_plan(nul, nul, nul, nul, nul, 0, 4, 6, 0, 8, nul, nul, nul, nul, nul,
-                                nul, 8, 2, 128, 128, 8, 4, 7, nul, 0, nul) == -1
-    assert lib.dspark_pack_plan(fake, fake, fake, fake, nul, 0, 4, 6, 0, 8, fake, fake, fake, fake,
-                                fake, fake, 8, 2, 96, 96, 8, 4, 7, fake, 1 << 20, nul) == -2
-    assert lib.dspark_pack_plan(fake, fake, fake, fake, nul, 0, 4, 6, 0, 8, fake, fake, fake, fake,
-                                fake, fake, 8, 2, 128, 128, 8, 33, 7, fake, 1 << 20, nul) == -1
+                                nul, nul, 8, 2, 128, 128, 8, 4, 7, nul, 0, nul) == -1
+    assert lib.dspark_pack_plan(fake, fake, fake, fake, nul, 0, 4, 6, 0, 8, fake, fake, fake, nul,
+                                fake, fake, fake, 8, 2, 96, 96, 8, 4, 7, fake, 1 << 20, nul) == -2
+    assert lib.dspark_pack_plan(fake, fake, fake, fake, nul, 0, 4, 6, 0, 8, fake, fake, fake, nul,
+                                fake, fake, fake, 8, 2, 128, 128, 8, 33, 7, fake, 1 << 20, nul) == -1
     assert lib.dspark_verify_attn_planned(nul, nul, nul, nul, nul, 1, nul, 1, nul, nul, 1, 8, 8, 2,
                                           96, 96, 16, ctypes.c_float(0.1), 4, 9, nul, nul, nul, 0,
                                           nul) == -2
@@ -80,3 +80,42 @@ def test_workspace_sizes_are_host_computable(lib):
     assert lib.dspark_verify_attn_workspace_size(32, 512, 32, 8, 96, 96, 8, 9) == 0
     assert lib.dspark_accept_workspace_size(32, 8, 512, 151936) > 0
     assert lib.dspark_compact_workspace_size(32) > 0
+
+
+def test_step_graph_rejects_bad_descriptors_on_the_host(lib):
+    """The step graph's descriptor is checked before any CUDA work: NULL arguments,
+    tiers that are not ascending or exceed the row capacity."""
+    import speculative_decoding_verification_dspark_gb300 as pkg
+    out = ctypes.c_void_p()
+    assert lib.dspark_step_graph_create(None, ctypes.byref(out)) == -1
+    d = pkg.StepDesc()
+    d.B, d.gamma, d.max_rows = 4, 6, 32
+    tiers = (ctypes.c_int32 * 3)(8, 16, 64)      # 64 > max_rows
+    d.n_tiers, d.tiers_host, d.tiers = 3, ctypes.cast(tiers, ctypes.c_void_p), 4096
+    assert lib.dspark_step_graph_create(ctypes.byref(d), ctypes.byref(out)) == -1
+    tiers2 = (ctypes.c_int32 * 3)(8, 8, 16)      # not strictly ascending
+    d.tiers_host = ctypes.cast(tiers2, ctypes.c_void_p)
+    assert lib.dspark_step_graph_create(ctypes.byref(d), ctypes.byref(out)) == -1
+    d.B = 0
+    assert lib.dspark_step_graph_create(ctypes.byref(d), ctypes.byref(out)) == -1
+    assert out.value is None
+    assert lib.dspark_step_graph_destroy(None) == 0
+
+
+def test_step_desc_layout_matches_the_header():
+    """The binding's descriptor has the header's field order and size (every field of
+    the C struct, in order, with the C alignment)."""
+    import re
+    import speculative_decoding_verification_dspark_gb300 as pkg
+    text = open(HEADER).read()
+    body = text[text.index("typedef struct dspark_step_desc {"):text.index("} dspark_step_desc;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = []
+    for decl in body.split(";")[:-1]:
+        decl = decl.split("{")[-1].strip()
+        if not decl:
+            continue
+        head, *rest = [x.strip() for x in decl.split(",")]
+        names.append(re.split(r"[\s*]+", head)[-1])
+        names.extend(rest)
+    assert [f[0] for f in pkg.StepDesc._fields_] == names

@@ -1,7 +1,13 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle on the same
 seeded inputs.  Integers bit-exact (window decisions the oracle lists as
-within 1e-5 relative are reported, not failed); attention max-abs <= 1e-2,
-mean-abs <= 1e-3, lse max-abs <= 1e-3 against fp64; c* within 1e-5."""
+within 1e-5 relative are reported, not failed); attention max-abs <= 1e-2 and
+mean-abs <= 1e-3 against fp64; c* within 1e-5.
+
+lse within 4e-3: the GQA kernel multiplies V by P rounded to bf16 (8 significant
+bits: relative error at most 2^-8) and divides by the sum of those same rounded
+P, so that the weights applied to V are exactly normalised; its lse = m + log(sum
+of rounded P) then differs from the exact one by at most ln(1 + 2^-8) = 3.9e-3
+(plus fp32 rounding far below that)."""
 import math
 
 import numpy as np
@@ -14,7 +20,7 @@ from oracle import dspark_oracle as O
 
 pytestmark = pytest.mark.gpu
 
-ATT_MAX, ATT_MEAN, LSE_MAX, CSTAR_TOL = 1e-2, 1e-3, 1e-3, 1e-5
+ATT_MAX, ATT_MEAN, LSE_MAX, CSTAR_TOL = 1e-2, 1e-3, 4e-3, 1e-5
 MODES = {"compact": O.COMPACT, "static": O.STATIC, "cap_accept": O.CAP_ACCEPT}
 
 
@@ -42,20 +48,33 @@ def small_np(inp):
 # ------------------------------------------------------------------ checks
 
 def check_schedule(g, sch, B):
+    """Windows bit-exact, except the decisions the oracle lists as within 1e-5
+    relative of their margin: those are reported, not failed.  Returns the windows
+    the later stages are checked on (the GPU's own when a listed decision went the
+    other way, so that every stage is still compared on identical inputs)."""
     ow = sch.windows
     gw = g["windows"].numpy()
+    # calibrated survival: identical up to one fp32 ulp (fp64 exp/log of two libraries,
+    # each rounded once to fp32)
+    ga = g["a_hat"].numpy()
+    assert np.all(np.abs(ga.view(np.int32).astype(np.int64) - sch.a_hat.view(np.int32)) <= 1)
     if not sch.listed:
         assert np.array_equal(gw, ow), (gw, ow)
         assert g["M"] == sch.M
+        assert math.isclose(g["E"], sch.E, rel_tol=1e-9)
+        return ow
+    print(f"listed near-margin decisions: {sch.listed}")
+    if any(kind == "accept" for (kind, _, _, _) in sch.listed):
+        # an accepted candidate within the margin: if it flipped, every later decision
+        # moved with it, so only the greedy's shape is checked
+        assert g["M"] == B + int(gw.sum())
     else:
         listed_r = {r for (_, r, _, _) in sch.listed}
         other = [r for r in range(B) if r not in listed_r]
         assert np.array_equal(gw[other], ow[other])
-        print(f"listed near-margin decisions: {sch.listed}")
-    assert math.isclose(g["E"], sch.E, rel_tol=1e-9)
-    # calibrated survival: identical up to one fp32 ulp (exp/log of two libraries)
-    ga = g["a_hat"].numpy()
-    assert np.all(np.abs(ga.view(np.int32).astype(np.int64) - sch.a_hat.view(np.int32)) <= 1)
+    if not np.array_equal(gw, ow):
+        print(f"listed decision went the other way: GPU windows {gw.tolist()}")
+    return gw
 
 
 def check_pack(g, pk):
@@ -184,8 +203,8 @@ def run_and_check(inp, mode, attention_requests=None):
     assert err == 0, f"device error word {err:#x}"
     sch = O.schedule(snp["conf"], inp["conf_is_logit"], snp["sts_temp"], snp["cost_table"],
                      wl.max_tokens, mode)
-    check_schedule(g, sch, wl.B)
-    pk = O.pack(sch.windows, snp["ctx_len"], snp["anchor"], snp["draft_tok"], snp["tiers"], mode,
+    windows = check_schedule(g, sch, wl.B)
+    pk = O.pack(windows, snp["ctx_len"], snp["anchor"], snp["draft_tok"], snp["tiers"], mode,
                 wl.gamma)
     check_pack(g, pk)
     M = pk.M
@@ -194,7 +213,7 @@ def run_and_check(inp, mode, attention_requests=None):
     check_attention(npy(step.out[rows]), npy(step.lse[rows]), o, l)
     p_t = npy(d["p_target"][:M])
     acc = O.accept(p_t, npy(inp["p_draft"]), snp["draft_tok"], snp["uniforms"],
-                   npy(inp["exp_noise"]), sch.windows, pk.cu_seqlens, mode, wl.gamma)
+                   npy(inp["exp_noise"]), windows, pk.cu_seqlens, mode, wl.gamma)
     check_accept(g, acc)
     cm = oracle_compact_state(snp, pk, acc, wl)
     check_compact(g, cm, inp, pk, acc, wl, d)
@@ -319,28 +338,210 @@ def _full(name, seed=0):
 
 
 def test_full_qwen3_8b():
+    """The timed shape, every request's attention against fp64 (all split groups and
+    stream-K pieces of the timed launch configuration)."""
     inp = _full("qwen3_8b")
-    run_and_check(inp, O.COMPACT, attention_requests=[0, 13, 31])
+    run_and_check(inp, O.COMPACT)
 
 
 @pytest.mark.parametrize("mode", list(MODES))
 def test_full_mixed256(mode):
+    """B=256, gamma=16: attention checked on 32 requests spread over the batch (all
+    three confidence classes, short and long contexts)."""
     inp = _full("mixed256")
-    run_and_check(inp, MODES[mode], attention_requests=[0, 128, 255])
+    run_and_check(inp, MODES[mode], attention_requests=list(range(0, 256, 8)))
 
 
 def test_full_mla():
+    """Latent-KV shape at full size: every request's attention against fp64."""
     inp = _full("mla")
-    run_and_check(inp, O.COMPACT, attention_requests=[0, 63])
+    run_and_check(inp, O.COMPACT)
 
 
-@pytest.mark.parametrize("B,c,theta", [(1, 0.95, 0.05), (32, 0.85, 0.19), (256, 0.70, 0.5),
-                                       (128, 0.95, 0.19)])
+def _sweep_grid():
+    """Points of the budget/tier sweep: every (confidence mean, cost slope) pair once,
+    the batch sizes taken in turn, plus the largest batch at every confidence mean."""
+    pts = []
+    i = 0
+    for c in W.SWEEP_CONF_MEANS:
+        for theta in W.SWEEP_THETA:
+            pts.append((W.SWEEP_B[i % len(W.SWEEP_B)], c, theta))
+            i += 1
+    for c in W.SWEEP_CONF_MEANS:
+        pts.append((256, c, 0.19))
+    return pts
+
+
+@pytest.mark.parametrize("B,c,theta", _sweep_grid())
 def test_sweep_points(B, c, theta):
     wl = W.sweep_point(B, c, theta)
     inp = W.make_inputs(wl, 0, device=W.gen_device(wl))
     for mode in (O.COMPACT, O.STATIC, O.CAP_ACCEPT):
-        run_and_check(inp, mode, attention_requests=[0, B - 1])
+        run_and_check(inp, mode, attention_requests=sorted({0, B // 2, B - 1}))
+
+
+# ------------------------------------------------------------------ peaked softmax
+
+def _peaked(inp, factor):
+    """Queries scaled by a power of two (exact in bf16): logits of standard deviation
+    `factor`, so a few keys carry most of the softmax mass.  This is where the bf16
+    rounding of P, the deferred rescale of the output accumulator and (latent KV) the
+    exchange of partial scores between the two CTAs of a cluster matter."""
+    inp = dict(inp)
+    inp["q_dense"] = (inp["q_dense"].float() * factor).to(torch.bfloat16)
+    return inp
+
+
+@pytest.mark.parametrize("factor,gamma,mode", [(8, 8, "compact"), (16, 8, "compact"),
+                                               (8, 16, "static"), (16, 16, "cap_accept")])
+def test_peaked_softmax_gqa(factor, gamma, mode):
+    """GQA with peaked scores; gamma = 16 in static/cap-accept mode puts 17 rows x 4
+    heads on the 128-column query tile."""
+    wl = W.Workload(
+        name=f"peaked_gqa_g{gamma}", B=6, gamma=gamma, attn="gqa", Hq=32, Hkv=8, d_qk=128,
+        d_v=128, page_size=16, ctx=("uniform", 700, 3000), conf=("logit", 1.5, 1.0), vocab=1024,
+        p_dtype="f32", target_logit_std=3.0, draft_noise_std=0.7,
+        tiers=W.pow2_tiers(8, 6 * (gamma + 1)))
+    inp = _peaked(W.make_inputs(wl, 21), factor)
+    run_and_check(inp, MODES[mode])
+
+
+@pytest.mark.parametrize("factor,page_size", [(4, 64), (8, 64), (8, 16)])
+def test_peaked_softmax_mla(factor, page_size):
+    """Latent KV with peaked scores (standard deviation 4 or 8 instead of 1)."""
+    wl = W.Workload(
+        name=f"peaked_mla_p{page_size}", B=4, gamma=6, attn="mla", Hq=128, Hkv=1, d_qk=576,
+        d_v=512, page_size=page_size, ctx=("uniform", 1000, 6000), conf=("logit", 1.2, 1.0),
+        vocab=1024, p_dtype="f32", target_logit_std=3.0, draft_noise_std=0.7,
+        tiers=(8, 16, 32))
+    inp = _peaked(W.make_inputs(wl, 22), factor)
+    run_and_check(inp, O.COMPACT)
+
+
+# ------------------------------------------------------------------ crafted acceptance
+
+def _accept_direct(p_t, p_d, draft, u, e, windows, cu, mode):
+    """dspark_accept on crafted host tensors; returns the GPU outputs (host)."""
+    import speculative_decoding_verification_dspark_gb300 as dspark
+    dev = torch.device("cuda")
+    B, gamma, V = p_d.shape
+    i32 = dict(dtype=torch.int32, device=dev)
+    t = {k: torch.as_tensor(v).to(dev) for k, v in dict(p_t=p_t, p_d=p_d, e=e, u=u).items()}
+    draft_d = torch.as_tensor(draft, dtype=torch.int32).to(dev)
+    win_d = torch.as_tensor(windows, dtype=torch.int32).to(dev)
+    cu_d = torch.as_tensor(cu, dtype=torch.int32).to(dev)
+    out = {"accept_len": torch.full((B,), -7, **i32), "cap_len": torch.full((B,), -7, **i32),
+           "out_tok": torch.full((B,), -7, **i32), "fallback": torch.full((B,), -7, **i32),
+           "cstar": torch.full((B, gamma), 3.0, dtype=torch.float32, device=dev)}
+    ws = torch.empty(dspark.accept_workspace_size(B, gamma, p_t.shape[0], V), dtype=torch.uint8,
+                     device=dev)
+    dspark.read_device_error()
+    dspark.accept(t["p_t"], t["p_d"], draft_d, t["u"], t["e"], win_d, cu_d, mode,
+                  out["accept_len"], out["cap_len"], out["out_tok"], out["cstar"],
+                  out["fallback"], ws)
+    torch.cuda.synchronize()
+    assert dspark.read_device_error() == 0
+    return {k: v.cpu() for k, v in out.items()}
+
+
+@pytest.mark.parametrize("maxima", [
+    [36, 37, 300, 8193, 8200, 20000],      # same lane, other warps, later chunks
+    [20000, 8200, 4100, 4099],              # lowest in the first chunk, last warps
+    [24000, 16384, 8192],                   # chunk boundaries only
+    [25575, 12345],                          # last entry of the vocabulary
+])
+@pytest.mark.parametrize("dtype", [np.float32, "bf16"])
+def test_race_ties_lowest_index_on_gpu(maxima, dtype):
+    """The largest race key duplicated across lanes, warps and 8192-entry chunks: the
+    lowest index wins, on a bonus row (request 0) and on a correction row (request 1);
+    request 2 tests u * p_d = p_t exactly (accepted: the test is inclusive) followed by
+    p_t one ulp below u * p_d (rejected)."""
+    V, gamma, B = 3 * 8192 + 1000, 4, 3
+    rng = np.random.default_rng(sum(maxima))
+    n = gamma + 1
+    cu = np.arange(B + 1, dtype=np.int32) * n
+    p_t = rng.uniform(1e-6, 1e-4, size=(B * n, V)).astype(np.float32)
+    p_d = rng.uniform(1e-6, 1e-4, size=(B, gamma, V)).astype(np.float32)
+    e = rng.uniform(1.0, 2.0, size=(B, V)).astype(np.float32)
+    draft = np.zeros((B, gamma), np.int32)
+    u = np.full((B, gamma), 2.0 ** -20, np.float32)
+    # request 0: every draft accepted (u tiny), bonus drawn on row 4 from p_t
+    for j in range(gamma):
+        draft[0, j] = 11 + j
+    for m in maxima:
+        p_t[cu[0] + gamma, m] = 0.5
+        e[0, m] = 1.0
+    # request 1: draft 1 rejected (p_t = 0 there), correction from max(0, p_t - p_d) on
+    # row 0 with the maximal residual 0.25 at the duplicated indices
+    draft[1, 0] = 77
+    p_t[cu[1], 77] = 0.0
+    for m in maxima:
+        p_t[cu[1], m] = 0.375
+        p_d[1, 0, m] = 0.125
+        e[1, m] = 1.0
+    # request 2: u * p_d == p_t exactly at positions 1, 2; one ulp below at 3
+    u[2] = 0.75
+    for j, x in enumerate((5, 6, 7)):
+        draft[2, j] = x
+        p_d[2, j, x] = 0.5
+        p_t[cu[2] + j, x] = 0.375 if j < 2 else np.nextafter(np.float32(0.375), np.float32(0))
+    windows = np.full(B, gamma, np.int32)
+    if dtype == "bf16":
+        # (bf16 cannot hold 0.375 minus one fp32 ulp: there request 2 accepts on)
+        pt_d = torch.from_numpy(p_t).to(torch.bfloat16)
+        pd_d = torch.from_numpy(p_d).to(torch.bfloat16)
+        pt_o, pd_o = pt_d.float().numpy(), pd_d.float().numpy()
+    else:
+        pt_d, pd_d = p_t, p_d
+        pt_o, pd_o = p_t, p_d
+    g = _accept_direct(pt_d, pd_d, draft, u, e, windows, cu, O.COMPACT)
+    acc = O.accept(pt_o, pd_o, draft, u, e, windows, cu, O.COMPACT, gamma)
+    assert acc.accept_len.tolist()[:2] == [gamma, 0]
+    assert acc.accept_len[2] >= 2 and (dtype == "bf16" or acc.accept_len[2] == 2)
+    assert acc.out_tok[0] == min(maxima) and acc.out_tok[1] == min(maxima)
+    assert np.array_equal(g["accept_len"].numpy(), acc.accept_len)
+    assert np.array_equal(g["cap_len"].numpy(), acc.cap_len)
+    assert np.array_equal(g["out_tok"].numpy(), acc.out_tok)
+    assert np.array_equal(g["fallback"].numpy().astype(bool), acc.residual_fallback)
+    cs = g["cstar"].numpy()
+    assert np.nanmax(np.abs(cs - acc.cstar)) <= CSTAR_TOL
+
+
+def test_race_zero_weights_with_zero_noise_on_gpu():
+    """Zero noise entries placed on zero weights (their w / e is NaN), and a row whose
+    only positive residual entries carry large noise: the zero-weight entries never
+    win, on the GPU as in the oracle (reading A11)."""
+    V, gamma, B = 2 * 8192 + 64, 2, 2
+    rng = np.random.default_rng(5)
+    n = gamma + 1
+    cu = np.arange(B + 1, dtype=np.int32) * n
+    p_t = rng.uniform(0.0, 1e-4, size=(B * n, V)).astype(np.float32)
+    p_d = rng.uniform(0.0, 1e-4, size=(B, gamma, V)).astype(np.float32)
+    e = rng.uniform(0.5, 2.0, size=(B, V)).astype(np.float32)
+    draft = np.array([[3, 4], [9, 10]], np.int32)
+    u = np.full((B, gamma), 2.0 ** -20, np.float32)
+    # request 0: bonus row with zero weights and zero noise on every 7th entry
+    zero = np.arange(0, V, 7)
+    p_t[cu[0] + gamma, zero] = 0.0
+    e[0, zero] = 0.0
+    # request 1: rejected at position 1; residual positive only at 3 entries, the rest
+    # zero, and zero noise on many zero-residual entries
+    p_t[cu[1], 9] = 0.0
+    p_d[1, 0] = p_t[cu[1]] + np.float32(1e-3)
+    for m, ev in ((100, 1e6), (9000, 3e6), (16000, 2e6)):
+        p_t[cu[1], m] = 0.01
+        p_d[1, 0, m] = 0.005
+        e[1, m] = ev
+    e[1, np.arange(1, V, 5)] = 0.0
+    e[1, [100, 9000, 16000]] = [1e6, 3e6, 2e6]
+    windows = np.full(B, gamma, np.int32)
+    g = _accept_direct(p_t, p_d, draft, u, e, windows, cu, O.COMPACT)
+    acc = O.accept(p_t, p_d, draft, u, e, windows, cu, O.COMPACT, gamma)
+    assert acc.out_tok[1] == 100 and not acc.residual_fallback[1]
+    assert acc.out_tok[0] % 7 != 0
+    assert np.array_equal(g["out_tok"].numpy(), acc.out_tok)
+    assert np.array_equal(g["accept_len"].numpy(), acc.accept_len)
+    assert np.array_equal(g["fallback"].numpy().astype(bool), acc.residual_fallback)
 
 
 def test_cap_accept_commits_match_compact_on_gpu():
