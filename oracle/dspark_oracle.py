@@ -25,7 +25,8 @@ Sources, cited by short name below:
 
 Parity status per function (what pins it is listed in tests/test_oracle_pins.py):
 pinned: confidence sigmoid, survival/STS, greedy schedule, pack, verify
-attention (GQA and MLA), acceptance (test, race, fallback, c*), compaction.  The composed ``step`` adds no arithmetic of its own and
+attention (GQA and MLA), acceptance (test, race, fallback, c*), compaction,
+calibration samples, ECE and the STS refit.  The composed ``step`` adds no arithmetic of its own and
 is pinned only through its parts (no page prints end-to-end values).
 """
 from __future__ import annotations
@@ -523,7 +524,95 @@ def compact(k_new, v_new, cu_seqlens, accept_len, out_tok, draft_tok, page_size,
 
 
 # ----------------------------------------------------------------------------
-# 7. The whole step
+# 7. Calibration of the confidence head: labelled samples, ECE, STS refit
+# ----------------------------------------------------------------------------
+
+def calib_samples(survival, a_hat, windows, cap_len, mode, gamma):
+    """Labelled accept outcomes of one step, per draft position ([csdn] §5
+    "可观测性": per-request confidence and calibration metrics such as ECE;
+    [notes] §07: the head's cumulative survival a_j predicts that the prefix
+    1..j is accepted).
+
+    Position j (1-based) of request r is verified iff j <= v_r (v_r = w_r in
+    compact/static mode, gamma in cap-accept mode); its label is y = 1 iff the
+    accepted prefix over the verified positions reaches it, j <= cap_r.
+    Returns, per position j (0-based index), the list of (a_{r,j}, a_hat_{r,j}, y)
+    in request order.
+    """
+    B = len(windows)
+    out = [[] for _ in range(gamma)]
+    for r in range(B):
+        v = gamma if mode == CAP_ACCEPT else int(windows[r])
+        for j in range(v):
+            y = 1 if j + 1 <= int(cap_len[r]) else 0
+            out[j].append((F32(survival[r, j]), F32(a_hat[r, j]), y))
+    return out
+
+
+def ece(samples, n_bins):
+    """Expected calibration error of the calibrated survival a_hat against the
+    labels, over all positions' samples: equal-width bins over [0, 1], bin of p
+    = min(floor(p * n_bins), n_bins - 1), and
+    ECE = sum_b (n_b / N) |mean(y in b) - mean(p in b)| = (1/N) sum_b |sum y - sum p|.
+    fp64 sums.  Returns (ece, counts, sum_p, sum_y) per bin; ece = 0 when N = 0.
+    """
+    cnt = np.zeros(n_bins, dtype=np.int64)
+    sp = np.zeros(n_bins, dtype=np.float64)
+    sy = np.zeros(n_bins, dtype=np.float64)
+    for pos in samples:
+        for (_, p, y) in pos:
+            b = min(int(math.floor(float(p) * n_bins)), n_bins - 1)
+            cnt[b] += 1
+            sp[b] += float(p)
+            sy[b] += y
+    N = int(cnt.sum())
+    e = float(np.abs(sy - sp).sum() / N) if N else 0.0
+    return e, cnt, sp, sy
+
+
+STS_LOG_BETA_RANGE = (-math.log(64.0), math.log(64.0))
+
+
+def sts_fit(samples_j, iters):
+    """Refit one position's STS temperature from labelled samples ([notes] §07,
+    Sequential Temperature Scaling: a_hat = sigmoid(logit(a) / T)).
+
+    T minimises the binary cross-entropy of sigmoid(beta z) against the labels,
+    beta = 1/T, z = logit(a) = log a - log1p(-a) (samples with a <= 0 or a >= 1
+    have an infinite logit and are left out).  The loss is convex in beta, so its
+    derivative g(beta) = sum (sigmoid(beta z) - y) z is increasing; the root is
+    found by `iters` bisections of log beta over [log 1/64, log 64] (beta outside
+    the range is clamped to it): g(mid) > 0 moves the upper end, else the lower.
+    fp64 throughout.  No usable sample: T = 1.
+    """
+    zs, ys = [], []
+    for (a, _, y) in samples_j:
+        a = float(a)
+        if 0.0 < a < 1.0:
+            zs.append(math.log(a) - math.log1p(-a))
+            ys.append(float(y))
+    if not zs:
+        return F32(1.0)
+    z = np.array(zs, dtype=np.float64)
+    y = np.array(ys, dtype=np.float64)
+    lo, hi = STS_LOG_BETA_RANGE
+    for _ in range(iters):
+        mid = 0.5 * (lo + hi)
+        beta = math.exp(mid)
+        g = 0.0
+        for zi, yi in zip(z, y):                     # plain loop: order is sample order
+            t = beta * zi
+            sig = 1.0 / (1.0 + math.exp(-t)) if t >= 0 else math.exp(t) / (1.0 + math.exp(t))
+            g += (sig - yi) * zi
+        if g > 0.0:
+            hi = mid
+        else:
+            lo = mid
+    return F32(1.0 / math.exp(0.5 * (lo + hi)))
+
+
+# ----------------------------------------------------------------------------
+# 8. The whole step
 # ----------------------------------------------------------------------------
 
 def step(inp: dict, mode: int, packed: dict | None = None, with_attention: bool = True,

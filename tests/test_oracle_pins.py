@@ -606,3 +606,84 @@ def test_generator_uniforms_are_exact_and_open():
         assert float(u.min()) > 0.0 and float(u.max()) < 1.0
     e = inp["exp_noise"]
     assert torch.all(torch.isfinite(e)) and float(e.min()) > 0.0
+
+
+# ---------------------------------------------------------------- calibration tooling
+
+def test_calib_samples_label_rule():
+    """Verified positions only; label 1 iff the accepted prefix reaches the position."""
+    a = np.array([[0.9, 0.8, 0.5], [0.7, 0.6, 0.2]], np.float32)
+    ah = a * np.float32(0.5)
+    s = O.calib_samples(a, ah, np.array([2, 0], np.int32), np.array([1, 0], np.int32),
+                        O.COMPACT, 3)
+    assert [[y for (_, _, y) in pos] for pos in s] == [[1], [0], []]
+    assert s[0][0][0] == np.float32(0.9) and s[0][0][1] == np.float32(0.45)
+    # cap-accept verifies the whole block: every position of every request is labelled
+    s2 = O.calib_samples(a, ah, np.array([2, 0], np.int32), np.array([2, 0], np.int32),
+                         O.CAP_ACCEPT, 3)
+    assert [[y for (_, _, y) in pos] for pos in s2] == [[1, 0], [1, 0], [0, 0]]
+
+
+def test_ece_hand_example_and_one_bin_identity():
+    p = [0.1, 0.45, 0.55, 0.95]
+    y = [0, 0, 1, 1]
+    samples = [[(np.float32(0.5), np.float32(pi), yi) for pi, yi in zip(p, y)]]
+    e, cnt, sp, sy = O.ece(samples, 2)
+    # bin 0: p 0.1, 0.45 (sum 0.55), y 0;  bin 1: p 0.55, 0.95 (sum 1.5), y 2
+    assert cnt.tolist() == [2, 2] and sy.tolist() == [0.0, 2.0]
+    assert abs(e - (0.55 + 0.5) / 4) < 1e-7
+    # one bin: |mean(y) - mean(p)|
+    e1, _, _, _ = O.ece(samples, 1)
+    assert abs(e1 - abs(2 - sum(float(np.float32(x)) for x in p)) / 4) < 1e-12
+    # bin edges: p = 1 falls in the last bin, p = 0.5 in the upper of two
+    e2, c2, _, _ = O.ece([[(0.5, np.float32(1.0), 1), (0.5, np.float32(0.5), 1)]], 2)
+    assert c2.tolist() == [0, 2] and abs(e2 - 0.25) < 1e-12
+    assert O.ece([[]], 10)[0] == 0.0
+
+
+def test_ece_of_calibrated_predictions_is_small():
+    rng = np.random.default_rng(31)
+    p = rng.uniform(0, 1, 200_000).astype(np.float32)
+    y = (rng.uniform(0, 1, p.size) < p).astype(int)
+    e, _, _, _ = O.ece([[(0.5, pi, yi) for pi, yi in zip(p, y)]], 10)
+    assert e < 0.01
+    # a miscalibrated predictor (p^2 against labels drawn with p) has a clearly larger ECE
+    e_bad, _, _, _ = O.ece([[(0.5, np.float32(pi * pi), yi) for pi, yi in zip(p, y)]], 10)
+    assert e_bad > 0.1
+
+
+def _logit_samples(z, y):
+    a = (1.0 / (1.0 + np.exp(-z))).astype(np.float32)
+    return [(ai, ai, int(yi)) for ai, yi in zip(a, y)]
+
+
+def test_sts_fit_recovers_the_temperature_and_the_optimum():
+    """Labels drawn with probability sigmoid(z / T_true): the refit is the exact
+    minimiser of the binary cross-entropy (checked against scipy's bounded scalar
+    minimiser) and lies within a few standard errors of T_true."""
+    from scipy.optimize import minimize_scalar
+    rng = np.random.default_rng(32)
+    T_true = 1.7
+    z = rng.normal(0.0, 2.5, 20_000)
+    y = (rng.uniform(0, 1, z.size) < 1.0 / (1.0 + np.exp(-z / T_true))).astype(int)
+    samples = _logit_samples(z, y)
+    T = float(O.sts_fit(samples, 60))
+    za = np.array([float(np.log(a) - np.log1p(-a)) for (a, _, _) in samples])
+
+    def nll(lb):
+        t = np.exp(lb) * za
+        return float(np.sum(np.logaddexp(0.0, t) - y * t))
+    res = minimize_scalar(nll, bounds=(-3, 3), method="bounded", options={"xatol": 1e-12})
+    assert abs(T - float(np.exp(-res.x))) < 1e-5 * T
+    assert abs(T - T_true) < 0.1 * T_true
+
+
+def test_sts_fit_degenerate_cases():
+    # no sample, or only a = 1 (infinite logit): the identity temperature
+    assert O.sts_fit([], 40) == np.float32(1.0)
+    assert O.sts_fit([(np.float32(1.0), np.float32(1.0), 1)], 40) == np.float32(1.0)
+    # every positive logit accepted and every negative one rejected: the sharpest
+    # temperature the range allows (beta clamped at 64)
+    s = [(np.float32(0.8), np.float32(0.8), 1), (np.float32(0.3), np.float32(0.3), 0)]
+    T = float(O.sts_fit(s, 60))
+    assert abs(T - 1.0 / 64) < 1e-6
