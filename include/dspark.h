@@ -78,6 +78,7 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
 #define DSPARK_MAX_GAMMA    32     /* draft block length                         */
 #define DSPARK_MAX_CANDS    4096   /* B * gamma for the scheduler's sort          */
 #define DSPARK_MAX_TIERS    64
+#define DSPARK_MAX_ECE_BINS 256
 
 const char* dspark_status_string(int status);
 
@@ -87,6 +88,21 @@ int dspark_read_device_error(void* stream);
 
 /* Number of SMs the persistent kernels size their grids by (current device). */
 int dspark_num_sms(void);
+
+/* Time limit of each bounded in-kernel wait of the acceptance pass on the current
+ * device, for calls enqueued after this one (ns; 0 restores the default, 2 s).  A
+ * wait that runs past it sets DSPARK_DEVERR_WAIT_TIMEOUT and makes its kernel stop:
+ * every role leaves its loop, the copies already issued are waited for (always on
+ * the 2 s limit), and the kernel returns; the outputs of that call are undefined
+ * and the next call is unaffected.  (The attention kernels keep their fixed 2 s
+ * limit.)  A calibration of failure handling, not a tuning knob. */
+int dspark_set_wait_limit_ns(unsigned long long ns);
+/* Failure-detection test hook: while on (for calls enqueued after it, on the
+ * current device), the acceptance pass first waits on a barrier nothing arrives at,
+ * so that its bounded wait must run out (after the limit above) and the timeout
+ * path runs: DSPARK_DEVERR_WAIT_TIMEOUT, every role stops, nothing is left in
+ * flight.  Off by default; it never faults or hangs the device. */
+int dspark_set_wait_probe(int on);
 
 /* ---------------------------------------------------------------------------
  * dspark_schedule -- per-request verify windows.
@@ -102,6 +118,8 @@ int dspark_num_sms(void);
  *   mode        dspark_mode; STATIC sets every window to gamma
  *   windows     int32 [B]  out: verified drafts w_r in [0, gamma]
  *   a_hat       fp32 [B, gamma]  out: calibrated survival (non-increasing in j)
+ *   survival    fp32 [B, gamma]  out, nullable: the uncalibrated prefix survival
+ *               a_j (what dspark_calib_collect records for a temperature refit)
  *   M_out       int32 [1]  out: B + sum w_r
  *   E_out       fp64 [1]   out: expected committed tokens B + sum of chosen a_hat
  *
@@ -115,8 +133,8 @@ int dspark_num_sms(void);
  * ------------------------------------------------------------------------- */
 int dspark_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
                     const float* cost_table, int cost_len, int B, int gamma, int max_tokens,
-                    int mode, int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
-                    void* stream);
+                    int mode, int32_t* windows, float* a_hat, float* survival, int32_t* M_out,
+                    double* E_out, void* stream);
 
 /* ---------------------------------------------------------------------------
  * dspark_pack -- head-to-tail ragged packing ([lesson] "Ragged verify under full
@@ -325,6 +343,51 @@ int dspark_compact(const void* k_new, const void* v_new, int row_bytes, int max_
                    void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Calibration of the confidence head from the step's own accept outcomes
+ * ([csdn] 5. "可观测性": per-request confidence and calibration metrics such as
+ * ECE; [notes] 07: a_j predicts that prefix 1..j is accepted, and Sequential
+ * Temperature Scaling a_hat_j = sigmoid(logit(a_j) / T_j) calibrates it).
+ *
+ * Sample store (device, caller-owned, per draft position j = 0..gamma-1, each
+ * region `capacity` entries): s_a, s_ahat fp32 [gamma, capacity], s_y int8
+ * [gamma, capacity], count int32 [gamma] (the caller zeroes count once).
+ *
+ * dspark_calib_collect appends one step's samples: every verified position j of
+ * request r (j < windows[r], or j < gamma in CAP_ACCEPT mode; in request order)
+ * adds (survival[r][j], a_hat[r][j], y = [j + 1 <= cap_len[r]]) at index count[j]
+ * of position j's region (dropped once the region is full; count keeps counting).
+ * survival/a_hat are dspark_schedule's outputs, cap_len dspark_accept's.  One CTA;
+ * B <= 1024.  CAP_ACCEPT steps give unbiased samples (every position verified).
+ *
+ * dspark_calib_ece: expected calibration error of the stored a_hat against y over
+ * all stored samples: equal-width bins b = min(floor(a_hat * n_bins), n_bins - 1),
+ * bin_n int32 / bin_p fp64 (sum of a_hat) / bin_y fp64 (sum of y) [n_bins], and
+ * ece fp64 [1] = (1/N) sum_b |bin_y - bin_p| (0 with no sample).  n_bins <= 256.
+ * The bin sums of a_hat add each a_hat rounded to a multiple of 2^-32, exactly
+ * (fixed point within a CTA, fp64 across CTAs while a bin's sum stays below 2^21):
+ * the result does not depend on the order of the atomics.
+ *
+ * dspark_sts_fit: per position, the temperature T_j minimising the binary
+ * cross-entropy of sigmoid(logit(a) / T) against y over the stored samples (those
+ * with 0 < a < 1): `iters` bisections of log(1/T) in [log 1/64, log 64] on the
+ * sign of the derivative sum (sigmoid(z/T) - y) z, z = logit(a) (evaluated in fp64,
+ * kept as fp32; the sigmoid in fp32, the sum in fp32 per thread and fp64 across
+ * threads); temps fp32 [gamma] out (1 for a position with no usable sample).
+ * Workspace: at least dspark_sts_fit_workspace_size(gamma, capacity) bytes,
+ * 4-byte aligned.
+ * ------------------------------------------------------------------------- */
+int dspark_calib_collect(const float* survival, const float* a_hat, const int32_t* windows,
+                         const int32_t* cap_len, int mode, int B, int gamma, float* s_a,
+                         float* s_ahat, int8_t* s_y, int32_t* count, int capacity, void* stream);
+int dspark_calib_ece(const float* s_ahat, const int8_t* s_y, const int32_t* count, int capacity,
+                     int gamma, int n_bins, int32_t* bin_n, double* bin_p, double* bin_y,
+                     double* ece, void* stream);
+size_t dspark_sts_fit_workspace_size(int gamma, int capacity);
+int dspark_sts_fit(const float* s_a, const int8_t* s_y, const int32_t* count, int capacity,
+                   int gamma, int iters, float* temps, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/* ---------------------------------------------------------------------------
  * dspark_step_graph -- the whole verification step as one CUDA graph, with the
  * captured tier chosen on the device ([lesson] "Ragged verify under full CUDA
  * graphs": the packed batch is rounded up to a captured tier and that tier's
@@ -391,6 +454,7 @@ typedef struct dspark_step_desc {
   /* outputs */
   int32_t* windows;
   float* a_hat;
+  float* survival;            /* nullable */
   int32_t* M;
   double* E;
   int32_t* cu_seqlens;

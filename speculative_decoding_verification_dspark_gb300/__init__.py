@@ -17,7 +17,7 @@ __all__ = [
     "COMPACT", "STATIC", "CAP_ACCEPT", "F32", "BF16", "DSparkError", "lib", "load",
     "schedule", "pack", "verify_attn", "accept", "accept_noalloc", "compact", "read_device_error",
     "verify_attn_workspace_size", "accept_workspace_size", "compact_workspace_size",
-    "VerifyStep", "StepGraph", "DEVERR",
+    "VerifyStep", "StepGraph", "CalibStore", "DEVERR",
 ]
 
 COMPACT, STATIC, CAP_ACCEPT = 0, 1, 2
@@ -39,7 +39,13 @@ _SIGNATURES = {
     "dspark_status_string": (ctypes.c_char_p, [_I]),
     "dspark_read_device_error": (_I, [_P]),
     "dspark_num_sms": (_I, []),
-    "dspark_schedule": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "dspark_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
+    "dspark_set_wait_probe": (_I, [_I]),
+    "dspark_schedule": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "dspark_calib_collect": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _P]),
+    "dspark_calib_ece": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "dspark_sts_fit_workspace_size": (_Z, [_I, _I]),
+    "dspark_sts_fit": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
     "dspark_pack": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dspark_verify_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "dspark_verify_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I,
@@ -123,13 +129,67 @@ def num_sms() -> int:
     return lib().dspark_num_sms()
 
 
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of the acceptance pass's bounded waits on the current device (0: 2 s)."""
+    _check("dspark_set_wait_limit_ns", lib().dspark_set_wait_limit_ns(int(ns)))
+
+
+def set_wait_probe(on: bool) -> None:
+    """Test hook: the acceptance pass first waits on a barrier nothing arrives at."""
+    _check("dspark_set_wait_probe", lib().dspark_set_wait_probe(1 if on else 0))
+
+
 def schedule(conf, conf_is_logit, sts_temp, cost_table, max_tokens, mode, windows, a_hat, M_out,
-             E_out, stream=None):
+             E_out, stream=None, survival=None):
+    """``survival``: optional fp32 [B, gamma] output of the uncalibrated prefix survival."""
     B, gamma = conf.shape
     _check("dspark_schedule", lib().dspark_schedule(
         _ptr(conf), int(conf_is_logit), _ptr(sts_temp), _ptr(cost_table), cost_table.numel(), B,
-        gamma, int(max_tokens), int(mode), _ptr(windows), _ptr(a_hat), _ptr(M_out), _ptr(E_out),
-        _stream(stream)))
+        gamma, int(max_tokens), int(mode), _ptr(windows), _ptr(a_hat), _ptr(survival),
+        _ptr(M_out), _ptr(E_out), _stream(stream)))
+
+
+class CalibStore:
+    """Device store of labelled accept outcomes per draft position (dspark_calib_*):
+    ``collect`` after a step, ``ece`` and ``sts_fit`` on demand."""
+
+    def __init__(self, gamma, capacity, device="cuda"):
+        dev = torch.device(device)
+        self.gamma, self.capacity = gamma, capacity
+        self.s_a = torch.zeros(gamma, capacity, dtype=torch.float32, device=dev)
+        self.s_ahat = torch.zeros(gamma, capacity, dtype=torch.float32, device=dev)
+        self.s_y = torch.zeros(gamma, capacity, dtype=torch.int8, device=dev)
+        self.count = torch.zeros(gamma, dtype=torch.int32, device=dev)
+        self.ws = torch.empty(lib().dspark_sts_fit_workspace_size(gamma, capacity),
+                              dtype=torch.uint8, device=dev)
+
+    def collect(self, survival, a_hat, windows, cap_len, mode, stream=None):
+        B = windows.numel()
+        _check("dspark_calib_collect", lib().dspark_calib_collect(
+            _ptr(survival), _ptr(a_hat), _ptr(windows), _ptr(cap_len), int(mode), B, self.gamma,
+            _ptr(self.s_a), _ptr(self.s_ahat), _ptr(self.s_y), _ptr(self.count), self.capacity,
+            _stream(stream)))
+
+    def ece(self, n_bins, stream=None):
+        """(ece fp64 [1], bin counts, bin sums of a_hat, bin sums of y) on the device."""
+        dev = self.count.device
+        bn = torch.zeros(n_bins, dtype=torch.int32, device=dev)
+        bp = torch.zeros(n_bins, dtype=torch.float64, device=dev)
+        by = torch.zeros(n_bins, dtype=torch.float64, device=dev)
+        e = torch.zeros(1, dtype=torch.float64, device=dev)
+        _check("dspark_calib_ece", lib().dspark_calib_ece(
+            _ptr(self.s_ahat), _ptr(self.s_y), _ptr(self.count), self.capacity, self.gamma,
+            int(n_bins), _ptr(bn), _ptr(bp), _ptr(by), _ptr(e), _stream(stream)))
+        return e, bn, bp, by
+
+    def sts_fit(self, iters, temps=None, stream=None):
+        """Refitted STS temperatures fp32 [gamma] (device)."""
+        if temps is None:
+            temps = torch.empty(self.gamma, dtype=torch.float32, device=self.count.device)
+        _check("dspark_sts_fit", lib().dspark_sts_fit(
+            _ptr(self.s_a), _ptr(self.s_y), _ptr(self.count), self.capacity, self.gamma,
+            int(iters), _ptr(temps), _ptr(self.ws), self.ws.numel(), _stream(stream)))
+        return temps
 
 
 def _host_ptr(t):
@@ -257,7 +317,8 @@ class StepDesc(ctypes.Structure):
         + [(n, _P) for n in ("conf", "sts_temp", "cost_table", "draft_tok", "q", "k_new", "v_new",
                              "p_target", "p_draft", "uniforms", "exp_noise", "free_pages",
                              "page_table", "ctx_len", "anchor", "free_top", "k_cache", "v_cache",
-                             "windows", "a_hat", "M", "E", "cu_seqlens", "M_pack", "tier",
+                             "windows", "a_hat", "survival", "M", "E", "cu_seqlens", "M_pack",
+                             "tier",
                              "row_req", "row_pos", "row_tok", "out", "lse", "accept_len",
                              "cap_len", "out_tok", "cstar", "fallback", "committed",
                              "n_committed", "tier_host", "body_log")]
@@ -318,6 +379,7 @@ class VerifyStep:
         i32 = dict(dtype=torch.int32, device=dev)
         self.windows = torch.zeros(B, **i32)
         self.a_hat = torch.zeros(B, gamma, dtype=torch.float32, device=dev)
+        self.survival = torch.zeros(B, gamma, dtype=torch.float32, device=dev)
         self.M = torch.zeros(1, **i32)
         self.E = torch.zeros(1, dtype=torch.float64, device=dev)
         self.cu_seqlens = torch.zeros(B + 1, **i32)
@@ -345,7 +407,8 @@ class VerifyStep:
 
     def schedule(self, inp, mode, stream=None):
         schedule(inp["conf"], inp["conf_is_logit"], inp["sts_temp"], inp["cost_table"],
-                 inp["max_tokens"], mode, self.windows, self.a_hat, self.M, self.E, stream)
+                 inp["max_tokens"], mode, self.windows, self.a_hat, self.M, self.E, stream,
+                 survival=self.survival)
 
     def pack(self, inp, mode, stream=None):
         pack(self.windows, inp["ctx_len"], inp["anchor"], inp["draft_tok"], inp["tiers"], mode,
@@ -407,7 +470,8 @@ class VerifyStep:
                   "free_top", "k_cache"):
             setattr(d, k, _ptr(inp[k]))
         d.v_new, d.v_cache = _ptr(inp.get("v_new")), _ptr(inp.get("v_cache"))
-        for k in ("windows", "a_hat", "M", "E", "cu_seqlens", "M_pack", "tier", "row_req",
+        for k in ("windows", "a_hat", "survival", "M", "E", "cu_seqlens", "M_pack", "tier",
+                  "row_req",
                   "row_pos", "row_tok", "out", "lse", "accept_len", "cap_len", "out_tok", "cstar",
                   "fallback", "committed", "n_committed"):
             setattr(d, k, _ptr(getattr(self, k)))

@@ -30,6 +30,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -156,7 +158,7 @@ constexpr int kNoiseBytes = 64 * 1024;        // noise ring, sampled rows only
 constexpr int kConsumerWarps = 16;
 constexpr int kProducerWarp = 16, kReducerWarp = 17;
 constexpr int kVocabCtaThreads = 18 * 32;
-constexpr uint64_t kVocabWaitNs = 2000000000ull;
+constexpr uint64_t kDrainWaitNs = 2000000000ull;  // draining own copies: always 2 s
 
 struct WarpPart {
   double l1;
@@ -171,18 +173,21 @@ struct VocabSmem {
   WarpPart red[2][kConsumerWarps];
   int4 meta[kVStages];  // item, sub-chunk | sub-chunks << 8, request, row flags
   uint64_t full[kVStages], empty[kVStages], nempty[4], red_full[2], red_free[2];
+  uint64_t never;  // a barrier nothing arrives at (the wait probe)
   int abort_flag;
 };
 
+// Bounded wait: false once this CTA aborts (another role's wait ran out, or this
+// one ran past wait_ns, which then raises DSPARK_DEVERR_WAIT_TIMEOUT).
 __device__ __forceinline__ bool vwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                      unsigned int* err) {
+                                      unsigned int* err, uint64_t wait_ns) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   uint32_t n = 0;
   while (!ptx::mbar_try_wait(bar, parity)) {
     if ((++n & 31u) == 0) {
       if (*abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > kVocabWaitNs) {
+      if (ptx::globaltimer_ns() - t0 > wait_ns) {
         *abort_flag = 1;
         raise_error(err, DSPARK_DEVERR_WAIT_TIMEOUT);
         return false;
@@ -197,8 +202,7 @@ struct RowWork {
   int r, j;
   bool l1, samp, residual, need_d;
 };
-__device__ __forceinline__ RowWork row_work(const int2* row_desc, int row) {
-  const int2 d = row_desc[row];
+__device__ __forceinline__ RowWork decode_row(int2 d) {
   RowWork w;
   w.r = d.x;
   w.j = d.y & 0xffff;
@@ -257,7 +261,8 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
                         const float* __restrict__ exp_noise, int V, int n_chunks,
                         const int32_t* __restrict__ cu, int B, int gamma, int max_rows,
                         const int2* __restrict__ row_desc, Partial* __restrict__ part,
-                        int* __restrict__ claim, unsigned int* __restrict__ err) {
+                        int* __restrict__ claim, unsigned int* __restrict__ err,
+                        uint64_t wait_ns, int probe) {
   extern __shared__ __align__(128) uint8_t vsmem_raw[];
   VocabSmem& S = *reinterpret_cast<VocabSmem*>(vsmem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -280,6 +285,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
       ptx::mbar_init(ptx::smem_addr(&S.red_full[p]), kConsumerWarps);
       ptx::mbar_init(ptx::smem_addr(&S.red_free[p]), 1);
     }
+    ptx::mbar_init(ptx::smem_addr(&S.never), 1);
     ptx::fence_mbar_init();
   }
   __syncthreads();
@@ -297,16 +303,25 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
     // sampled rows then balance out); each stage carries its item in meta[].
     if (lane == 0) {
       int g = 0, gn = 0;  // main-ring and noise-ring sub-chunks issued
-      bool ok = true;
-      long long item = atomicAdd(claim, 1);
+      bool ok = true, marker = false;
+      // the wait probe (a failure-detection test): a wait that must run out
+      if (probe) ok = vwait(ptx::smem_addr(&S.never), 0, abort_flag, err, wait_ns);
+      long long item = ok ? atomicAdd(claim, 1) : n_items;
       while (ok) {
         long long next = n_items;
         RowWork w{};
         bool work = false;
+        int2 desc = make_int2(0, 0);
         if (item < n_items) {
           next = atomicAdd(claim, 1);  // taken ahead: its latency hides behind this item
-          w = row_work(row_desc, static_cast<int>(item / n_chunks));
+          desc = row_desc[item / n_chunks];
+          w = decode_row(desc);
           work = w.l1 || w.samp;
+          if (w.r < 0 || w.r >= B || w.j < 0 || w.j > gamma) {
+            // not a descriptor the test kernel writes: touch no row, report
+            raise_error(err, DSPARK_DEVERR_BAD_INPUT);
+            work = false;
+          }
         }
         const int s = g % kVStages;
         if (item < n_items && !work) {  // nothing to do on this row: next claim
@@ -318,7 +333,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
         for (int sb = 0; sb < ns; ++sb, ++g) {
           const int st = g % kVStages;
           if (g >= kVStages &&
-              !vwait(ptx::smem_addr(&S.empty[st]), ((g / kVStages) - 1) & 1, abort_flag, err)) {
+              !vwait(ptx::smem_addr(&S.empty[st]), ((g / kVStages) - 1) & 1, abort_flag, err, wait_ns)) {
             ok = false;
             break;
           }
@@ -326,12 +341,13 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
           if (item >= n_items) {  // end marker: a stage without data
             S.meta[st] = make_int4(-1, 0, 0, 0);
             ptx::mbar_arrive(full);
+            marker = true;
             ok = false;  // done
             break;
           }
           const int sn = gn % kNStages;
           if (w.samp && gn >= kNStages &&
-              !vwait(ptx::smem_addr(&S.nempty[sn]), ((gn / kNStages) - 1) & 1, abort_flag, err)) {
+              !vwait(ptx::smem_addr(&S.nempty[sn]), ((gn / kNStages) - 1) & 1, abort_flag, err, wait_ns)) {
             ok = false;
             break;
           }
@@ -342,7 +358,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
           const uint32_t len = static_cast<uint32_t>(min(kSubT, V - v0));
           const uint32_t base = ptx::smem_addr(S.stage[st]);
           const uint32_t bytes = len * ES * (w.need_d ? 2u : 1u) + (w.samp ? len * 4u : 0u);
-          S.meta[st] = make_int4(static_cast<int>(item), sb | (ns << 8), w.r, row_desc[row].y);
+          S.meta[st] = make_int4(static_cast<int>(item), sb | (ns << 8), w.r, desc.y);
           ptx::mbar_expect_tx(full, bytes);
           ptx::bulk_load_g2s(base, pt_row + v0, len * ES, full);
           if (w.need_d) ptx::bulk_load_g2s(base + kSub * 4, pd_row + v0, len * ES, full);
@@ -355,6 +371,23 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
         (void)s;
         item = next;
       }
+      // Never leave copies in flight: wait for the last data phase of every ring slot
+      // (on the fixed drain limit, also after an abort).  The slot the end marker
+      // reused held a stage the consumers had already released (the empty wait
+      // before the marker), and its barrier has moved past that phase: skipped.
+      const int first = g - kVStages > 0 ? g - kVStages : 0;
+      for (int gg = first; gg < g; ++gg) {
+        if (marker && gg % kVStages == g % kVStages) continue;
+        const uint32_t bar = ptx::smem_addr(&S.full[gg % kVStages]);
+        const uint32_t par = (gg / kVStages) & 1;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar, par)) {
+          if (ptx::globaltimer_ns() - t0 > kDrainWaitNs) {
+            raise_error(err, DSPARK_DEVERR_WAIT_TIMEOUT);
+            break;
+          }
+        }
+      }
     }
   } else if (warp == kReducerWarp) {
     // the consumer warps' results of an item -> its partial (fixed order: deterministic)
@@ -362,7 +395,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
     bool ok = true;
     while (ok) {
       const int p = n_it & 1;
-      ok = vwait(ptx::smem_addr(&S.red_full[p]), (n_it >> 1) & 1, abort_flag, err);
+      ok = vwait(ptx::smem_addr(&S.red_full[p]), (n_it >> 1) & 1, abort_flag, err, wait_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       const int item = S.red[p][0].pad[0];
@@ -393,14 +426,14 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
     int ibest = kNoIndex;
     while (ok) {
       const int s = g % kVStages;
-      ok = vwait(ptx::smem_addr(&S.full[s]), (g / kVStages) & 1, abort_flag, err);
+      ok = vwait(ptx::smem_addr(&S.full[s]), (g / kVStages) & 1, abort_flag, err, wait_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       const int4 m = S.meta[s];
       if (m.x < 0) {  // end: tell the reducer
         const int p = n_it & 1;
         if (n_it >= 2) {
-          ok = vwait(ptx::smem_addr(&S.red_free[p]), ((n_it >> 1) - 1) & 1, abort_flag, err);
+          ok = vwait(ptx::smem_addr(&S.red_free[p]), ((n_it >> 1) - 1) & 1, abort_flag, err, wait_ns);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
         }
@@ -510,7 +543,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
       const int p = n_it & 1;
       // slot p was last read by the reducer for item n_it - 2
       if (n_it >= 2) {
-        ok = vwait(ptx::smem_addr(&S.red_free[p]), ((n_it >> 1) - 1) & 1, abort_flag, err);
+        ok = vwait(ptx::smem_addr(&S.red_free[p]), ((n_it >> 1) - 1) & 1, abort_flag, err, wait_ns);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
@@ -596,6 +629,42 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The acceptance pass's wait limit per device (0: the default 2 s), and the wait
+// probe (a failure-detection test: the pass first waits on a barrier nothing
+// arrives at).
+namespace {
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+std::atomic<unsigned long long> g_accept_wait_ns[kMaxDevices];
+std::atomic<int> g_accept_wait_probe[kMaxDevices];
+}  // namespace
+
+uint64_t accept_wait_limit_ns() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kDefaultWaitNs;
+  const unsigned long long v = g_accept_wait_ns[dev].load(std::memory_order_relaxed);
+  return v ? v : kDefaultWaitNs;
+}
+
+int set_accept_wait_limit_ns(unsigned long long ns) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSPARK_ECUDA;
+  g_accept_wait_ns[dev].store(ns, std::memory_order_relaxed);
+  return DSPARK_OK;
+}
+
+int accept_wait_probe() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return g_accept_wait_probe[dev].load(std::memory_order_relaxed);
+}
+
+int set_accept_wait_probe(int on) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSPARK_ECUDA;
+  g_accept_wait_probe[dev].store(on ? 1 : 0, std::memory_order_relaxed);
+  return DSPARK_OK;
+}
+
 bool vocab_configure() {
   static PerDevice<bool> done;
   return once_per_device(done, false, [] {
@@ -647,6 +716,8 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
   if (!vocab_configure()) return DSPARK_ECUDA;
+  const uint64_t wait_ns = accept_wait_limit_ns();
+  const int probe = accept_wait_probe();
   if (pdt == DSPARK_F32) {
     const float* t = static_cast<const float*>(p_t);
     const float* d = static_cast<const float*>(p_d);
@@ -656,7 +727,7 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
       return DSPARK_ECUDA;
     if (launch_pdl(accept_vocab_kernel<float>, dim3((int)grid), dim3(kVocabCtaThreads),
                    sizeof(VocabSmem), stream, t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows,
-                   row_desc, part, claim, err) != cudaSuccess)
+                   row_desc, part, claim, err, wait_ns, probe) != cudaSuccess)
       return DSPARK_ECUDA;
   } else {
     const __nv_bfloat16* t = static_cast<const __nv_bfloat16*>(p_t);
@@ -667,7 +738,7 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
       return DSPARK_ECUDA;
     if (launch_pdl(accept_vocab_kernel<__nv_bfloat16>, dim3((int)grid), dim3(kVocabCtaThreads),
                    sizeof(VocabSmem), stream, t, d, exp_noise, V, n_chunks, cu, B, gamma, max_rows,
-                   row_desc, part, claim, err) != cudaSuccess)
+                   row_desc, part, claim, err, wait_ns, probe) != cudaSuccess)
       return DSPARK_ECUDA;
   }
   cudaError_t e;

@@ -138,6 +138,10 @@ const char* dspark_status_string(int status) {
 
 int dspark_num_sms(void) { return num_sms_cached(); }
 
+int dspark_set_wait_limit_ns(unsigned long long ns) { return set_accept_wait_limit_ns(ns); }
+
+int dspark_set_wait_probe(int on) { return set_accept_wait_probe(on); }
+
 int dspark_read_device_error(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned int* w = device_error_word();
@@ -151,8 +155,8 @@ int dspark_read_device_error(void* stream) {
 
 int dspark_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
                     const float* cost_table, int cost_len, int B, int gamma, int max_tokens,
-                    int mode, int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
-                    void* stream) {
+                    int mode, int32_t* windows, float* a_hat, float* survival, int32_t* M_out,
+                    double* E_out, void* stream) {
   CHECK(conf && sts_temp && cost_table && windows && a_hat && M_out && E_out, DSPARK_EINVAL);
   CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
   CHECK(B * gamma <= DSPARK_MAX_CANDS, DSPARK_EINVAL);
@@ -165,7 +169,8 @@ int dspark_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
   int rc = device_ok();
   if (rc != DSPARK_OK) return rc;
   return launch_schedule(conf, conf_is_logit ? 1 : 0, sts_temp, cost_table, B, gamma, max_tokens,
-                         mode, windows, a_hat, M_out, E_out, static_cast<cudaStream_t>(stream));
+                         mode, windows, a_hat, survival, M_out, E_out,
+                         static_cast<cudaStream_t>(stream));
 }
 
 int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
@@ -347,6 +352,50 @@ int dspark_compact(const void* k_new, const void* v_new, int row_bytes, int max_
                         gamma, page_size, max_pages, n_pages, page_table, ctx_len, anchor,
                         free_pages, free_top, k_cache, v_cache, committed, n_committed, workspace,
                         static_cast<cudaStream_t>(stream));
+}
+
+int dspark_calib_collect(const float* survival, const float* a_hat, const int32_t* windows,
+                         const int32_t* cap_len, int mode, int B, int gamma, float* s_a,
+                         float* s_ahat, int8_t* s_y, int32_t* count, int capacity, void* stream) {
+  CHECK(survival && a_hat && windows && cap_len && s_a && s_ahat && s_y && count, DSPARK_EINVAL);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
+  CHECK(mode >= DSPARK_COMPACT && mode <= DSPARK_CAP_ACCEPT, DSPARK_EINVAL);
+  CHECK(capacity >= 1, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  return launch_calib_collect(survival, a_hat, windows, cap_len, mode, B, gamma, s_a, s_ahat, s_y,
+                              count, capacity, static_cast<cudaStream_t>(stream));
+}
+
+int dspark_calib_ece(const float* s_ahat, const int8_t* s_y, const int32_t* count, int capacity,
+                     int gamma, int n_bins, int32_t* bin_n, double* bin_p, double* bin_y,
+                     double* ece, void* stream) {
+  CHECK(s_ahat && s_y && count && bin_n && bin_p && bin_y && ece, DSPARK_EINVAL);
+  CHECK(gamma >= 1 && gamma <= DSPARK_MAX_GAMMA && capacity >= 1, DSPARK_EINVAL);
+  CHECK(n_bins >= 1 && n_bins <= DSPARK_MAX_ECE_BINS, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  return launch_calib_ece(s_ahat, s_y, count, capacity, gamma, n_bins, bin_n, bin_p, bin_y, ece,
+                          static_cast<cudaStream_t>(stream));
+}
+
+size_t dspark_sts_fit_workspace_size(int gamma, int capacity) {
+  if (gamma < 1 || capacity < 1) return 0;
+  return static_cast<size_t>(gamma) * static_cast<size_t>(capacity) * sizeof(float);
+}
+
+int dspark_sts_fit(const float* s_a, const int8_t* s_y, const int32_t* count, int capacity,
+                   int gamma, int iters, float* temps, void* workspace, size_t ws_bytes,
+                   void* stream) {
+  CHECK(s_a && s_y && count && temps && workspace, DSPARK_EINVAL);
+  CHECK(gamma >= 1 && gamma <= DSPARK_MAX_GAMMA && capacity >= 1, DSPARK_EINVAL);
+  CHECK(iters >= 0 && iters <= 1000, DSPARK_EINVAL);
+  CHECK((reinterpret_cast<uintptr_t>(workspace) & 3u) == 0, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  CHECK(ws_bytes >= dspark_sts_fit_workspace_size(gamma, capacity), DSPARK_ENOSPACE);
+  return launch_sts_fit(s_a, s_y, count, capacity, gamma, iters, static_cast<float*>(workspace),
+                        temps, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -17,8 +17,8 @@ struct TierSel {
 
 int launch_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
                     const float* cost_table, int B, int gamma, int max_tokens, int mode,
-                    int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
-                    cudaStream_t stream);
+                    int32_t* windows, float* a_hat, float* survival, int32_t* M_out,
+                    double* E_out, cudaStream_t stream);
 
 int launch_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* anchor,
                 const int32_t* draft_tok, const int32_t* tiers, int n_tiers, int B, int gamma,
@@ -49,6 +49,13 @@ int pack_plan_checked(const int32_t* windows, const int32_t* ctx_len, const int3
                       const TierSel& ts, cudaStream_t stream);
 
 size_t accept_workspace(int B, int max_rows, int V);
+// Wait limit of the acceptance pass's bounded waits on the current device (ns).
+uint64_t accept_wait_limit_ns();
+int set_accept_wait_limit_ns(unsigned long long ns);
+// The wait probe: while on, the acceptance pass first waits on a barrier nothing
+// arrives at (its limit must run out).
+int accept_wait_probe();
+int set_accept_wait_probe(int on);
 int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_t* draft_tok,
                   const float* uniforms, const float* exp_noise, const int32_t* windows,
                   const int32_t* cu, int mode, int B, int gamma, int max_rows, int32_t* accept_len,
@@ -58,6 +65,16 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
 // Address of the fixed scratch array on the current device (looked up once per
 // device); nullptr if the lookup fails.
 void* accept_fixed_scratch();
+
+int launch_calib_collect(const float* survival, const float* a_hat, const int32_t* windows,
+                         const int32_t* cap_len, int mode, int B, int gamma, float* s_a,
+                         float* s_ahat, int8_t* s_y, int32_t* count, int cap,
+                         cudaStream_t stream);
+int launch_calib_ece(const float* s_ahat, const int8_t* s_y, const int32_t* count, int cap,
+                     int gamma, int n_bins, int32_t* bin_n, double* bin_p, double* bin_y,
+                     double* ece, cudaStream_t stream);
+int launch_sts_fit(const float* s_a, const int8_t* s_y, const int32_t* count, int cap, int gamma,
+                   int iters, float* zbuf, float* temps, cudaStream_t stream);
 
 size_t compact_workspace(int B);
 int launch_compact(const void* k_new, const void* v_new, int row_bytes, int max_rows,

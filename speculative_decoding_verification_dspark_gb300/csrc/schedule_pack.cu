@@ -64,7 +64,7 @@ __device__ __forceinline__ int warp_incl_scan_i(int v) {
 __global__ void __launch_bounds__(64)
     calibrate_kernel(const float* __restrict__ conf, int conf_is_logit,
                      const float* __restrict__ sts_temp, int B, int gamma,
-                     float* __restrict__ a_hat) {
+                     float* __restrict__ a_hat, float* __restrict__ survival) {
   pdl_release();
   pdl_wait();  // inputs come from the kernels before this one
   const int r = blockIdx.x * 2 + (threadIdx.x >> 5);
@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(64)
     if (i == 0) a = ci;
     else if (i <= j) a = __fmul_rn(a, ci);
   }
+  if (survival && j < gamma) survival[r * gamma + j] = a;  // uncalibrated, for refits
   float v = 1.f;
   if (j < gamma) {
     const double ad = static_cast<double>(a);
@@ -390,10 +391,10 @@ __global__ void __launch_bounds__(1024)
 
 int launch_schedule(const float* conf, int conf_is_logit, const float* sts_temp,
                     const float* cost_table, int B, int gamma, int max_tokens, int mode,
-                    int32_t* windows, float* a_hat, int32_t* M_out, double* E_out,
-                    cudaStream_t stream) {
+                    int32_t* windows, float* a_hat, float* survival, int32_t* M_out,
+                    double* E_out, cudaStream_t stream) {
   if (launch_pdl(calibrate_kernel, dim3(ceil_div(B, 2)), dim3(64), 0, stream, conf, conf_is_logit,
-                 sts_temp, B, gamma, a_hat) != cudaSuccess)
+                 sts_temp, B, gamma, a_hat, survival) != cudaSuccess)
     return DSPARK_ECUDA;
   int npow = 1;
   while (npow < B * gamma) npow <<= 1;

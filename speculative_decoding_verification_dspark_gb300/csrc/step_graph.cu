@@ -82,7 +82,8 @@ int build(const dspark_step_desc& d, cudaStream_t cs, cudaGraph_t g) {
     return DSPARK_ECUDA;
   cap.on = true;
   int rc = dspark_schedule(d.conf, d.conf_is_logit, d.sts_temp, d.cost_table, d.cost_len, d.B,
-                           d.gamma, d.max_tokens, d.mode, d.windows, d.a_hat, d.M, d.E, cs);
+                           d.gamma, d.max_tokens, d.mode, d.windows, d.a_hat, d.survival, d.M,
+                           d.E, cs);
   if (rc != DSPARK_OK) return rc;
   const TierSel ts{d.tier_host, static_cast<unsigned long long>(sel), 1};
   rc = pack_plan_checked(d.windows, d.ctx_len, d.anchor, d.draft_tok, d.tiers, d.n_tiers, d.B,

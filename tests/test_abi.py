@@ -44,7 +44,7 @@ def test_status_strings(lib):
 def test_host_validation_without_device(lib):
     # NULL pointers and out-of-range sizes are rejected before any device work
     nul = None
-    assert lib.dspark_schedule(nul, 1, nul, nul, 10, 4, 6, 32, 0, nul, nul, nul, nul, nul) == -1
+    assert lib.dspark_schedule(nul, 1, nul, nul, 10, 4, 6, 32, 0, nul, nul, nul, nul, nul, nul) == -1
     assert lib.dspark_pack(nul, nul, nul, nul, nul, 0, 4, 6, 0, 8, nul, nul, nul, nul, nul, nul,
                            nul, nul) == -1
     # unsupported attention shape (head dim 96)
