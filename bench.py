@@ -1,14 +1,21 @@
 """Benchmark of the DSpark confidence-scheduled ragged verification step on GB300.
 
-Default: the Qwen3-8B-shaped workload (B=32, gamma=8, 32/8 heads x 128, context
+Headline: the Qwen3-8B-shaped workload (B=32, gamma=8, 32/8 heads x 128, context
 U[1024,4096], page 16, vocab 151936 fp32 probabilities, compact mode) on one GPU.
 One step = schedule -> pack -> verify attention -> accept -> compact over one
 batch, captured once in a CUDA graph and replayed; the small mutable state
 (page table, ctx_len, anchor, free-stack top) is restored inside the step so
 that every step does identical work.
 
+The same run also measures (keys of the one JSON line): the B=256 mixed-traffic
+workload in its three modes and the latent-KV (MLA) workload (``workloads``), and
+the budget/tier sweep over B x confidence mean x cost slope x mode (``sweep``);
+``--no-extra`` skips both.  The CPU oracle is timed on complete steps, on one
+core and on all the host's cores (``cpu_baseline``).
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     [--workload qwen3_8b|mixed256|mla|tiny] [--mode compact|static|cap_accept]
+                    [--no-extra] [--no-cpu-baseline]
 
 Prints one JSON line (rank 0).
 """
@@ -110,7 +117,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -208,130 +215,210 @@ def restore_pairs(d, keys):
     return [(flat, flat.clone())]
 
 
-def gpu_arm(args, wl, mode, dist, world, rank, device, with_e2e=True):
-    import harness
-    import speculative_decoding_verification_dspark_gb300 as dspark
+class StepRunner:
+    """One workload's inputs on the device, its VerifyStep, and one step captured in
+    a CUDA graph (the small mutable state is restored inside the graph, so every
+    replay does identical work)."""
 
-    inp = W.make_inputs(wl, seed=args.seed + rank, device=W.gen_device(wl))
-    d, step = harness.prepare(inp, mode)
-    snap = harness.snapshot_state(d)
-    small = restore_pairs(d, ("page_table", "ctx_len", "anchor", "free_top"))
-    stream = torch.cuda.Stream()
-    # inputs, packed rows and the state snapshot were made on the default stream
-    stream.wait_stream(torch.cuda.current_stream())
-    torch.cuda.synchronize()
+    def __init__(self, inp, mode):
+        import harness
+        self.wl, self.mode = inp["workload"], mode
+        self.d, self.step = harness.prepare(inp, mode)
+        self.ctx0 = self.d["ctx_len"].cpu().numpy()
+        self.small = restore_pairs(self.d, ("page_table", "ctx_len", "anchor", "free_top"))
+        self.stream = torch.cuda.Stream()
+        # inputs, packed rows and the state copies were made on the default stream
+        self.stream.wait_stream(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        with torch.cuda.stream(self.stream):
+            for _ in range(2):  # eager warm-up (all kernels are precompiled)
+                self.one_step()
+        torch.cuda.synchronize()
+        check_device_error("warm-up")
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self.one_step()
+        torch.cuda.synchronize()
+        st = self.step
+        self.windows = st.windows.cpu().numpy()
+        self.cu = st.cu_seqlens.cpu().numpy()
+        self.n_rows = np.diff(self.cu)
+        self.M = int(self.cu[-1])
+        self.tier = int(st.tier.item())
 
-    def one_step():
-        for dst, src in small:
+    def one_step(self):
+        for dst, src in self.small:
             dst.copy_(src, non_blocking=True)
-        step.run(d, mode)
+        self.step.run(self.d, self.mode)
 
-    # eager warm-up (also compiles nothing: all kernels are precompiled)
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            one_step()
-    torch.cuda.synchronize()
-    err = dspark.read_device_error()
-    if err:
-        raise RuntimeError(f"device error word {err:#x} during warm-up")
+    def replay(self, n):
+        with torch.cuda.stream(self.stream):
+            for _ in range(n):
+                self.graph.replay()
 
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        one_step()
-    torch.cuda.synchronize()
-
-    windows = step.windows.cpu().numpy()
-    cu = step.cu_seqlens.cpu().numpy()
-    n_rows = np.diff(cu)
-    ctx0 = snap["ctx_len"].cpu().numpy()
-    M = int(cu[-1])
-    tier = int(step.tier.item())
-
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist, device)
-    with ClockSampler(device.index or 0) as clk:
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(args.steps):
-                graph.replay()
-            ev1.record(stream)
+    def time_replays(self, n, dist=None, device=None):
+        """Device time (ms) of n graph replays between CUDA events on the launching
+        stream, with a barrier and synchronize on both sides."""
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist, device or torch.device("cuda"))
+        with torch.cuda.stream(self.stream):
+            ev0.record(self.stream)
+            for _ in range(n):
+                self.graph.replay()
+            ev1.record(self.stream)
         ev1.synchronize()
-    barrier(dist, device)
-    ms = ev0.elapsed_time(ev1)
-    ms_max = max_over_ranks(ms, dist, device)
-    err = dspark.read_device_error()
-    if err:
-        raise RuntimeError(f"device error word {err:#x} in the timed region")
-    acc_len = step.accept_len.cpu().numpy()
+        barrier(dist, device or torch.device("cuda"))
+        return ev0.elapsed_time(ev1)
 
-    # ---- per-kernel timing of the HBM-bound calls (graphs of repeated launches)
-    def time_call(fn, reps):
+    def steps_for(self, seconds, lo=30, hi=2000):
+        """Replays that fill about `seconds` of device time (bounded)."""
+        ms = self.time_replays(5) / 5
+        return int(min(hi, max(lo, seconds * 1e3 / max(ms, 1e-3))))
+
+    def time_call(self, fn, reps, iters):
+        """us per call of fn, from a graph of `reps` back-to-back calls replayed
+        `iters` times between CUDA events on the launching stream."""
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
+        with torch.cuda.graph(g, stream=self.stream):
             for _ in range(reps):
                 fn()
-        for _ in range(2):
-            g.replay()
+        with torch.cuda.stream(self.stream):
+            for _ in range(2):
+                g.replay()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a.record(stream)
-            for _ in range(args.kernel_iters):
+        with torch.cuda.stream(self.stream):
+            a.record(self.stream)
+            for _ in range(iters):
                 g.replay()
-            b.record(stream)
+            b.record(self.stream)
         b.synchronize()
-        return a.elapsed_time(b) * 1e3 / (reps * args.kernel_iters)  # us per call
+        return a.elapsed_time(b) * 1e3 / (reps * iters)
 
-    # the attention call of the step: over the work list its pack call built, from the
-    # step's own state (restored, then packed once more)
-    for dst, src in small:
-        dst.copy_(src, non_blocking=True)
-    step.pack_plan(d, mode)
-    attn_us = time_call(lambda: step.attention_planned(d), 10)
-    accept_us = time_call(lambda: step.accept(d, mode), 10)
-    a_bytes = attn_bytes(wl, ctx0, n_rows)
-    a_flops = attn_flops(wl, ctx0, n_rows)
-    c_bytes = accept_bytes(wl, windows, n_rows, acc_len, mode)
+    def kernel_figures(self, iters, reps=10):
+        """The step's attention call (over the work list its own pack call built, from
+        the restored state) and its acceptance call, each timed alone; algorithmic
+        bytes, flops and roofline fractions."""
+        st, d, wl = self.step, self.d, self.wl
+        with torch.cuda.stream(self.stream):
+            for dst, src in self.small:
+                dst.copy_(src, non_blocking=True)
+            st.pack_plan(d, self.mode)
+        torch.cuda.synchronize()
+        attn_us = self.time_call(lambda: st.attention_planned(d), reps, iters)
+        accept_us = self.time_call(lambda: st.accept(d, self.mode), reps, iters)
+        check_device_error("per-call timing")
+        acc_len = st.accept_len.cpu().numpy()
+        a_bytes = attn_bytes(wl, self.ctx0, self.n_rows)
+        a_flops = attn_flops(wl, self.ctx0, self.n_rows)
+        c_bytes = accept_bytes(wl, self.windows, self.n_rows, acc_len, self.mode)
+        peaks = peak_values()
+        attn_gbs = a_bytes / (attn_us * 1e-6) / 1e9
+        attn_tfs = a_flops / (attn_us * 1e-6) / 1e12
+        acc_gbs = c_bytes / (accept_us * 1e-6) / 1e9
+        return {
+            "verify_attn": {"us": attn_us, "GB/s": attn_gbs, "frac_hbm": attn_gbs / peaks["hbm"],
+                            "TFLOP/s": attn_tfs, "frac_tensor": attn_tfs / peaks["tf"],
+                            "bytes": a_bytes, "flops": a_flops},
+            "accept": {"us": accept_us, "GB/s": acc_gbs, "frac_hbm": acc_gbs / peaks["hbm"],
+                       "bytes": c_bytes},
+        }
+
+    def time_step_graph(self, n):
+        """The same step as the library's own step graph (tier chosen on the device by a
+        switch node; dspark_step_graph_*), launched n times back to back on the stream,
+        each launch preceded by the copy that restores the small mutable state: two
+        stream operations per step and no host synchronisation between steps.  Returns
+        (ms for the n steps, step rate)."""
+        g = self.step.graph(self.d, self.mode)
+        try:
+            def one():
+                for dst, src in self.small:
+                    dst.copy_(src, non_blocking=True)
+                g.launch(self.stream)
+            with torch.cuda.stream(self.stream):
+                for _ in range(5):
+                    one()
+            torch.cuda.synchronize()
+            check_device_error("step graph warm-up")
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(self.stream):
+                a.record(self.stream)
+                for _ in range(n):
+                    one()
+                b.record(self.stream)
+            b.synchronize()
+            check_device_error("step graph")
+            ms = a.elapsed_time(b)
+            self.step_graph_pdl = g.pdl
+        finally:
+            g.close()
+        return ms, n / (ms / 1e3)
+
+    def outcome(self):
+        """Accepted tokens of the step (committed drafts + one bonus/correction per
+        request) and, in cap-accept mode, the commit/cap utilisation."""
+        acc = self.step.accept_len.cpu().numpy()
+        out = {"accepted_tokens_per_step": int(acc.sum() + self.wl.B),
+               "mean_window": float(self.windows.mean())}
+        if self.mode == W.MODE_CAP_ACCEPT:
+            cap = self.step.cap_len.cpu().numpy()
+            out["commit_over_cap"] = float(acc.sum() / max(1, cap.sum()))
+        return out
+
+
+def check_device_error(where):
+    import speculative_decoding_verification_dspark_gb300 as dspark
+    err = dspark.read_device_error()
+    if err:
+        raise RuntimeError(f"device error word {err:#x} ({where})")
+
+
+def peak_values():
     peaks = load_peaks()
-    hbm = peaks.get("hbm_gbs")
-    peak_src = "measured" if hbm else "fallback"
-    hbm = hbm or 6800.0
-    attn_gbs = a_bytes / (attn_us * 1e-6) / 1e9
-    acc_gbs = c_bytes / (accept_us * 1e-6) / 1e9
-    attn_tfs = a_flops / (attn_us * 1e-6) / 1e12
+    hbm, tf = peaks.get("hbm_gbs"), peaks.get("bf16_tflops")
+    return {"hbm": hbm or 6800.0, "hbm_src": "measured" if hbm else "fallback",
+            "tf": tf or 1900.0, "tf_src": "measured" if tf else "fallback"}
+
+
+def roofline_block(wl, kf):
+    """The dominant kernel's roofline: the attention call, HBM-bound unless its flops
+    per algorithmic byte exceed the ridge point of the measured peaks."""
+    pk = peak_values()
+    a = kf["verify_attn"]
     traffic = load_traffic("verify_attn", wl.name, attn_src(wl))
-    # the attention call is tensor-bound when its flops per algorithmic byte exceed the
-    # ridge point of the measured peaks (the latent-KV shape), else HBM-bound
-    tf_peak = peaks.get("bf16_tflops")
-    tf_src = "measured" if tf_peak else "fallback"
-    tf_peak = tf_peak or 1900.0
-    tensor_bound = a_flops / max(a_bytes, 1) > tf_peak * 1e12 / (hbm * 1e9)
-    if tensor_bound:
-        roof = {"bound": "tensor", "kernel": "dspark_verify_attn (work list + main + combine)",
-                "achieved": attn_tfs, "peak": tf_peak, "unit": "TFLOP/s", "frac": attn_tfs / tf_peak,
-                "traffic": traffic, "algorithmic_flops": a_flops, "algorithmic_bytes": a_bytes,
-                "us_per_launch": attn_us,
-                "peak_source": f"{tf_src} bf16_tflops (burst cuBLAS GEMM; the kernel is timed alone)"}
-    else:
-        roof = {"bound": "hbm", "kernel": "dspark_verify_attn (work list + main + combine)",
-                "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
-                "traffic": traffic, "algorithmic_bytes": a_bytes, "us_per_launch": attn_us,
-                "peak_source": f"{peak_src} hbm_gbs (burst copy)"}
+    common = {"kernel": "dspark_verify_attn (main kernel + combine; work list from the pack call)",
+              "traffic": traffic, "algorithmic_bytes": a["bytes"], "us_per_launch": a["us"]}
+    if a["flops"] / max(a["bytes"], 1) > pk["tf"] * 1e12 / (pk["hbm"] * 1e9):
+        return {"bound": "tensor", "achieved": a["TFLOP/s"], "peak": pk["tf"], "unit": "TFLOP/s",
+                "frac": a["TFLOP/s"] / pk["tf"], "algorithmic_flops": a["flops"], **common,
+                "peak_source": f"{pk['tf_src']} bf16_tflops (burst cuBLAS GEMM; the call is "
+                               "timed alone)"}
+    return {"bound": "hbm", "achieved": a["GB/s"], "peak": pk["hbm"], "unit": "GB/s",
+            "frac": a["GB/s"] / pk["hbm"], **common,
+            "peak_source": f"{pk['hbm_src']} hbm_gbs (burst copy)"}
 
-    err = dspark.read_device_error()
-    if err:
-        raise RuntimeError(f"device error word {err:#x} while timing the calls")
-    # ---- end to end through the public API with host buffers
-    e2e = e2e_arm(args, wl, mode, d, step, small, stream) if with_e2e else None
-    err = dspark.read_device_error()
-    if err:
-        raise RuntimeError(f"device error word {err:#x} in the end-to-end arm")
 
-    steps_per_s = args.steps / (ms_max / 1e3)
+def gpu_arm(args, wl, mode, dist, world, rank, device, with_e2e=True):
+    """The headline: timed graph replays of the step, per-call kernel figures, the
+    end-to-end leg through the public API with host buffers, and the clocks sampled
+    over the whole busy window (warm-up, timed steps, per-call timing)."""
+    inp = W.make_inputs(wl, seed=args.seed + rank, device=W.gen_device(wl))
+    run = StepRunner(inp, mode)
+    with ClockSampler(device.index or 0) as clk:
+        # warm-up: W replays at least, and at least ~0.5 s of device time so that the
+        # clock record has samples under load before the timed region
+        n_warm = max(args.warmup, run.steps_for(0.5))
+        run.replay(n_warm)
+        torch.cuda.synchronize()
+        ms = run.time_replays(args.steps, dist, device)
+        ms_max = max_over_ranks(ms, dist, device)
+        check_device_error("timed region")
+        kf = run.kernel_figures(args.kernel_iters)
+    kf["accept"]["traffic"] = load_traffic("accept", wl.name, ACCEPT_SRC)
+    sg_ms, sg_rate = run.time_step_graph(max(args.steps, 200))
+    e2e = e2e_arm(args, run) if with_e2e else None
+    check_device_error("end-to-end leg")
     value = world * args.steps / (ms_max / 1e3)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -340,80 +427,158 @@ def gpu_arm(args, wl, mode, dist, world, rank, device, with_e2e=True):
         "dtype_detail": "attention bf16 operands / fp32 accumulate and softmax; acceptance fp32",
         "data": "synthetic",
         "config": {"workload": workload_desc(wl, args.mode), "mode": args.mode,
-                   "global_batch": wl.B * world, "packed_rows_M": M, "tier": tier,
+                   "global_batch": wl.B * world, "packed_rows_M": run.M, "tier": run.tier,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (no flush): KV %.2f GB, probabilities %.2f GB"
-                         % (a_bytes / 1e9, c_bytes / 1e9)},
-        "packed_tokens_per_s": M * value,
-        "accepted_tokens_per_step": int(acc_len.sum() + wl.B),
-        "mean_window": float(windows.mean()),
-        "roofline": roof,
-        "kernels": {
-            "verify_attn": {"us": attn_us, "GB/s": attn_gbs, "frac_hbm": attn_gbs / hbm,
-                            "TFLOP/s": attn_tfs, "frac_tensor": attn_tfs / tf_peak,
-                            "bytes": a_bytes},
-            "accept": {"us": accept_us, "GB/s": acc_gbs, "frac_hbm": acc_gbs / hbm,
-                       "bytes": c_bytes,
-                       "traffic": load_traffic("accept", wl.name, ACCEPT_SRC)},
-        },
+                         % (kf["verify_attn"]["bytes"] / 1e9, kf["accept"]["bytes"] / 1e9)},
+        "packed_tokens_per_s": run.M * value,
+        **run.outcome(),
+        "roofline": roofline_block(wl, kf),
+        "kernels": kf,
         "e2e": e2e,
+        "step_graph": {"steps_per_s": sg_rate, "ms_per_step": sg_ms / max(args.steps, 200),
+                       "steps": max(args.steps, 200), "pdl": run.step_graph_pdl,
+                       "what": "the library's step graph (tier chosen on the device by a switch "
+                               "node), launched back to back after the state-restore copy: "
+                               "two host launches per step, no host synchronisation"},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
-        "clocks": clk.summary(),
+        "clocks": {**clk.summary(), "window": "warm-up (>= 0.5 s), timed steps and per-call "
+                                              "timing of the headline"},
     }
-    if mode == W.MODE_CAP_ACCEPT:
-        cap = step.cap_len.cpu().numpy()
-        result["commit_over_cap"] = float(acc_len.sum() / max(1, cap.sum()))
+    del run
+    torch.cuda.empty_cache()
     return result, inp
 
 
-def sweep_arm(args, dist, world, rank, device):
-    """Step rate over the batch sizes of the budget/tier sweep (Qwen3-8B shape, gamma 16,
-    ctx 2048, confidence mean 0.85, cost slope 0.19 ms/token) in the three modes.
-    Points whose inputs fit in L2 are marked: their per-kernel fractions are not HBM
-    figures."""
-    import copy
-    sargs = copy.copy(args)
-    sargs.steps = min(args.steps, 300)
-    sargs.warmup = max(3, min(args.warmup, 20))
-    sargs.kernel_iters = min(args.kernel_iters, 5)
+def point_figures(run, seconds=0.15, kernel_iters=3):
+    """Step rate and per-call figures of one extra workload point."""
+    n = run.steps_for(seconds)
+    run.replay(3)
+    ms = run.time_replays(n)
+    check_device_error("extra point")
+    kf = run.kernel_figures(kernel_iters, reps=5)
+    run.last_kernels = kf
+    sps = n / (ms / 1e3)
+    pt = {"steps_per_s": sps, "ms_per_step": ms / n, "steps_timed": n, "M": run.M,
+          "tier": run.tier, "packed_tokens_per_s": run.M * sps, **run.outcome(),
+          "attn_us": kf["verify_attn"]["us"], "attn_frac_hbm": kf["verify_attn"]["frac_hbm"],
+          "attn_frac_tensor": kf["verify_attn"]["frac_tensor"],
+          "accept_us": kf["accept"]["us"], "accept_frac_hbm": kf["accept"]["frac_hbm"],
+          "l2_resident": kf["verify_attn"]["bytes"] + kf["accept"]["bytes"] < 129e6}
+    return pt
+
+
+def workloads_arm(seed):
+    """The other full-size workloads: mixed traffic at B=256 in its three modes, and
+    the latent-KV shape, each a CUDA-graph step timed like the headline."""
+    out = {}
+    for name, modes in (("mixed256", ("compact", "static", "cap_accept")), ("mla", ("compact",))):
+        wl = W.WORKLOADS[name]
+        inp = W.make_inputs(wl, seed=seed, device=W.gen_device(wl))
+        out[name] = {"workload": workload_desc(wl, "/".join(modes))}
+        for mname in modes:
+            run = StepRunner(inp, W.MODE_NAMES[mname])
+            pt = point_figures(run, seconds=0.3, kernel_iters=5)
+            pt["roofline"] = roofline_block(wl, run.last_kernels)
+            out[name][mname] = pt
+            del run
+            torch.cuda.empty_cache()
+        del inp
+        torch.cuda.empty_cache()
+    return out
+
+
+def sweep_arm(seed):
+    """The budget/tier sweep: B in {1, 8, 32, 128, 256} x confidence mean in
+    {.95, .85, .70} x cost slope in {.05, .19, .5} ms/token (Qwen3-8B heads,
+    gamma 16, ctx 2048, tiers 4..4096), compact and cap-accept at every point;
+    static verifies the whole block whatever the slope, so it is timed once per
+    (B, confidence).  Inputs are drawn once per (B, confidence); the slope changes
+    only the cost table.  Points whose inputs fit in L2 are marked."""
     pts = []
     for B in W.SWEEP_B:
-        for mname in ("compact", "static", "cap_accept"):
-            wl = W.sweep_point(B, 0.85, 0.19)
-            sargs.mode = mname
-            try:
-                res, inp = gpu_arm(sargs, wl, W.MODE_NAMES[mname], dist, world, rank, device,
-                                   with_e2e=False)
-            except RuntimeError as e:  # reported in the line, the other points still run
-                pts.append({"B": B, "mode": mname, "error": str(e)})
-                torch.cuda.empty_cache()
-                continue
-            k = res["kernels"]
-            pt = {"B": B, "mode": mname, "steps_per_s": res["value"],
-                  "ms_per_step": res["ms_per_step"],
-                  "packed_tokens_per_s": res["packed_tokens_per_s"],
-                  "accepted_tokens_per_step": res["accepted_tokens_per_step"],
-                  "M": res["config"]["packed_rows_M"], "tier": res["config"]["tier"],
-                  "attn_us": k["verify_attn"]["us"], "attn_frac_hbm": k["verify_attn"]["frac_hbm"],
-                  "accept_us": k["accept"]["us"], "accept_frac_hbm": k["accept"]["frac_hbm"],
-                  "l2_resident": k["verify_attn"]["bytes"] + k["accept"]["bytes"] < 129e6}
-            if "commit_over_cap" in res:
-                pt["commit_over_cap"] = res["commit_over_cap"]
-            pts.append(pt)
-            del inp
+        for c in W.SWEEP_CONF_MEANS:
+            base = W.make_inputs(W.sweep_point(B, c, W.SWEEP_THETA[0]), seed,
+                                 device=W.gen_device(W.sweep_point(B, c, 0.19)))
+            for theta in W.SWEEP_THETA:
+                wl = W.sweep_point(B, c, theta)
+                m = torch.arange(base["cost_table"].numel(), dtype=torch.float64,
+                                 device=base["cost_table"].device)
+                inp = dict(base, workload=wl,
+                           cost_table=(wl.cost_bias_ms + theta * m).to(torch.float32))
+                modes = ("compact", "cap_accept") + (("static",) if theta == 0.19 else ())
+                for mname in modes:
+                    try:
+                        run = StepRunner(inp, W.MODE_NAMES[mname])
+                        pt = point_figures(run)
+                        del run
+                    except RuntimeError as e:  # reported in the line; the others still run
+                        pt = {"error": str(e)}
+                    pts.append({"B": B, "conf_mean": c,
+                                "theta_ms": theta if mname != "static" else "any",
+                                "mode": mname, **pt})
+                    torch.cuda.empty_cache()
+            del base
             torch.cuda.empty_cache()
     return pts
 
 
-def e2e_arm(args, wl, mode, d, step, small, stream):
-    """Same step through the public API with the per-step inputs in pinned host
-    memory: H2D copies of the step's inputs, the five calls, D2H of the results,
-    all inside the timed region."""
-    tier = int(step.tier.item())
+def calib_arm(seed):
+    """Calibration tooling at a serving-sized store: B = 1024 requests, gamma = 8, one
+    collect per step (cap-accept outcomes, every position labelled) until 2^17
+    samples per position, then the ECE (15 bins) and the STS refit (36 bisections)
+    over the full store.  Times: collect per call (a graph of calls), ECE and refit
+    per call."""
+    import speculative_decoding_verification_dspark_gb300 as dspark
+    dev = torch.device("cuda")
+    B, gamma, cap = 1024, 8, 1 << 17
+    g = torch.Generator(device=dev).manual_seed(seed * 7919 + 17)
+    c = 0.6 + 0.4 * torch.rand((B, gamma), generator=g, device=dev)
+    a = torch.cumprod(c, dim=1).float().contiguous()          # synthetic survival input
+    a_hat = (a * 0.9).contiguous()
+    windows = torch.full((B,), gamma, dtype=torch.int32, device=dev)
+    cap_len = torch.randint(0, gamma + 1, (B,), generator=g, device=dev, dtype=torch.int32)
+    store = dspark.CalibStore(gamma, cap)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    calls = cap // B
+    reps = 8
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(reps):
+            store.collect(a, a_hat, windows, cap_len, W.MODE_CAP_ACCEPT)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    with torch.cuda.stream(stream):
+        store.count.zero_()
+        ev[0].record(stream)
+        for _ in range(calls // reps):
+            graph.replay()
+        ev[1].record(stream)
+        ev[2].record(stream)
+        store.ece(15)
+        ev[3].record(stream)
+        ev[4].record(stream)
+        store.sts_fit(36)
+        ev[5].record(stream)
+    ev[5].synchronize()
+    check_device_error("calibration")
+    n = int(store.count.min().item())
+    return {"requests_per_collect": B, "gamma": gamma, "samples_per_position": n,
+            "collect_us": ev[0].elapsed_time(ev[1]) * 1e3 / calls,
+            "ece_ms": ev[2].elapsed_time(ev[3]), "sts_fit_ms": ev[4].elapsed_time(ev[5]),
+            "sts_fit_bisections": 36, "ece_bins": 15}
+
+
+def e2e_arm(args, run):
+    """The same step through the public API with the step's inputs in pinned host
+    memory: host-to-device copies of the inputs (the M packed rows of the per-row
+    tensors, as the target forward hands them over, and the per-request tensors),
+    the five calls, and the device-to-host copy of the results, all inside the
+    timed region."""
+    d, step, M = run.d, run.step, run.M
     row_keys = ["p_target", "q", "k_new"] + (["v_new"] if d.get("v_new") is not None else [])
     in_keys = ["conf", "draft_tok", "uniforms", "exp_noise", "p_draft"] + row_keys
-    # per-row inputs: the tier's rows, as the target forward would hand them over
-    dev_view = {k: (d[k][:tier] if k in row_keys else d[k]) for k in in_keys}
+    dev_view = {k: (d[k][:M] if k in row_keys else d[k]) for k in in_keys}
     host = {k: v.cpu().pin_memory() for k, v in dev_view.items()}
     out_keys = ["windows", "accept_len", "out_tok", "cstar", "committed", "n_committed"]
     host_out = {k: torch.empty_like(getattr(step, k), device="cpu").pin_memory() for k in out_keys}
@@ -423,13 +588,14 @@ def e2e_arm(args, wl, mode, d, step, small, stream):
     def one():
         for k, v in host.items():
             dev_view[k].copy_(v, non_blocking=True)
-        for dst, src in small:
+        for dst, src in run.small:
             dst.copy_(src, non_blocking=True)
-        step.run(d, mode)
+        step.run(d, run.mode)
         for k in out_keys:
             host_out[k].copy_(getattr(step, k), non_blocking=True)
 
     n = max(3, min(args.steps, 20))
+    stream = run.stream
     with torch.cuda.stream(stream):
         for _ in range(2):
             one()
@@ -478,97 +644,164 @@ def load_traffic(kernel, workload, src):
 
 
 # ------------------------------------------------------------------ oracle (CPU baseline)
+#
+# The oracle times complete steps: the global schedule and pack, the attention of
+# every request, the acceptance of every request, and the compaction of the batch,
+# each by the oracle's own functions as they stand.  The per-request attention and
+# acceptance run either one after another in this process (one core) or spread
+# over a pool of worker processes, one per host core (all cores).  The workers read
+# the step's inputs from memory-mapped files written once before the timing (the
+# inputs as the target forward would hand them over), so no input is copied
+# between processes inside the timed region.
 
-def oracle_sample(inp_np, wl, mode, reqs):
-    """One bounded sample of the step on the CPU oracle: the global schedule and
-    pack over the whole batch, then attention, acceptance and compaction for the
-    sampled requests only.  Returns (seconds global, seconds for the sample)."""
+_OW = {}  # worker-side: the memory-mapped inputs of the step
+
+
+def _oracle_worker_init(folder, meta):
+    import numpy as _np
+    _OW.clear()
+    _OW["meta"] = meta
+    for k, (shape, dtype) in meta["arrays"].items():
+        _OW[k] = _np.memmap(os.path.join(folder, k + ".bin"), dtype=dtype, mode="r",
+                            shape=tuple(shape))
+
+
+def _oracle_request(task):
+    """Attention and acceptance of one request by the oracle's functions."""
     from oracle import dspark_oracle as O
-    t0 = time.perf_counter()
-    sch = O.schedule(inp_np["conf"], inp_np["conf_is_logit"], inp_np["sts_temp"],
-                     inp_np["cost_table"], wl.max_tokens, mode)
-    pk = O.pack(sch.windows, inp_np["ctx_len"], inp_np["anchor"], inp_np["draft_tok"],
-                inp_np["tiers"], mode, wl.gamma)
-    t1 = time.perf_counter()
-    P = wl.page_size
-    for r in reqs:
-        c0, c1 = int(pk.cu_seqlens[r]), int(pk.cu_seqlens[r + 1])
-        n = c1 - c0
-        ctx = int(inp_np["ctx_len"][r])
-        sub_cu = np.array([0, n])
-        q = inp_np["q_dense"][r, :n]
-        kn = inp_np["k_new_dense"][r, :n]
-        if wl.attn == "gqa":
-            O.verify_attention_gqa(q, kn, inp_np["v_new_dense"][r, :n], inp_np["k_cache"],
-                                   inp_np["v_cache"], inp_np["page_table"][r:r + 1],
-                                   np.array([ctx]), sub_cu, wl.Hq, wl.Hkv, 1 / math.sqrt(wl.d_qk))
+    r, c0, c1, w_r = task
+    m = _OW["meta"]
+    a = _OW
+    sub_cu = np.array([0, c1 - c0])
+    ctx = a["ctx_len"][r:r + 1]
+    if m["attn"] == "gqa":
+        o, lse = O.verify_attention_gqa(a["q"][c0:c1], a["k_new"][c0:c1], a["v_new"][c0:c1],
+                                        a["k_cache"], a["v_cache"], a["page_table"][r:r + 1], ctx,
+                                        sub_cu, m["Hq"], m["Hkv"], m["scale"])
+    else:
+        o, lse = O.verify_attention_mla(a["q"][c0:c1], a["k_new"][c0:c1], a["k_cache"],
+                                        a["page_table"][r:r + 1], ctx, sub_cu, m["d_v"],
+                                        m["scale"])
+    acc = O.accept(a["p_target"][c0:c1], a["p_draft"][r:r + 1], a["draft_tok"][r:r + 1],
+                   a["uniforms"][r:r + 1], a["exp_noise"][r:r + 1], np.array([w_r], np.int32),
+                   sub_cu, m["mode"], m["gamma"])
+    return r, float(np.sum(o)), int(acc.accept_len[0]), int(acc.out_tok[0])
+
+
+class OracleBaseline:
+    """Complete oracle steps of one workload on the host cores."""
+
+    def __init__(self, inp, mode, cores=None):
+        import tempfile
+        from oracle import dspark_oracle as O
+        wl = inp["workload"]
+        self.wl, self.mode = wl, mode
+        h = {k: (v.float() if v.dtype == torch.bfloat16 else v).cpu().numpy()
+             for k, v in inp.items() if isinstance(v, torch.Tensor)}
+        h["conf_is_logit"] = inp["conf_is_logit"]
+        self.h = h
+        # the packed rows the target forward hands over (laid out with the oracle's
+        # own cu_seqlens, as in the GPU tests)
+        sch = O.schedule(h["conf"], h["conf_is_logit"], h["sts_temp"], h["cost_table"],
+                         wl.max_tokens, mode)
+        pk = O.pack(sch.windows, h["ctx_len"], h["anchor"], h["draft_tok"], h["tiers"], mode,
+                    wl.gamma)
+        cu = torch.as_tensor(pk.cu_seqlens)
+        packed = {"q": inp["q_dense"], "k_new": inp["k_new_dense"],
+                  "p_target": inp["p_target_dense"]}
+        if inp.get("v_new_dense") is not None:
+            packed["v_new"] = inp["v_new_dense"]
+        for k, v in packed.items():
+            h[k] = W.to_packed(v.cpu(), cu, pk.tier).float().numpy()
+        self.folder = tempfile.mkdtemp(prefix="dspark_oracle_")
+        arrays = {}
+        for k in ("q", "k_new", "v_new", "p_target", "k_cache", "v_cache", "page_table",
+                  "ctx_len", "p_draft", "draft_tok", "uniforms", "exp_noise"):
+            if h.get(k) is None:
+                continue
+            a = np.ascontiguousarray(h[k])
+            a.tofile(os.path.join(self.folder, k + ".bin"))
+            arrays[k] = (list(a.shape), a.dtype.str)
+        self.meta = {"arrays": arrays, "attn": wl.attn, "Hq": wl.Hq, "Hkv": wl.Hkv,
+                     "d_v": wl.d_v, "scale": 1.0 / math.sqrt(wl.d_qk), "mode": mode,
+                     "gamma": wl.gamma}
+        _oracle_worker_init(self.folder, self.meta)  # this process serves the one-core runs
+        self.cores = cores or len(os.sched_getaffinity(0))
+        self.pool = None
+
+    def start_pool(self):
+        import multiprocessing as mp
+        if self.pool is None:
+            ctx = mp.get_context("spawn")
+            self.pool = ctx.Pool(self.cores, initializer=_oracle_worker_init,
+                                 initargs=(self.folder, self.meta))
+            self.pool.map(_oracle_request_noop, range(self.cores))  # workers up
+        return self.pool
+
+    def step(self, parallel):
+        """One complete oracle step; returns its wall time in seconds."""
+        from oracle import dspark_oracle as O
+        h, wl, mode = self.h, self.wl, self.mode
+        t0 = time.perf_counter()
+        sch = O.schedule(h["conf"], h["conf_is_logit"], h["sts_temp"], h["cost_table"],
+                         wl.max_tokens, mode)
+        pk = O.pack(sch.windows, h["ctx_len"], h["anchor"], h["draft_tok"], h["tiers"], mode,
+                    wl.gamma)
+        tasks = [(r, int(pk.cu_seqlens[r]), int(pk.cu_seqlens[r + 1]), int(sch.windows[r]))
+                 for r in range(wl.B)]
+        if parallel:
+            res = self.start_pool().map(_oracle_request, tasks, chunksize=1)
         else:
-            O.verify_attention_mla(q, kn, inp_np["k_cache"], inp_np["page_table"][r:r + 1],
-                                   np.array([ctx]), sub_cu, wl.d_v, 1 / math.sqrt(wl.d_qk))
-        pt = inp_np["p_target_dense"][r, :n]
-        O.accept(pt, inp_np["p_draft"][r:r + 1], inp_np["draft_tok"][r:r + 1],
-                 inp_np["uniforms"][r:r + 1], inp_np["exp_noise"][r:r + 1], sch.windows[r:r + 1],
-                 sub_cu, mode, wl.gamma)
-    t2 = time.perf_counter()
-    return t1 - t0, t2 - t1
+            res = [_oracle_request(t) for t in tasks]
+        res.sort()
+        L = np.array([x[2] for x in res], np.int32)
+        tok = np.array([x[3] for x in res], np.int32)
+        O.compact(_OW["k_new"], _OW.get("v_new"), pk.cu_seqlens, L, tok, h["draft_tok"],
+                  wl.page_size, h["page_table"], h["ctx_len"], h["anchor"], h["free_pages"],
+                  int(h["free_top"][0]), _OW["k_cache"], _OW.get("v_cache"))
+        return time.perf_counter() - t0
+
+    def time_steps(self, parallel, budget_s, max_steps, warmup=1):
+        for _ in range(warmup):
+            self.step(parallel)
+        ts = []
+        t_start = time.perf_counter()
+        while len(ts) < max_steps and (not ts or time.perf_counter() - t_start < budget_s):
+            ts.append(self.step(parallel))
+        return ts
+
+    def close(self):
+        import shutil
+        if self.pool is not None:
+            self.pool.terminate()
+            self.pool.join()
+            self.pool = None
+        _OW.clear()
+        shutil.rmtree(self.folder, ignore_errors=True)
 
 
-def oracle_inputs(inp, reqs):
-    """Host copies of what the sampled oracle step reads (only the sampled
-    requests' pages of the cache, relabelled)."""
+def _oracle_request_noop(i):
+    return i
+
+
+def cpu_baseline(inp, mode, budget_s):
+    """The oracle as it stands on the host cores: complete steps on one core, then on
+    all cores.  The all-cores figure is the line's value."""
+    ob = OracleBaseline(inp, mode)
+    try:
+        t1 = ob.time_steps(False, budget_s / 2, 20)
+        tn = ob.time_steps(True, budget_s / 2, 50)
+    finally:
+        ob.close()
     wl = inp["workload"]
-    P = wl.page_size
-    out = {}
-    for k in ("conf", "sts_temp", "cost_table", "tiers", "ctx_len", "anchor", "draft_tok",
-              "uniforms"):
-        out[k] = inp[k].cpu().numpy()
-    out["conf_is_logit"] = inp["conf_is_logit"]
-    B = wl.B
-    pt = np.full((B, inp["page_table"].shape[1]), -1, np.int64)
-    pages, k = [], 0
-    for r in reqs:
-        n = (int(inp["ctx_len"][r]) + P - 1) // P
-        pages.append(inp["page_table"][r, :n].long())
-        pt[r, :n] = np.arange(k, k + n)
-        k += n
-    pages = torch.cat(pages) if pages else torch.zeros(0, dtype=torch.long)
-    if len(pages) == 0:
-        pages = torch.zeros(1, dtype=torch.long, device=inp["k_cache"].device)
-    out["page_table"] = pt
-    out["k_cache"] = inp["k_cache"][pages.to(inp["k_cache"].device)].float().cpu().numpy()
-    out["v_cache"] = (inp["v_cache"][pages.to(inp["v_cache"].device)].float().cpu().numpy()
-                      if inp.get("v_cache") is not None else None)
-    idx = torch.tensor(list(reqs), device=inp["q_dense"].device)
-    for k in ("q_dense", "k_new_dense", "v_new_dense", "p_target_dense", "p_draft", "exp_noise"):
-        if inp.get(k) is None:
-            out[k] = None
-            continue
-        full = torch.zeros((B,) + tuple(inp[k].shape[1:]), dtype=torch.float32)
-        full[idx.cpu()] = inp[k][idx].float().cpu()
-        out[k] = full.numpy()
-    out["uniforms"] = inp["uniforms"].cpu().numpy()
-    return out
-
-
-def oracle_timing(inp, wl, mode, budget_s, n_req):
-    reqs = list(range(0, wl.B, max(1, wl.B // n_req)))[:n_req]
-    inp_np = oracle_inputs(inp, reqs)
-    t_glob, t_req, reps = 0.0, 0.0, 0
-    t_start = time.perf_counter()
-    while reps < 1 or (time.perf_counter() - t_start < budget_s and reps < 50):
-        g, s = oracle_sample(inp_np, wl, mode, reqs)
-        t_glob += g
-        t_req += s
-        reps += 1
-    t_step = t_glob / reps + (t_req / reps) * wl.B / len(reqs)
-    return t_step, reps, reqs
-
-
-def cpu_baseline_block(t_step, reps, reqs, wl):
-    return {"value": 1.0 / t_step, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": (f"{reps} x (global schedule+pack over all {wl.B} requests + attention, "
-                       f"acceptance for requests {reqs}); per-request time scaled x{wl.B}/"
-                       f"{len(reqs)}; numpy, one thread")}
+    m1, mn = statistics.median(t1), statistics.median(tn)
+    return {"value": 1.0 / mn, "unit": UNIT, "cores": ob.cores, "kind": "oracle",
+            "value_1core": 1.0 / m1, "steps_timed": len(tn), "steps_timed_1core": len(t1),
+            "host_cores": ob.cores,
+            "sample": (f"complete steps of the {wl.name} workload (global schedule and pack, "
+                       f"attention and acceptance of all {wl.B} requests, compaction of the "
+                       f"batch; median of {len(tn)} steps on {ob.cores} worker processes, "
+                       f"{len(t1)} steps on one core); numpy, one BLAS thread per process")}
 
 
 # ------------------------------------------------------------------ main
@@ -584,9 +817,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--kernel-iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
-    ap.add_argument("--sweep", action="store_true",
-                    help="also report the step rate at B = 1..256 in the three modes")
+    ap.add_argument("--cpu-budget-s", type=float, default=20.0)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time the headline only (no other workloads, no sweep)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -596,42 +829,37 @@ def main():
     mode = W.MODE_NAMES[args.mode]
 
     if args.impl == "reference":
-        # the reference arm is the CPU oracle itself, on rank 0 only
+        # the reference arm is the CPU oracle itself, on rank 0 only, on all the
+        # host's cores; each step is a complete step of the workload
         if rank != 0:
             return
         inp = W.make_inputs(wl, seed=args.seed, device="cpu")
-        per = []
-        n_req = 1
-        reqs = list(range(0, wl.B, max(1, wl.B // n_req)))[:n_req]
-        inp_np = oracle_inputs(inp, reqs)
-        # Each step is one bounded sample (the global schedule + pack, and one
-        # request's attention and acceptance scaled to the batch).  The oracle is
-        # slow, so the run stops after ~3 minutes of samples; "steps" reports
-        # how many were timed.
-        t0 = time.perf_counter()
-        oracle_sample(inp_np, wl, mode, reqs)
-        t_one = time.perf_counter() - t0
-        warm = min(args.warmup, max(1, int(20.0 / max(t_one, 1e-6))))
-        n_steps = min(args.steps, max(3, int(150.0 / max(t_one, 1e-6))))
-        for _ in range(warm):
-            oracle_sample(inp_np, wl, mode, reqs)
-        for _ in range(n_steps):
-            g, s = oracle_sample(inp_np, wl, mode, reqs)
-            per.append(g + s * wl.B / len(reqs))
-        t_step = sum(per) / len(per)
+        ob = OracleBaseline(inp, mode)
+        try:
+            t0 = time.perf_counter()
+            ob.step(True)  # also starts the worker pool
+            t_one = max(time.perf_counter() - t0, 1e-6)
+            # the whole run within ~3 minutes: fewer steps than asked if need be
+            warm = min(args.warmup, max(1, int(20.0 / t_one)))
+            n_steps = min(args.steps, max(3, int(150.0 / t_one)))
+            ts = ob.time_steps(True, 1e9, n_steps, warmup=warm)
+        finally:
+            ob.close()
+        t_step = statistics.mean(ts)
         v = 1.0 / t_step
         line = {
             "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
-            "steps": n_steps, "steps_requested": args.steps, "warmup": warm,
+            "steps": len(ts), "steps_requested": args.steps, "warmup": warm,
             "ms_per_step": t_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": workload_desc(wl, args.mode), "mode": args.mode,
-                       "global_batch": wl.B, "parallelism": "cpu oracle, one thread"},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": (f"each step: global schedule+pack over {wl.B} requests + "
-                                        f"attention/acceptance for requests {reqs}, per-request "
-                                        f"time scaled x{wl.B}/{len(reqs)}")},
+                       "global_batch": wl.B,
+                       "parallelism": f"cpu oracle, {ob.cores} worker processes"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": ob.cores, "kind": "oracle",
+                             "sample": (f"{len(ts)} complete steps (schedule, pack, attention "
+                                        f"and acceptance of all {wl.B} requests, compaction) "
+                                        f"on {ob.cores} worker processes")},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }
         print(json.dumps(line), flush=True)
@@ -645,11 +873,16 @@ def main():
     import __graft_entry__ as g
     g.build()
     result, inp = gpu_arm(args, wl, mode, dist, world, rank, device)
-    if args.sweep:
-        result["sweep"] = sweep_arm(args, dist, world, rank, device)
+    # the extra workloads and the sweep: one-GPU runs only (the scaling runs time the
+    # headline alone)
+    if world == 1 and not args.no_extra:
+        t0 = time.perf_counter()
+        result["workloads"] = workloads_arm(args.seed)
+        result["sweep"] = sweep_arm(args.seed)
+        result["calibration"] = calib_arm(args.seed)
+        result["extra_wall_s"] = time.perf_counter() - t0
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        t_step, reps, reqs = oracle_timing(inp, wl, mode, args.cpu_budget_s, 2)
-        result["cpu_baseline"] = cpu_baseline_block(t_step, reps, reqs, wl)
+        result["cpu_baseline"] = cpu_baseline(inp, mode, args.cpu_budget_s)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist is not None:

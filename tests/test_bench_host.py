@@ -69,3 +69,26 @@ def test_traffic_sources_follow_the_head_shape():
     assert {"verify_attn.cu", "worklist.cuh", "attn.h", "ptx.cuh", "common.cuh"} <= gqa & mla
     for p in bench.attn_src(W.WORKLOADS["mla"]) + bench.ACCEPT_SRC:
         assert os.path.isfile(p), p
+
+
+def test_oracle_baseline_complete_steps_one_core_and_pool():
+    """The CPU baseline times complete oracle steps; the pooled run (spawned worker
+    processes over memory-mapped inputs) computes what the one-core run computes."""
+    from oracle import dspark_oracle as O
+    inp = W.make_inputs(W.WORKLOADS["tiny"], 1)
+    ob = bench.OracleBaseline(inp, O.COMPACT, cores=2)
+    try:
+        h = ob.h
+        sch = O.schedule(h["conf"], h["conf_is_logit"], h["sts_temp"], h["cost_table"],
+                         ob.wl.max_tokens, O.COMPACT)
+        pk = O.pack(sch.windows, h["ctx_len"], h["anchor"], h["draft_tok"], h["tiers"],
+                    O.COMPACT, ob.wl.gamma)
+        tasks = [(r, int(pk.cu_seqlens[r]), int(pk.cu_seqlens[r + 1]), int(sch.windows[r]))
+                 for r in range(ob.wl.B)]
+        one = [bench._oracle_request(t) for t in tasks]
+        many = sorted(ob.start_pool().map(bench._oracle_request, tasks))
+        assert one == many
+        assert ob.step(False) > 0 and ob.step(True) > 0
+    finally:
+        ob.close()
+    assert not os.path.exists(ob.folder)
