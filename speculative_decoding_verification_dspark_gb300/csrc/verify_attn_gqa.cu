@@ -88,11 +88,14 @@ struct Cfg {
   static constexpr int OFF_RED = OFF_P + P_BUFS * P_BYTES;         // float wmax[2][4][NT]
   static constexpr int OFF_REF = OFF_RED + 2 * 4 * NT * 4;         // float mref[4][NT], alpha[4][NT]
   static constexpr int OFF_LS = OFF_REF + 2 * 4 * NT * 4;          // float lsum[4][NT]
-  static constexpr int OFF_ITEMS = OFF_LS + 4 * NT * 4;            // AttnItem[kSmemItems]
+  static constexpr int OFF_MT = OFF_LS + 4 * NT * 4;               // float mtrue[4][NT]
+  static constexpr int OFF_OVER = OFF_MT + 4 * NT * 4;              // int over[2][4]
+  static constexpr int OFF_ITEMS = OFF_OVER + 32;                   // AttnItem[kSmemItems]
   static constexpr int OFF_BAR = OFF_ITEMS + kSmemItems * (int)sizeof(AttnItem);
   // k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], xw[2], ep[2],
-  // o_free[2], stg_full, stg_free, p_full[PB], p_empty[PB], q_full[QB], q_empty[QB]
-  static constexpr int N_BARS = 20 + 2 * P_BUFS + 2 * Q_BUFS;
+  // o_free[2], stg_full, stg_free, p_full[PB], p_empty[PB], q_full[QB], q_empty[QB],
+  // xs[2]
+  static constexpr int N_BARS = 22 + 2 * P_BUFS + 2 * Q_BUFS;
   // epilogue: O / l is staged row-major (512 B per query row) in the P buffers
   static constexpr int STG_ROWS = P_BUFS * P_BYTES / (kD * 4);
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
@@ -216,6 +219,7 @@ struct Layout {
   __device__ uint32_t q_empty(int b) const {
     return bar(20 + 2 * Cfg<NT>::P_BUFS + Cfg<NT>::Q_BUFS + b);
   }
+  __device__ uint32_t xs(int b) const { return bar(20 + 2 * Cfg<NT>::P_BUFS + 2 * Cfg<NT>::Q_BUFS + b); }
 };
 
 // Work item `it` of this CTA: from shared memory for the first kSmemItems items.
@@ -284,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(L.s_full(b), 1);
       mbar_init(L.s_free(b), 4);
       mbar_init(L.xw(b), 4);
+      mbar_init(L.xs(b), 4);
       mbar_init(L.ep(b), 4);
       mbar_init(L.o_free(b), 4);
     }
@@ -541,7 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = prm.scale_log2;
     float* my_mref = s_mref + sw * NT;
     float* my_alpha = s_alpha + sw * NT;
-    int g = 0, n_it = 0, n_stg = 0, n_sf = 0;
+    float* my_mtrue = reinterpret_cast<float*>(bp + C::OFF_MT) + sw * NT;
+    int* s_over = reinterpret_cast<int*>(bp + C::OFF_OVER);  // [2][4]
+    int g = 0, n_it = 0, n_stg = 0, n_sf = 0, n_ov = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
       const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
@@ -567,9 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(L.s_full(sb), (g >> 1) & 1, cx)) { ok = false; break; }
         tc_fence_after();
         if constexpr (NT == 128) {
-        // NT = 128: two passes over the 32-column groups of S^T in rolled loops (the
-        // fully unrolled 128-column code outgrows the instruction cache next to the
-        // other roles' loops); the second pass reads S^T from TMEM again.
+        // NT = 128: passes over the 32-column groups of S^T in rolled loops (the fully
+        // unrolled 128-column code outgrows the instruction cache next to the other
+        // roles' loops).
         // Keys of this tile visible to column (query row) n: cache tile -> key < ctx;
         // block tile -> block row b visible to n iff b < n_r and n >= (b - i0) * G.
         const bool cache_tile = t < ct;
@@ -580,8 +587,81 @@ __global__ void __launch_bounds__(kThreads, 1)
           nmin = b < n_r ? (b - item.i0) * G : 0x7fffffff;
         }
         const uint32_t s_col = t_lane + C::TMEM_S + sb * NT;
-        // ---- pass 1: tile max per row (warp transpose-reduce), then across the 4 warps
         float* wmax = s_wmax + (g & 1) * 4 * NT;
+        const int pb = g % C::P_BUFS;
+        const uint32_t prow = L.pbuf(pb);
+        // ---- fast path (items with at most 32 query rows, every tile but the first):
+        // the references rarely move once a tile has set them, so P is computed in one
+        // pass against the current references; the 2^8 test that would move a
+        // reference is taken per key (a key above its row's reference + 8 is exactly a
+        // tile maximum above it), and only if some key of some warp passes it does the
+        // tile take the full path below, overwriting this P -- so P, the sums and the
+        // references are those of the full path bit for bit.  P is formed in registers
+        // while PV(g - 1) may still read the single P buffer; only the stores wait.
+        // (The epilogue's staging reads of the P buffer were waited for at the first
+        // tile's exchange.)  Items with more rows keep the two passes: there the max
+        // pass is what overlaps PV(g - 1).
+        bool full = l == 0 || ng > 1;
+        const bool tried_fast = !full;  // the fast pass used this tile's xw exchange
+        if (!full) {
+          float lnew0 = lacc[0];
+          bool over = false;
+          uint32_t pk[16];
+          {
+            float v[32];
+            tmem_ld32(s_col, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              v[k] = (key_dead || k < nmin) ? -INFINITY : v[k];
+              over = over || (v[k] * sl2 > my_mtrue[k] + 8.0f);
+            }
+#pragma unroll
+            for (int h = 0; h < 16; ++h) {
+              const int k = 2 * h;
+              const float p0 = fast_exp2(fmaf(v[k], sl2, -my_mref[k]));
+              const float p1 = fast_exp2(fmaf(v[k + 1], sl2, -my_mref[k + 1]));
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              v[k] = __low2float(b2);
+              v[k + 1] = __high2float(b2);
+              pk[h] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            lnew0 += transpose_reduce<false>(v, lane);
+          }
+          // the single P buffer: PV(g - 1) must be done with it
+          if (!wait_warp(L.p_empty((g - 1) % C::P_BUFS), ((g - 1) / C::P_BUFS) & 1, cx)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (q < nc8) {
+              const uint32_t off = sw128_off(kl, q);
+              st_shared_v4(prow + off, make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                                                  pk[4 * q + 3]));
+            }
+          }
+          // one flag per warp, exchanged once: does any reference move?
+          over = __any_sync(0xffffffffu, over);
+          if (lane == 0) s_over[(g & 1) * 4 + sw] = over ? 1 : 0;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(L.xw(g & 1));
+          if (!wait_warp(L.xw(g & 1), (g >> 1) & 1, cx)) { ok = false; break; }
+          full = (s_over[(g & 1) * 4] | s_over[(g & 1) * 4 + 1] | s_over[(g & 1) * 4 + 2] |
+                  s_over[(g & 1) * 4 + 3]) != 0;
+          if (!full) {
+            lacc[0] = lnew0;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(L.s_free(sb));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(L.p_full(pb));
+            continue;  // next tile
+          }
+        }
+        // ---- full path, pass 1: tile max per row (warp transpose-reduce), then across
+        // the 4 warps (on xw, or on xs when a fast pass already used xw for this tile)
 #pragma unroll 1
         for (int gi = 0; gi < ng; ++gi) {
           float v[32];
@@ -596,8 +676,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P buffers double as the epilogue's staging area: its bulk reads must be done
         // before any warp passes this exchange and writes P
         if (warp == kSoftmaxWarp0 && lane == 0) bulk_wait_read_all();
-        if (lane == 0) mbar_arrive(L.xw(g & 1));
-        if (!wait_warp(L.xw(g & 1), (g >> 1) & 1, cx)) { ok = false; break; }
+        if (!tried_fast) {
+          if (lane == 0) mbar_arrive(L.xw(g & 1));
+          if (!wait_warp(L.xw(g & 1), (g >> 1) & 1, cx)) { ok = false; break; }
+        } else {
+          if (lane == 0) mbar_arrive(L.xs(n_ov & 1));
+          if (!wait_warp(L.xs(n_ov & 1), (n_ov >> 1) & 1, cx)) { ok = false; break; }
+          ++n_ov;
+        }
         bool need_any = false;
 #pragma unroll
         for (int gi = 0; gi < C::G32; ++gi) {
@@ -612,12 +698,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             need_any = true;
           }
           my_mref[n] = mref[gi] == -INFINITY ? 0.f : mref[gi];
+          my_mtrue[n] = mref[gi];
           my_alpha[n] = alpha;
         }
         const bool rescale = __any_sync(0xffffffffu, need_any) && l > 0;
         __syncwarp();
         // P buffer of this tile must be free: PV(g - P_BUFS) done
-        const int pb = g % C::P_BUFS;
         if (g >= C::P_BUFS &&
             !wait_warp(L.p_empty((g - C::P_BUFS) % C::P_BUFS), ((g - C::P_BUFS) / C::P_BUFS) & 1, cx)) {
           ok = false;
@@ -646,7 +732,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // per-row partial sums over this warp's 32 keys.  Only the 8-column chunks
         // holding valid rows are written: padding columns of P^T are left as they are
         // -- they only reach their own columns of O^T, which are never stored.
-        const uint32_t prow = L.pbuf(pb);
 #pragma unroll 1
         for (int gi = 0; gi < ng; ++gi) {
           float v[32];
