@@ -26,7 +26,7 @@ Sources, cited by short name below:
 Parity status per function (what pins it is listed in tests/test_oracle_pins.py):
 pinned: confidence sigmoid, survival/STS, greedy schedule, pack, verify
 attention (GQA and MLA), acceptance (test, race, fallback, c*), compaction,
-calibration samples, ECE and the STS refit.  The composed ``step`` adds no arithmetic of its own and
+calibration samples, ECE and the STS refit, Markov-head draft sampling.  The composed ``step`` adds no arithmetic of its own and
 is pinned only through its parts (no page prints end-to-end values).
 """
 from __future__ import annotations
@@ -669,3 +669,50 @@ def attention_for(inp, packed, cu_seqlens, requests=None):
                 1.0 / math.sqrt(wl.d_qk))
         o[c0:c1], lse[c0:c1] = o_r, l_r
     return o, lse
+
+
+# ----------------------------------------------------------------------------
+# 9. Draft-side sampling with a Markov head
+# ----------------------------------------------------------------------------
+
+def markov_draft(U, W1, W2, anchor, exp_noise, tokens_given=None):
+    """The drafter's block sampled position by position ([notes] §05 "Core
+    Innovation A", 5.1-5.3): the parallel backbone gives base logits U_k for every
+    position k of the block, the sequential Markov head adds a bias that depends only
+    on the previous token, B(x_{k-1}, v) = (W1 W2)[x_{k-1}, v] (low rank, r = 256):
+
+        p_k(v | x_{<k}) = exp(U_k(v) + B(x_{k-1}, v)) / sum_u exp(U_k(u) + B(x_{k-1}, u))
+
+    with x_0 the anchor (the last committed token).  x_k is drawn by the Gumbel-max
+    in its exponential-race form, argmax_v p_k(v) / e_k(v) with e ~ Exp(1) given
+    (lowest index on ties; [notes] §02 sampling, reading A11).
+
+    U fp32 [B, gamma, V]; W1 [V, r] and W2 [r, V] (bf16 values, given as float);
+    anchor int [B]; exp_noise fp32 [B, gamma, V].  fp64 throughout (the bias is the
+    plain product of the previous token's W1 row with W2).  ``tokens_given``
+    (int [B, gamma], optional) makes position k condition on tokens_given[:, k-1]
+    instead of the oracle's own draw, so a chain can follow another sampler's tokens.
+    Returns (tokens int32 [B, gamma], p fp64 [B, gamma, V], keys fp64 [B, gamma, V]).
+    """
+    U = np.asarray(U, dtype=np.float64)
+    W1 = np.asarray(W1, dtype=np.float64)
+    W2 = np.asarray(W2, dtype=np.float64)
+    e = np.asarray(exp_noise, dtype=np.float64)
+    B, gamma, V = U.shape
+    tokens = np.zeros((B, gamma), dtype=np.int32)
+    P = np.zeros((B, gamma, V), dtype=np.float64)
+    K = np.zeros((B, gamma, V), dtype=np.float64)
+    for r in range(B):
+        prev = int(anchor[r])
+        for k in range(gamma):
+            logits = U[r, k] + W1[prev] @ W2
+            z = logits - logits.max()
+            w = np.exp(z)
+            p = w / w.sum()
+            keys = np.where(p > 0.0, p / e[r, k], -np.inf)
+            x = int(np.argmax(keys))          # first maximum: lowest index on ties
+            P[r, k], K[r, k] = p, keys
+            tokens[r, k] = x
+            prev = x if tokens_given is None else int(tokens_given[r, k])
+    return tokens, P, K
+

@@ -687,3 +687,74 @@ def test_sts_fit_degenerate_cases():
     s = [(np.float32(0.8), np.float32(0.8), 1), (np.float32(0.3), np.float32(0.3), 0)]
     T = float(O.sts_fit(s, 60))
     assert abs(T - 1.0 / 64) < 1e-6
+
+
+# ---------------------------------------------------------------- Markov-head draft sampling
+
+def test_markov_without_bias_is_the_backbone_softmax():
+    """W2 = 0: the Markov head adds nothing, so p_k = softmax(U_k) at every position
+    whatever the previous tokens (checked against scipy's softmax)."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(40)
+    B, gamma, V, r = 3, 4, 37, 8
+    U = rng.normal(0, 3, (B, gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 1, (V, r))
+    W2 = np.zeros((r, V))
+    e = rng.exponential(size=(B, gamma, V)).astype(np.float32)
+    _, P, _ = O.markov_draft(U, W1, W2, np.array([0, 5, 36]), e)
+    np.testing.assert_allclose(P, softmax(U.astype(np.float64), axis=-1), rtol=1e-12, atol=0)
+
+
+def test_markov_chain_follows_the_previous_token():
+    """A dominant transition bias B(x, v) = 50 [v == x + 1 mod V] (W1 = 50 I, W2 the
+    shift) with flat backbone logits: each position takes the token after the previous
+    one, starting from the anchor -- a bias read from the anchor at every position,
+    or from any other position, gives another chain."""
+    V = 8
+    W1 = 50.0 * np.eye(V)
+    W2 = np.roll(np.eye(V), 1, axis=1)          # W2[i, (i + 1) % V] = 1
+    B, gamma = 3, 6
+    U = np.zeros((B, gamma, V), np.float32)
+    rng = np.random.default_rng(41)
+    e = rng.uniform(0.5, 2.0, (B, gamma, V)).astype(np.float32)
+    anchor = np.array([0, 3, 7])
+    tok, P, _ = O.markov_draft(U, W1, W2, anchor, e)
+    for b in range(B):
+        assert tok[b].tolist() == [(anchor[b] + k + 1) % V for k in range(gamma)]
+    assert np.all(P.max(-1) >= 1 - 1e-15)
+
+
+def test_markov_race_is_the_gumbel_max():
+    """The exponential race argmax p / e is the Gumbel-max argmax log p + G with
+    G = -log e, by brute force over every entry, and equal keys go to the lowest index."""
+    rng = np.random.default_rng(42)
+    B, gamma, V, r = 4, 3, 23, 5
+    U = rng.normal(0, 2, (B, gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.5, (V, r))
+    W2 = rng.normal(0, 0.5, (r, V))
+    e = rng.exponential(size=(B, gamma, V)).astype(np.float32)
+    tok, P, _ = O.markov_draft(U, W1, W2, rng.integers(0, V, B), e)
+    for b in range(B):
+        for k in range(gamma):
+            gumbel = np.log(P[b, k]) - np.log(e[b, k].astype(np.float64))
+            assert tok[b, k] == int(np.argmax(gumbel))
+    # ties: flat logits, no bias, equal noise -> every key equal -> index 0
+    tok, _, _ = O.markov_draft(np.zeros((1, 2, 9), np.float32), np.zeros((9, 2)),
+                               np.zeros((2, 9)), np.array([4]), np.ones((1, 2, 9), np.float32))
+    assert tok.tolist() == [[0, 0]]
+
+
+def test_markov_conditioning_on_given_tokens():
+    """With tokens_given, position k is the one-step draw after tokens_given[:, k-1]:
+    the same p as a one-position block whose anchor is that token."""
+    rng = np.random.default_rng(43)
+    B, gamma, V, r = 2, 4, 19, 6
+    U = rng.normal(0, 2, (B, gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 1, (V, r))
+    W2 = rng.normal(0, 1, (r, V))
+    e = rng.exponential(size=(B, gamma, V)).astype(np.float32)
+    given = rng.integers(0, V, (B, gamma))
+    _, P, _ = O.markov_draft(U, W1, W2, np.array([1, 2]), e, tokens_given=given)
+    for k in range(1, gamma):
+        _, P1, _ = O.markov_draft(U[:, k:k + 1], W1, W2, given[:, k - 1], e[:, k:k + 1])
+        np.testing.assert_allclose(P[:, k], P1[:, 0], rtol=0, atol=0)
