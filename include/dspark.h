@@ -14,7 +14,7 @@
  *   [lesson] "DFlash 到 DSpark in SGLang：解码提速 4.3×，以及 DeepSeek-V4 支持"
  *            (AI Infra Visualized lesson on DSpark)
  *   [csdn]   DevPress/CSDN article on DSpark in SGLang (sections 2-5)
- *   [notes]  "DSpark：投机解码与生产级 Serving 学习笔记" (sections 02, 07, 08, 09)
+ *   [notes]  "DSpark：投机解码与生产级 Serving 学习笔记" (sections 02, 05, 07, 08, 09)
  *
  * Conventions shared by every entry point
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless the
@@ -386,6 +386,47 @@ size_t dspark_sts_fit_workspace_size(int gamma, int capacity);
 int dspark_sts_fit(const float* s_a, const int8_t* s_y, const int32_t* count, int capacity,
                    int gamma, int iters, float* temps, void* workspace, size_t ws_bytes,
                    void* stream);
+
+/* ---------------------------------------------------------------------------
+ * dspark_markov_draft -- draft-side sampling of one block with a Markov head
+ * ([notes] 05 "Core Innovation A", 5.1-5.3: the parallel backbone gives base
+ * logits U_1..U_gamma for the whole block, the sequential head adds the bias
+ * B(x_{k-1}, v) ~ (W1 W2)[x_{k-1}, v] of the previous token, rank 256; [lesson]
+ * "Zero-overhead scheduling 与 kernel": the drafter's sampling folded into fused
+ * kernels).  For k = 0..gamma-1, every request r:
+ *     logit[v] = U[r, k, v] + sum_j W1[x, j] W2[j, v]     x = anchor[r] (k = 0)
+ *                                                          or draft_tok[r, k-1]
+ *     p_draft[r, k, :] = softmax(logit)
+ *     draft_tok[r, k]  = argmax_v p_draft[r, k, v] / exp_noise[r, k, v]
+ * (the exponential race, lowest index on ties; decided on logit - ln(noise), the
+ * same order up to rounding).  p_draft and exp_noise then feed dspark_accept.
+ *
+ *   U          fp32 [B, gamma, V]  the backbone's base logits
+ *   W1         bf16 [V, rank]      token embedding of the head (row x = token x)
+ *   W2         bf16 [rank, V]      projection of the head
+ *   rank       must be 256 (DSPARK_EUNSUPPORTED otherwise)
+ *   anchor     int32 [B]           the last committed token of each request
+ *   exp_noise  fp32 [B, gamma, V]  Exp(1) draws, > 0
+ *   draft_tok  int32 [B, gamma]    out
+ *   p_draft    fp32 [B, gamma, V]  out
+ * V a multiple of 128 with V / 128 <= 16 x (SM count) (311,296 on GB300);
+ * B <= DSPARK_MAX_B (one launch per 32 requests, or per 16 when V / 128 is above
+ * 8 x the SM count); gamma <= DSPARK_MAX_GAMMA; U, W1, W2, exp_noise, p_draft
+ * 16-byte aligned.  An anchor outside [0, V) sets DSPARK_DEVERR_BAD_INPUT and
+ * reads row 0.  Computation: bf16 products with fp32 accumulation, the softmax
+ * and race in fp32.
+ *
+ * Each launch is a cooperative grid of one CTA per SM that meets at one grid
+ * barrier per position; all of its waits are bounded (DSPARK_DEVERR_WAIT_TIMEOUT).
+ * Workspace: dspark_markov_draft_workspace_size(V) bytes, 256-byte aligned, ZEROED
+ * by the caller before its first use and again after any device error; calls on
+ * one stream may share it, calls that may run at once may not.
+ * ------------------------------------------------------------------------- */
+size_t dspark_markov_draft_workspace_size(int V);
+int dspark_markov_draft(const float* U, const void* W1, const void* W2, int rank,
+                        const int32_t* anchor, const float* exp_noise, int B, int gamma, int V,
+                        int32_t* draft_tok, float* p_draft, void* workspace, size_t ws_bytes,
+                        void* stream);
 
 /* ---------------------------------------------------------------------------
  * dspark_step_graph -- the whole verification step as one CUDA graph, with the

@@ -46,6 +46,8 @@ _SIGNATURES = {
     "dspark_calib_ece": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "dspark_sts_fit_workspace_size": (_Z, [_I, _I]),
     "dspark_sts_fit": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
+    "dspark_markov_draft_workspace_size": (_Z, [_I]),
+    "dspark_markov_draft": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "dspark_pack": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dspark_verify_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "dspark_verify_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I,
@@ -190,6 +192,32 @@ class CalibStore:
             _ptr(self.s_a), _ptr(self.s_y), _ptr(self.count), self.capacity, self.gamma,
             int(iters), _ptr(temps), _ptr(self.ws), self.ws.numel(), _stream(stream)))
         return temps
+
+
+class MarkovDraft:
+    """Draft-side sampling of one block with a Markov head (dspark_markov_draft).
+    Holds the call's workspace, zeroed once at construction; calls on one stream
+    share it."""
+
+    def __init__(self, V, device="cuda"):
+        n = lib().dspark_markov_draft_workspace_size(int(V))
+        if n == 0:
+            raise ValueError(f"vocabulary size {V} is not supported (a multiple of 128 is needed)")
+        self.V = int(V)
+        self.ws = torch.zeros(n, dtype=torch.uint8, device=torch.device(device))
+
+    def __call__(self, U, W1, W2, anchor, exp_noise, draft_tok=None, p_draft=None, stream=None):
+        """U, exp_noise fp32 [B, gamma, V]; W1 bf16 [V, 256]; W2 bf16 [256, V]; anchor
+        int32 [B].  Returns (draft_tok int32 [B, gamma], p_draft fp32 [B, gamma, V])."""
+        B, gamma, V = U.shape
+        if draft_tok is None:
+            draft_tok = torch.empty(B, gamma, dtype=torch.int32, device=U.device)
+        if p_draft is None:
+            p_draft = torch.empty(B, gamma, V, dtype=torch.float32, device=U.device)
+        _check("dspark_markov_draft", lib().dspark_markov_draft(
+            _ptr(U), _ptr(W1), _ptr(W2), int(W2.shape[0]), _ptr(anchor), _ptr(exp_noise), B, gamma,
+            V, _ptr(draft_tok), _ptr(p_draft), _ptr(self.ws), self.ws.numel(), _stream(stream)))
+        return draft_tok, p_draft
 
 
 def _host_ptr(t):

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdspark.so")
 SOURCES = ["api.cu", "schedule_pack.cu", "accept.cu", "compact.cu", "verify_attn.cu", "step_graph.cu",
-           "calib.cu",
+           "calib.cu", "markov_draft.cu",
            "verify_attn_gqa.cu", "verify_attn_mla.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -398,4 +398,28 @@ int dspark_sts_fit(const float* s_a, const int8_t* s_y, const int32_t* count, in
                         temps, static_cast<cudaStream_t>(stream));
 }
 
+size_t dspark_markov_draft_workspace_size(int V) {
+  if (V < 128 || V % 128 != 0) return 0;
+  return markov_workspace(V);
+}
+
+int dspark_markov_draft(const float* U, const void* W1, const void* W2, int rank,
+                        const int32_t* anchor, const float* exp_noise, int B, int gamma, int V,
+                        int32_t* draft_tok, float* p_draft, void* workspace, size_t ws_bytes,
+                        void* stream) {
+  CHECK(U && W1 && W2 && anchor && exp_noise && draft_tok && p_draft && workspace, DSPARK_EINVAL);
+  CHECK(rank == 256, DSPARK_EUNSUPPORTED);
+  CHECK(V >= 128 && V % 128 == 0, DSPARK_EUNSUPPORTED);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
+  CHECK(aligned16(U) && aligned16(W1) && aligned16(W2) && aligned16(exp_noise) && aligned16(p_draft),
+        DSPARK_EINVAL);
+  CHECK((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  CHECK(markov_supported(V, nullptr), DSPARK_EUNSUPPORTED);
+  CHECK(ws_bytes >= markov_workspace(V), DSPARK_ENOSPACE);
+  return launch_markov_draft(U, W1, W2, anchor, exp_noise, B, gamma, V, draft_tok, p_draft,
+                             workspace, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -63,6 +63,9 @@ constexpr int kKeyTile = 128;
 // bf16 tiled tensor map, 128-byte swizzle (rank <= 5; strides in bytes of dims 1..).
 bool encode_bf16_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                      const uint64_t* strides, const uint32_t* box);
+// The same for fp32 data without swizzle (rows land in shared memory packed).
+bool encode_f32_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box);
 }  // namespace gqa
 
 namespace mla {

@@ -76,6 +76,14 @@ int launch_calib_ece(const float* s_ahat, const int8_t* s_y, const int32_t* coun
 int launch_sts_fit(const float* s_a, const int8_t* s_y, const int32_t* count, int cap, int gamma,
                    int iters, float* zbuf, float* temps, cudaStream_t stream);
 
+// Markov-head draft sampling (markov_draft.cu).  markov_supported: whether a vocabulary
+// of V fits the kernel on the current device, and the requests one launch takes.
+bool markov_supported(int V, int* group);
+size_t markov_workspace(int V);
+int launch_markov_draft(const float* U, const void* W1, const void* W2, const int32_t* anchor,
+                        const float* exp_noise, int B, int gamma, int V, int32_t* draft_tok,
+                        float* p_draft, void* ws, cudaStream_t stream);
+
 size_t compact_workspace(int B);
 int launch_compact(const void* k_new, const void* v_new, int row_bytes, int max_rows,
                    const int32_t* cu,

@@ -71,6 +71,19 @@ def test_host_validation_without_device(lib):
                                      16384, fake, fake, fake, fake, nul, nul) == -4
     assert lib.dspark_accept_noalloc(fake, fake, 0, 1001, fake, fake, fake, fake, fake, 0, 4, 6, 8,
                                      fake, fake, fake, fake, nul, nul) == -2
+    # Markov-head draft: NULL pointers, a rank other than 256, a vocabulary that is not a
+    # multiple of 128, gamma above the maximum, misaligned logits
+    ws = lib.dspark_markov_draft_workspace_size(1024)
+    assert lib.dspark_markov_draft(nul, fake, fake, 256, fake, fake, 4, 6, 1024, fake, fake, fake,
+                                   ws, nul) == -1
+    assert lib.dspark_markov_draft(fake, fake, fake, 128, fake, fake, 4, 6, 1024, fake, fake, fake,
+                                   ws, nul) == -2
+    assert lib.dspark_markov_draft(fake, fake, fake, 256, fake, fake, 4, 6, 1000, fake, fake, fake,
+                                   ws, nul) == -2
+    assert lib.dspark_markov_draft(fake, fake, fake, 256, fake, fake, 4, 33, 1024, fake, fake, fake,
+                                   ws, nul) == -1
+    assert lib.dspark_markov_draft(ctypes.c_void_p(4100), fake, fake, 256, fake, fake, 4, 6, 1024,
+                                   fake, fake, fake, ws, nul) == -1
 
 
 def test_workspace_sizes_are_host_computable(lib):
@@ -80,6 +93,9 @@ def test_workspace_sizes_are_host_computable(lib):
     assert lib.dspark_verify_attn_workspace_size(32, 512, 32, 8, 96, 96, 8, 9) == 0
     assert lib.dspark_accept_workspace_size(32, 8, 512, 151936) > 0
     assert lib.dspark_compact_workspace_size(32) > 0
+    assert lib.dspark_markov_draft_workspace_size(151936) > 0
+    assert lib.dspark_markov_draft_workspace_size(151936) == lib.dspark_markov_draft_workspace_size(1024)
+    assert lib.dspark_markov_draft_workspace_size(1000) == 0
 
 
 def test_step_graph_rejects_bad_descriptors_on_the_host(lib):

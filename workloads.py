@@ -275,6 +275,42 @@ def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
     return out
 
 
+# Markov-head draft sampling: the drafter's block of base logits and a random head.
+MARKOV_WORKLOADS = {
+    # Qwen3-8B vocabulary, the verification workload's batch and block
+    "markov_qwen3_8b": dict(B=32, gamma=8, V=151936),
+    # parity cases: one request; a ragged column group; one tile per CTA; a partly
+    # filled last round of tiles over two launches; sixteen tiles per CTA
+    "markov_one": dict(B=1, gamma=1, V=1024),
+    "markov_small": dict(B=5, gamma=6, V=1024),
+    "markov_g32": dict(B=32, gamma=6, V=4096),
+    "markov_ragged": dict(B=37, gamma=4, V=40960),
+    "markov_wide": dict(B=20, gamma=2, V=311296),
+}
+
+
+@torch.no_grad()
+def make_markov_inputs(B: int, gamma: int, V: int, seed: int = 0, device: str = "cpu",
+                       rank: int = 256, u_std: float = 3.0, w_std: float = 0.25) -> dict:
+    """Base logits U ~ N(0, u_std^2) fp32 [B, gamma, V]; head weights W1 [V, rank] and
+    W2 [rank, V] ~ N(0, w_std^2) rounded to bf16 (with rank 256 and w_std 0.25 the bias
+    of a token has standard deviation about 1); anchors uniform on [0, V); exp_noise
+    = -ln(U) with U uniform on the open interval (Exp(1) draws), fp32 [B, gamma, V]."""
+    dev = torch.device(device)
+    out = {}
+    out["U"] = u_std * torch.randn((B, gamma, V), generator=_gen(seed, "markov_U", dev), device=dev,
+                                   dtype=torch.float32)
+    out["W1"] = (w_std * torch.randn((V, rank), generator=_gen(seed, "markov_W1", dev), device=dev,
+                                     dtype=torch.float32)).to(torch.bfloat16)
+    out["W2"] = (w_std * torch.randn((rank, V), generator=_gen(seed, "markov_W2", dev), device=dev,
+                                     dtype=torch.float32)).to(torch.bfloat16)
+    out["anchor"] = torch.randint(0, V, (B,), generator=_gen(seed, "markov_anchor", dev), device=dev,
+                                  dtype=torch.int32)
+    u = _uniform_open01_f32((B, gamma, V), _gen(seed, "markov_noise", dev), dev)
+    out["exp_noise"] = (-torch.log(u.to(torch.float64))).to(torch.float32)
+    return out
+
+
 def to_packed(dense: torch.Tensor, cu_seqlens: torch.Tensor, total_rows: int) -> torch.Tensor:
     """Lay per-position rows out head-to-tail: row cu_seqlens[r] + i <- dense[r, i].
 
