@@ -9,8 +9,9 @@ that every step does identical work.
 
 The same run also measures (keys of the one JSON line): the B=256 mixed-traffic
 workload in its three modes and the latent-KV (MLA) workload (``workloads``), and
-the budget/tier sweep over B x confidence mean x cost slope x mode (``sweep``);
-``--no-extra`` skips both.  The CPU oracle is timed on complete steps, on one
+the budget/tier sweep over B x confidence mean x cost slope x mode (``sweep``), the
+calibration tooling (``calibration``) and the Markov-head draft sampler at the
+Qwen3-8B vocabulary (``markov_draft``); ``--no-extra`` skips them.  The CPU oracle is timed on complete steps, on one
 core and on all the host's cores (``cpu_baseline``).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -569,6 +570,74 @@ def calib_arm(seed):
             "sts_fit_bisections": 36, "ece_bins": 15}
 
 
+MARKOV_SRC = [os.path.join(_CSRC, f) for f in ("markov_draft.cu", "ptx.cuh", "common.cuh")]
+
+
+def markov_bytes(B, gamma, V, rank=256):
+    """Algorithmic bytes of one draft block: W2 read once, the base logits U and the
+    noise read once, p written once, the W1 rows of the B*gamma conditioning tokens,
+    the anchors and the tokens."""
+    return rank * V * 2 + 3 * B * gamma * V * 4 + B * gamma * rank * 2 + B * 4 + B * gamma * 4
+
+
+def markov_arm(seed, reps=20, oracle_rows=2):
+    """Markov-head draft sampling of one block (dspark_markov_draft) at the Qwen3-8B
+    vocabulary with the verification workload's batch and block (B = 32, gamma = 8,
+    V = 151936, rank 256): device time per block with L2 flushed before each call,
+    its HBM roofline, and the oracle timed on `oracle_rows` request rows (fp64)."""
+    import speculative_decoding_verification_dspark_gb300 as dspark
+    cfg = W.MARKOV_WORKLOADS["markov_qwen3_8b"]
+    B, gamma, V = cfg["B"], cfg["gamma"], cfg["V"]
+    inp = W.make_markov_inputs(B, gamma, V, seed=seed, device="cuda")
+    md = dspark.MarkovDraft(V)
+    tok = torch.empty(B, gamma, dtype=torch.int32, device="cuda")
+    p = torch.empty(B, gamma, V, dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    args = (inp["U"], inp["W1"], inp["W2"], inp["anchor"], inp["exp_noise"], tok, p)
+    for _ in range(3):
+        md(*args)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        md(*args)
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    check_device_error("markov draft")
+    us = statistics.median(ts)
+    nbytes = markov_bytes(B, gamma, V)
+    pk = peak_values()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    # the oracle (CPU baseline leg): the same block for a few request rows
+    from oracle import dspark_oracle as O
+    rows = slice(0, oracle_rows)
+    U = inp["U"][rows].cpu().numpy()
+    W1 = inp["W1"].float().cpu().numpy()
+    W2 = inp["W2"].float().cpu().numpy()
+    e = inp["exp_noise"][rows].cpu().numpy()
+    anc = inp["anchor"][rows].cpu().numpy()
+    t0 = time.perf_counter()
+    O.markov_draft(U, W1, W2, anc, e)
+    t_row = (time.perf_counter() - t0) / oracle_rows
+    del inp, p, flush
+    torch.cuda.empty_cache()
+    return {"workload": f"Markov-head draft block: B={B}, gamma={gamma}, V={V}, rank 256, "
+                        "fp32 U and noise, bf16 W1/W2 (random weights)",
+            "us_per_block": us, "us_min": min(ts), "blocks_per_s": 1e6 / us,
+            "draft_tokens_per_s": B * gamma * 1e6 / us, "launches_per_block": -(-B // 32),
+            "l2": "flushed before each call (256 MB written)",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm"], "algorithmic_bytes": nbytes,
+                         "traffic": load_traffic("markov_draft", "markov_qwen3_8b", MARKOV_SRC),
+                         "peak_source": f"{pk['hbm_src']} hbm_gbs (burst copy)"},
+            "cpu_oracle": {"blocks_per_s": 1.0 / (t_row * B), "cores": 1, "kind": "oracle",
+                           "sample": f"{oracle_rows} request rows of the block (fp64), scaled "
+                                     f"to {B} rows"}}
+
+
 def e2e_arm(args, run):
     """The same step through the public API with the step's inputs in pinned host
     memory: host-to-device copies of the inputs (the M packed rows of the per-row
@@ -880,6 +949,7 @@ def main():
         result["workloads"] = workloads_arm(args.seed)
         result["sweep"] = sweep_arm(args.seed)
         result["calibration"] = calib_arm(args.seed)
+        result["markov_draft"] = markov_arm(args.seed)
         result["extra_wall_s"] = time.perf_counter() - t0
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, mode, args.cpu_budget_s)
