@@ -18,7 +18,8 @@ Sources, cited by short name below:
             "DSpark：sequential head 加验证预算", "Confidence scheduler 与 verify 模式",
             "Ragged verify under full CUDA graphs", "Zero-overhead scheduling 与 kernel".
 * [csdn]    DevPress/CSDN article on DSpark in SGLang, sections "2." (verify modes),
-            "3." (ragged packing), "4." (additive cost model T(bs,K)), "5." (observability).
+            "3." (ragged packing), "4." (additive cost model T(bs,K)), "5." (observability,
+            including the block-accept estimator).
 * [notes]   "DSpark：投机解码与生产级 Serving 学习笔记", sections "02 · Speculative
             Decoding", "07 · Confidence Head", "08 · Hardware-Aware Prefix Scheduler",
             "09 · End-to-End Cycle".
@@ -26,7 +27,8 @@ Sources, cited by short name below:
 Parity status per function (what pins it is listed in tests/test_oracle_pins.py):
 pinned: confidence sigmoid, survival/STS, greedy schedule, pack, verify
 attention (GQA and MLA), acceptance (test, race, fallback, c*), compaction,
-calibration samples, ECE and the STS refit, Markov-head draft sampling.  The composed ``step`` adds no arithmetic of its own and
+calibration samples, ECE and the STS refit, Markov-head draft sampling, the
+block-accept estimate.  The composed ``step`` adds no arithmetic of its own and
 is pinned only through its parts (no page prints end-to-end values).
 """
 from __future__ import annotations
@@ -716,3 +718,47 @@ def markov_draft(U, W1, W2, anchor, exp_noise, tokens_given=None):
             prev = x if tokens_given is None else int(tokens_given[r, k])
     return tokens, P, K
 
+
+
+# ----------------------------------------------------------------------------
+# 10. Block-accept estimator: the uncut cap from inside a compact run
+# ----------------------------------------------------------------------------
+
+def block_accept_estimate(p_target, p_draft, draft_tok, uniforms, windows, cu_seqlens,
+                          accept_len, cap_len, mode, gamma):
+    """The accepted-prefix length a full-block verification would have seen (the
+    cap that cap-accept exposes), recovered inside the step ([csdn] 5 "可观测性":
+    compact verifies only the window, so the uncut cap is censored; the estimator
+    recovers an interval for it from tensors the run already has).
+
+    Reading A29.  Compact mode, request r with window w and L accepted drafts:
+      * L < w: a draft inside the window was rejected, the cap is L;
+      * L = w = gamma: the whole block was verified and accepted, the cap is gamma;
+      * L = w < gamma: the step holds the target row of position w + 1 (the bonus
+        row, packed row cu_seqlens[r] + w) and the drafter's row of that position,
+        so the test a full-block run makes at w + 1 is made here with the same
+        operands (u_{w+1} p_d(d_{w+1}) <= p_t(d_{w+1}), fp32):
+          rejected -> the cap is w;  accepted -> the cap lies in [w + 1, gamma].
+    Static and cap-accept modes verify the whole block: the cap is cap_len.
+
+    Returns (cap_lo, cap_hi) int32 [B]; cap_lo == cap_hi where the cap is known.
+    """
+    B = len(windows)
+    lo = np.zeros(B, dtype=np.int32)
+    hi = np.zeros(B, dtype=np.int32)
+    for r in range(B):
+        if mode != COMPACT:
+            lo[r] = hi[r] = int(cap_len[r])
+            continue
+        w, L = int(windows[r]), int(accept_len[r])
+        if L < w or w == gamma:
+            lo[r] = hi[r] = L
+            continue
+        x = int(draft_tok[r, w])                       # d_{w+1}
+        pt = F32(p_target[int(cu_seqlens[r]) + w, x])  # target row of position w + 1
+        pd = F32(p_draft[r, w, x])
+        if F32(F32(uniforms[r, w]) * pd) <= pt:
+            lo[r], hi[r] = w + 1, gamma
+        else:
+            lo[r] = hi[r] = w
+    return lo, hi

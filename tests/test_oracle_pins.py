@@ -758,3 +758,84 @@ def test_markov_conditioning_on_given_tokens():
     for k in range(1, gamma):
         _, P1, _ = O.markov_draft(U[:, k:k + 1], W1, W2, given[:, k - 1], e[:, k:k + 1])
         np.testing.assert_allclose(P[:, k], P1[:, 0], rtol=0, atol=0)
+
+
+# ------------------------------------------------------------------ block-accept estimate
+
+def _estimate_case(rng, B=64, gamma=6, V=16):
+    """Per-position target rows for positions 1..gamma+1 (the same rows in every mode,
+    reading A18), drafter rows, drafts drawn from them, uniforms, windows 0..gamma;
+    the target leans towards the drafter by a per-request amount so that accepted
+    prefixes of every length occur."""
+    p_d = rng.dirichlet(np.ones(V) * 0.5, size=(B, gamma)).astype(np.float32)
+    mix = rng.uniform(0.0, 1.0, size=(B, 1, 1))
+    mix[:2] = 1.0   # p_t = p_d: every draft is accepted (u < 1)
+    rnd = rng.dirichlet(np.ones(V) * 0.5, size=(B, gamma + 1))
+    pd_ext = np.concatenate([p_d, p_d[:, -1:]], axis=1)
+    p_t = (mix * pd_ext + (1 - mix) * rnd).astype(np.float32)
+    def draw(row):
+        q = row.astype(np.float64)
+        return rng.choice(V, p=q / q.sum())
+    d = np.array([[draw(p_d[r, j]) for j in range(gamma)] for r in range(B)], np.int32)
+    u = rng.uniform(1e-6, 1.0, size=(B, gamma)).astype(np.float32)
+    e = rng.exponential(size=(B, V)).astype(np.float32) + np.float32(1e-3)
+    win = rng.integers(0, gamma + 1, size=B).astype(np.int32)
+    win[0], win[1] = gamma, gamma // 2   # a whole-block window; an open interval
+    return p_t, p_d, d, u, e, win
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_block_accept_estimate_brackets_the_full_block_cap(seed):
+    """The interval from a compact run contains the cap a cap-accept run on the same
+    inputs sees (the definition of the censored quantity), and is exact wherever the
+    compact run holds the deciding test: a rejection inside the window, the whole
+    block as window, or a rejection at position w + 1 (the bonus row)."""
+    rng = np.random.default_rng(100 + seed)
+    gamma = 6
+    p_t, p_d, d, u, e, win = _estimate_case(rng, gamma=gamma)
+    B = len(win)
+    cu_c = np.concatenate([[0], np.cumsum(1 + win)])
+    a_c = O.accept(_rows_for(p_t, cu_c, B), p_d, d, u, e, win, cu_c, O.COMPACT, gamma)
+    full = np.full(B, gamma, np.int32)
+    cu_f = np.concatenate([[0], np.cumsum(1 + full)])
+    a_f = O.accept(_rows_for(p_t, cu_f, B), p_d, d, u, e, win, cu_f, O.CAP_ACCEPT, gamma)
+    lo, hi = O.block_accept_estimate(_rows_for(p_t, cu_c, B), p_d, d, u, win, cu_c,
+                                     a_c.accept_len, a_c.cap_len, O.COMPACT, gamma)
+    cap = a_f.cap_len
+    assert np.all(lo <= cap) and np.all(cap <= hi)
+    for r in range(B):
+        w, L = int(win[r]), int(a_c.accept_len[r])
+        if L < w or w == gamma or cap[r] == w:
+            assert lo[r] == hi[r] == cap[r], r
+        else:   # the test at w + 1 accepted: only the lower end is known
+            assert (lo[r], hi[r]) == (w + 1, gamma) and cap[r] >= w + 1, r
+    # every kind of case occurs
+    kinds = {("in" if a_c.accept_len[r] < win[r] else "full" if win[r] == gamma else
+              "w+1 rejects" if lo[r] == hi[r] else "open") for r in range(B)}
+    assert kinds == {"in", "full", "w+1 rejects", "open"}
+    # the other modes report the cap they verified
+    for mode in (O.STATIC, O.CAP_ACCEPT):
+        lo2, hi2 = O.block_accept_estimate(_rows_for(p_t, cu_f, B), p_d, d, u, full, cu_f,
+                                           a_f.accept_len, a_f.cap_len, mode, gamma)
+        assert np.array_equal(lo2, a_f.cap_len) and np.array_equal(hi2, a_f.cap_len)
+
+
+@pytest.mark.parametrize("accept_first", [2, 3, 4])
+def test_block_accept_estimate_on_the_page_example(accept_first):
+    """The three-mode example of [lesson] "Confidence scheduler 与 verify 模式" (block 6,
+    window 3) with the target accepting the first k drafts: a rejection inside the
+    window (k = 2) gives 2; the rejection right after the window (k = 3) is seen in the
+    bonus row and gives 3; the page's own case (k = 4, the cap that cap-accept exposes)
+    gives the interval [4, 6], which holds the cap-accept run's cap."""
+    g = _gold("three_mode_example.json")
+    gamma, w = g["gamma"], g["window"]
+    p_t, p_d, d, u, e = _three_mode_setup(accept_first, gamma)
+    win = np.array([w], np.int32)
+    cu = np.array([0, w + 1])
+    a = O.accept(_rows_for(p_t, cu, 1), p_d, d, u, e, win, cu, O.COMPACT, gamma)
+    lo, hi = O.block_accept_estimate(_rows_for(p_t, cu, 1), p_d, d, u, win, cu, a.accept_len,
+                                     a.cap_len, O.COMPACT, gamma)
+    want = {2: (2, 2), 3: (3, 3), 4: (4, gamma)}[accept_first]
+    assert (int(lo[0]), int(hi[0])) == want
+    if accept_first == g["target_accepts_first"]:
+        assert lo[0] <= g["expect"]["cap_accept"]["cap_len"] <= hi[0]
