@@ -310,6 +310,36 @@ int dspark_accept_noalloc(const void* p_target, const void* p_draft, int pdt, in
                           int32_t* fallback, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * dspark_block_accept_estimate -- the uncut cap from inside a compact run
+ * ([csdn] 5 "可观测性": compact verifies only the scheduler's window, so how many
+ * drafts a full-block verification would have accepted is censored; the block-
+ * accept estimator recovers an interval for it inside the compact run, without a
+ * companion cap-accept run).  Run after dspark_accept on the same step's tensors.
+ *
+ * For request r (compact mode), window w, accepted length L = accept_len[r]:
+ *   L < w          -> cap_lo = cap_hi = L   (a draft inside the window was rejected)
+ *   L = w = gamma  -> cap_lo = cap_hi = gamma
+ *   L = w < gamma  -> the step holds the target row of position w + 1 (the bonus
+ *                     row, packed row cu_seqlens[r] + w) and the drafter's row of
+ *                     that position, so the full-block test at w + 1 is made here
+ *                     with the same operands: u_{w+1} p_d(d_{w+1}) <= p_t(d_{w+1})
+ *                     (fp32) rejected -> cap_lo = cap_hi = w; accepted ->
+ *                     cap_lo = w + 1, cap_hi = gamma.
+ * Static and cap-accept modes verified the whole block: cap_lo = cap_hi = cap_len[r].
+ * Arguments as dspark_accept's (p_target packed [max_rows, V], p_draft [B, gamma, V]
+ * of type pdt; draft_tok, uniforms [B, gamma]; windows [B]; cu_seqlens [B+1]) plus
+ * accept_len, cap_len [B] from dspark_accept; cap_lo, cap_hi int32 [B] out.  A bonus
+ * row outside the request's segment or past max_rows, or a draft token outside
+ * [0, V), sets DSPARK_DEVERR_BAD_INPUT and gives cap_lo = cap_hi = L.
+ * ------------------------------------------------------------------------- */
+int dspark_block_accept_estimate(const void* p_target, const void* p_draft, int pdt, int V,
+                                 const int32_t* draft_tok, const float* uniforms,
+                                 const int32_t* windows, const int32_t* cu_seqlens,
+                                 const int32_t* accept_len, const int32_t* cap_len, int mode,
+                                 int B, int gamma, int max_rows, int32_t* cap_lo, int32_t* cap_hi,
+                                 void* stream);
+
+/* ---------------------------------------------------------------------------
  * dspark_compact -- commit the step ([lesson] "Zero-overhead scheduling 与
  * kernel": compact scatter, device-resident page table).
  *

@@ -46,6 +46,8 @@ _SIGNATURES = {
     "dspark_calib_ece": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "dspark_sts_fit_workspace_size": (_Z, [_I, _I]),
     "dspark_sts_fit": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
+    "dspark_block_accept_estimate": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                          _P, _P, _P]),
     "dspark_markov_draft_workspace_size": (_Z, [_I]),
     "dspark_markov_draft": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "dspark_pack": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -315,6 +317,23 @@ def accept_noalloc(p_target, p_draft, draft_tok, uniforms, exp_noise, windows, c
         _ptr(p_target), _ptr(p_draft), pdt, V, _ptr(draft_tok), _ptr(uniforms), _ptr(exp_noise),
         _ptr(windows), _ptr(cu_seqlens), int(mode), B, gamma, p_target.shape[0], _ptr(accept_len),
         _ptr(cap_len), _ptr(out_tok), _ptr(cstar), _ptr(fallback), _stream(stream)))
+
+
+def block_accept_estimate(p_target, p_draft, draft_tok, uniforms, windows, cu_seqlens, mode,
+                          accept_len, cap_len, cap_lo=None, cap_hi=None, stream=None):
+    """The uncut cap's interval (cap_lo, cap_hi) int32 [B] from a step's acceptance
+    outputs (dspark_block_accept_estimate)."""
+    B, gamma, V = p_draft.shape
+    pdt = BF16 if p_target.dtype == torch.bfloat16 else F32
+    if cap_lo is None:
+        cap_lo = torch.empty(B, dtype=torch.int32, device=p_draft.device)
+    if cap_hi is None:
+        cap_hi = torch.empty(B, dtype=torch.int32, device=p_draft.device)
+    _check("dspark_block_accept_estimate", lib().dspark_block_accept_estimate(
+        _ptr(p_target), _ptr(p_draft), pdt, V, _ptr(draft_tok), _ptr(uniforms), _ptr(windows),
+        _ptr(cu_seqlens), _ptr(accept_len), _ptr(cap_len), int(mode), B, gamma,
+        p_target.shape[0], _ptr(cap_lo), _ptr(cap_hi), _stream(stream)))
+    return cap_lo, cap_hi
 
 
 def compact_workspace_size(B) -> int:

@@ -696,6 +696,71 @@ void* accept_fixed_scratch() {
   });
 }
 
+// Block-accept estimate, thread per request: in compact mode a request whose whole
+// window was accepted is tested at position w + 1 on its bonus row (the target row of
+// that position, packed row cu[r] + w) against the drafter's row w + 1, as a
+// full-block verification would test it; the cap is then w (rejected) or lies in
+// [w + 1, gamma].  Otherwise the cap is the accepted length (compact) or cap_len.
+template <class T>
+__global__ void __launch_bounds__(128)
+    accept_estimate_kernel(const T* __restrict__ p_t, const T* __restrict__ p_d, int V,
+                           const int32_t* __restrict__ draft_tok, const float* __restrict__ uniforms,
+                           const int32_t* __restrict__ windows, const int32_t* __restrict__ cu,
+                           const int32_t* __restrict__ accept_len, const int32_t* __restrict__ cap_len,
+                           int mode, int B, int gamma, int max_rows, int32_t* __restrict__ cap_lo,
+                           int32_t* __restrict__ cap_hi, unsigned int* __restrict__ err) {
+  pdl_release();
+  pdl_wait();  // the acceptance's outputs
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= B) return;
+  if (mode != DSPARK_COMPACT) {
+    cap_lo[r] = cap_len[r];
+    cap_hi[r] = cap_len[r];
+    return;
+  }
+  const int w = windows[r], L = accept_len[r];
+  int lo = L, hi = L;
+  if (L >= w && w < gamma) {
+    const int row = cu[r] + w;
+    const int x = w >= 0 ? draft_tok[r * gamma + w] : -1;
+    if (w < 0 || row >= cu[r + 1] || row >= max_rows || x < 0 || x >= V) {
+      raise_error(err, DSPARK_DEVERR_BAD_INPUT);
+    } else {
+      const float pt = ld_p(p_t, (long long)row * V + x);
+      const float pd = ld_p(p_d, ((long long)r * gamma + w) * V + x);
+      if (__fmul_rn(uniforms[r * gamma + w], pd) <= pt) {
+        lo = w + 1;
+        hi = gamma;
+      } else {
+        lo = hi = w;
+      }
+    }
+  }
+  cap_lo[r] = lo;
+  cap_hi[r] = hi;
+}
+
+int launch_accept_estimate(const void* p_t, const void* p_d, int pdt, int V,
+                           const int32_t* draft_tok, const float* uniforms, const int32_t* windows,
+                           const int32_t* cu, const int32_t* accept_len, const int32_t* cap_len,
+                           int mode, int B, int gamma, int max_rows, int32_t* cap_lo,
+                           int32_t* cap_hi, cudaStream_t stream) {
+  unsigned int* err = device_error_word();
+  const dim3 grid(ceil_div(B, 128)), block(128);
+  cudaError_t e;
+  if (pdt == DSPARK_F32)
+    e = launch_pdl(accept_estimate_kernel<float>, grid, block, 0, stream,
+                   static_cast<const float*>(p_t), static_cast<const float*>(p_d), V, draft_tok,
+                   uniforms, windows, cu, accept_len, cap_len, mode, B, gamma, max_rows, cap_lo,
+                   cap_hi, err);
+  else
+    e = launch_pdl(accept_estimate_kernel<__nv_bfloat16>, grid, block, 0, stream,
+                   static_cast<const __nv_bfloat16*>(p_t), static_cast<const __nv_bfloat16*>(p_d),
+                   V, draft_tok, uniforms, windows, cu, accept_len, cap_len, mode, B, gamma,
+                   max_rows, cap_lo, cap_hi, err);
+  return e == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
+}
+
 int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_t* draft_tok,
                   const float* uniforms, const float* exp_noise, const int32_t* windows,
                   const int32_t* cu, int mode, int B, int gamma, int max_rows, int32_t* accept_len,

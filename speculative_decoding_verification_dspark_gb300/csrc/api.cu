@@ -321,6 +321,27 @@ int dspark_accept_noalloc(const void* p_target, const void* p_draft, int pdt, in
                        fallback, scratch, static_cast<cudaStream_t>(stream));
 }
 
+int dspark_block_accept_estimate(const void* p_target, const void* p_draft, int pdt, int V,
+                                 const int32_t* draft_tok, const float* uniforms,
+                                 const int32_t* windows, const int32_t* cu_seqlens,
+                                 const int32_t* accept_len, const int32_t* cap_len, int mode,
+                                 int B, int gamma, int max_rows, int32_t* cap_lo, int32_t* cap_hi,
+                                 void* stream) {
+  CHECK(p_target && p_draft && draft_tok && uniforms && windows && cu_seqlens && accept_len &&
+            cap_len && cap_lo && cap_hi,
+        DSPARK_EINVAL);
+  CHECK(pdt == DSPARK_F32 || pdt == DSPARK_BF16, DSPARK_EINVAL);
+  CHECK(V >= 1, DSPARK_EINVAL);
+  CHECK(B >= 1 && B <= DSPARK_MAX_B && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA, DSPARK_EINVAL);
+  CHECK(mode >= DSPARK_COMPACT && mode <= DSPARK_CAP_ACCEPT, DSPARK_EINVAL);
+  CHECK(max_rows >= 1, DSPARK_EINVAL);
+  int rc = device_ok();
+  if (rc != DSPARK_OK) return rc;
+  return launch_accept_estimate(p_target, p_draft, pdt, V, draft_tok, uniforms, windows,
+                                cu_seqlens, accept_len, cap_len, mode, B, gamma, max_rows, cap_lo,
+                                cap_hi, static_cast<cudaStream_t>(stream));
+}
+
 size_t dspark_compact_workspace_size(int B) {
   if (B < 1) return 0;
   return compact_workspace(B);

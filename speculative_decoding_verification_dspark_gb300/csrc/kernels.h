@@ -62,6 +62,12 @@ int launch_accept(const void* p_t, const void* p_d, int pdt, int V, const int32_
                   int32_t* cap_len, int32_t* out_tok, float* cstar, int32_t* fallback, void* ws,
                   cudaStream_t stream);
 
+int launch_accept_estimate(const void* p_t, const void* p_d, int pdt, int V,
+                           const int32_t* draft_tok, const float* uniforms, const int32_t* windows,
+                           const int32_t* cu, const int32_t* accept_len, const int32_t* cap_len,
+                           int mode, int B, int gamma, int max_rows, int32_t* cap_lo,
+                           int32_t* cap_hi, cudaStream_t stream);
+
 // Address of the fixed scratch array on the current device (looked up once per
 // device); nullptr if the lookup fails.
 void* accept_fixed_scratch();

@@ -71,6 +71,13 @@ def test_host_validation_without_device(lib):
                                      16384, fake, fake, fake, fake, nul, nul) == -4
     assert lib.dspark_accept_noalloc(fake, fake, 0, 1001, fake, fake, fake, fake, fake, 0, 4, 6, 8,
                                      fake, fake, fake, fake, nul, nul) == -2
+    # block-accept estimate: NULL pointers, an unknown probability type, a mode out of range
+    assert lib.dspark_block_accept_estimate(nul, fake, 0, 1024, fake, fake, fake, fake, fake, fake,
+                                            0, 4, 6, 8, fake, fake, nul) == -1
+    assert lib.dspark_block_accept_estimate(fake, fake, 7, 1024, fake, fake, fake, fake, fake, fake,
+                                            0, 4, 6, 8, fake, fake, nul) == -1
+    assert lib.dspark_block_accept_estimate(fake, fake, 0, 1024, fake, fake, fake, fake, fake, fake,
+                                            3, 4, 6, 8, fake, fake, nul) == -1
     # Markov-head draft: NULL pointers, a rank other than 256, a vocabulary that is not a
     # multiple of 128, gamma above the maximum, misaligned logits
     ws = lib.dspark_markov_draft_workspace_size(1024)
