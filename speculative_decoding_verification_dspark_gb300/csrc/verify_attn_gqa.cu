@@ -63,7 +63,6 @@ constexpr int kVWarp = 1;
 constexpr int kQWarp = 2;
 constexpr int kMmaWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;
-constexpr int kThreads = 8 * 32;
 constexpr int kTileHalf = kKT * 128;  // one 64-wide column block of a [128 x 128] bf16 tile
 constexpr int kKVBytes = 2 * kTileHalf;
 constexpr int kStageBytes = 2 * kKVBytes;  // K and V
@@ -82,6 +81,12 @@ struct Cfg {
   static constexpr int P_BUFS = NT <= 64 ? 2 : 1;
   static constexpr SwizzleMode P_SW = NT == 32 ? SW_64B : SW_128B;
   static constexpr int G32 = NT / 32;                    // 32-row groups
+  // softmax warpgroups: the 128-column tile has two, each owning 64 query rows (its own
+  // half of P^T, released to its own PV product)
+  static constexpr int WGS = NT == 128 ? 2 : 1;
+  static constexpr int THREADS = (4 + 4 * WGS) * 32;
+  static constexpr int G32_WG = G32 / WGS;               // 32-row groups per warpgroup
+  static constexpr int PH = WGS;                          // P^T halves with their own barriers
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_STAGE = OFF_Q + Q_BUFS * Q_BYTES;
   static constexpr int OFF_P = OFF_STAGE + kStages * kStageBytes;
@@ -89,15 +94,17 @@ struct Cfg {
   static constexpr int OFF_REF = OFF_RED + 2 * 4 * NT * 4;         // float mref[4][NT], alpha[4][NT]
   static constexpr int OFF_LS = OFF_REF + 2 * 4 * NT * 4;          // float lsum[4][NT]
   static constexpr int OFF_MT = OFF_LS + 4 * NT * 4;               // float mtrue[4][NT]
-  static constexpr int OFF_OVER = OFF_MT + 4 * NT * 4;              // int over[2][4]
-  static constexpr int OFF_ITEMS = OFF_OVER + 32;                   // AttnItem[kSmemItems]
+  static constexpr int OFF_OVER = OFF_MT + 4 * NT * 4;              // int over[2][WGS][4]
+  static constexpr int OFF_ITEMS = OFF_OVER + 32 * WGS;             // AttnItem[kSmemItems]
   static constexpr int OFF_BAR = OFF_ITEMS + kSmemItems * (int)sizeof(AttnItem);
-  // k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], xw[2], ep[2],
-  // o_free[2], stg_full, stg_free, p_full[PB], p_empty[PB], q_full[QB], q_empty[QB],
-  // xs[2]
-  static constexpr int N_BARS = 22 + 2 * P_BUFS + 2 * Q_BUFS;
-  // epilogue: O / l is staged row-major (512 B per query row) in the P buffers
-  static constexpr int STG_ROWS = P_BUFS * P_BYTES / (kD * 4);
+  // k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], o_free[2];
+  // per warpgroup xw[2], xs[2], ep[2], stg_full, stg_free; p_full[PB][PH],
+  // p_empty[PB][PH], q_full[QB], q_empty[QB]
+  static constexpr int N_BARS = 14 + 8 * WGS + 2 * P_BUFS * PH + 2 * Q_BUFS;
+  // epilogue: O / l is staged row-major (512 B per query row) in the P buffers, each
+  // warpgroup in its own share of them
+  static constexpr int STG_BYTES_WG = P_BUFS * P_BYTES / WGS;
+  static constexpr int STG_ROWS = STG_BYTES_WG / (kD * 4);
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
   static constexpr int TMEM_S = 0;          // S^T, two buffers of NT columns
@@ -105,6 +112,7 @@ struct Cfg {
   static constexpr int TMEM_COLS = 4 * NT <= 128 ? 128 : (4 * NT <= 256 ? 256 : 512);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(NT == 32 || NT == 64 || NT == 128, "query tile");
+  static_assert(NT != 128 || P_BUFS == 1, "the 128-column tile's halves count phases on one P buffer");
 };
 
 struct Ctx {
@@ -112,19 +120,19 @@ struct Ctx {
   unsigned int* err;
 };
 
+// Waits sleep in the barrier (up to 20 us at a time, so that a waiting warp takes no
+// issue slots from the softmax warp beside it) between checks of the abort flag and of
+// the time limit.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctx& cx) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  uint32_t n = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++n & 31u) == 0) {
-      if (*cx.abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *cx.abort_flag = 1;
-        raise_error(cx.err, DSPARK_DEVERR_WAIT_TIMEOUT);
-        return false;
-      }
+    if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
+    if (*cx.abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *cx.abort_flag = 1;
+      raise_error(cx.err, DSPARK_DEVERR_WAIT_TIMEOUT);
+      return false;
     }
   }
 }
@@ -208,18 +216,23 @@ struct Layout {
   __device__ uint32_t v_empty(int s) const { return bar(6 + s); }
   __device__ uint32_t s_full(int b) const { return bar(8 + b); }
   __device__ uint32_t s_free(int b) const { return bar(10 + b); }
-  __device__ uint32_t xw(int b) const { return bar(12 + b); }
-  __device__ uint32_t ep(int b) const { return bar(14 + b); }
-  __device__ uint32_t o_free(int b) const { return bar(16 + b); }
-  __device__ uint32_t stg_full() const { return bar(18); }
-  __device__ uint32_t stg_free() const { return bar(19); }
-  __device__ uint32_t p_full(int b) const { return bar(20 + b); }
-  __device__ uint32_t p_empty(int b) const { return bar(20 + Cfg<NT>::P_BUFS + b); }
-  __device__ uint32_t q_full(int b) const { return bar(20 + 2 * Cfg<NT>::P_BUFS + b); }
-  __device__ uint32_t q_empty(int b) const {
-    return bar(20 + 2 * Cfg<NT>::P_BUFS + Cfg<NT>::Q_BUFS + b);
+  __device__ uint32_t o_free(int b) const { return bar(12 + b); }
+  // per softmax warpgroup w
+  __device__ uint32_t xw(int w, int b) const { return bar(14 + 8 * w + b); }
+  __device__ uint32_t xs(int w, int b) const { return bar(14 + 8 * w + 2 + b); }
+  __device__ uint32_t ep(int w, int b) const { return bar(14 + 8 * w + 4 + b); }
+  __device__ uint32_t stg_full(int w) const { return bar(14 + 8 * w + 6); }
+  __device__ uint32_t stg_free(int w) const { return bar(14 + 8 * w + 7); }
+  static constexpr int P0 = 14 + 8 * Cfg<NT>::WGS;
+  // P buffer b, half h (the 128-column tile's halves; one half otherwise)
+  __device__ uint32_t p_full(int b, int h) const { return bar(P0 + b * Cfg<NT>::PH + h); }
+  __device__ uint32_t p_empty(int b, int h) const {
+    return bar(P0 + Cfg<NT>::P_BUFS * Cfg<NT>::PH + b * Cfg<NT>::PH + h);
   }
-  __device__ uint32_t xs(int b) const { return bar(20 + 2 * Cfg<NT>::P_BUFS + 2 * Cfg<NT>::Q_BUFS + b); }
+  __device__ uint32_t q_full(int b) const { return bar(P0 + 2 * Cfg<NT>::P_BUFS * Cfg<NT>::PH + b); }
+  __device__ uint32_t q_empty(int b) const {
+    return bar(P0 + 2 * Cfg<NT>::P_BUFS * Cfg<NT>::PH + Cfg<NT>::Q_BUFS + b);
+  }
 };
 
 // Work item `it` of this CTA: from shared memory for the first kSmemItems items.
@@ -257,7 +270,7 @@ struct Params {
 };
 
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
     verify_attn_gqa_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_kn,
@@ -286,18 +299,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(L.v_full(b), 1);
       mbar_init(L.v_empty(b), 1);
       mbar_init(L.s_full(b), 1);
-      mbar_init(L.s_free(b), 4);
-      mbar_init(L.xw(b), 4);
-      mbar_init(L.xs(b), 4);
-      mbar_init(L.ep(b), 4);
-      mbar_init(L.o_free(b), 4);
+      mbar_init(L.s_free(b), 4 * C::WGS);
+      mbar_init(L.o_free(b), 4 * C::WGS);
+      for (int w = 0; w < C::WGS; ++w) {
+        mbar_init(L.xw(w, b), 4);
+        mbar_init(L.xs(w, b), 4);
+        mbar_init(L.ep(w, b), 4);
+      }
     }
-    mbar_init(L.stg_full(), 4);
-    mbar_init(L.stg_free(), 1);
-    for (int b = 0; b < C::P_BUFS; ++b) {
-      mbar_init(L.p_full(b), 4);
-      mbar_init(L.p_empty(b), 1);
+    for (int w = 0; w < C::WGS; ++w) {
+      mbar_init(L.stg_full(w), 4);
+      mbar_init(L.stg_free(w), 1);
     }
+    for (int b = 0; b < C::P_BUFS; ++b)
+      for (int h = 0; h < C::PH; ++h) {
+        mbar_init(L.p_full(b, h), 4);
+        mbar_init(L.p_empty(b, h), 1);
+      }
     for (int b = 0; b < C::Q_BUFS; ++b) {
       mbar_init(L.q_full(b), 1);
       mbar_init(L.q_empty(b), 1);
@@ -323,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   {
     const int n_s = min(kSmemItems, it_end - it_begin);
     constexpr int kWords = (int)(sizeof(AttnItem) / sizeof(uint4));
-    for (int i = threadIdx.x; i < n_s * kWords; i += kThreads)
+    for (int i = threadIdx.x; i < n_s * kWords; i += C::THREADS)
       reinterpret_cast<uint4*>(s_items)[i] = reinterpret_cast<const uint4*>(prm.items + it_begin)[i];
   }
   tc_fence_before();
@@ -461,14 +479,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk's V rows past them (TMA copied the whole chunk), so that no stale or
     // foreign value meets a zero probability.
     constexpr uint32_t IDESC_QK = idesc_bf16_f32(kKT, NT, 0, 0);
-    constexpr uint32_t IDESC_PV = idesc_bf16_f32(kD, NT, 1, 1);
+    constexpr uint32_t IDESC_PV = idesc_bf16_f32(kD, NT / C::PH, 1, 1);
     int g = 0, n_it = 0, last_pv = -1;
+    int nh1 = 0;  // products of the second P^T half issued (tiles whose item has rows there)
     bool ok = true;
     // PV of tile gp (local index `local` in its item) into O^T buffer ob, over the
-    // 16-key chunks that hold visible keys only
-    auto issue_pv = [&](int gp, int local, int vis, int ob) -> bool {
+    // 16-key chunks that hold visible keys only; one product per half of P^T as its
+    // warpgroup releases it (a half without query rows of the item is released but not
+    // multiplied)
+    auto issue_pv = [&](int gp, int local, int vis, int ob, int nq) -> bool {
       const int pb = gp % C::P_BUFS;
-      if (!wait_warp(L.p_full(pb), (gp / C::P_BUFS) & 1, cx)) return false;
+      if (!wait_warp(L.p_full(pb, 0), (gp / C::P_BUFS) & 1, cx)) return false;
       const int s = gp % kStages;
       if (!wait_warp(L.v_full(s), (gp / kStages) & 1, cx)) return false;
       const uint32_t vb = L.stage(s) + kKVBytes;
@@ -483,18 +504,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t d_o = tmem + C::TMEM_O + ob * NT;
-        for (int kk = 0; kk < nch; ++kk) {
-          // A = V^T (M = d, MN-major), B = P^T (N = query rows, MN-major); K = 16 keys
-          const uint64_t a = smem_desc(vb + kk * 2048, kTileHalf, 1024, SW_128B);
-          const uint64_t b = smem_desc(L.pbuf(pb) + kk * 16 * C::P_ROW, kKT * 128, 8 * C::P_ROW, C::P_SW);
-          umma_bf16(d_o, a, b, IDESC_PV, (local > 0 || kk > 0) ? 1u : 0u);
+      for (int h = 0; h < C::PH; ++h) {
+        // the second half exists only for items with rows in it (128-column tile, one P
+        // buffer): its barriers count those tiles alone
+        if (h > 0 && h * (NT / C::PH) >= nq) continue;
+        if (h > 0 && !wait_warp(L.p_full(pb, h), nh1 & 1, cx)) return false;
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t d_o = tmem + C::TMEM_O + ob * NT + h * (NT / C::PH);
+          for (int kk = 0; kk < nch; ++kk) {
+            // A = V^T (M = d, MN-major), B = P^T (N = query rows, MN-major); K = 16 keys
+            const uint64_t a = smem_desc(vb + kk * 2048, kTileHalf, 1024, SW_128B);
+            const uint64_t b = smem_desc(L.pbuf(pb) + h * (kKT * 128) + kk * 16 * C::P_ROW, kKT * 128,
+                                         8 * C::P_ROW, C::P_SW);
+            umma_bf16(d_o, a, b, IDESC_PV, (local > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(L.p_empty(pb, h));
         }
-        umma_commit(L.p_empty(pb));
-        umma_commit(L.v_empty(s));
+        __syncwarp();
+        if (h > 0) ++nh1;
       }
+      if (lane == 0) umma_commit(L.v_empty(s));
       __syncwarp();
       last_pv = gp;
       return true;
@@ -530,25 +560,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (l == ntiles - 1) umma_commit(L.q_empty(qb));
         }
         __syncwarp();
-        if (l >= 1 && !issue_pv(g - 1, l - 1, prev_vis, ob)) { ok = false; break; }
+        if (l >= 1 && !issue_pv(g - 1, l - 1, prev_vis, ob, item.ni * G)) { ok = false; break; }
         prev_vis = visible_keys(item.tb + l, ct, ctx, n_r);
       }
       if (!ok) break;
-      if (!issue_pv(g - 1, ntiles - 1, prev_vis, ob)) { ok = false; break; }
+      if (!issue_pv(g - 1, ntiles - 1, prev_vis, ob, item.ni * G)) { ok = false; break; }
     }
     if (lane == 0 && last_pv >= 0)
-      drain_bar(L.p_empty(last_pv % C::P_BUFS), (last_pv / C::P_BUFS) & 1, prm.err);
+      drain_bar(L.p_empty(last_pv % C::P_BUFS, 0), (last_pv / C::P_BUFS) & 1, prm.err);
+    if (lane == 0 && nh1 > 0) drain_bar(L.p_empty(0, 1), (nh1 - 1) & 1, prm.err);
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------- softmax / epilogue
     const int sw = warp & 3;                          // TMEM lane quadrant
+    const int wg = (warp - kSoftmaxWarp0) >> 2;       // softmax warpgroup: rows of its own
     const int kl = sw * 32 + lane;                    // key of this thread within a tile (= d in O^T)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sw * 32) << 16);
     const float sl2 = prm.scale_log2;
     float* my_mref = s_mref + sw * NT;
     float* my_alpha = s_alpha + sw * NT;
     float* my_mtrue = reinterpret_cast<float*>(bp + C::OFF_MT) + sw * NT;
-    int* s_over = reinterpret_cast<int*>(bp + C::OFF_OVER);  // [2][4]
-    int g = 0, n_it = 0, n_stg = 0, n_sf = 0, n_ov = 0;
+    // [2][WGS][4]: this warpgroup's flags
+    int* s_over = reinterpret_cast<int*>(bp + C::OFF_OVER) + wg * 4;
+    // exchange counters of this warpgroup (xw: one per tile it holds rows in; ep: one
+    // per item it holds rows in)
+    // na: tiles this warpgroup wrote its half of P^T for (the 128-column tile's P
+    // barriers of a half count those tiles)
+    int g = 0, n_it = 0, n_stg = 0, n_sf = 0, n_ov = 0, n_xw = 0, n_ep = 0, na = 0;
     bool ok = true;
     for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
       const AttnItem item = fetch_item(s_items, prm.items, it, it_begin);
@@ -559,6 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nq = item.ni * G;                     // valid query rows (columns)
       const int ng = (nq + 31) >> 5;                  // 32-row groups holding valid rows
       const int nc8 = (nq + 7) >> 3;                  // 8-row chunks holding valid rows
+      const int gbeg = wg * C::G32_WG;                // this warpgroup's 32-row groups
+      const int gend = min(ng, gbeg + C::G32_WG);     // (none when gend <= gbeg)
       const uint32_t t_o = t_lane + C::TMEM_O + (n_it & 1) * NT;  // this item's O^T
       // per-row state, lane-distributed: row = gi*32 + lane
       // per-row sums of the bf16 P the PV product multiplies, so that the weights
@@ -587,20 +626,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           nmin = b < n_r ? (b - item.i0) * G : 0x7fffffff;
         }
         const uint32_t s_col = t_lane + C::TMEM_S + sb * NT;
-        float* wmax = s_wmax + (g & 1) * 4 * NT;
         const int pb = g % C::P_BUFS;
         const uint32_t prow = L.pbuf(pb);
-        // ---- fast path (items with at most 32 query rows, every tile but the first):
-        // the references rarely move once a tile has set them, so P is computed in one
-        // pass against the current references; the 2^8 test that would move a
-        // reference is taken per key (a key above its row's reference + 8 is exactly a
-        // tile maximum above it), and only if some key of some warp passes it does the
-        // tile take the full path below, overwriting this P -- so P, the sums and the
-        // references are those of the full path bit for bit.  P is formed in registers
-        // while PV(g - 1) may still read the single P buffer; only the stores wait.
-        // (The epilogue's staging reads of the P buffer were waited for at the first
-        // tile's exchange.)  Items with more rows keep the two passes: there the max
-        // pass is what overlaps PV(g - 1).
+        if (gend <= gbeg) {
+          // no query row of the item in this warpgroup: release S^T of the tile (its
+          // half of P^T takes no part in this item's products)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(L.s_free(sb));
+          continue;
+        }
+        const int xslot = n_xw & 1;
+        float* wmax = s_wmax + xslot * 4 * NT;
+        // ---- fast path (items with at most 32 query rows -- warpgroup 0 alone --, every
+        // tile but the first): the references rarely move once a tile has set them, so P
+        // is computed in one pass against the current references; the 2^8 test that
+        // would move a reference is taken per key (a key above its row's reference + 8
+        // is exactly a tile maximum above it), and only if some key of some warp passes
+        // it does the tile take the full path below, overwriting this P -- so P, the
+        // sums and the references are those of the full path bit for bit.  P is formed
+        // in registers while the last product of this half may still read the single P
+        // buffer; only the stores wait.  (The epilogue's staging reads of the P buffer
+        // were waited for at the first tile's exchange.)  Items with more rows keep the
+        // two passes: there the max pass is what overlaps the previous product.
         bool full = l == 0 || ng > 1;
         const bool tried_fast = !full;  // the fast pass used this tile's xw exchange
         if (!full) {
@@ -628,8 +676,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             lnew0 += transpose_reduce<false>(v, lane);
           }
-          // the single P buffer: PV(g - 1) must be done with it
-          if (!wait_warp(L.p_empty((g - 1) % C::P_BUFS), ((g - 1) / C::P_BUFS) & 1, cx)) {
+          // the single P buffer: the last product of this half must be done with it
+          if (na >= 1 && !wait_warp(L.p_empty(0, wg), (na - 1) & 1, cx)) {
             ok = false;
             break;
           }
@@ -643,12 +691,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // one flag per warp, exchanged once: does any reference move?
           over = __any_sync(0xffffffffu, over);
-          if (lane == 0) s_over[(g & 1) * 4 + sw] = over ? 1 : 0;
+          if (lane == 0) s_over[xslot * 4 * C::WGS + sw] = over ? 1 : 0;
           __syncwarp();
-          if (lane == 0) mbar_arrive(L.xw(g & 1));
-          if (!wait_warp(L.xw(g & 1), (g >> 1) & 1, cx)) { ok = false; break; }
-          full = (s_over[(g & 1) * 4] | s_over[(g & 1) * 4 + 1] | s_over[(g & 1) * 4 + 2] |
-                  s_over[(g & 1) * 4 + 3]) != 0;
+          if (lane == 0) mbar_arrive(L.xw(wg, xslot));
+          if (!wait_warp(L.xw(wg, xslot), (n_xw >> 1) & 1, cx)) { ok = false; break; }
+          ++n_xw;
+          const int* ov = s_over + xslot * 4 * C::WGS;
+          full = (ov[0] | ov[1] | ov[2] | ov[3]) != 0;
           if (!full) {
             lacc[0] = lnew0;
             tc_fence_before();
@@ -656,14 +705,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(L.s_free(sb));
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(L.p_full(pb));
+            if (lane == 0) mbar_arrive(L.p_full(pb, wg));
+            ++na;
             continue;  // next tile
           }
         }
-        // ---- full path, pass 1: tile max per row (warp transpose-reduce), then across
-        // the 4 warps (on xw, or on xs when a fast pass already used xw for this tile)
+        // ---- full path, pass 1: tile max per row of this warpgroup's groups (warp
+        // transpose-reduce), then across its 4 warps (on xw, or on xs when a fast pass
+        // already used xw for this tile)
 #pragma unroll 1
-        for (int gi = 0; gi < ng; ++gi) {
+        for (int gi = gbeg; gi < gend; ++gi) {
           float v[32];
           tmem_ld32(s_col + gi * 32, v);
           tmem_wait_ld();
@@ -673,21 +724,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           wmax[sw * NT + gi * 32 + lane] = transpose_reduce<true>(v, lane) * sl2;
         }
         __syncwarp();
-        // P buffers double as the epilogue's staging area: its bulk reads must be done
-        // before any warp passes this exchange and writes P
-        if (warp == kSoftmaxWarp0 && lane == 0) bulk_wait_read_all();
+        // this warpgroup's share of the P buffer doubles as its epilogue's staging area:
+        // those bulk reads must be done before any of its warps passes this exchange and
+        // writes P
+        if (sw == 0 && lane == 0) bulk_wait_read_all();
         if (!tried_fast) {
-          if (lane == 0) mbar_arrive(L.xw(g & 1));
-          if (!wait_warp(L.xw(g & 1), (g >> 1) & 1, cx)) { ok = false; break; }
+          if (lane == 0) mbar_arrive(L.xw(wg, xslot));
+          if (!wait_warp(L.xw(wg, xslot), (n_xw >> 1) & 1, cx)) { ok = false; break; }
+          ++n_xw;
         } else {
-          if (lane == 0) mbar_arrive(L.xs(n_ov & 1));
-          if (!wait_warp(L.xs(n_ov & 1), (n_ov >> 1) & 1, cx)) { ok = false; break; }
+          if (lane == 0) mbar_arrive(L.xs(wg, n_ov & 1));
+          if (!wait_warp(L.xs(wg, n_ov & 1), (n_ov >> 1) & 1, cx)) { ok = false; break; }
           ++n_ov;
         }
         bool need_any = false;
 #pragma unroll
         for (int gi = 0; gi < C::G32; ++gi) {
-          if (gi >= ng) break;
+          if (gi < gbeg) continue;
+          if (gi >= gend) break;
           const int n = gi * 32 + lane;
           const float tm = fmaxf(fmaxf(wmax[n], wmax[NT + n]), fmaxf(wmax[2 * NT + n], wmax[3 * NT + n]));
           float alpha = 1.f;
@@ -703,22 +757,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool rescale = __any_sync(0xffffffffu, need_any) && l > 0;
         __syncwarp();
-        // P buffer of this tile must be free: PV(g - P_BUFS) done
-        if (g >= C::P_BUFS &&
-            !wait_warp(L.p_empty((g - C::P_BUFS) % C::P_BUFS), ((g - C::P_BUFS) / C::P_BUFS) & 1, cx)) {
+        // the single P buffer, and with it this half's O^T columns: the half's last
+        // product must be done
+        if (na >= 1 && !wait_warp(L.p_empty(0, wg), (na - 1) & 1, cx)) {
           ok = false;
           break;
         }
         if (rescale) {
-          // O^T must hold PV(g-1) before its columns are rescaled
-          if (C::P_BUFS > 1 &&
-              !wait_warp(L.p_empty((g - 1) % C::P_BUFS), ((g - 1) / C::P_BUFS) & 1, cx)) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < NT / 32; ++c) {
+          for (int c = gbeg; c < gend; ++c) {
             float o[32];
             tmem_ld32(t_o + c * 32, o);
             tmem_wait_ld();
@@ -733,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // holding valid rows are written: padding columns of P^T are left as they are
         // -- they only reach their own columns of O^T, which are never stored.
 #pragma unroll 1
-        for (int gi = 0; gi < ng; ++gi) {
+        for (int gi = gbeg; gi < gend; ++gi) {
           float v[32];
           tmem_ld32(s_col + gi * 32, v);
           tmem_wait_ld();
@@ -770,7 +818,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(L.s_free(sb));
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(L.p_full(pb));
+        if (lane == 0) mbar_arrive(L.p_full(pb, wg));
+        ++na;
         } else {
         float s[NT];
 #pragma unroll
@@ -811,8 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P buffers double as the epilogue's staging area: its bulk reads must be done
         // before any warp passes this exchange and writes P
         if (warp == kSoftmaxWarp0 && lane == 0) bulk_wait_read_all();
-        if (lane == 0) mbar_arrive(L.xw(g & 1));
-        if (!wait_warp(L.xw(g & 1), (g >> 1) & 1, cx)) { ok = false; break; }
+        if (lane == 0) mbar_arrive(L.xw(0, g & 1));
+        if (!wait_warp(L.xw(0, g & 1), (g >> 1) & 1, cx)) { ok = false; break; }
         bool need_any = false;
 #pragma unroll
         for (int gi = 0; gi < C::G32; ++gi) {
@@ -834,14 +883,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P buffer of this tile must be free: PV(g - P_BUFS) done
         const int pb = g % C::P_BUFS;
         if (g >= C::P_BUFS &&
-            !wait_warp(L.p_empty((g - C::P_BUFS) % C::P_BUFS), ((g - C::P_BUFS) / C::P_BUFS) & 1, cx)) {
+            !wait_warp(L.p_empty((g - C::P_BUFS) % C::P_BUFS, 0), ((g - C::P_BUFS) / C::P_BUFS) & 1, cx)) {
           ok = false;
           break;
         }
         if (rescale) {
           // O^T must hold PV(g-1) before its columns are rescaled
           if (C::P_BUFS > 1 &&
-              !wait_warp(L.p_empty((g - 1) % C::P_BUFS), ((g - 1) / C::P_BUFS) & 1, cx)) {
+              !wait_warp(L.p_empty((g - 1) % C::P_BUFS, 0), ((g - 1) / C::P_BUFS) & 1, cx)) {
             ok = false;
             break;
           }
@@ -883,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(L.p_full(pb));
+        if (lane == 0) mbar_arrive(L.p_full(pb, 0));
         // ---- per-row partial sums over this warp's 32 keys
 #pragma unroll
         for (int gi = 0; gi < C::G32; ++gi) {
@@ -896,16 +945,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // ---- epilogue: l across warps, then O^T / l for the valid rows
-      {
+      // ---- epilogue of this warpgroup's rows: l across its warps, then O^T / l
+      if (gend > gbeg) {
         float* lsum = s_lsum;
 #pragma unroll
-        for (int gi = 0; gi < C::G32; ++gi) lsum[sw * NT + gi * 32 + lane] = lacc[gi];
+        for (int gi = 0; gi < C::G32; ++gi)
+          if (gi >= gbeg && gi < gend) lsum[sw * NT + gi * 32 + lane] = lacc[gi];
         __syncwarp();
-        if (lane == 0) mbar_arrive(L.ep(n_it & 1));
-        if (!wait_warp(L.ep(n_it & 1), (n_it >> 1) & 1, cx)) { ok = false; break; }
-        const int gl = g - 1;
-        if (!wait_warp(L.p_empty(gl % C::P_BUFS), (gl / C::P_BUFS) & 1, cx)) { ok = false; break; }
+        if (lane == 0) mbar_arrive(L.ep(wg, n_ep & 1));
+        if (!wait_warp(L.ep(wg, n_ep & 1), (n_ep >> 1) & 1, cx)) { ok = false; break; }
+        ++n_ep;
+        // the item's last product of this warpgroup's rows is complete
+        if constexpr (NT == 128) {
+          if (!wait_warp(L.p_empty(0, wg), (na - 1) & 1, cx)) { ok = false; break; }
+        } else {
+          const int gl = g - 1;
+          if (!wait_warp(L.p_empty(gl % C::P_BUFS, 0), (gl / C::P_BUFS) & 1, cx)) { ok = false; break; }
+        }
         tc_fence_after();
         const bool split = item.nsplit > 1;
         // Row n = gi*32 + lane: 1/l, computed once per row and broadcast below.
@@ -914,10 +970,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int gi = 0; gi < C::G32; ++gi) {
           const int n = gi * 32 + lane;
           inv_l[gi] = 0.f;
-          if (gi < ng && n < nq) {
+          if (gi >= gbeg && gi < gend && n < nq) {
             const float lt = lsum[n] + lsum[NT + n] + lsum[2 * NT + n] + lsum[3 * NT + n];
             inv_l[gi] = lt > 0.f ? 1.f / lt : 0.f;
-            if (sw == 0) {  // warp 0 of the group writes the lse
+            if (sw == 0) {  // warp 0 of the warpgroup writes the lse
               const float lse_v = (mref[gi] + log2f(lt)) * 0.69314718055994530942f;
               if (split)
                 prm.ws_lse[(long long)item.slot * kKT + n] = lse_v;  // this piece's slot
@@ -926,14 +982,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // O^T / l -> row-major rows in the (now idle) P buffers, STG_ROWS rows per pass;
-        // one thread then writes each pass out with bulk copies: a slot of ws_o is one
-        // contiguous run, an output block row is G consecutive heads.
-        float* stg = reinterpret_cast<float*>(bp + C::OFF_P);
-        for (int p0 = 0; p0 < nq; p0 += C::STG_ROWS) {
-          const int p1 = min(nq, p0 + C::STG_ROWS);
-          if (p0 > 0) {  // the previous pass must have been read out of the buffers
-            if (!wait_warp(L.stg_free(), n_sf & 1, cx)) { ok = false; break; }
+        // O^T / l -> row-major rows in this warpgroup's share of the (now idle) P
+        // buffers, STG_ROWS rows per pass; one thread then writes each pass out with bulk
+        // copies: a slot of ws_o is one contiguous run, an output block row is G
+        // consecutive heads.
+        float* stg = reinterpret_cast<float*>(bp + C::OFF_P + wg * C::STG_BYTES_WG);
+        const int rb = gbeg * 32, re = min(nq, gend * 32);
+        for (int p0 = rb; p0 < re; p0 += C::STG_ROWS) {
+          const int p1 = min(re, p0 + C::STG_ROWS);
+          if (p0 > rb) {  // the previous pass must have been read out of the buffers
+            if (!wait_warp(L.stg_free(wg), n_sf & 1, cx)) { ok = false; break; }
             ++n_sf;
           }
 #pragma unroll
@@ -950,12 +1008,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(L.stg_full());
-          if (warp == kSoftmaxWarp0 && lane == 0) {
-            if (!wait_bar(L.stg_full(), n_stg & 1, cx)) {
+          if (lane == 0) mbar_arrive(L.stg_full(wg));
+          if (sw == 0 && lane == 0) {
+            if (!wait_bar(L.stg_full(wg), n_stg & 1, cx)) {
               ok = false;
             } else {
-              const uint32_t src = L.pbuf(0);
+              const uint32_t src = L.pbuf(0) + wg * C::STG_BYTES_WG;
               if (split) {
                 bulk_store_s2g(prm.ws_o + ((long long)item.slot * kKT + p0) * kD, src,
                                (uint32_t)(p1 - p0) * kD * 4);
@@ -969,9 +1027,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
               bulk_commit();
-              if (p1 < nq) {
+              if (p1 < re) {
                 bulk_wait_read_all();
-                mbar_arrive(L.stg_free());
+                mbar_arrive(L.stg_free(wg));
               }
             }
           }
@@ -979,15 +1037,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!__all_sync(0xffffffffu, ok)) break;
         }
         if (!ok) break;
-        // O^T of this item is read: its TMEM columns may take item n_it + 2
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(L.o_free(n_it & 1));
-        // lsum is rewritten by the next item only after every warp passed its ep barrier
-        // and the next tile's cross-warp barrier; the latter orders it.
+        // lsum is rewritten by the next item only after every warp of the warpgroup
+        // passed its ep barrier and the next tile's cross-warp barrier; the latter
+        // orders it.
       }
+      // O^T of this item is read: its TMEM columns may take item n_it + 2
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(L.o_free(n_it & 1));
     }
-    if (warp == kSoftmaxWarp0 && lane == 0) bulk_wait_all();  // output writes complete
+    if (sw == 0 && lane == 0) bulk_wait_all();  // output writes complete
   }
 
   tc_fence_before();
@@ -1146,19 +1205,19 @@ int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, c
   switch (nt) {
     case 32:
       if (!configure<32>()) return DSPARK_ECUDA;
-      if (launch_pdl(verify_attn_gqa_kernel<32>, dim3(grid), dim3(kThreads), Cfg<32>::SMEM_BYTES,
+      if (launch_pdl(verify_attn_gqa_kernel<32>, dim3(grid), dim3(Cfg<32>::THREADS), Cfg<32>::SMEM_BYTES,
                      stream, tk, tv, tkn, tvn, prm) != cudaSuccess)
         return DSPARK_ECUDA;
       break;
     case 64:
       if (!configure<64>()) return DSPARK_ECUDA;
-      if (launch_pdl(verify_attn_gqa_kernel<64>, dim3(grid), dim3(kThreads), Cfg<64>::SMEM_BYTES,
+      if (launch_pdl(verify_attn_gqa_kernel<64>, dim3(grid), dim3(Cfg<64>::THREADS), Cfg<64>::SMEM_BYTES,
                      stream, tk, tv, tkn, tvn, prm) != cudaSuccess)
         return DSPARK_ECUDA;
       break;
     default:
       if (!configure<128>()) return DSPARK_ECUDA;
-      if (launch_pdl(verify_attn_gqa_kernel<128>, dim3(grid), dim3(kThreads), Cfg<128>::SMEM_BYTES,
+      if (launch_pdl(verify_attn_gqa_kernel<128>, dim3(grid), dim3(Cfg<128>::THREADS), Cfg<128>::SMEM_BYTES,
                      stream, tk, tv, tkn, tvn, prm) != cudaSuccess)
         return DSPARK_ECUDA;
       break;
