@@ -298,7 +298,11 @@ __device__ inline void pack_body(const TierSel ts, const int32_t* __restrict__ w
   __shared__ int s_cu[DSPARK_MAX_B + 1];
   __shared__ int s_warp[32];
   __shared__ int s_tier;
+  __shared__ int s_tiers[DSPARK_MAX_TIERS];
   const int tid = threadIdx.x;
+  // the tiers, one load per thread beside the windows' (the tier search below then
+  // reads shared memory instead of a chain of global loads)
+  if (tid < n_tiers) s_tiers[tid] = tiers[tid];
   int cnt = 0;
   if (tid < B) {
     int w = windows[tid];
@@ -325,8 +329,8 @@ __device__ inline void pack_body(const TierSel ts, const int32_t* __restrict__ w
   if (tid == 0) {
     int tier = M;
     for (int i = 0; i < n_tiers; ++i) {
-      if (tiers[i] >= M) {
-        tier = tiers[i];
+      if (s_tiers[i] >= M) {
+        tier = s_tiers[i];
         break;
       }
     }
@@ -335,7 +339,7 @@ __device__ inline void pack_body(const TierSel ts, const int32_t* __restrict__ w
     *tier_out = tier;
     int body = n_tiers;
     for (int i = 0; i < n_tiers; ++i)
-      if (tiers[i] == tier) {
+      if (s_tiers[i] == tier) {
         body = i;
         break;
       }
