@@ -16,7 +16,7 @@ core and on all the host's cores (``cpu_baseline``).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     [--workload qwen3_8b|mixed256|mla|tiny] [--mode compact|static|cap_accept]
-                    [--no-extra] [--no-cpu-baseline]
+                    [--no-extra] [--no-cpu-baseline] [--markov-only]
 
 Prints one JSON line (rank 0).
 """
@@ -580,7 +580,7 @@ def markov_bytes(B, gamma, V, rank=256):
     return rank * V * 2 + 3 * B * gamma * V * 4 + B * gamma * rank * 2 + B * 4 + B * gamma * 4
 
 
-def markov_arm(seed, reps=20, oracle_rows=2):
+def markov_arm(seed, reps=20, oracle_rows=2, with_oracle=True):
     """Markov-head draft sampling of one block (dspark_markov_draft) at the Qwen3-8B
     vocabulary with the verification workload's batch and block (B = 32, gamma = 8,
     V = 151936, rank 256): device time per block with L2 flushed before each call,
@@ -611,17 +611,19 @@ def markov_arm(seed, reps=20, oracle_rows=2):
     nbytes = markov_bytes(B, gamma, V)
     pk = peak_values()
     gbs = nbytes / (us * 1e-6) / 1e9
-    # the oracle (CPU baseline leg): the same block for a few request rows
-    from oracle import dspark_oracle as O
-    rows = slice(0, oracle_rows)
-    U = inp["U"][rows].cpu().numpy()
-    W1 = inp["W1"].float().cpu().numpy()
-    W2 = inp["W2"].float().cpu().numpy()
-    e = inp["exp_noise"][rows].cpu().numpy()
-    anc = inp["anchor"][rows].cpu().numpy()
-    t0 = time.perf_counter()
-    O.markov_draft(U, W1, W2, anc, e)
-    t_row = (time.perf_counter() - t0) / oracle_rows
+    t_row = None
+    if with_oracle:
+        # the oracle (CPU baseline leg): the same block for a few request rows
+        from oracle import dspark_oracle as O
+        rows = slice(0, oracle_rows)
+        U = inp["U"][rows].cpu().numpy()
+        W1 = inp["W1"].float().cpu().numpy()
+        W2 = inp["W2"].float().cpu().numpy()
+        e = inp["exp_noise"][rows].cpu().numpy()
+        anc = inp["anchor"][rows].cpu().numpy()
+        t0 = time.perf_counter()
+        O.markov_draft(U, W1, W2, anc, e)
+        t_row = (time.perf_counter() - t0) / oracle_rows
     del inp, p, flush
     torch.cuda.empty_cache()
     return {"workload": f"Markov-head draft block: B={B}, gamma={gamma}, V={V}, rank 256, "
@@ -633,9 +635,9 @@ def markov_arm(seed, reps=20, oracle_rows=2):
                          "frac": gbs / pk["hbm"], "algorithmic_bytes": nbytes,
                          "traffic": load_traffic("markov_draft", "markov_qwen3_8b", MARKOV_SRC),
                          "peak_source": f"{pk['hbm_src']} hbm_gbs (burst copy)"},
-            "cpu_oracle": {"blocks_per_s": 1.0 / (t_row * B), "cores": 1, "kind": "oracle",
-                           "sample": f"{oracle_rows} request rows of the block (fp64), scaled "
-                                     f"to {B} rows"}}
+            "cpu_oracle": None if t_row is None else {
+                "blocks_per_s": 1.0 / (t_row * B), "cores": 1, "kind": "oracle",
+                "sample": f"{oracle_rows} request rows of the block (fp64), scaled to {B} rows"}}
 
 
 def e2e_arm(args, run):
@@ -889,6 +891,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-extra", action="store_true",
                     help="time the headline only (no other workloads, no sweep)")
+    ap.add_argument("--markov-only", action="store_true",
+                    help="time the Markov-head draft block alone (its JSON key, one line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -941,6 +945,13 @@ def main():
     dist = init_dist(world, "nccl")
     import __graft_entry__ as g
     g.build()
+    if args.markov_only:
+        if rank == 0:
+            mk = markov_arm(args.seed, reps=max(args.steps, 3), with_oracle=not args.no_cpu_baseline)
+            print(json.dumps({"markov_draft": mk}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     result, inp = gpu_arm(args, wl, mode, dist, world, rank, device)
     # the extra workloads and the sweep: one-GPU runs only (the scaling runs time the
     # headline alone)
