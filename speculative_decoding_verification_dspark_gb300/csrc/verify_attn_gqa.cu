@@ -37,6 +37,11 @@
 //              second transpose-reduction of the bf16 P the PV product multiplies
 //              (so the weights applied to V are exactly the normalised rounded P).
 //              Epilogue: O / l, lse.
+//   warps 8-11 (128-column tile only) a second softmax warpgroup: warps 4-7 own
+//              query columns 0-63 and warps 8-11 columns 64-127, each with its
+//              own half of P^T, its own PV product (N = 64) and its own share
+//              of the epilogue staging.  A half with no rows in an item only
+//              releases S^T; the PV product of that half is skipped.
 // Every wait is bounded in time (DSPARK_DEVERR_WAIT_TIMEOUT on expiry).
 
 #include <cuda.h>
