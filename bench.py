@@ -30,6 +30,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import statistics
@@ -691,11 +692,17 @@ def load_peaks():
         return {}
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def src_hash(paths):
+    """Hash of the sources' code: comments and whitespace left out, so that a change
+    of wording alone keeps a capture taken on the same code."""
     h = hashlib.sha256()
     for path in paths:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            code = _COMMENT.sub(" ", f.read())
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

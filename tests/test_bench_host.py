@@ -71,6 +71,18 @@ def test_traffic_sources_follow_the_head_shape():
         assert os.path.isfile(p), p
 
 
+def test_source_hash_keys_code_not_comments(tmp_path):
+    """A committed traffic figure stays valid through a comment or layout edit of its
+    sources and is dropped by any change of code."""
+    a = tmp_path / "k.cu"
+    a.write_text("int f(int x) {\n  return x + 1;  // one\n}\n/* note */\n")
+    h0 = bench.src_hash([str(a)])
+    a.write_text("// header\nint f(int x)\n{\n    return x + 1;  // other words\n}\n")
+    assert bench.src_hash([str(a)]) == h0
+    a.write_text("int f(int x) {\n  return x + 2;\n}\n")
+    assert bench.src_hash([str(a)]) != h0
+
+
 def test_oracle_baseline_complete_steps_one_core_and_pool():
     """The CPU baseline times complete oracle steps; the pooled run (spawned worker
     processes over memory-mapped inputs) computes what the one-core run computes."""
