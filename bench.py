@@ -64,6 +64,17 @@ def attn_src(wl):
 ACCEPT_SRC = [os.path.join(_CSRC, f) for f in ("accept.cu", "common.cuh")]
 
 
+def query_tile(wl, hint):
+    """The attention launch a block-rows hint selects: the GQA query tile (32, 64 or 128
+    columns for `hint` block rows of G heads, as the library picks it) or the latent-KV
+    kernel's one tile.  A label that keys a committed DRAM-traffic figure to the launch
+    configuration it was captured on."""
+    if wl.attn == "mla":
+        return "mla"
+    rows = (wl.Hq // wl.Hkv) * max(int(hint), 1)
+    return f"nt{32 if rows <= 32 else (64 if rows <= 64 else 128)}"
+
+
 def workload_desc(wl: W.Workload, mode: str) -> str:
     head = (f"GQA {wl.Hq}/{wl.Hkv} heads x {wl.d_qk}" if wl.attn == "gqa"
             else f"MLA {wl.Hq} heads, latent {wl.d_qk} (v {wl.d_v})")
@@ -321,7 +332,8 @@ class StepRunner:
         return {
             "verify_attn": {"us": attn_us, "GB/s": attn_gbs, "frac_hbm": attn_gbs / peaks["hbm"],
                             "TFLOP/s": attn_tfs, "frac_tensor": attn_tfs / peaks["tf"],
-                            "bytes": a_bytes, "flops": a_flops},
+                            "bytes": a_bytes, "flops": a_flops,
+                            "launch": query_tile(wl, st.block_rows_hint)},
             "accept": {"us": accept_us, "GB/s": acc_gbs, "frac_hbm": acc_gbs / peaks["hbm"],
                        "bytes": c_bytes},
         }
@@ -388,9 +400,9 @@ def roofline_block(wl, kf):
     per algorithmic byte exceed the ridge point of the measured peaks."""
     pk = peak_values()
     a = kf["verify_attn"]
-    traffic = load_traffic("verify_attn", wl.name, attn_src(wl))
+    traffic = load_traffic("verify_attn", wl.name, attn_src(wl), a.get("launch"))
     common = {"kernel": "dspark_verify_attn (main kernel + combine; work list from the pack call)",
-              "traffic": traffic, "algorithmic_bytes": a["bytes"], "us_per_launch": a["us"]}
+              "launch": a.get("launch"), "traffic": traffic, "algorithmic_bytes": a["bytes"], "us_per_launch": a["us"]}
     if a["flops"] / max(a["bytes"], 1) > pk["tf"] * 1e12 / (pk["hbm"] * 1e9):
         return {"bound": "tensor", "achieved": a["TFLOP/s"], "peak": pk["tf"], "unit": "TFLOP/s",
                 "frac": a["TFLOP/s"] / pk["tf"], "algorithmic_flops": a["flops"], **common,
@@ -706,15 +718,16 @@ def src_hash(paths):
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel, workload, src):
+def load_traffic(kernel, workload, src, launch=None):
     """Per-launch DRAM bytes from a committed ncu summary, if it was taken on the
-    current source of the kernel."""
+    current source of the kernel (and, for the attention, on the same launch
+    configuration)."""
     p = os.path.join(PROFILES, "traffic.json")
     try:
         with open(p) as f:
             t = json.load(f)
         e = t[f"{kernel}/{workload}"]
-        if e.get("src_sha256_16") == src_hash(src):
+        if e.get("src_sha256_16") == src_hash(src) and e.get("launch") == launch:
             return e["dram_bytes_per_launch"]
     except (OSError, KeyError, ValueError):
         pass

@@ -194,9 +194,14 @@ int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* a
  * boundary (into at most max_splits pieces, 2..32) is merged by a log-sum-exp
  * combine.  If cu_seqlens[B] > max_rows the device sets
  * DSPARK_DEVERR_ROWS_OVERFLOW and nothing is computed.  max_block_rows is a
- * hint: the largest row count of one request's segment (gamma + 1), used to size
- * the query tile of the GQA kernel (<= 0: unknown); any segment length is
- * handled correctly whatever its value.
+ * hint: the rows of one request's segment the query tile of the GQA kernel is
+ * sized for (32, 64 or 128 columns for max_block_rows x Hq/Hkv query rows; <= 0
+ * counts as 1).  Any segment length is handled correctly
+ * whatever its value: a longer segment runs as several row tiles, each over all
+ * of its keys.  The whole block (gamma + 1) suits segments that are all long
+ * (static and cap-accept verification); a compact step's short windows run
+ * fastest on the 32-column tile (floor(32 / G) rows).  The workspace size
+ * depends on it: a smaller hint needs more work items.
  * ------------------------------------------------------------------------- */
 size_t dspark_verify_attn_workspace_size(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v,
                                          int max_splits, int max_block_rows);

@@ -15,6 +15,7 @@ import torch
 
 __all__ = [
     "COMPACT", "STATIC", "CAP_ACCEPT", "F32", "BF16", "DSparkError", "lib", "load",
+    "block_rows_hint_for",
     "schedule", "pack", "verify_attn", "accept", "accept_noalloc", "compact", "read_device_error",
     "verify_attn_workspace_size", "accept_workspace_size", "compact_workspace_size",
     "VerifyStep", "StepGraph", "CalibStore", "DEVERR",
@@ -407,6 +408,20 @@ class StepGraph:
             pass
 
 
+def block_rows_hint_for(gamma, Hq, Hkv, mode) -> int:
+    """Rows per request the attention's query tile is sized for in ``mode`` (the
+    ``max_block_rows`` hint); a request with more rows is split into row tiles (exact;
+    its keys are then read once per row tile, mostly from L2).
+
+    Static and cap-accept verify the whole block: gamma + 1.  A compact window is short
+    -- a few rows -- and the smallest tile (32 query rows: floor(32 / G) block rows of
+    G = Hq / Hkv heads) does far less softmax work per key tile than one sized for the
+    whole block, while the rare longer window takes a second row tile."""
+    if int(mode) == COMPACT:
+        return max(1, min(gamma + 1, 32 // max(1, Hq // Hkv)))
+    return gamma + 1
+
+
 class VerifyStep:
     """Device buffers and workspaces for repeated verification steps of one shape.
 
@@ -419,9 +434,18 @@ class VerifyStep:
     """
 
     def __init__(self, B, gamma, Hq, Hkv, d_qk, d_v, vocab, max_rows, p_dtype=torch.float32,
-                 max_splits=8, device="cuda"):
+                 max_splits=8, device="cuda", block_rows_hint=None):
         self.B, self.gamma, self.Hq, self.Hkv, self.d_qk, self.d_v = B, gamma, Hq, Hkv, d_qk, d_v
         self.vocab, self.max_rows, self.max_splits = vocab, max_rows, max_splits
+        # the attention's query tile per mode (block_rows_hint); ``block_rows_hint``
+        # fixes one hint for every mode
+        if block_rows_hint is None:
+            self._hints = {m: block_rows_hint_for(gamma, Hq, Hkv, m)
+                           for m in (COMPACT, STATIC, CAP_ACCEPT)}
+        else:
+            h = int(block_rows_hint)
+            self._hints = {COMPACT: h, STATIC: h, CAP_ACCEPT: h}
+        self.block_rows_hint = self._hints[COMPACT]  # of the last pack call
         dev = torch.device(device)
         i32 = dict(dtype=torch.int32, device=dev)
         self.windows = torch.zeros(B, **i32)
@@ -444,7 +468,9 @@ class VerifyStep:
         self.cstar = torch.zeros(B, gamma, dtype=torch.float32, device=dev)
         self.committed = torch.zeros(B, gamma + 1, **i32)
         self.n_committed = torch.zeros(B, **i32)
-        sz = verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits, gamma + 1)
+        # sized for the smallest tile (the most work items)
+        sz = verify_attn_workspace_size(B, max_rows, Hq, Hkv, d_qk, d_v, max_splits,
+                                        min(self._hints.values()))
         if sz == 0:
             raise ValueError("unsupported attention shape")
         self.ws_attn = torch.empty(sz, dtype=torch.uint8, device=dev)
@@ -458,6 +484,7 @@ class VerifyStep:
                  survival=self.survival)
 
     def pack(self, inp, mode, stream=None):
+        self.block_rows_hint = self.hint(mode)  # for a following attention()
         pack(self.windows, inp["ctx_len"], inp["anchor"], inp["draft_tok"], inp["tiers"], mode,
              self.cu_seqlens, self.M_pack, self.tier, self.row_req, self.row_pos, self.row_tok,
              stream)
@@ -466,20 +493,26 @@ class VerifyStep:
         verify_attn(inp["q"], inp["k_new"], inp.get("v_new"), inp["k_cache"], inp.get("v_cache"),
                     inp["page_table"], inp["ctx_len"], self.cu_seqlens, inp["scale"],
                     self.max_splits, self.out, self.lse, self.ws_attn, stream,
-                    max_block_rows=self.gamma + 1)
+                    max_block_rows=self.block_rows_hint)
+
+    def hint(self, mode) -> int:
+        """The block-rows hint (query tile) the step uses in ``mode``."""
+        return self._hints[int(mode)]
 
     def pack_plan(self, inp, mode, stream=None):
-        """pack, with the attention work list built in the same kernel (for attention_planned)."""
+        """pack, with the attention work list built in the same kernel (for attention_planned,
+        which takes the query tile chosen here)."""
+        self.block_rows_hint = self.hint(mode)
         pack_plan(self.windows, inp["ctx_len"], inp["anchor"], inp["draft_tok"], inp["tiers"], mode,
                   self.cu_seqlens, self.M_pack, self.tier, self.row_req, self.row_pos,
                   self.row_tok, self.Hq, self.Hkv, self.d_qk, self.d_v, self.max_rows,
-                  self.max_splits, self.ws_attn, stream, max_block_rows=self.gamma + 1)
+                  self.max_splits, self.ws_attn, stream, max_block_rows=self.block_rows_hint)
 
     def attention_planned(self, inp, stream=None):
         verify_attn_planned(inp["q"], inp["k_new"], inp.get("v_new"), inp["k_cache"],
                             inp.get("v_cache"), inp["page_table"], inp["ctx_len"],
                             self.cu_seqlens, inp["scale"], self.max_splits, self.out, self.lse,
-                            self.ws_attn, stream, max_block_rows=self.gamma + 1)
+                            self.ws_attn, stream, max_block_rows=self.block_rows_hint)
 
     def accept(self, inp, mode, stream=None):
         accept(inp["p_target"], inp["p_draft"], inp["draft_tok"], inp["uniforms"],
@@ -510,7 +543,8 @@ class VerifyStep:
         d.max_rows, d.n_tiers = self.max_rows, tiers_host.numel()
         d.tiers_host, d.tiers = tiers_host.data_ptr(), _ptr(tiers_dev)
         d.conf_is_logit, d.cost_len = int(inp["conf_is_logit"]), inp["cost_table"].numel()
-        d.max_tokens, d.max_splits, d.max_block_rows = int(inp["max_tokens"]), self.max_splits, self.gamma + 1
+        d.max_tokens, d.max_splits, d.max_block_rows = (int(inp["max_tokens"]), self.max_splits,
+                                                      self.hint(mode))
         d.scale = float(inp["scale"])
         for k in ("conf", "sts_temp", "cost_table", "draft_tok", "q", "k_new", "p_target", "p_draft",
                   "uniforms", "exp_noise", "free_pages", "page_table", "ctx_len", "anchor",

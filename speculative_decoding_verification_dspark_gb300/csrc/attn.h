@@ -50,8 +50,9 @@ int launch(const void* q, const void* k_new, const void* v_new, const void* k_ca
            void* ws, const Plan& pl, cudaStream_t stream, bool planned = false);
 
 namespace gqa {
-// Query-row tile (32, 64 or 128) for G = Hq/Hkv heads per KV head and at most
-// max_block_rows rows per request segment (<= 0: unknown, take 128).
+// Query-row tile (32, 64 or 128) for G = Hq/Hkv heads per KV head and
+// max_block_rows rows per request segment (<= 0 counts as 1); a longer segment
+// runs as several row tiles.
 int query_tile(int Hq, int Hkv, int max_block_rows);
 int launch_kernel(int nt, const void* q, const void* k_new, const void* v_new, const void* k_cache,
                   const void* v_cache, int n_pages, const int32_t* page_table, int max_pages,

@@ -71,6 +71,25 @@ def test_traffic_sources_follow_the_head_shape():
         assert os.path.isfile(p), p
 
 
+def test_query_tile_policy():
+    """Compact mode sizes the attention's query tile for floor(32 / G) block rows (the
+    32-column tile), static and cap-accept for the whole block; the traffic key names
+    the tile each selects."""
+    import speculative_decoding_verification_dspark_gb300 as dspark
+    q = W.WORKLOADS["qwen3_8b"]                     # G = 4, gamma = 8
+    assert dspark.block_rows_hint_for(q.gamma, q.Hq, q.Hkv, dspark.COMPACT) == 8
+    assert dspark.block_rows_hint_for(q.gamma, q.Hq, q.Hkv, dspark.STATIC) == 9
+    assert dspark.block_rows_hint_for(q.gamma, q.Hq, q.Hkv, dspark.CAP_ACCEPT) == 9
+    assert bench.query_tile(q, 8) == "nt32" and bench.query_tile(q, 9) == "nt64"
+    m = W.WORKLOADS["mixed256"]                     # G = 5, gamma = 16
+    assert dspark.block_rows_hint_for(m.gamma, m.Hq, m.Hkv, dspark.COMPACT) == 6
+    assert bench.query_tile(m, 6) == "nt32" and bench.query_tile(m, 17) == "nt128"
+    t = W.WORKLOADS["tiny"]                         # the whole block already fits 32 columns
+    assert dspark.block_rows_hint_for(t.gamma, t.Hq, t.Hkv, dspark.COMPACT) == t.gamma + 1
+    assert dspark.block_rows_hint_for(8, 128, 2, dspark.COMPACT) == 1   # G > 32
+    assert bench.query_tile(W.WORKLOADS["mla"], 9) == "mla"
+
+
 def test_source_hash_keys_code_not_comments(tmp_path):
     """A committed traffic figure stays valid through a comment or layout edit of its
     sources and is dropped by any change of code."""
