@@ -289,6 +289,26 @@ def test_group_sizes_and_row_tiles(B, G):
     run_and_check(inp, O.STATIC)
 
 
+@pytest.mark.parametrize("G,B", [(4, 6), (5, 5), (3, 7)])
+def test_compact_windows_longer_than_the_query_tile(G, B):
+    """Compact mode sizes the query tile for floor(32 / G) block rows; confident drafts
+    make windows of up to gamma + 1 = 13 rows, so requests run as two or three row tiles
+    of the 32-column tile, beside requests that fit one.  Every request's attention
+    against fp64."""
+    import speculative_decoding_verification_dspark_gb300 as dspark
+    wl = W.Workload(
+        name=f"rowtiles_g{G}", B=B, gamma=12, attn="gqa", Hq=2 * G, Hkv=2, d_qk=128, d_v=128,
+        page_size=16, ctx=("uniform", 40, 700), conf=("logit", 3.0, 1.5), vocab=512,
+        p_dtype="f32", target_logit_std=2.0, draft_noise_std=0.3, tiers=(32, 64, 128),
+        cost_theta_ms=0.5)
+    inp = W.make_inputs(wl, seed=5)
+    hint = dspark.block_rows_hint_for(wl.gamma, wl.Hq, wl.Hkv, O.COMPACT)
+    g, sch, pk, acc = run_and_check(inp, O.COMPACT)
+    rows = np.diff(np.asarray(pk.cu_seqlens))
+    assert hint == 32 // G
+    assert int(rows.max()) > hint >= int(rows.min())  # split requests beside whole ones
+
+
 def test_mla_small():
     wl = W.Workload(
         name="mla_small", B=3, gamma=4, attn="mla", Hq=128, Hkv=1, d_qk=576, d_v=512, page_size=64,
