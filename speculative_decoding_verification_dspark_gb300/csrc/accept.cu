@@ -146,15 +146,17 @@ __global__ void __launch_bounds__(128)
 // Persistent, one CTA per SM over a contiguous range of (packed row, 8192-entry
 // chunk) items.  One thread streams the rows the method needs (p_t always, p_d for
 // c* rows and corrections, the noise row on the sampled row) with bulk copies into a
-// five-slot shared-memory ring (noise into a ring of its own), running ahead across
-// items; sixteen consumer warps reduce each slot from shared memory; a reducer warp
-// combines the sixteen warps' results of an item into its partial.  A slot holds
-// 16 KB of each probability row: 4096 fp32 or 8192 bf16 entries (so a bf16 item is
-// one slot, and the per-slot bookkeeping is spread over twice the entries).
-constexpr int kSub = 4096;                    // entries per stage
-constexpr int kVStages = 5;                   // main ring: p_t | p_d
-constexpr int kVStageBytes = 2 * kSub * 4;    // (fp32 sizes)
-constexpr int kNoiseBytes = 64 * 1024;        // noise ring, sampled rows only
+// shared-memory ring of whole items (noise into a ring of its own), running ahead
+// across items; sixteen consumer warps reduce each slot from shared memory; a reducer
+// warp combines the sixteen warps' results of an item into its partial.  A slot holds
+// the item's 8192 entries of each probability row: 32 KB copies per row in fp32 (a
+// single issuing thread streams 32 KB copies about 15% faster than 16 KB ones), 16 KB
+// in bf16.  fp32 takes three slots and one noise slot, bf16 five and two: 224 KB.
+template <int ES> struct RingGeom;
+template <> struct RingGeom<4> { static constexpr int kStages = 3, kNoise = 1; };
+template <> struct RingGeom<2> { static constexpr int kStages = 5, kNoise = 2; };
+constexpr int kMaxVStages = 5;
+constexpr int kRingBytes = 224 * 1024;        // main ring, then the noise ring
 constexpr int kConsumerWarps = 16;
 constexpr int kProducerWarp = 16, kReducerWarp = 17;
 constexpr int kVocabCtaThreads = 18 * 32;
@@ -168,11 +170,10 @@ struct WarpPart {
 };
 
 struct VocabSmem {
-  uint8_t stage[kVStages][kVStageBytes];
-  uint8_t noise[kNoiseBytes];  // 4 slots of 4096 fp32 noise entries, or 2 of 8192
+  uint8_t ring[kRingBytes];  // RingGeom<ES>::kStages slots of p_t | p_d, then noise slots
   WarpPart red[2][kConsumerWarps];
-  int4 meta[kVStages];  // item, sub-chunk | sub-chunks << 8, request, row flags
-  uint64_t full[kVStages], empty[kVStages], nempty[4], red_full[2], red_free[2];
+  int4 meta[kMaxVStages];  // item, sub-chunk | sub-chunks << 8, request, row flags
+  uint64_t full[kMaxVStages], empty[kMaxVStages], nempty[4], red_full[2], red_free[2];
   uint64_t never;  // a barrier nothing arrives at (the wait probe)
   int abort_flag;
 };
@@ -274,6 +275,14 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
   // sampled rows) spread over many SMs
   const long long n_items = (long long)M * n_chunks;
   volatile int* abort_flag = &S.abort_flag;
+  constexpr int ES = static_cast<int>(sizeof(T));
+  constexpr int kSubT = kChunk;                         // entries per slot: one item
+  constexpr int kRowB = kSubT * ES;                     // one probability row in a slot
+  constexpr int kVStages = RingGeom<ES>::kStages;
+  constexpr int kNStages = RingGeom<ES>::kNoise;         // noise slots
+  constexpr int kNoiseOff = kVStages * 2 * kRowB;
+  static_assert(kNoiseOff + kNStages * kSubT * 4 <= kRingBytes && kVStages <= kMaxVStages,
+                "ring");
   if (threadIdx.x == 0) {
     S.abort_flag = 0;
     for (int s = 0; s < kVStages; ++s) {
@@ -289,10 +298,6 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
     ptx::fence_mbar_init();
   }
   __syncthreads();
-  constexpr int ES = static_cast<int>(sizeof(T));
-  constexpr int kSubT = kSub * 4 / ES;                  // entries per slot
-  constexpr int kNStages = kNoiseBytes / (kSubT * 4);   // noise slots
-  static_assert(kNStages >= 2 && kNStages <= 4, "noise ring");
   auto n_sub_of = [&](int ch) {
     const int len = min(kChunk, V - ch * kChunk);
     return (len + kSubT - 1) / kSubT;
@@ -356,14 +361,15 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
           const float* e_row = exp_noise + (long long)w.r * V;
           const int v0 = ch * kChunk + sb * kSubT;
           const uint32_t len = static_cast<uint32_t>(min(kSubT, V - v0));
-          const uint32_t base = ptx::smem_addr(S.stage[st]);
+          const uint32_t base = ptx::smem_addr(S.ring + st * 2 * kRowB);
           const uint32_t bytes = len * ES * (w.need_d ? 2u : 1u) + (w.samp ? len * 4u : 0u);
           S.meta[st] = make_int4(static_cast<int>(item), sb | (ns << 8), w.r, desc.y);
           ptx::mbar_expect_tx(full, bytes);
           ptx::bulk_load_g2s(base, pt_row + v0, len * ES, full);
-          if (w.need_d) ptx::bulk_load_g2s(base + kSub * 4, pd_row + v0, len * ES, full);
+          if (w.need_d) ptx::bulk_load_g2s(base + kRowB, pd_row + v0, len * ES, full);
           if (w.samp) {
-            ptx::bulk_load_g2s(ptx::smem_addr(S.noise + sn * kSubT * 4), e_row + v0, len * 4, full);
+            ptx::bulk_load_g2s(ptx::smem_addr(S.ring + kNoiseOff + sn * kSubT * 4), e_row + v0,
+                               len * 4, full);
             ++gn;
           }
           ptx::mbar_arrive(full);
@@ -461,9 +467,9 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
       {
         const int v0 = ch * kChunk + sb * kSubT;
         const int len = min(kSubT, V - v0);
-        const uint8_t* st = S.stage[s];
+        const uint8_t* st = S.ring + s * 2 * kRowB;
         const int sn = gn % kNStages;
-        const uint8_t* nz = S.noise + sn * kSubT * 4;
+        const uint8_t* nz = S.ring + kNoiseOff + sn * kSubT * 4;
 #pragma unroll
         for (int k = 0; k < kSubT / (kConsumerWarps * 32 * 8); ++k) {
           const int e = (k * kConsumerWarps * 32 + threadIdx.x) * 8;
@@ -473,7 +479,7 @@ __global__ void __launch_bounds__(kVocabCtaThreads, 1)
           for (int q = 0; q < 8; ++q) { a[q] = 0.f; d[q] = 0.f; en[q] = 1.f; ka[q] = kDead; }
           if (valid) {
             smem_vec8<T>(st + e * ES, a);
-            if (w.need_d) smem_vec8<T>(st + kSub * 4 + e * ES, d);
+            if (w.need_d) smem_vec8<T>(st + kRowB + e * ES, d);
             if (w.l1) {
 #pragma unroll
               for (int q = 0; q < 8; ++q) l1 += fabsf(d[q] - a[q]);
