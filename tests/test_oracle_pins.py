@@ -499,6 +499,69 @@ def test_compact_hand_worked_example():
     assert c.n_committed.tolist() == [3, 1, 5]
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_compact_invariants_on_random_states(seed):
+    """Commit invariants on random states (page sizes 1..16, contexts on and off page
+    boundaries, windows 0..gamma): the committed counts sum to sum(L + 1) and hold
+    d_1..d_L then the token; old page-table entries are unchanged; the new entries are
+    the top sum(new pages) entries of the free stack, taken in request order (so each
+    page once, none already held); free_top drops by their number; ctx grows by L + 1
+    and the anchor is the token; every kept row lands at its position through the new
+    table, and no other cache slot changes."""
+    rng = np.random.default_rng(100 + seed)
+    B, gamma = int(rng.integers(1, 13)), int(rng.integers(2, 9))
+    P = int(rng.choice([1, 2, 4, 16]))
+    max_pages = (6 * P + gamma + 4) // P + 2
+    ctx = rng.integers(0, 5 * P + 4, B).astype(np.int32)
+    L = rng.integers(0, gamma + 1, B).astype(np.int32)
+    have = (ctx + P - 1) // P
+    n_pages = int(have.sum()) + B * max_pages + 3
+    perm = rng.permutation(n_pages).astype(np.int32)
+    pt = np.full((B, max_pages), -1, np.int32)
+    o = 0
+    for r in range(B):
+        pt[r, :have[r]] = perm[o:o + have[r]]
+        o += int(have[r])
+    free = perm[o:].copy()
+    top = len(free) - int(rng.integers(0, 3))  # entries above top are not free
+    cu = np.concatenate([[0], np.cumsum(L + 1 + rng.integers(0, 3, B))]).astype(np.int32)
+    M = int(cu[-1])
+    kn = (np.arange(M, dtype=np.float32) + 1000.0).reshape(M, 1, 1)
+    vn = -kn
+    kc = -(np.arange(n_pages * P, dtype=np.float32) + 1.0).reshape(n_pages, P, 1, 1)
+    vc = kc * 3.0
+    draft = rng.integers(0, 50000, (B, gamma)).astype(np.int32)
+    tok = rng.integers(0, 50000, B).astype(np.int32)
+    anchor = rng.integers(0, 50000, B).astype(np.int32)
+    c = O.compact(kn, vn, cu, L, tok, draft, P, pt, ctx, anchor, free, top, kc, vc)
+    keep = L + 1
+    nn = (ctx + keep + P - 1) // P - have
+    assert int(c.n_committed.sum()) == int(keep.sum())
+    for r in range(B):
+        assert c.committed[r, :L[r]].tolist() == draft[r, :L[r]].tolist()
+        assert c.committed[r, L[r]] == tok[r] and (c.committed[r, L[r] + 1:] == -1).all()
+    assert (c.ctx_len == ctx + keep).all() and (c.anchor == tok).all()
+    assert c.free_top == top - int(nn.sum())
+    held = set(int(x) for x in pt[pt >= 0])
+    taken = []
+    for r in range(B):
+        assert (c.page_table[r, :have[r]] == pt[r, :have[r]]).all()        # old entries
+        assert (c.page_table[r, have[r] + nn[r]:] == -1).all()
+        taken += c.page_table[r, have[r]:have[r] + nn[r]].tolist()
+    assert taken == free[top - int(nn.sum()):top][::-1].tolist()          # stack order
+    assert len(set(taken)) == len(taken) and not (set(taken) & held)
+    changed = np.zeros(kc.shape[:2], bool)
+    for r in range(B):
+        for i in range(int(keep[r])):
+            pos = int(ctx[r]) + i
+            page = int(c.page_table[r, pos // P])
+            assert c.k_cache[page, pos % P, 0, 0] == kn[cu[r] + i, 0, 0]
+            assert c.v_cache[page, pos % P, 0, 0] == vn[cu[r] + i, 0, 0]
+            changed[page, pos % P] = True
+    assert (c.k_cache[~changed] == kc[~changed]).all()
+    assert (c.v_cache[~changed] == vc[~changed]).all()
+
+
 def test_compact_no_space_raises():
     kn = np.zeros((2, 1, 1), np.float32)
     with pytest.raises(O.NoSpace):
