@@ -443,6 +443,35 @@ def test_identical_and_disjoint_distributions():
     assert a2.out_tok[0] < V // 2           # the correction comes from the target's support
 
 
+@pytest.mark.parametrize("mode", [O.COMPACT, O.STATIC, O.CAP_ACCEPT])
+def test_cstar_positions_and_hand_values(mode):
+    """c* (reading A13) exists for the draft positions whose target row was verified:
+    j = 1..min(w + 1, gamma) in compact mode, 1..gamma in static and cap-accept; the
+    others are NaN.  Values by hand: identical rows give 1; p_t = (1/2, 1/2, 0, 0)
+    against a uniform draft gives 1 - (1/4 + 1/4 + 1/4 + 1/4) / 2 = 1/2; a target row
+    (1, 0, 0, 0) against (0, 1/2, 1/2, 0) gives 0."""
+    gamma, V, w = 4, 4, 1
+    q = np.full(V, 0.25, np.float32)
+    half = np.array([0.5, 0.5, 0.0, 0.0], np.float32)
+    one = np.array([1.0, 0.0, 0.0, 0.0], np.float32)
+    mid = np.array([0.0, 0.5, 0.5, 0.0], np.float32)
+    p_d = np.stack([q, q, mid, q])[None]                  # draft rows j = 1..4
+    p_t = np.stack([q, half, one, q, q])[None]            # target rows 0..4
+    d = np.zeros((1, gamma), np.int32)                    # the target keeps mass on 0
+    u = np.full((1, gamma), 0.5, np.float32)
+    e = np.ones((1, V), np.float32)
+    win = np.array([gamma if mode == O.STATIC else w], np.int32)
+    n = w + 1 if mode == O.COMPACT else gamma + 1
+    cu = np.array([0, n])
+    a = O.accept(_rows_for(p_t, cu, 1), p_d, d, u, e, win, cu, mode, gamma)
+    c = a.cstar[0]
+    assert c[0] == 1.0 and c[1] == 0.5
+    if mode == O.COMPACT:
+        assert np.isnan(c[2]) and np.isnan(c[3])
+    else:
+        assert c[2] == 0.0 and c[3] == 1.0
+
+
 def test_race_argmax_lowest_index_on_ties():
     w = np.array([0.1, 0.4, 0.2, 0.4], np.float32)
     e = np.ones(4, np.float32)
