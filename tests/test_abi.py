@@ -105,6 +105,18 @@ def test_workspace_sizes_are_host_computable(lib):
     assert lib.dspark_markov_draft_workspace_size(1000) == 0
 
 
+def test_attention_workspace_follows_the_query_tile(lib):
+    """A smaller block-rows hint (a smaller query tile, more row tiles per request)
+    needs at least as many work items, so at least as large a workspace; a hint <= 0
+    counts as one row, and the latent-KV shape ignores the hint."""
+    ws = lambda h: lib.dspark_verify_attn_workspace_size(32, 512, 32, 8, 128, 128, 8, h)
+    sizes = [ws(h) for h in (17, 9, 8, 4, 1)]
+    assert all(a <= b for a, b in zip(sizes, sizes[1:])) and sizes[0] < sizes[-1]
+    assert ws(0) == ws(-3) == ws(1)
+    mla = lambda h: lib.dspark_verify_attn_workspace_size(64, 1024, 128, 1, 576, 512, 8, h)
+    assert mla(9) == mla(1) == mla(0) > 0
+
+
 def test_step_graph_rejects_bad_descriptors_on_the_host(lib):
     """The step graph's descriptor is checked before any CUDA work: NULL arguments,
     tiers that are not ascending or exceed the row capacity."""
