@@ -200,7 +200,8 @@ int dspark_pack(const int32_t* windows, const int32_t* ctx_len, const int32_t* a
  * whatever its value: a longer segment runs as several row tiles, each over all
  * of its keys.  The whole block (gamma + 1) suits segments that are all long
  * (static and cap-accept verification); a compact step's short windows run
- * fastest on the 32-column tile (floor(32 / G) rows).  The workspace size
+ * fastest on the smallest tile that holds a few rows (floor(32 / G) rows, the
+ * 32-column tile, for G <= 8).  The workspace size
  * depends on it: a smaller hint needs more work items.
  * ------------------------------------------------------------------------- */
 size_t dspark_verify_attn_workspace_size(int B, int max_rows, int Hq, int Hkv, int d_qk, int d_v,

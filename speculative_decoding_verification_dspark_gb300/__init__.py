@@ -414,11 +414,18 @@ def block_rows_hint_for(gamma, Hq, Hkv, mode) -> int:
     its keys are then read once per row tile, mostly from L2).
 
     Static and cap-accept verify the whole block: gamma + 1.  A compact window is short
-    -- a few rows -- and the smallest tile (32 query rows: floor(32 / G) block rows of
-    G = Hq / Hkv heads) does far less softmax work per key tile than one sized for the
-    whole block, while the rare longer window takes a second row tile."""
+    -- a few rows -- and the smallest tile holding four block rows of G = Hq / Hkv heads
+    (32 query rows: floor(32 / G) block rows for G <= 8; 64 or 128 for larger groups)
+    does far less softmax work per key tile than one sized for the whole block, while
+    the rare longer window takes a second row tile.  (Measured with G = 4 and 5; the
+    four-row floor keeps wide groups from splitting a typical window into many row
+    tiles, each of which reads the request's keys again.)"""
+    G = max(1, Hq // Hkv)
     if int(mode) == COMPACT:
-        return max(1, min(gamma + 1, 32 // max(1, Hq // Hkv)))
+        for cols in (32, 64, 128):
+            if cols // G >= 4:
+                return min(gamma + 1, cols // G)
+        return gamma + 1
     return gamma + 1
 
 

@@ -86,7 +86,10 @@ def test_query_tile_policy():
     assert bench.query_tile(m, 6) == "nt32" and bench.query_tile(m, 17) == "nt128"
     t = W.WORKLOADS["tiny"]                         # the whole block already fits 32 columns
     assert dspark.block_rows_hint_for(t.gamma, t.Hq, t.Hkv, dspark.COMPACT) == t.gamma + 1
-    assert dspark.block_rows_hint_for(8, 128, 2, dspark.COMPACT) == 1   # G > 32
+    assert dspark.block_rows_hint_for(8, 64, 8, dspark.COMPACT) == 4    # G = 8: 32 columns
+    assert dspark.block_rows_hint_for(8, 32, 2, dspark.COMPACT) == 4    # G = 16: 64 columns
+    assert dspark.block_rows_hint_for(8, 64, 2, dspark.COMPACT) == 4    # G = 32: 128 columns
+    assert dspark.block_rows_hint_for(8, 128, 2, dspark.COMPACT) == 9   # G = 64: whole block
     assert bench.query_tile(W.WORKLOADS["mla"], 9) == "mla"
 
 
