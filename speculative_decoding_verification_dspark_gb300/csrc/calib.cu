@@ -46,13 +46,6 @@ __device__ __forceinline__ int warp_scan_incl(int v) {
   return v;
 }
 
-// sigmoid without overflow for either sign of t
-__device__ __forceinline__ double sigmoid_d(double t) {
-  if (t >= 0.0) return 1.0 / (1.0 + exp(-t));
-  const double e = exp(t);
-  return e / (1.0 + e);
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(kCollectThreads)
